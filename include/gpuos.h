@@ -1,0 +1,315 @@
+/*
+ * gpuos.h -- C ABI of the GB300 persistent micro-op dispatcher.
+ *
+ * The method is the one described in "GPUOS: A GPU Operating System Primitive
+ * for Transparent Operation Fusion" (Yang et al., 2026), §2 and §3 Q2:
+ *   - a persistent executor kernel is launched once, one block per SM, and
+ *     never exits while the context lives (§3 Q2 "2. Persistent Kernel
+ *     Executor");
+ *   - the host writes 64-128 B task descriptors {op_id, input_a, input_b,
+ *     output, size, flags} into a lock-free single-producer ring in memory
+ *     the device can see, committing each with a store-release; the device
+ *     polls with load-acquire, claims work atomically, dispatches and
+ *     releases the slot (§3 Q2 "1. Ring Buffer Communication Channel");
+ *   - dispatch goes through a device-resident table of device-function
+ *     pointers indexed by op_id, kept in two slots (active / inactive) that a
+ *     version counter flips with a store-release (§3 Q2 "3. Dynamic Operator
+ *     Table");
+ *   - the ops are the page's operator library: element-wise add, mul, ReLU,
+ *     GELU, softmax, LayerNorm; vector-matrix products; SDPA and rotary
+ *     embeddings; KV-cache update; small sum/max/min reductions (§3 Q2,
+ *     "Operator library").
+ *
+ * Conventions for every call:
+ *   - Returns GPUOS_OK (0) or a negative GPUOS_E* code; nothing throws, aborts
+ *     or falls back to the CPU.
+ *   - Tensors named in descriptors are caller-owned device memory and must stay
+ *     alive until their descriptor has completed. The library owns the ring,
+ *     the completion records, the operator table, loaded modules and the
+ *     executor's stream.
+ *   - One producer thread per context (the ring is single-producer).
+ *   - While the executor is resident, do not call cudaDeviceSynchronize() (it
+ *     would wait for a kernel that does not end), and launch only kernels that
+ *     were loaded before gpuos_init (under lazy module loading, loading a new
+ *     kernel may wait for the device to go idle). The executor leaves by
+ *     itself after `idle_exit_ms` without host activity, so no such mistake
+ *     can hang the GPU for good.
+ */
+#ifndef GPUOS_H
+#define GPUOS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GPUOS_API __attribute__((visibility("default")))
+#else
+#define GPUOS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define GPUOS_OK 0
+#define GPUOS_EINVAL (-1)    /* bad argument, op id, pointer or dims */
+#define GPUOS_EAGAIN (-2)    /* ring full until the timeout ran out */
+#define GPUOS_ETIMEDOUT (-3) /* a wait ran out */
+#define GPUOS_EDEVICE (-4)   /* a descriptor completed with a device status != 0 */
+#define GPUOS_ECUDA (-5)     /* a CUDA runtime/driver call failed */
+#define GPUOS_ESTOPPED (-6)  /* the executor is no longer running */
+#define GPUOS_ENOMEM (-7)
+#define GPUOS_EBUSY (-8)     /* needs the executor not resident (see gpuos_load_module) */
+
+/* ---- device status codes (gpuos_record.status) -------------------------- */
+#define GPUOS_ST_OK 0
+#define GPUOS_ST_BAD_OP 1        /* op_id out of range or empty table entry */
+#define GPUOS_ST_BAD_ARGS 2      /* dims / positions / lengths out of range */
+#define GPUOS_ST_DEP_TIMEOUT 3   /* a dependency or fence wait ran out */
+#define GPUOS_ST_ABORTED 4       /* the executor was leaving */
+#define GPUOS_ST_BAD_DESC 5      /* ring slot did not hold the expected ticket */
+
+/* ---- op ids (built-in operator library) --------------------------------- */
+enum {
+    GPUOS_OP_NOP = 0,       /* no effect; latency probe */
+    GPUOS_OP_ADD = 1,       /* out[i] = a[i] + b[i]            dims = {n}          f32|bf16 */
+    GPUOS_OP_MUL = 2,       /* out[i] = a[i] * b[i]            dims = {n}          f32|bf16 */
+    GPUOS_OP_RELU = 3,      /* out[i] = max(a[i], +0)          dims = {n}          f32|bf16 */
+    GPUOS_OP_GELU = 4,      /* out[i] = a Phi(a), erf form     dims = {n}          f32|bf16 */
+    GPUOS_OP_SOFTMAX = 5,   /* row softmax of a[R][H] -> out   dims = {R, H}       bf16 */
+    GPUOS_OP_LAYERNORM = 6, /* a[R][H], b=gamma[H], aux0=beta[H] -> out; fparam[0] = eps; bf16 */
+    GPUOS_OP_ROWSUM = 7,    /* out f32[R] = sum_j a[r][j]      dims = {R, H}       bf16 in */
+    GPUOS_OP_ROWMAX = 8,    /* out bf16[R] = max_j a[r][j]     dims = {R, H} */
+    GPUOS_OP_ROWMIN = 9,    /* out bf16[R] = min_j a[r][j]     dims = {R, H} */
+    GPUOS_OP_ROPE = 10,     /* in place on a=q[B][H][D], b=k[B][H][D]; aux0 = lens i32[B],
+                               position lens[b]-1; half-split pairs (i, i+D/2);
+                               fparam[0] = theta; dims = {B, H, D}, D even, D <= 256 */
+    GPUOS_OP_KV_WRITE = 11, /* Kc[b][h][lens[b]-1][:] = a[b][h][:], same for Vc; out = Kc,
+                               aux1 = Vc laid out [B][H][Lcap][D]; aux0 = lens i32[B];
+                               dims = {B, H, D, Lcap}; bit-exact copy */
+    GPUOS_OP_SDPA = 12,     /* o = softmax(scale q.K^T) V over rows 0..lens[b]-1; a = q[B][H][D],
+                               b = Kc, aux1 = Vc [B][H][Lcap][D], aux0 = lens, out = o[B][H][D],
+                               aux2 = 16-byte aligned fp32 workspace: first round_up(Ccap, 4)
+                               uint32 counters, then B*H*ceil(Lmax/512) partials of D+2 floats
+                               (gpuos_sdpa_workspace_bytes(Bcap, H, D, Lmax) with Ccap = Bcap*H);
+                               the counters must be zero before first use and every descriptor
+                               leaves them zero; descriptors sharing a workspace use one Ccap;
+                               dims = {B, H, D=128, Lcap, Lmax >= every lens[b], Ccap >= B*H};
+                               fparam[0] = scale */
+    GPUOS_OP_VECMAT = 13,   /* out[n] = sum_k a[k] b[k][n]; b row-major [K][N]; dims = {K, N}; bf16 */
+    GPUOS_OP_BUILTIN_COUNT = 14,
+    GPUOS_OP_USER_FIRST = 64, /* ids >= this are free for gpuos_register_op */
+    GPUOS_MAX_OPS = 256
+};
+
+#define GPUOS_F32 0
+#define GPUOS_BF16 1
+
+/* descriptor flags */
+#define GPUOS_FLAG_FENCE 1u   /* start only after every earlier descriptor completed */
+#define GPUOS_FLAG_DEP_REL 2u /* dep[i] holds a backward distance (1 = the previous
+                                 descriptor) instead of an absolute ticket + 1 */
+
+/*
+ * Task descriptor: 128 bytes, one ring slot (the page gives 64-128 B holding
+ * {op_id, input_a, input_b, output, size, flags}, §3 Q2 "1. Ring Buffer
+ * Communication Channel"). Fields marked [lib] are written by the library.
+ *
+ * dep[i]: 0 = none; otherwise ticket + 1 of an earlier descriptor this one
+ * must wait for (or a distance with GPUOS_FLAG_DEP_REL). ntiles is computed by
+ * the library for built-in ops; for user ops (id >= GPUOS_OP_USER_FIRST) the
+ * caller sets it (>= 0; each tile is handed to one warp).
+ */
+typedef struct gpuos_desc {
+    uint16_t op_id;
+    uint8_t dtype;  /* GPUOS_F32 | GPUOS_BF16 */
+    uint8_t flags;  /* GPUOS_FLAG_* */
+    uint32_t ntiles;
+    uint64_t dep[2];
+    uint64_t a, b, out;       /* device pointers */
+    uint64_t aux0, aux1, aux2; /* device pointers, per op */
+    uint32_t dims[6];
+    float fparam[2];
+    uint64_t user;   /* caller tag, not read by the device */
+    uint64_t ticket; /* [lib] */
+    uint64_t seq;    /* [lib] commit word: ticket + 1 once the slot is published */
+} gpuos_desc;
+
+/* Executor / ring configuration. gpuos_default_config() fills defaults. */
+typedef struct gpuos_config {
+    uint32_t ring_entries;    /* power of two in [64, 65536]; default 4096 (the page's default) */
+    uint32_t warps_per_block; /* 2..16; default 8 */
+    uint32_t blocks;          /* 0 = one block per SM */
+    uint32_t backoff_min_ns;  /* first idle sleep; default 32 */
+    uint32_t backoff_max_ns;  /* idle sleep cap; default 256 */
+    uint32_t spin_polls;      /* polls of pure spinning before backing off; default 4096 */
+    uint32_t idle_exit_ms;    /* leave after this long with no host activity; 0 = never; default 10000 */
+    uint32_t dep_timeout_ms;  /* bound of every device-side wait; default 5000 */
+    uint32_t ring_in_device_mem; /* 0: ring in pinned host memory (default);
+                                    1: managed memory preferred on the device */
+    int32_t device;           /* CUDA device ordinal; default 0 */
+    uint64_t exit_after;      /* 0 = run until shutdown; n = leave once n descriptors completed */
+    uint32_t tq_entries;      /* work-queue entries, power of two in [1024, 2^20]; default 65536 */
+    uint32_t deferred_start;  /* 1: gpuos_init does not launch; gpuos_start does (descriptors
+                                 may be submitted before, up to ring_entries of them) */
+    uint32_t reserved[4];
+} gpuos_config;
+
+/* Completion record of one ticket (device clock = %globaltimer, host clock =
+ * CLOCK_REALTIME in ns; gpuos_calibrate bounds their offset). */
+typedef struct gpuos_record {
+    uint64_t ticket;
+    int32_t status;             /* GPUOS_ST_* */
+    uint32_t version;           /* operator-table version the descriptor ran with */
+    uint64_t t_commit_host_ns;  /* host clock just before the commit store-release */
+    uint64_t t_dispatch_dev_ns; /* when the executor saw the commit (picked it off the ring) */
+    uint64_t t_publish_dev_ns;  /* when its tiles were published to the work queue */
+    uint64_t t_start_dev_ns;    /* when a warp began its tile 0 */
+    uint64_t t_done_dev_ns;     /* when its last tile finished */
+} gpuos_record;
+
+typedef struct gpuos_stats_t {
+    uint64_t submitted;     /* host: descriptors committed */
+    uint64_t completed;     /* host: completions harvested */
+    uint64_t errors;        /* host: completions with status != 0 */
+    uint64_t sequenced;     /* device: descriptors taken off the ring */
+    uint64_t tiles;         /* device: tiles executed */
+    uint64_t idle_polls;    /* device: empty polls of workers and sequencer */
+    uint64_t sleeps;        /* device: __nanosleep backoffs */
+    uint64_t dep_waits;     /* device: tiles that waited on a dependency */
+    uint32_t version;       /* current operator-table version */
+    uint32_t running;       /* 1 while the executor kernel is resident */
+    uint32_t exit_reason;   /* 0 running, 1 stop, 2 idle watchdog, 3 exit_after, 4 internal */
+    uint32_t blocks;
+    uint32_t warps_per_block;
+    uint32_t regs_per_thread; /* of the executor kernel */
+    uint32_t static_smem_bytes;
+    uint32_t reserved;
+    uint64_t seq_body_ns;    /* device: sequencer time reading descriptors (after seeing commits) */
+    uint64_t seq_mirror_ns;  /* device: sequencer time mirroring + fencing */
+    uint64_t seq_publish_ns; /* device: sequencer time publishing work-queue entries */
+} gpuos_stats_t;
+
+typedef struct gpuos_ctx gpuos_ctx;
+
+/* Fill *cfg with defaults. */
+GPUOS_API void gpuos_default_config(gpuos_config *cfg);
+
+/* Allocate the ring, completion records and operator table, fill both table
+ * slots with the built-in ops (version 0) and launch the executor once on a
+ * non-blocking stream (grid = blocks, block = 32 * warps_per_block). *out
+ * receives the context. Errors: EINVAL (bad config), ECUDA, ENOMEM. */
+GPUOS_API int gpuos_init(const gpuos_config *cfg, gpuos_ctx **out);
+
+/* Launch the executor of a context made with deferred_start (once). Lets a
+ * caller fill the ring first (a bounded, replayable run for profilers) or put
+ * the single launch inside a timed region. Errors: EINVAL (already started),
+ * ECUDA. */
+GPUOS_API int gpuos_start(gpuos_ctx *ctx);
+
+/* The non-blocking stream the executor runs on (a cudaStream_t), so callers
+ * can bracket the kernel with CUDA events. */
+GPUOS_API int gpuos_executor_stream(gpuos_ctx *ctx, void **stream);
+
+/* Submit one descriptor (§3 Q2 ring protocol: acquire slot, write, commit
+ * with store-release). Validates op_id, pointers, dims and deps on the host,
+ * computes ntiles for built-in ops, waits up to timeout_us for a free slot
+ * (EAGAIN after that, nothing submitted). *ticket (may be NULL) receives the
+ * ticket. Errors: EINVAL, EAGAIN, ESTOPPED. */
+GPUOS_API int gpuos_submit(gpuos_ctx *ctx, const gpuos_desc *d, uint64_t *ticket, uint32_t timeout_us);
+
+/* Submit count descriptors in order (same as count gpuos_submit calls);
+ * *first_ticket receives the first ticket. Stops at the first failure and
+ * returns its code; *n_done (may be NULL) receives how many were submitted. */
+GPUOS_API int gpuos_submit_batch(gpuos_ctx *ctx, const gpuos_desc *d, uint32_t count, uint64_t *first_ticket,
+                       uint32_t *n_done, uint32_t timeout_us);
+
+/* Wait until `ticket` (or, with ticket == UINT64_MAX, everything submitted so
+ * far) has completed, up to timeout_ms. Returns EDEVICE if any descriptor
+ * harvested by this call completed with a nonzero status, ETIMEDOUT on
+ * timeout, ESTOPPED if the executor left with work outstanding. */
+GPUOS_API int gpuos_sync(gpuos_ctx *ctx, uint64_t ticket, uint32_t timeout_ms);
+
+/* Completion record of a finished ticket still in the history window (the
+ * last `ring_entries` tickets, or the whole run with gpuos_set_history).
+ * Errors: EAGAIN (not finished yet), EINVAL (outside the window). */
+GPUOS_API int gpuos_query(gpuos_ctx *ctx, uint64_t ticket, gpuos_record *rec);
+
+/* Keep every harvested completion record of tickets [base, base + capacity)
+ * in caller memory (host), for latency statistics. buf may be NULL to stop. */
+GPUOS_API int gpuos_set_history(gpuos_ctx *ctx, gpuos_record *buf, uint64_t base, uint64_t capacity);
+
+/* Load a precompiled sm_103a cubin image into the context (driver API; the
+ * bytes are copied). On this driver a module load waits for the device to go
+ * idle, which a resident executor never does, so loading is allowed only
+ * while the executor is not resident: before gpuos_start (deferred_start) or
+ * after gpuos_stop. Loading an image already loaded is a no-op. Modules stay
+ * loaded until gpuos_shutdown. Errors: EINVAL (not a loadable image), EBUSY
+ * (executor resident), ECUDA. */
+GPUOS_API int gpuos_load_module(gpuos_ctx *ctx, const void *image, size_t len);
+
+/* Runtime operator injection (§3 Q2 "3. Dynamic Operator Table", steps 3-5):
+ * find the loaded module holding `image` (gpuos_load_module; loaded here if
+ * the executor is not resident), read its `__device__` variable
+ * `fnptr_symbol` holding the address of a device function with the op
+ * signature, write it into the inactive table slot (a copy of the active one
+ * with entry op_id replaced), then flip the version with a store-release.
+ * Nothing stops: descriptors sequenced before the flip finish with the old
+ * entry; later ones use the new one. Before a later flip reuses that slot the
+ * call waits until every descriptor sequenced under the older version has
+ * completed. The function must use at most the executor's registers per
+ * thread (compile it with the same -maxrregcount). Errors: EINVAL, EBUSY
+ * (image not loaded and executor resident), ECUDA, ETIMEDOUT. */
+GPUOS_API int gpuos_register_op(gpuos_ctx *ctx, uint16_t op_id, const void *image, size_t len,
+                      const char *fnptr_symbol);
+
+/* Point op_id back at a built-in op or an earlier registered function:
+ * `source_op` names the entry to copy from the active table. Same flip and
+ * grace-period protocol as gpuos_register_op. */
+GPUOS_API int gpuos_alias_op(gpuos_ctx *ctx, uint16_t op_id, uint16_t source_op);
+
+/* Live counters (host and device). */
+GPUOS_API int gpuos_stats(gpuos_ctx *ctx, gpuos_stats_t *st);
+
+/* NOP ping-pong: `pings` round trips, each committing a NOP (host clock t0)
+ * and spinning on its completion record (host clock t1). Since the device
+ * picks the NOP up between t0 and t1, every ping bounds the offset
+ * off = device clock - host clock to [t_dispatch - t1, t_dispatch - t0];
+ * *off_lo / *off_hi receive the intersection over all pings and *min_rtt_ns
+ * the smallest t1 - t0. rtts (may be NULL) receives every round trip. */
+GPUOS_API int gpuos_calibrate(gpuos_ctx *ctx, uint32_t pings, int64_t *off_lo, int64_t *off_hi,
+                              uint64_t *min_rtt_ns, uint64_t *rtts);
+
+/* Drain (wait for everything submitted, up to timeout_ms), set the stop flag
+ * and wait (up to timeout_ms) for the executor kernel to end; the context
+ * stays valid (stats, queries) but accepts no more work. */
+GPUOS_API int gpuos_stop(gpuos_ctx *ctx, uint32_t timeout_ms);
+
+/* gpuos_stop, then free everything. The context is freed even on error. */
+GPUOS_API int gpuos_shutdown(gpuos_ctx *ctx, uint32_t timeout_ms);
+
+/* Host tiling rule of a built-in op (what ntiles the library will write). */
+GPUOS_API int gpuos_op_ntiles(const gpuos_desc *d, uint32_t *ntiles);
+
+/* Workspace bytes a decode-SDPA descriptor needs (fp32 partials of 512-row
+ * chunks plus one counter per (b, h)). */
+GPUOS_API size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, uint32_t Lmax);
+
+/* Eager baseline: launch the same op bodies as ordinary kernels, one
+ * cudaLaunchKernel per descriptor, in order, on `stream` (a cudaStream_t; 0 =
+ * legacy default). Deps are implied by stream order. Does not synchronize.
+ * Errors: EINVAL (as gpuos_submit), ECUDA. */
+GPUOS_API int gpuos_eager_run(const gpuos_desc *d, uint32_t count, void *stream);
+
+/* CLOCK_REALTIME in ns (the host clock of gpuos_record). */
+GPUOS_API uint64_t gpuos_host_now_ns(void);
+
+/* Text for a return code or, with is_status != 0, a device status. */
+GPUOS_API const char *gpuos_strerror(int code, int is_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPUOS_H */

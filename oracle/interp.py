@@ -166,11 +166,18 @@ class Machine:
             self.exact[j] = ex
 
     # -- many ops -------------------------------------------------------------
-    def run(self, keep: Optional[Iterable[int]] = None, upto: Optional[int] = None) -> None:
-        """Apply ops 0..upto-1 in order; keep exact results for ``keep``."""
+    def run(self, keep: Optional[Iterable[int]] = None, upto: Optional[int] = None,
+            skip: Optional[Iterable[int]] = None) -> None:
+        """Apply ops 0..upto-1 in order; keep exact results for ``keep``.
+
+        ``skip`` names ops whose outputs no later op reads (the caller's
+        claim); leaving them out does not change any other op's result."""
         keep_set: Set[int] = set(keep) if keep is not None else set()
+        skip_set: Set[int] = set(skip) if skip is not None else set()
         n = len(self.s.ops) if upto is None else upto
         for j in range(n):
+            if j in skip_set and j not in keep_set:
+                continue
             self.apply(j, keep=j in keep_set)
 
     def run_closure(self, targets: Iterable[int]) -> List[int]:

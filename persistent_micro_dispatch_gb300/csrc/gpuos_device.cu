@@ -1,0 +1,1226 @@
+/*
+ * Device side of the GB300 persistent micro-op dispatcher (sm_103a).
+ *
+ * Method: "GPUOS: A GPU Operating System Primitive for Transparent Operation
+ * Fusion", §2 and §3 Q2. A persistent executor, launched once with one block
+ * per SM, polls a single-producer ring of task descriptors with load-acquire,
+ * claims work atomically, dispatches it through a device-resident operator
+ * table indexed by op_id, releases the slot and backs off exponentially when
+ * idle; new operators enter through a dual-slot table flipped by a version
+ * counter.
+ *
+ * GB300 design (what differs from the page's per-warp poll/claim):
+ *   - One warp of block 0 is the *sequencer*. It alone polls the host ring
+ *     (32 slots per poll, one per lane, ld.acquire.sys across NVLink-C2C),
+ *     copies each committed descriptor into a device-memory mirror, fixes the
+ *     table version the descriptor runs with, and publishes one work-queue
+ *     entry per tile. The host ring therefore sees one reader, and workers
+ *     never touch host memory on the hot path.
+ *   - Every other warp is a *worker*. It claims work-queue entries with one
+ *     64-bit atomicAdd each (the page's atomic claim), so a large op is split
+ *     across many warps on many SMs (the page lists in-kernel multi-block
+ *     cooperation as missing, §4 "design binding critique"), while a tiny op
+ *     is one tile on one warp.
+ *   - The last tile of a descriptor completes it: status and timestamps into
+ *     the host-visible record, a device-memory done stamp for dependency waits
+ *     and the store-release of the record's done_seq, which also releases the
+ *     ring slot to the host.
+ *   - Every wait is bounded (dependency and fence waits by dep_timeout_ns,
+ *     idle polling by the host-heartbeat watchdog) and ends in a status, never
+ *     a trap.
+ *   - Ops are memory-bound and use no tensor cores: 16-byte vector loads that
+ *     bypass L1 (data produced by other SMs inside this same kernel must not
+ *     be read from a stale L1 line), fp32 arithmetic, warp shuffles for
+ *     reductions, registers for row staging.
+ */
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "gpuos_internal.h"
+
+#define DEV __device__ __forceinline__
+
+/* ---------------------------------------------------------------------------
+ * Memory-order primitives (PTX memory model).
+ * ------------------------------------------------------------------------- */
+DEV uint64_t ld_acquire_sys(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+DEV uint64_t ld_acquire_gpu(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+DEV uint32_t ld_acquire_gpu32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+DEV uint64_t ld_relaxed_sys(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+DEV uint32_t ld_relaxed_sys32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+DEV uint32_t ld_relaxed_gpu32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+DEV void st_release_sys(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+DEV void st_release_gpu(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+DEV void st_relaxed_sys(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.relaxed.sys.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+DEV void st_relaxed_sys32(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.relaxed.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+DEV void st_relaxed_gpu32(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+DEV uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+DEV uint32_t lane_id() { return threadIdx.x & 31u; }
+
+/* Idle backoff: spin for `spin` polls, then sleep min_ns << k up to max_ns. */
+DEV void backoff(uint32_t &polls, uint32_t spin, uint32_t min_ns, uint32_t max_ns, uint64_t *sleeps)
+{
+    if (polls < spin) {
+        polls++;
+        return;
+    }
+    uint32_t k = polls - spin;
+    k = k > 16 ? 16 : k;
+    uint32_t ns = min_ns << k;
+    ns = ns > max_ns ? max_ns : ns;
+    __nanosleep(ns);
+    polls++;
+    (*sleeps)++;
+}
+
+/* ---------------------------------------------------------------------------
+ * bf16 helpers. Widening is exact; narrowing rounds to nearest-even.
+ * ------------------------------------------------------------------------- */
+DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+DEV float bf1(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+DEV uint32_t pack_bf2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+DEV uint16_t to_bf(float x)
+{
+    __nv_bfloat16 v = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&v);
+}
+DEV void unpack8(const uint4 &v, float *f)
+{
+    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+}
+DEV uint4 pack8(const float *f)
+{
+    return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));
+}
+DEV float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+DEV float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+DEV float warp_min(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+/* ===========================================================================
+ * Operator library. Every op is a warp-cooperative device function
+ *     int op(const gpuos_devdesc *d, uint32_t tile)
+ * called by all 32 lanes of one warp with the same arguments; it returns a
+ * GPUOS_ST_* status, identical on every lane. Tiles past the end of an op
+ * are no-ops.
+ * ======================================================================== */
+
+enum { EW_ADD = 0, EW_MUL = 1, EW_RELU = 2, EW_GELU = 3 };
+
+template <int OP>
+DEV float ew1(float a, float b)
+{
+    if (OP == EW_ADD) return __fadd_rn(a, b);
+    if (OP == EW_MUL) return __fmul_rn(a, b);
+    if (OP == EW_RELU) return a > 0.0f ? a : 0.0f;
+    /* GELU, exact form x * Phi(x) with Phi(x) = erfc(-x / sqrt 2) / 2: the
+     * complementary error function keeps full relative accuracy for x < 0,
+     * where 1 + erf(x / sqrt 2) would cancel */
+    return 0.5f * a * erfcf(-a * 0.70710678118654752f);
+}
+
+template <int OP, bool BF>
+DEV uint4 ew_vec(const uint4 &va, const uint4 &vb)
+{
+    if (BF) {
+        float fa[8], fb[8], r[8];
+        unpack8(va, fa);
+        unpack8(vb, fb);
+#pragma unroll
+        for (int i = 0; i < 8; i++) r[i] = ew1<OP>(fa[i], fb[i]);
+        return pack8(r);
+    } else {
+        uint4 r;
+        r.x = __float_as_uint(ew1<OP>(__uint_as_float(va.x), __uint_as_float(vb.x)));
+        r.y = __float_as_uint(ew1<OP>(__uint_as_float(va.y), __uint_as_float(vb.y)));
+        r.z = __float_as_uint(ew1<OP>(__uint_as_float(va.z), __uint_as_float(vb.z)));
+        r.w = __float_as_uint(ew1<OP>(__uint_as_float(va.w), __uint_as_float(vb.w)));
+        return r;
+    }
+}
+
+/* Element-wise tile: 32 lanes x GPUOS_EW_VPT 16-byte vectors, in rounds of 8
+ * independent vector loads per operand per lane. Unaligned operands take a
+ * scalar path with the same arithmetic. */
+template <int OP, bool BF>
+DEV int ew_tile(const gpuos_devdesc *d, uint32_t tile)
+{
+    constexpr uint32_t VEC = BF ? 8 : 4;
+    constexpr uint32_t ES = BF ? 2 : 4;
+    constexpr uint32_t TILE = 32 * GPUOS_EW_VPT * VEC;
+    constexpr bool BIN = (OP == EW_ADD || OP == EW_MUL);
+    constexpr int U = 8;
+    const uint32_t lane = lane_id();
+    const uint64_t n = d->dims[0];
+    const uint64_t start = (uint64_t)tile * TILE;
+    if (start >= n) return GPUOS_ST_OK;
+    const uint32_t cnt = (uint32_t)((n - start) < TILE ? (n - start) : TILE);
+    const char *pa = reinterpret_cast<const char *>(d->a) + start * ES;
+    const char *pb = BIN ? reinterpret_cast<const char *>(d->b) + start * ES : pa;
+    char *po = reinterpret_cast<char *>(d->out) + start * ES;
+    const bool aligned = (((uintptr_t)pa | (uintptr_t)pb | (uintptr_t)po) & 15u) == 0;
+    const uint32_t nvec = aligned ? cnt / VEC : 0;
+    const uint4 *va = reinterpret_cast<const uint4 *>(pa);
+    const uint4 *vb = reinterpret_cast<const uint4 *>(pb);
+    uint4 *vo = reinterpret_cast<uint4 *>(po);
+    for (uint32_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+        uint4 ra[U], rb[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const uint32_t v = v0 + u * 32 + lane;
+            if (v < nvec) {
+                ra[u] = __ldcg(va + v);
+                rb[u] = BIN ? __ldcg(vb + v) : ra[u];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const uint32_t v = v0 + u * 32 + lane;
+            if (v < nvec) __stcg(vo + v, ew_vec<OP, BF>(ra[u], rb[u]));
+        }
+    }
+    for (uint32_t i = nvec * VEC + lane; i < cnt; i += 32) {
+        if (BF) {
+            const uint16_t *a16 = reinterpret_cast<const uint16_t *>(pa);
+            const uint16_t *b16 = reinterpret_cast<const uint16_t *>(pb);
+            reinterpret_cast<uint16_t *>(po)[i] = to_bf(ew1<OP>(bf1(a16[i]), bf1(b16[i])));
+        } else {
+            const float *a32 = reinterpret_cast<const float *>(pa);
+            const float *b32 = reinterpret_cast<const float *>(pb);
+            reinterpret_cast<float *>(po)[i] = ew1<OP>(a32[i], b32[i]);
+        }
+    }
+    return GPUOS_ST_OK;
+}
+
+template <int OP>
+DEV int ew_dispatch(const gpuos_devdesc *d, uint32_t tile)
+{
+    if (d->dtype == GPUOS_BF16) return ew_tile<OP, true>(d, tile);
+    if (d->dtype == GPUOS_F32) return ew_tile<OP, false>(d, tile);
+    return GPUOS_ST_BAD_ARGS;
+}
+
+/* ---- row ops: one row per tile -------------------------------------------- */
+enum { ROW_SOFTMAX = 0, ROW_LN = 1, ROW_SUM = 2, ROW_MAX = 3, ROW_MIN = 4 };
+
+/* Rows of H <= GPUOS_ROW_REG_MAX bf16 with H % 8 == 0 and 16-byte aligned
+ * operands: the row is read once into registers (16 vectors per lane). */
+template <int K>
+DEV int row_reg(const gpuos_devdesc *d, uint32_t row, uint32_t H)
+{
+    constexpr int J = GPUOS_ROW_REG_MAX / 256;
+    const uint32_t lane = lane_id();
+    const uint32_t nv = H / 8;
+    const uint4 *x = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)row * H);
+    uint4 r[J];
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        const uint32_t v = lane + 32u * j;
+        if (v < nv) r[j] = __ldcg(x + v);
+    }
+    if (K == ROW_SUM || K == ROW_MAX || K == ROW_MIN) {
+        float acc = (K == ROW_SUM) ? 0.0f : (K == ROW_MAX ? -INFINITY : INFINITY);
+#pragma unroll
+        for (int j = 0; j < J; j++) {
+            const uint32_t v = lane + 32u * j;
+            if (v < nv) {
+                float f[8];
+                unpack8(r[j], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    if (K == ROW_SUM) acc += f[i];
+                    else if (K == ROW_MAX) acc = fmaxf(acc, f[i]);
+                    else acc = fminf(acc, f[i]);
+                }
+            }
+        }
+        if (K == ROW_SUM) acc = warp_sum(acc);
+        else if (K == ROW_MAX) acc = warp_max(acc);
+        else acc = warp_min(acc);
+        if (lane == 0) {
+            if (K == ROW_SUM) reinterpret_cast<float *>(d->out)[row] = acc;
+            else reinterpret_cast<uint16_t *>(d->out)[row] = to_bf(acc);
+        }
+        return GPUOS_ST_OK;
+    }
+    uint4 *y = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(d->out) + (uint64_t)row * H);
+    if (K == ROW_SOFTMAX) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < J; j++) {
+            if (lane + 32u * j < nv) {
+                float f[8];
+                unpack8(r[j], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) m = fmaxf(m, f[i]);
+            }
+        }
+        m = warp_max(m);
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < J; j++) {
+            if (lane + 32u * j < nv) {
+                float f[8];
+                unpack8(r[j], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) s += __expf(f[i] - m);
+            }
+        }
+        const float inv = 1.0f / warp_sum(s);
+#pragma unroll
+        for (int j = 0; j < J; j++) {
+            const uint32_t v = lane + 32u * j;
+            if (v < nv) {
+                float f[8];
+                unpack8(r[j], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) f[i] = __expf(f[i] - m) * inv;
+                __stcg(y + v, pack8(f));
+            }
+        }
+        return GPUOS_ST_OK;
+    }
+    /* LayerNorm: biased variance, two passes over the registers. */
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        if (lane + 32u * j < nv) {
+            float f[8];
+            unpack8(r[j], f);
+#pragma unroll
+            for (int i = 0; i < 8; i++) s += f[i];
+        }
+    }
+    const float mean = warp_sum(s) / (float)H;
+    float q = 0.0f;
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        if (lane + 32u * j < nv) {
+            float f[8];
+            unpack8(r[j], f);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const float t = f[i] - mean;
+                q += t * t;
+            }
+        }
+    }
+    const float rstd = rsqrtf(warp_sum(q) / (float)H + d->fparam[0]);
+    const uint4 *g = reinterpret_cast<const uint4 *>(d->b);
+    const uint4 *bt = reinterpret_cast<const uint4 *>(d->aux0);
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        const uint32_t v = lane + 32u * j;
+        if (v < nv) {
+            float f[8], gf[8], bf[8];
+            unpack8(r[j], f);
+            unpack8(__ldcg(g + v), gf);
+            unpack8(__ldcg(bt + v), bf);
+#pragma unroll
+            for (int i = 0; i < 8; i++) f[i] = (f[i] - mean) * rstd * gf[i] + bf[i];
+            __stcg(y + v, pack8(f));
+        }
+    }
+    return GPUOS_ST_OK;
+}
+
+/* Any width or alignment: scalar passes re-reading the row. */
+template <int K>
+DEV int row_generic(const gpuos_devdesc *d, uint32_t row, uint32_t H)
+{
+    const uint32_t lane = lane_id();
+    const uint16_t *x = reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)row * H;
+    if (K == ROW_SUM || K == ROW_MAX || K == ROW_MIN) {
+        float acc = (K == ROW_SUM) ? 0.0f : (K == ROW_MAX ? -INFINITY : INFINITY);
+        for (uint32_t j = lane; j < H; j += 32) {
+            const float f = bf1(__ldcg(x + j));
+            if (K == ROW_SUM) acc += f;
+            else if (K == ROW_MAX) acc = fmaxf(acc, f);
+            else acc = fminf(acc, f);
+        }
+        if (K == ROW_SUM) acc = warp_sum(acc);
+        else if (K == ROW_MAX) acc = warp_max(acc);
+        else acc = warp_min(acc);
+        if (lane == 0) {
+            if (K == ROW_SUM) reinterpret_cast<float *>(d->out)[row] = acc;
+            else reinterpret_cast<uint16_t *>(d->out)[row] = to_bf(acc);
+        }
+        return GPUOS_ST_OK;
+    }
+    uint16_t *y = reinterpret_cast<uint16_t *>(d->out) + (uint64_t)row * H;
+    if (K == ROW_SOFTMAX) {
+        float m = -INFINITY;
+        for (uint32_t j = lane; j < H; j += 32) m = fmaxf(m, bf1(__ldcg(x + j)));
+        m = warp_max(m);
+        float s = 0.0f;
+        for (uint32_t j = lane; j < H; j += 32) s += __expf(bf1(__ldcg(x + j)) - m);
+        const float inv = 1.0f / warp_sum(s);
+        for (uint32_t j = lane; j < H; j += 32) y[j] = to_bf(__expf(bf1(__ldcg(x + j)) - m) * inv);
+        return GPUOS_ST_OK;
+    }
+    float s = 0.0f;
+    for (uint32_t j = lane; j < H; j += 32) s += bf1(__ldcg(x + j));
+    const float mean = warp_sum(s) / (float)H;
+    float q = 0.0f;
+    for (uint32_t j = lane; j < H; j += 32) {
+        const float t = bf1(__ldcg(x + j)) - mean;
+        q += t * t;
+    }
+    const float rstd = rsqrtf(warp_sum(q) / (float)H + d->fparam[0]);
+    const uint16_t *g = reinterpret_cast<const uint16_t *>(d->b);
+    const uint16_t *bt = reinterpret_cast<const uint16_t *>(d->aux0);
+    for (uint32_t j = lane; j < H; j += 32)
+        y[j] = to_bf((bf1(__ldcg(x + j)) - mean) * rstd * bf1(__ldcg(g + j)) + bf1(__ldcg(bt + j)));
+    return GPUOS_ST_OK;
+}
+
+template <int K>
+DEV int row_tile(const gpuos_devdesc *d, uint32_t row)
+{
+    const uint32_t R = d->dims[0], H = d->dims[1];
+    if (row >= R) return GPUOS_ST_OK;
+    if (H == 0) return GPUOS_ST_BAD_ARGS;
+    bool ok = H <= GPUOS_ROW_REG_MAX && (H & 7u) == 0 && (d->a & 15u) == 0;
+    if (K == ROW_SOFTMAX || K == ROW_LN) ok = ok && (d->out & 15u) == 0;
+    if (K == ROW_LN) ok = ok && ((d->b | d->aux0) & 15u) == 0;
+    return ok ? row_reg<K>(d, row, H) : row_generic<K>(d, row, H);
+}
+
+/* ---- RoPE: one request (all heads of q and k) per tile -------------------- */
+DEV int rope_tile(const gpuos_devdesc *d, uint32_t b)
+{
+    const uint32_t B = d->dims[0], H = d->dims[1], D = d->dims[2];
+    if (b >= B) return GPUOS_ST_OK;
+    if (D == 0 || (D & 1u) || D > 256) return GPUOS_ST_BAD_ARGS;
+    const int32_t pos = __ldcg(reinterpret_cast<const int32_t *>(d->aux0) + b) - 1;
+    if (pos < 0) return GPUOS_ST_BAD_ARGS;
+    const uint32_t lane = lane_id(), half = D / 2;
+    const float theta = d->fparam[0];
+    float c[4], s[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const uint32_t i = lane + 32u * j;
+        c[j] = 1.0f;
+        s[j] = 0.0f;
+        if (i < half) {
+            const float inv = powf(theta, -(2.0f * (float)i) / (float)D);
+            sincosf((float)pos * inv, &s[j], &c[j]);
+        }
+    }
+    for (int which = 0; which < 2; which++) {
+        uint16_t *base = reinterpret_cast<uint16_t *>(which ? d->b : d->a) + (uint64_t)b * H * D;
+        for (uint32_t h0 = 0; h0 < H; h0 += 4) {
+            float x0[4][4], x1[4][4];
+#pragma unroll
+            for (int hh = 0; hh < 4; hh++) {
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint32_t i = lane + 32u * j;
+                    if (h0 + hh < H && i < half) {
+                        const uint16_t *row = base + (uint64_t)(h0 + hh) * D;
+                        x0[hh][j] = bf1(__ldcg(row + i));
+                        x1[hh][j] = bf1(__ldcg(row + i + half));
+                    }
+                }
+            }
+#pragma unroll
+            for (int hh = 0; hh < 4; hh++) {
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint32_t i = lane + 32u * j;
+                    if (h0 + hh < H && i < half) {
+                        uint16_t *row = base + (uint64_t)(h0 + hh) * D;
+                        row[i] = to_bf(x0[hh][j] * c[j] - x1[hh][j] * s[j]);
+                        row[i + half] = to_bf(x1[hh][j] * c[j] + x0[hh][j] * s[j]);
+                    }
+                }
+            }
+        }
+    }
+    return GPUOS_ST_OK;
+}
+
+/* ---- KV-cache slot write: one request per tile, bit-exact copy ------------- */
+DEV int kv_tile(const gpuos_devdesc *d, uint32_t b)
+{
+    const uint32_t B = d->dims[0], H = d->dims[1], D = d->dims[2], Lcap = d->dims[3];
+    if (b >= B) return GPUOS_ST_OK;
+    const int32_t pos = __ldcg(reinterpret_cast<const int32_t *>(d->aux0) + b) - 1;
+    if (pos < 0 || (uint32_t)pos >= Lcap) return GPUOS_ST_BAD_ARGS;
+    const uint32_t lane = lane_id();
+    for (int which = 0; which < 2; which++) {
+        const uint16_t *src = reinterpret_cast<const uint16_t *>(which ? d->b : d->a) + (uint64_t)b * H * D;
+        uint16_t *dst = reinterpret_cast<uint16_t *>(which ? d->aux1 : d->out) +
+                        ((uint64_t)b * H * Lcap + (uint64_t)pos) * D;
+        const uint64_t hstride = (uint64_t)Lcap * D; /* elements between heads in the cache */
+        if ((D & 7u) == 0 && (((uintptr_t)src | (uintptr_t)dst) & 15u) == 0) {
+            const uint32_t nvr = D / 8, total = H * nvr;
+#pragma unroll 4
+            for (uint32_t i = lane; i < total; i += 32) {
+                const uint32_t h = i / nvr, v = i - h * nvr;
+                const uint4 val = __ldcg(reinterpret_cast<const uint4 *>(src + (uint64_t)h * D) + v);
+                __stcg(reinterpret_cast<uint4 *>(dst + h * hstride) + v, val);
+            }
+        } else {
+            for (uint32_t i = lane; i < H * D; i += 32) {
+                const uint32_t h = i / D, e = i - h * D;
+                dst[h * hstride + e] = src[(uint64_t)h * D + e];
+            }
+        }
+    }
+    return GPUOS_ST_OK;
+}
+
+/* ---- decode SDPA: one (request, head, 512-row chunk) per tile -------------
+ * Four 8-lane groups walk interleaved key rows; in a group lane li owns dims
+ * [16 li, 16 li + 16) of q, K and V. Scores use exp2 with log2(e) folded into
+ * the query scale; each group keeps an online-softmax state (m, l, acc),
+ * the four states merge by shuffles, and multi-chunk heads merge through the
+ * workspace in the last chunk to finish. */
+DEV void sdpa_merge(float &m, float &l, float *acc, float mo, float lo, const float *acco)
+{
+    const float mn = fmaxf(m, mo);
+    const float mu = (mn == -INFINITY) ? 0.0f : mn;
+    const float a = exp2f(m - mu), b = exp2f(mo - mu);
+    l = l * a + lo * b;
+#pragma unroll
+    for (int i = 0; i < 16; i++) acc[i] = acc[i] * a + acco[i] * b;
+    m = mn;
+}
+
+DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
+{
+    const uint32_t B = d->dims[0], H = d->dims[1], D = d->dims[2], Lcap = d->dims[3], Lmax = d->dims[4];
+    if (D != 128 || Lmax == 0 || Lmax > Lcap || d->dims[5] < B * H) return GPUOS_ST_BAD_ARGS;
+    const uint32_t nch = (Lmax + GPUOS_SDPA_CHUNK - 1) / GPUOS_SDPA_CHUNK;
+    if (tile >= B * H * nch) return GPUOS_ST_OK;
+    const uint32_t b = tile / (H * nch), rem = tile - b * H * nch, h = rem / nch, c = rem - h * nch;
+    const int32_t L = __ldcg(reinterpret_cast<const int32_t *>(d->aux0) + b);
+    if (L < 1 || (uint32_t)L > Lmax) return GPUOS_ST_BAD_ARGS;
+    const uint32_t nchb = ((uint32_t)L + GPUOS_SDPA_CHUNK - 1) / GPUOS_SDPA_CHUNK;
+    if (c >= nchb) return GPUOS_ST_OK;
+    const uint32_t t0 = c * GPUOS_SDPA_CHUNK;
+    const uint32_t t1 = min((uint32_t)L, t0 + GPUOS_SDPA_CHUNK);
+    const uint32_t lane = lane_id(), g = lane >> 3, li = lane & 7u;
+    const uint64_t bh = (uint64_t)b * H + h;
+    const float qs = d->fparam[0] * 1.4426950408889634f;
+
+    float q[16];
+    {
+        const uint4 *qp = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(d->a) + bh * 128) + 2 * li;
+        unpack8(__ldcg(qp), q);
+        unpack8(__ldcg(qp + 1), q + 8);
+#pragma unroll
+        for (int i = 0; i < 16; i++) q[i] *= qs;
+    }
+    const uint4 *Kp = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(d->b) + bh * Lcap * 128) + 2 * li;
+    const uint4 *Vp = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(d->aux1) + bh * Lcap * 128) + 2 * li;
+    float m = -INFINITY, l = 0.0f, acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) acc[i] = 0.0f;
+
+    constexpr int UK = 2; /* keys per group per step */
+    for (uint32_t tb = t0; tb < t1; tb += 4 * UK) {
+        uint4 kv[UK][2], vv[UK][2];
+        bool valid[UK];
+#pragma unroll
+        for (int u = 0; u < UK; u++) {
+            const uint32_t t = tb + g + 4 * u;
+            valid[u] = t < t1;
+            if (valid[u]) {
+                kv[u][0] = __ldcg(Kp + (uint64_t)t * 16);
+                kv[u][1] = __ldcg(Kp + (uint64_t)t * 16 + 1);
+                vv[u][0] = __ldcg(Vp + (uint64_t)t * 16);
+                vv[u][1] = __ldcg(Vp + (uint64_t)t * 16 + 1);
+            } else {
+                kv[u][0] = kv[u][1] = vv[u][0] = vv[u][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        float sc[UK];
+#pragma unroll
+        for (int u = 0; u < UK; u++) {
+            float kf[16];
+            unpack8(kv[u][0], kf);
+            unpack8(kv[u][1], kf + 8);
+            float p = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; i++) p = fmaf(q[i], kf[i], p);
+            p += __shfl_xor_sync(0xFFFFFFFFu, p, 1);
+            p += __shfl_xor_sync(0xFFFFFFFFu, p, 2);
+            p += __shfl_xor_sync(0xFFFFFFFFu, p, 4);
+            sc[u] = valid[u] ? p : -INFINITY;
+        }
+        float mn = m;
+#pragma unroll
+        for (int u = 0; u < UK; u++) mn = fmaxf(mn, sc[u]);
+        const float mu = (mn == -INFINITY) ? 0.0f : mn;
+        const float corr = exp2f(m - mu);
+        l *= corr;
+#pragma unroll
+        for (int i = 0; i < 16; i++) acc[i] *= corr;
+#pragma unroll
+        for (int u = 0; u < UK; u++) {
+            const float p = exp2f(sc[u] - mu);
+            l += p;
+            float vf[16];
+            unpack8(vv[u][0], vf);
+            unpack8(vv[u][1], vf + 8);
+#pragma unroll
+            for (int i = 0; i < 16; i++) acc[i] = fmaf(p, vf[i], acc[i]);
+        }
+        m = mn;
+    }
+    /* merge the four groups (lanes li, li+8, li+16, li+24) */
+#pragma unroll
+    for (int o = 8; o <= 16; o <<= 1) {
+        float acco[16];
+        const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const float lo = __shfl_xor_sync(0xFFFFFFFFu, l, o);
+#pragma unroll
+        for (int i = 0; i < 16; i++) acco[i] = __shfl_xor_sync(0xFFFFFFFFu, acc[i], o);
+        sdpa_merge(m, l, acc, mo, lo, acco);
+    }
+    uint16_t *o16 = reinterpret_cast<uint16_t *>(d->out) + bh * 128;
+    if (nchb == 1) {
+        if (g == 0) {
+            const float inv = 1.0f / l;
+            float r[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) r[i] = acc[i] * inv;
+            uint4 *op = reinterpret_cast<uint4 *>(o16) + 2 * li;
+            op[0] = pack8(r);
+            op[1] = pack8(r + 8);
+        }
+        return GPUOS_ST_OK;
+    }
+    /* split-K: publish this chunk's (m, l, acc[128]) and let the last chunk merge */
+    /* workspace: ctr_cap uint32 counters (rounded up to 4), then partials */
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(d->aux2);
+    float *ws = reinterpret_cast<float *>(d->aux2) + ((d->dims[5] + 3u) & ~3u);
+    float *part = ws + (bh * nch + c) * 130;
+    if (g == 0) {
+#pragma unroll
+        for (int i = 0; i < 16; i++) __stcg(part + 2 + 16 * li + i, acc[i]);
+        if (li == 0) {
+            __stcg(part, m);
+            __stcg(part + 1, l);
+        }
+    }
+    __syncwarp();
+    uint32_t last = 0;
+    if (lane == 0) {
+        __threadfence();
+        last = (atomicAdd(cnt + bh, 1u) == nchb - 1) ? 1u : 0u;
+        if (last) __threadfence();
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (!last) return GPUOS_ST_OK;
+    float M = -INFINITY;
+    for (uint32_t k = 0; k < nchb; k++) M = fmaxf(M, __ldcg(ws + (bh * nch + k) * 130));
+    float den = 0.0f, o4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (uint32_t k = 0; k < nchb; k++) {
+        const float *pk = ws + (bh * nch + k) * 130;
+        const float w = exp2f(__ldcg(pk) - M);
+        den += __ldcg(pk + 1) * w;
+#pragma unroll
+        for (int i = 0; i < 4; i++) o4[i] += __ldcg(pk + 2 + 4 * lane + i) * w;
+    }
+    const float inv = 1.0f / den;
+    uint2 st;
+    st.x = pack_bf2(o4[0] * inv, o4[1] * inv);
+    st.y = pack_bf2(o4[2] * inv, o4[3] * inv);
+    reinterpret_cast<uint2 *>(o16)[lane] = st;
+    if (lane == 0) atomicExch(cnt + bh, 0u); /* leave the workspace zeroed */
+    return GPUOS_ST_OK;
+}
+
+/* ---- vector-matrix product: GPUOS_VM_COLS output columns per tile --------- */
+DEV int vecmat_tile(const gpuos_devdesc *d, uint32_t tile)
+{
+    const uint32_t K = d->dims[0], N = d->dims[1];
+    const uint32_t c0 = tile * GPUOS_VM_COLS;
+    if (c0 >= N) return GPUOS_ST_OK;
+    const uint32_t lane = lane_id();
+    const uint16_t *x = reinterpret_cast<const uint16_t *>(d->a);
+    const uint16_t *W = reinterpret_cast<const uint16_t *>(d->b);
+    uint16_t *y = reinterpret_cast<uint16_t *>(d->out);
+    const bool vec = (N & 7u) == 0 && ((d->b | d->out) & 15u) == 0;
+    if (vec) {
+        /* lane: 8 columns (cb = lane & 3) of rows k = g, g + 8, ... (g = lane >> 2) */
+        const uint32_t cb = lane & 3u, g = lane >> 2;
+        const uint32_t col = c0 + 8 * cb;
+        const bool active = col < N;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) acc[i] = 0.0f;
+        constexpr int UR = 4;
+        for (uint32_t k0 = 0; k0 < K; k0 += 8 * UR) {
+            uint4 w[UR];
+            float xv[UR];
+#pragma unroll
+            for (int u = 0; u < UR; u++) {
+                const uint32_t k = k0 + g + 8 * u;
+                if (active && k < K) {
+                    w[u] = __ldcg(reinterpret_cast<const uint4 *>(W + (uint64_t)k * N + col));
+                    xv[u] = bf1(__ldcg(x + k));
+                } else {
+                    w[u] = make_uint4(0, 0, 0, 0);
+                    xv[u] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UR; u++) {
+                float wf[8];
+                unpack8(w[u], wf);
+#pragma unroll
+                for (int i = 0; i < 8; i++) acc[i] = fmaf(xv[u], wf[i], acc[i]);
+            }
+        }
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 8; i++) acc[i] += __shfl_xor_sync(0xFFFFFFFFu, acc[i], o);
+        }
+        if (g == 0 && active) __stcg(reinterpret_cast<uint4 *>(y + col), pack8(acc));
+        return GPUOS_ST_OK;
+    }
+    const uint32_t col = c0 + lane;
+    if (col < N) {
+        float acc = 0.0f;
+        for (uint32_t k = 0; k < K; k++) acc = fmaf(bf1(__ldcg(x + k)), bf1(__ldcg(W + (uint64_t)k * N + col)), acc);
+        y[col] = to_bf(acc);
+    }
+    return GPUOS_ST_OK;
+}
+
+/* ---- table entries ----------------------------------------------------------- */
+__device__ __noinline__ int op_nop(const gpuos_devdesc *, uint32_t) { return GPUOS_ST_OK; }
+__device__ __noinline__ int op_add(const gpuos_devdesc *d, uint32_t t) { return ew_dispatch<EW_ADD>(d, t); }
+__device__ __noinline__ int op_mul(const gpuos_devdesc *d, uint32_t t) { return ew_dispatch<EW_MUL>(d, t); }
+__device__ __noinline__ int op_relu(const gpuos_devdesc *d, uint32_t t) { return ew_dispatch<EW_RELU>(d, t); }
+__device__ __noinline__ int op_gelu(const gpuos_devdesc *d, uint32_t t) { return ew_dispatch<EW_GELU>(d, t); }
+__device__ __noinline__ int op_softmax(const gpuos_devdesc *d, uint32_t t) { return row_tile<ROW_SOFTMAX>(d, t); }
+__device__ __noinline__ int op_layernorm(const gpuos_devdesc *d, uint32_t t) { return row_tile<ROW_LN>(d, t); }
+__device__ __noinline__ int op_rowsum(const gpuos_devdesc *d, uint32_t t) { return row_tile<ROW_SUM>(d, t); }
+__device__ __noinline__ int op_rowmax(const gpuos_devdesc *d, uint32_t t) { return row_tile<ROW_MAX>(d, t); }
+__device__ __noinline__ int op_rowmin(const gpuos_devdesc *d, uint32_t t) { return row_tile<ROW_MIN>(d, t); }
+__device__ __noinline__ int op_rope(const gpuos_devdesc *d, uint32_t t) { return rope_tile(d, t); }
+__device__ __noinline__ int op_kv_write(const gpuos_devdesc *d, uint32_t t) { return kv_tile(d, t); }
+__device__ __noinline__ int op_sdpa(const gpuos_devdesc *d, uint32_t t) { return sdpa_tile(d, t); }
+__device__ __noinline__ int op_vecmat(const gpuos_devdesc *d, uint32_t t) { return vecmat_tile(d, t); }
+
+__device__ gpuos_op_fn g_builtin_ops[GPUOS_OP_BUILTIN_COUNT] = {
+    op_nop, op_add, op_mul, op_relu, op_gelu, op_softmax, op_layernorm,
+    op_rowsum, op_rowmax, op_rowmin, op_rope, op_kv_write, op_sdpa, op_vecmat,
+};
+
+/* ===========================================================================
+ * Persistent executor
+ * ======================================================================== */
+
+/* Work-queue entry word: [63] consumed, [62:40] stamp = (index + 1) mod 2^23,
+ * [39:24] ring slot, [23:0] tile. One 64-bit word, so the claimer learns
+ * everything with the acquire load that finds the entry published. */
+DEV uint64_t tq_word(uint64_t idx, uint32_t slot, uint32_t tile)
+{
+    return (((idx + 1) & GPUOS_TQ_STAMP_MASK) << 40) | ((uint64_t)(slot & 0xFFFFu) << 24) | (tile & 0xFFFFFFu);
+}
+DEV bool tq_is(uint64_t w, uint64_t idx) { return ((w >> 40) & GPUOS_TQ_STAMP_MASK) == ((idx + 1) & GPUOS_TQ_STAMP_MASK); }
+
+DEV void fence_acq_rel_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
+
+/* Complete one descriptor (single thread). */
+DEV void complete_desc(const gpuos_exec_params &p, uint64_t ticket, uint32_t slot, int32_t status,
+                       uint32_t version, uint64_t t_dispatch)
+{
+    gpuos_rec_dev *r = p.rec + slot;
+    const uint64_t t_done = globaltimer();
+    st_relaxed_sys32(reinterpret_cast<uint32_t *>(&r->status), (uint32_t)status);
+    st_relaxed_sys32(&r->version, version);
+    st_relaxed_sys(&r->t_dispatch, t_dispatch);
+    st_relaxed_sys(&r->t_publish, *reinterpret_cast<volatile uint64_t *>(p.t_pub + slot));
+    st_relaxed_sys(&r->t_start, *reinterpret_cast<volatile uint64_t *>(p.t_start + slot));
+    st_relaxed_sys(&r->t_done, t_done);
+    st_relaxed_gpu32(p.err + slot, 0u);
+    st_relaxed_gpu32(p.tiles_done + slot, 0u);
+    st_relaxed_gpu32(p.tile_ctr + slot, 0u);
+    /* release: the record fields and the slot's counters before the stamps
+     * (the tiles' outputs were fenced before their counter increments) */
+    st_release_gpu(p.done_dev + slot, ticket + 1);
+    st_release_sys(&r->done_seq, ticket + 1);
+    atomicAdd(&p.dctl->completed, 1ull);
+}
+
+DEV void set_exit(const gpuos_exec_params &p, uint32_t reason)
+{
+    st_relaxed_gpu32(&p.dctl->exit_flag, reason);
+    st_relaxed_sys32(&p.hctl->exit_reason, reason);
+    st_relaxed_sys32(&p.hctl->state, 2u);
+}
+
+/* The sequencer warp: ring -> mirror + work queue. */
+DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
+{
+    const uint32_t lane = lane_id();
+    uint64_t *ws = p.warp_stats + (uint64_t)gw * GPUOS_WS_N;
+    uint64_t s = 0, e = 0;
+    uint64_t n_seq = 0, n_idle = 0, n_sleep = 0, t_body = 0, t_mirror = 0, t_pubs = 0;
+    uint32_t polls = 0;
+    uint64_t hb = ld_relaxed_sys(&p.hctl->heartbeat);
+    uint64_t t_active = globaltimer();
+    const uint32_t N = p.ring_mask + 1, Q = p.tq_mask + 1;
+    if (lane == 0) st_relaxed_sys32(&p.hctl->state, 1u);
+
+    while (true) {
+        /* poll 32 consecutive slots, one per lane (relaxed; one fence below) */
+        const uint64_t my_t = s + lane;
+        const uint32_t my_slot = (uint32_t)(my_t & p.ring_mask);
+        const uint64_t seq = ld_relaxed_sys(&p.ring[my_slot].seq);
+        const uint32_t ready = __ballot_sync(0xFFFFFFFFu, seq == my_t + 1);
+        uint32_t k = (ready == 0xFFFFFFFFu) ? 32u : (uint32_t)(__ffs(~ready) - 1);
+        if (k > N) k = N;
+        if (k == 0) {
+            /* idle: stop flag, exit_after, watchdog */
+            n_idle++;
+            if ((polls & 31u) == 0) {
+                uint32_t reason = 0;
+                if (ld_relaxed_sys32(&p.hctl->stop)) reason = 1;
+                if (p.exit_after && *reinterpret_cast<volatile unsigned long long *>(&p.dctl->completed) >= p.exit_after)
+                    reason = 3;
+                const uint64_t now = globaltimer();
+                const uint64_t h2 = ld_relaxed_sys(&p.hctl->heartbeat);
+                if (h2 != hb) {
+                    hb = h2;
+                    t_active = now;
+                }
+                if (p.idle_exit_ns && now - t_active > p.idle_exit_ns) reason = 2;
+                reason = __shfl_sync(0xFFFFFFFFu, reason, 0);
+                if (reason) {
+                    if (lane == 0) {
+                        /* what the decision saw, for the host's diagnostics */
+                        st_relaxed_sys(&p.hctl->exit_now, now);
+                        st_relaxed_sys(&p.hctl->exit_active, t_active);
+                        set_exit(p, reason);
+                    }
+                    break;
+                }
+            }
+            backoff(polls, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+            continue;
+        }
+        const uint64_t t_obs = globaltimer();
+        polls = 0;
+        /* the commits seen above happen-before everything below */
+        fence_acq_rel_sys();
+        gpuos_desc dsc;
+        uint4 *dv = reinterpret_cast<uint4 *>(&dsc);
+        if (lane < k) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.ring + my_slot);
+#pragma unroll
+            for (int i = 0; i < 8; i++) dv[i] = src[i];
+        }
+        uint32_t version = 0;
+        if (lane == 0) version = ld_acquire_gpu32(&p.dctl->version);
+        version = __shfl_sync(0xFFFFFFFFu, version, 0);
+        /* a FENCE descriptor must start a batch; cut the batch before it */
+        const uint32_t fmask = __ballot_sync(0xFFFFFFFFu, lane < k && (dsc.flags & GPUOS_FLAG_FENCE));
+        const uint32_t later = fmask & ~1u;
+        if (later) k = (uint32_t)(__ffs(later) - 1);
+        uint32_t fence_status = GPUOS_ST_OK;
+        if (fmask & 1u) {
+            if (lane == 0) {
+                const uint64_t t0 = globaltimer();
+                uint32_t fp = 0;
+                while (*reinterpret_cast<volatile unsigned long long *>(&p.dctl->completed) < s) {
+                    if (globaltimer() - t0 > p.dep_timeout_ns) {
+                        fence_status = GPUOS_ST_DEP_TIMEOUT;
+                        break;
+                    }
+                    backoff(fp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+                }
+                __threadfence();
+            }
+            fence_status = __shfl_sync(0xFFFFFFFFu, fence_status, 0);
+        }
+        const uint64_t t_b = globaltimer();
+
+        /* validate and mirror */
+        int32_t status = GPUOS_ST_OK;
+        uint32_t nt = 0;
+        if (lane < k) {
+            if (dsc.ticket != my_t) status = GPUOS_ST_BAD_DESC;
+            else if (dsc.op_id >= GPUOS_MAX_OPS) status = GPUOS_ST_BAD_OP;
+            else if (dsc.ntiles == 0 || dsc.ntiles > GPUOS_TILE_MAX) status = GPUOS_ST_BAD_ARGS;
+            if (lane == 0 && fence_status) status = (int32_t)fence_status;
+            if (status == GPUOS_ST_OK) {
+                /* one work-queue entry per helper warp (at most GPUOS_HELPERS);
+                 * helper h starts with tile h and takes later tiles from the
+                 * descriptor's tile counter */
+                nt = dsc.ntiles < GPUOS_HELPERS ? dsc.ntiles : GPUOS_HELPERS;
+                dsc.user = t_obs;                        /* -> t_dispatch */
+                dsc.seq = (uint64_t)version;             /* -> version, pad */
+                uint4 *mv = reinterpret_cast<uint4 *>(p.mirror + my_slot);
+#pragma unroll
+                for (int i = 0; i < 8; i++) __stcg(mv + i, dv[i]);
+            }
+        }
+        /* every lane's mirror writes happen-before every lane's fence */
+        __syncwarp();
+        __threadfence();
+        const uint64_t t_m = globaltimer();
+        /* exclusive prefix of tile counts -> work-queue ranges */
+        uint32_t incl = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= (uint32_t)o) incl += v;
+        }
+        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const uint32_t excl = incl - nt;
+        /* entries j = 0 .. total-1 of the batch, spread over the lanes; the
+         * descriptor owning j is the last lane whose range starts at or
+         * before it (a 5-step search over the exclusive prefix) */
+        for (uint32_t j0 = 0; j0 < total; j0 += 32) {
+            const uint32_t j = j0 + lane;
+            uint32_t i = 0;
+#pragma unroll
+            for (int step = 16; step > 0; step >>= 1) {
+                const uint32_t cand = i + (uint32_t)step; /* <= 31 */
+                if (__shfl_sync(0xFFFFFFFFu, excl, cand) <= j) i = cand;
+            }
+            const uint32_t bi = __shfl_sync(0xFFFFFFFFu, excl, i);
+            const uint32_t sloti = (uint32_t)((s + i) & p.ring_mask);
+            if (j < total) {
+                const uint32_t t = j - bi;
+                const uint64_t idx = e + j;
+                unsigned long long *ent = p.tq + (idx & p.tq_mask);
+                if (idx >= Q) {
+                    /* the previous lap's entry must have been read by its claimer */
+                    uint32_t wp = 0;
+                    const uint64_t tw = globaltimer();
+                    while (true) {
+                        const uint64_t w = *reinterpret_cast<volatile unsigned long long *>(ent);
+                        if ((w & GPUOS_TQ_CONSUMED) && tq_is(w, idx - Q)) break;
+                        if (globaltimer() - tw > p.dep_timeout_ns) break; /* cannot happen: claims progress */
+                        backoff(wp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+                    }
+                }
+                *reinterpret_cast<volatile unsigned long long *>(ent) = tq_word(idx, sloti, t);
+            }
+        }
+        const uint64_t t_pub = globaltimer();
+        if (lane < k && status == GPUOS_ST_OK)
+            *reinterpret_cast<volatile uint64_t *>(p.t_pub + my_slot) = t_pub;
+        /* descriptors that failed validation complete at once */
+        if (lane < k && status != GPUOS_ST_OK)
+            complete_desc(p, my_t, my_slot, status, version, t_obs);
+        e += total;
+        s += k;
+        n_seq += k;
+        t_body += t_b - t_obs;
+        t_mirror += t_m - t_b;
+        t_pubs += t_pub - t_m;
+        if (lane == 0) {
+            st_relaxed_sys(&p.hctl->sequenced, s);
+            ws[GPUOS_WS_SEQ] = n_seq;
+            ws[GPUOS_WS_IDLE] = n_idle;
+            ws[GPUOS_WS_SLEEPS] = n_sleep;
+            ws[GPUOS_WS_T_BODY] = t_body;
+            ws[GPUOS_WS_T_MIRROR] = t_mirror;
+            ws[GPUOS_WS_T_PUB] = t_pubs;
+        }
+        t_active = t_obs;
+    }
+    if (lane == 0) {
+        ws[GPUOS_WS_SEQ] = n_seq;
+        ws[GPUOS_WS_IDLE] = n_idle;
+        ws[GPUOS_WS_SLEEPS] = n_sleep;
+    }
+}
+
+/* A worker warp: claim a tile, wait for its dependencies, dispatch, count. */
+DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
+{
+    const uint32_t lane = lane_id();
+    uint64_t *ws = p.warp_stats + (uint64_t)gw * GPUOS_WS_N;
+    uint64_t n_tiles = 0, n_idle = 0, n_sleep = 0, n_depw = 0;
+    const uint32_t N = p.ring_mask + 1;
+    unsigned long long e = 0;
+    if (lane == 0) e = atomicAdd(&p.dctl->tq_claim, 1ull);
+    e = __shfl_sync(0xFFFFFFFFu, e, 0);
+    while (true) {
+        unsigned long long *ent = p.tq + (e & p.tq_mask);
+        uint32_t polls = 0;
+        uint32_t leave = 0;
+        uint64_t w = 0;
+        if (lane == 0) {
+            while (true) {
+                w = ld_acquire_gpu(reinterpret_cast<const uint64_t *>(ent));
+                if (tq_is(w, e) && !(w & GPUOS_TQ_CONSUMED)) break;
+                n_idle++;
+                if ((polls & 15u) == 0 && ld_relaxed_gpu32(&p.dctl->exit_flag)) {
+                    leave = 1;
+                    break;
+                }
+                backoff(polls, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+            }
+            if (!leave) *reinterpret_cast<volatile unsigned long long *>(ent) = w | GPUOS_TQ_CONSUMED;
+        }
+        leave = __shfl_sync(0xFFFFFFFFu, leave, 0);
+        if (leave) break;
+        w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        unsigned long long e_next = 0;
+        if (lane == 0) e_next = atomicAdd(&p.dctl->tq_claim, 1ull); /* overlaps the tile */
+        const uint32_t slot = (uint32_t)((w >> 24) & 0xFFFFu);
+        uint32_t tile = (uint32_t)(w & 0xFFFFFFu); /* helper index = its first tile */
+        /* descriptor -> shared memory */
+        reinterpret_cast<uint32_t *>(sd)[lane] = __ldcg(reinterpret_cast<const uint32_t *>(p.mirror + slot) + lane);
+        __syncwarp();
+        const uint64_t ticket = sd->ticket;
+        const uint32_t ntiles = sd->ntiles;
+        const uint32_t helpers = ntiles < GPUOS_HELPERS ? ntiles : GPUOS_HELPERS;
+        if (lane == 0 && tile == 0) *reinterpret_cast<volatile uint64_t *>(p.t_start + slot) = globaltimer();
+        int32_t dstatus = GPUOS_ST_OK;
+        if (lane == 0) {
+            for (int i = 0; i < 2; i++) {
+                const uint64_t dep = sd->dep[i];
+                if (dep == 0) continue;
+                if (dep > ticket) {
+                    dstatus = GPUOS_ST_BAD_DESC;
+                    break;
+                }
+                if (ticket + 1 - dep >= N) continue; /* older than the ring window: done */
+                const uint64_t *stamp = p.done_dev + ((dep - 1) & p.ring_mask);
+                if (ld_acquire_gpu(stamp) >= dep) continue;
+                n_depw++;
+                const uint64_t t0 = globaltimer();
+                uint32_t dp = 0;
+                while (ld_acquire_gpu(stamp) < dep) {
+                    if (globaltimer() - t0 > p.dep_timeout_ns) {
+                        dstatus = GPUOS_ST_DEP_TIMEOUT;
+                        break;
+                    }
+                    if ((dp & 15u) == 0 && ld_relaxed_gpu32(&p.dctl->exit_flag)) {
+                        dstatus = GPUOS_ST_ABORTED;
+                        break;
+                    }
+                    backoff(dp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+                }
+                if (dstatus) break;
+            }
+        }
+        dstatus = __shfl_sync(0xFFFFFFFFu, dstatus, 0);
+        __syncwarp();
+        const gpuos_op_fn fn = reinterpret_cast<gpuos_op_fn>(__ldcg(
+            reinterpret_cast<const unsigned long long *>(p.table) + (sd->version & 1u) * GPUOS_MAX_OPS + sd->op_id));
+        while (true) {
+            /* claim the helper's next tile before this one is counted: the
+             * descriptor cannot complete (and its counters be recycled)
+             * while this warp still holds an uncounted tile */
+            uint32_t next = ntiles;
+            if (ntiles > helpers && lane == 0) next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
+            int32_t status = dstatus;
+            if (status == GPUOS_ST_OK) {
+                if (fn == nullptr) status = GPUOS_ST_BAD_OP;
+                else status = fn(sd, tile);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (ntiles == 1) {
+                    /* sole tile: no counter round trip; the warp barrier above
+                     * orders every lane's writes before the completion releases */
+                    complete_desc(p, ticket, slot, status, sd->version, sd->t_dispatch);
+                } else {
+                    if (status) atomicCAS(p.err + slot, 0u, (uint32_t)status);
+                    __threadfence();
+                    const uint32_t old = atomicAdd(p.tiles_done + slot, 1u);
+                    if (old + 1 == ntiles) {
+                        __threadfence();
+                        const uint32_t st = ld_relaxed_gpu32(p.err + slot);
+                        complete_desc(p, ticket, slot, (int32_t)st, sd->version, sd->t_dispatch);
+                    }
+                }
+                n_tiles++;
+                if ((n_tiles & 63u) == 0) {
+                    ws[GPUOS_WS_TILES] = n_tiles;
+                    ws[GPUOS_WS_IDLE] = n_idle;
+                    ws[GPUOS_WS_SLEEPS] = n_sleep;
+                    ws[GPUOS_WS_DEPWAIT] = n_depw;
+                }
+            }
+            next = __shfl_sync(0xFFFFFFFFu, next, 0);
+            if (next >= ntiles) break;
+            tile = next;
+        }
+        e = __shfl_sync(0xFFFFFFFFu, e_next, 0);
+        __syncwarp();
+    }
+    if (lane == 0) {
+        ws[GPUOS_WS_TILES] = n_tiles;
+        ws[GPUOS_WS_IDLE] = n_idle;
+        ws[GPUOS_WS_SLEEPS] = n_sleep;
+        ws[GPUOS_WS_DEPWAIT] = n_depw;
+    }
+}
+
+extern "C" __global__ void __launch_bounds__(GPUOS_MAX_WPB * 32, 1) gpuos_executor_kernel(gpuos_exec_params p)
+{
+    __shared__ __align__(16) gpuos_devdesc sdesc[GPUOS_MAX_WPB];
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (blockIdx.x == 0 && warp == 0) sequencer(p, gw);
+    else worker(p, &sdesc[warp], gw);
+}
+
+/* ===========================================================================
+ * Eager baseline: the same op bodies, one launch per descriptor, one warp
+ * per tile, one warp per block (spreads a descriptor over many SMs).
+ * ======================================================================== */
+DEV int builtin_call(const gpuos_devdesc *d, uint32_t t)
+{
+    switch (d->op_id) {
+    case GPUOS_OP_NOP: return GPUOS_ST_OK;
+    case GPUOS_OP_ADD: return ew_dispatch<EW_ADD>(d, t);
+    case GPUOS_OP_MUL: return ew_dispatch<EW_MUL>(d, t);
+    case GPUOS_OP_RELU: return ew_dispatch<EW_RELU>(d, t);
+    case GPUOS_OP_GELU: return ew_dispatch<EW_GELU>(d, t);
+    case GPUOS_OP_SOFTMAX: return row_tile<ROW_SOFTMAX>(d, t);
+    case GPUOS_OP_LAYERNORM: return row_tile<ROW_LN>(d, t);
+    case GPUOS_OP_ROWSUM: return row_tile<ROW_SUM>(d, t);
+    case GPUOS_OP_ROWMAX: return row_tile<ROW_MAX>(d, t);
+    case GPUOS_OP_ROWMIN: return row_tile<ROW_MIN>(d, t);
+    case GPUOS_OP_ROPE: return rope_tile(d, t);
+    case GPUOS_OP_KV_WRITE: return kv_tile(d, t);
+    case GPUOS_OP_SDPA: return sdpa_tile(d, t);
+    case GPUOS_OP_VECMAT: return vecmat_tile(d, t);
+    default: return GPUOS_ST_BAD_OP;
+    }
+}
+
+#define EAGER_WPB 1
+extern "C" __global__ void __launch_bounds__(EAGER_WPB * 32) gpuos_eager_kernel(gpuos_devdesc d)
+{
+    __shared__ __align__(16) gpuos_devdesc sd[EAGER_WPB];
+    const uint32_t warp = threadIdx.x >> 5;
+    reinterpret_cast<uint32_t *>(&sd[warp])[lane_id()] = reinterpret_cast<const uint32_t *>(&d)[lane_id()];
+    __syncwarp();
+    const uint32_t tile = blockIdx.x * EAGER_WPB + warp;
+    if (tile < sd[warp].ntiles) (void)builtin_call(&sd[warp], tile);
+}
+
+/* ===========================================================================
+ * Host-side launch helpers
+ * ======================================================================== */
+extern "C" int gpuos_dev_launch_executor(const gpuos_exec_params *p, uint32_t blocks, uint32_t wpb, void *stream)
+{
+    gpuos_executor_kernel<<<blocks, wpb * 32, 0, (cudaStream_t)stream>>>(*p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+extern "C" int gpuos_dev_builtin_table(gpuos_op_fn *host_out, uint32_t n)
+{
+    if (n > GPUOS_OP_BUILTIN_COUNT) n = GPUOS_OP_BUILTIN_COUNT;
+    return cudaMemcpyFromSymbol(host_out, g_builtin_ops, n * sizeof(gpuos_op_fn)) == cudaSuccess ? 0 : -1;
+}
+
+extern "C" int gpuos_dev_executor_attrs(uint32_t *regs, uint32_t *smem)
+{
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, gpuos_executor_kernel) != cudaSuccess) return -1;
+    *regs = (uint32_t)a.numRegs;
+    *smem = (uint32_t)a.sharedSizeBytes;
+    return 0;
+}
+
+extern "C" int gpuos_dev_preload(void)
+{
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, gpuos_executor_kernel) != cudaSuccess) return -1;
+    if (cudaFuncGetAttributes(&a, gpuos_eager_kernel) != cudaSuccess) return -1;
+    return 0;
+}
+
+extern "C" int gpuos_dev_eager_launch(const gpuos_desc *d, uint32_t ntiles, void *stream)
+{
+    gpuos_devdesc dd;
+    static_assert(sizeof(dd) == sizeof(*d), "layout");
+    memcpy(&dd, d, sizeof(dd));
+    dd.ntiles = ntiles;
+    const uint32_t grid = (ntiles + EAGER_WPB - 1) / EAGER_WPB;
+    gpuos_eager_kernel<<<grid, EAGER_WPB * 32, 0, (cudaStream_t)stream>>>(dd);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}

@@ -1,0 +1,960 @@
+/*
+ * Host side of the GB300 persistent micro-op dispatcher: the C ABI declared
+ * in include/gpuos.h.
+ *
+ * Protocol ("GPUOS: A GPU Operating System Primitive for Transparent
+ * Operation Fusion", §3 Q2 "1. Ring Buffer Communication Channel"): the host
+ * takes the next ticket, acquires its slot (free once the descriptor that
+ * last used it has completed), writes the 128-byte descriptor and commits it
+ * with a store-release of the slot's commit word. The device's completion
+ * record of each ticket is written with a store-release at system scope; the
+ * host harvests records with load-acquire, in ticket order, and that is also
+ * what frees slots.
+ *
+ * Operator injection (§3 Q2 "3. Dynamic Operator Table"): a precompiled
+ * sm_103a cubin is loaded through the driver API, the address of its device
+ * function is read from a __device__ variable, the inactive half of the
+ * dual-slot table is written and the version counter flips. The sequencer
+ * warp reads the version once per descriptor, so a descriptor runs entirely
+ * with the old or entirely with the new entry.
+ */
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <ctime>
+#include <new>
+#include <vector>
+
+#include "gpuos_internal.h"
+
+namespace {
+
+/* ---- driver API, resolved through the runtime (no link-time libcuda) ---- */
+typedef CUresult (*pfn_cuModuleLoadData)(CUmodule *, const void *);
+typedef CUresult (*pfn_cuModuleGetGlobal)(CUdeviceptr *, size_t *, CUmodule, const char *);
+typedef CUresult (*pfn_cuModuleUnload)(CUmodule);
+
+struct Driver {
+    pfn_cuModuleLoadData load = nullptr;
+    pfn_cuModuleGetGlobal get_global = nullptr;
+    pfn_cuModuleUnload unload = nullptr;
+    bool ok = false;
+};
+
+bool resolve(const char *name, void **fn)
+{
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q) != cudaSuccess) return false;
+    return q == cudaDriverEntryPointSuccess && *fn != nullptr;
+}
+
+Driver &driver()
+{
+    static Driver d;
+    if (!d.ok) {
+        d.ok = resolve("cuModuleLoadData", (void **)&d.load) &&
+               resolve("cuModuleGetGlobal", (void **)&d.get_global) &&
+               resolve("cuModuleUnload", (void **)&d.unload);
+    }
+    return d;
+}
+
+uint64_t now_ns()
+{
+    timespec ts;
+    clock_gettime(CLOCK_REALTIME, &ts);
+    return (uint64_t)ts.tv_sec * 1000000000ull + (uint64_t)ts.tv_nsec;
+}
+
+inline void cpu_relax()
+{
+#if defined(__aarch64__)
+    asm volatile("yield" ::: "memory");
+#else
+    std::atomic_signal_fence(std::memory_order_seq_cst);
+#endif
+}
+
+template <typename T>
+T load_acq(const T *p)
+{
+    return __atomic_load_n(p, __ATOMIC_ACQUIRE);
+}
+template <typename T>
+void store_rel(T *p, T v)
+{
+    __atomic_store_n(p, v, __ATOMIC_RELEASE);
+}
+
+bool is_pow2(uint32_t x) { return x && !(x & (x - 1)); }
+
+}  // namespace
+
+struct gpuos_ctx {
+    gpuos_config cfg;
+    int device = 0;
+    uint32_t N = 0, mask = 0, Q = 0;
+    uint32_t blocks = 0, wpb = 0;
+    /* host-visible (pinned or managed) */
+    gpuos_desc *ring = nullptr;      /* host pointer */
+    gpuos_desc *ring_dev = nullptr;  /* device view */
+    gpuos_rec_dev *rec = nullptr;
+    gpuos_rec_dev *rec_dev = nullptr;
+    gpuos_hostctl *hctl = nullptr;
+    gpuos_hostctl *hctl_dev = nullptr;
+    bool ring_managed = false;
+    /* device memory */
+    gpuos_devdesc *mirror = nullptr;
+    uint32_t *tiles_done = nullptr, *err = nullptr, *tile_ctr = nullptr;
+    uint64_t *done_dev = nullptr;
+    uint64_t *t_start = nullptr;
+    unsigned long long *tq = nullptr;
+    uint64_t *t_pub = nullptr;
+    gpuos_devctl *dctl = nullptr;
+    gpuos_op_fn *table = nullptr;
+    uint64_t *warp_stats = nullptr;
+    uint32_t *version_stage = nullptr; /* pinned 4 bytes for version flips */
+    cudaStream_t exec_stream = nullptr, ctl_stream = nullptr;
+    /* host state */
+    uint64_t head = 0;     /* next ticket */
+    uint64_t low = 0;      /* every ticket < low harvested */
+    std::vector<uint64_t> commit_ns;
+    std::vector<uint64_t> hv; /* per slot: ticket + 1 last harvested */
+    std::vector<gpuos_record> recent; /* per slot: last harvested record */
+    gpuos_record *history = nullptr;
+    uint64_t hist_base = 0, hist_cap = 0;
+    uint64_t n_completed = 0, n_errors = 0;
+    uint64_t pending_errors = 0; /* errors harvested since the last sync report */
+    /* operator table shadow */
+    uint64_t table_host[2][GPUOS_MAX_OPS];
+    bool user_registered[GPUOS_MAX_OPS];
+    uint32_t version = 0;
+    uint64_t flip_head = 0; /* head when the current version was published */
+    struct Module {
+        CUmodule mod;
+        uint64_t hash;
+        std::vector<unsigned char> bytes;
+    };
+    std::vector<Module> modules;
+    uint32_t regs = 0, smem = 0;
+    gpuos_exec_params params;
+    bool accepting = false; /* submissions allowed (until stop) */
+    bool launched = false;  /* executor kernel launched */
+    bool running = false;   /* executor believed resident */
+};
+
+static inline void heartbeat(gpuos_ctx *c)
+{
+    __atomic_store_n(&c->hctl->heartbeat, c->hctl->heartbeat + 1, __ATOMIC_RELAXED);
+}
+
+extern "C" {
+
+uint64_t gpuos_host_now_ns(void) { return now_ns(); }
+
+const char *gpuos_strerror(int code, int is_status)
+{
+    if (is_status) {
+        switch (code) {
+        case GPUOS_ST_OK: return "ok";
+        case GPUOS_ST_BAD_OP: return "bad op id or empty table entry";
+        case GPUOS_ST_BAD_ARGS: return "dims, position or length out of range";
+        case GPUOS_ST_DEP_TIMEOUT: return "dependency or fence wait timed out";
+        case GPUOS_ST_ABORTED: return "executor was leaving";
+        case GPUOS_ST_BAD_DESC: return "ring slot did not hold the expected ticket";
+        default: return "unknown device status";
+        }
+    }
+    switch (code) {
+    case GPUOS_OK: return "ok";
+    case GPUOS_EINVAL: return "invalid argument";
+    case GPUOS_EAGAIN: return "ring full (timed out waiting for a slot)";
+    case GPUOS_ETIMEDOUT: return "timed out";
+    case GPUOS_EDEVICE: return "a descriptor completed with a device error status";
+    case GPUOS_ECUDA: return "CUDA call failed";
+    case GPUOS_ESTOPPED: return "executor is not running";
+    case GPUOS_ENOMEM: return "out of memory";
+    case GPUOS_EBUSY: return "not allowed while the executor is resident (load modules before gpuos_start)";
+    default: return "unknown error";
+    }
+}
+
+void gpuos_default_config(gpuos_config *c)
+{
+    memset(c, 0, sizeof(*c));
+    c->ring_entries = 4096;
+    c->warps_per_block = 8;
+    c->blocks = 0;
+    c->backoff_min_ns = 32;
+    c->backoff_max_ns = 256;
+    c->spin_polls = 4096;
+    c->idle_exit_ms = 10000;
+    c->dep_timeout_ms = 5000;
+    c->ring_in_device_mem = 0;
+    c->device = 0;
+    c->exit_after = 0;
+    c->tq_entries = 65536;
+}
+
+size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, uint32_t Lmax)
+{
+    uint64_t nch = (Lmax + GPUOS_SDPA_CHUNK - 1) / GPUOS_SDPA_CHUNK;
+    if (nch == 0) nch = 1;
+    (void)D; /* partials hold D + 2 floats; D is fixed at 128 */
+    const uint64_t ctr = ((uint64_t)B * H + 3u) & ~3ull;
+    return (size_t)(4ull * ctr + 4ull * B * H * nch * 130ull);
+}
+
+static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+static bool al16(uint64_t p) { return (p & 15u) == 0; }
+
+/* Host-side validation (the page's "bounds checking") and tiling rule. */
+static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool user_op_known)
+{
+    const uint32_t *m = d->dims;
+    uint64_t nt = 1;
+    if (d->op_id >= GPUOS_MAX_OPS) return GPUOS_EINVAL;
+    switch (d->op_id) {
+    case GPUOS_OP_NOP: nt = 1; break;
+    case GPUOS_OP_ADD:
+    case GPUOS_OP_MUL:
+    case GPUOS_OP_RELU:
+    case GPUOS_OP_GELU: {
+        if (d->dtype != GPUOS_F32 && d->dtype != GPUOS_BF16) return GPUOS_EINVAL;
+        const bool bin = d->op_id == GPUOS_OP_ADD || d->op_id == GPUOS_OP_MUL;
+        if (m[0] && (!d->a || !d->out || (bin && !d->b))) return GPUOS_EINVAL;
+        nt = ceil_div(m[0], d->dtype == GPUOS_F32 ? GPUOS_EW_TILE_F32 : GPUOS_EW_TILE_BF16);
+        break;
+    }
+    case GPUOS_OP_SOFTMAX:
+    case GPUOS_OP_LAYERNORM:
+    case GPUOS_OP_ROWSUM:
+    case GPUOS_OP_ROWMAX:
+    case GPUOS_OP_ROWMIN:
+        if (d->dtype != GPUOS_BF16) return GPUOS_EINVAL;
+        if (m[0] && (m[1] == 0 || !d->a || !d->out)) return GPUOS_EINVAL;
+        if (m[0] && d->op_id == GPUOS_OP_LAYERNORM && (!d->b || !d->aux0)) return GPUOS_EINVAL;
+        nt = m[0];
+        break;
+    case GPUOS_OP_ROPE:
+        if (m[0] && (!d->a || !d->b || !d->aux0 || m[1] == 0 || m[2] == 0 || (m[2] & 1) || m[2] > 256))
+            return GPUOS_EINVAL;
+        nt = m[0];
+        break;
+    case GPUOS_OP_KV_WRITE:
+        if (m[0] && (!d->a || !d->b || !d->aux0 || !d->out || !d->aux1 || m[1] == 0 || m[2] == 0 || m[3] == 0))
+            return GPUOS_EINVAL;
+        nt = m[0];
+        break;
+    case GPUOS_OP_SDPA:
+        if (m[0]) {
+            if (!d->a || !d->b || !d->aux0 || !d->aux1 || !d->out || !d->aux2) return GPUOS_EINVAL;
+            if (m[1] == 0 || m[2] != 128 || m[3] == 0 || m[4] == 0 || m[4] > m[3]) return GPUOS_EINVAL;
+            if ((uint64_t)m[5] < (uint64_t)m[0] * m[1]) return GPUOS_EINVAL;
+            if (!al16(d->a) || !al16(d->b) || !al16(d->aux1) || !al16(d->out) || !al16(d->aux2)) return GPUOS_EINVAL;
+        }
+        nt = (uint64_t)m[0] * m[1] * ceil_div(m[4], GPUOS_SDPA_CHUNK);
+        break;
+    case GPUOS_OP_VECMAT:
+        if (m[1] && (!d->a || !d->b || !d->out || m[0] == 0)) return GPUOS_EINVAL;
+        nt = ceil_div(m[1], GPUOS_VM_COLS);
+        break;
+    default:
+        if (d->op_id < GPUOS_OP_USER_FIRST && d->op_id >= GPUOS_OP_BUILTIN_COUNT) return GPUOS_EINVAL;
+        if (!user_op_known) return GPUOS_EINVAL;
+        nt = d->ntiles;
+        break;
+    }
+    if (d->flags & ~(GPUOS_FLAG_FENCE | GPUOS_FLAG_DEP_REL)) return GPUOS_EINVAL;
+    if (nt == 0) nt = 1; /* an empty op still waits for its dependencies */
+    if (nt > GPUOS_TILE_MAX) return GPUOS_EINVAL;
+    *ntiles_out = (uint32_t)nt;
+    return GPUOS_OK;
+}
+
+int gpuos_op_ntiles(const gpuos_desc *d, uint32_t *ntiles)
+{
+    if (!d || !ntiles) return GPUOS_EINVAL;
+    return validate_and_tile(d, ntiles, true);
+}
+
+static void free_all(gpuos_ctx *c)
+{
+    for (auto &m : c->modules) {
+        if (driver().ok) driver().unload(m.mod);
+    }
+    c->modules.clear();
+    if (c->ring) {
+        if (c->ring_managed) cudaFree(c->ring);
+        else cudaFreeHost(c->ring);
+    }
+    if (c->rec) cudaFreeHost(c->rec);
+    if (c->hctl) cudaFreeHost(c->hctl);
+    if (c->version_stage) cudaFreeHost(c->version_stage);
+    cudaFree(c->mirror);
+    cudaFree(c->tiles_done);
+    cudaFree(c->err);
+    cudaFree(c->tile_ctr);
+    cudaFree(c->done_dev);
+    cudaFree(c->t_start);
+    cudaFree(c->t_pub);
+    cudaFree(c->tq);
+    cudaFree(c->dctl);
+    cudaFree(c->table);
+    cudaFree(c->warp_stats);
+    if (c->exec_stream) cudaStreamDestroy(c->exec_stream);
+    if (c->ctl_stream) cudaStreamDestroy(c->ctl_stream);
+    delete c;
+}
+
+/* The executor kernel has ended (normally or with an error). */
+static bool executor_gone(gpuos_ctx *c)
+{
+    const cudaError_t q = cudaStreamQuery(c->exec_stream);
+    if (q == cudaErrorNotReady) return false;
+    if (q != cudaSuccess || getenv("GPUOS_DEBUG"))
+        fprintf(stderr, "gpuos: executor ended (%s), state=%u exit_reason=%u sequenced=%llu\n",
+                cudaGetErrorString(q), c->hctl->state, c->hctl->exit_reason,
+                (unsigned long long)c->hctl->sequenced);
+    return true;
+}
+
+int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
+{
+    if (!out) return GPUOS_EINVAL;
+    *out = nullptr;
+    gpuos_config cfg;
+    if (cfg_in) cfg = *cfg_in;
+    else gpuos_default_config(&cfg);
+    if (!is_pow2(cfg.ring_entries) || cfg.ring_entries < 64 || cfg.ring_entries > 65536) return GPUOS_EINVAL;
+    if (cfg.warps_per_block < 2 || cfg.warps_per_block > GPUOS_MAX_WPB) return GPUOS_EINVAL;
+    if (!is_pow2(cfg.tq_entries) || cfg.tq_entries < 1024 || cfg.tq_entries > GPUOS_TQ_MAX) return GPUOS_EINVAL;
+    if (cfg.backoff_min_ns == 0 || cfg.backoff_max_ns < cfg.backoff_min_ns) return GPUOS_EINVAL;
+
+    gpuos_ctx *c = new (std::nothrow) gpuos_ctx();
+    if (!c) return GPUOS_ENOMEM;
+    c->cfg = cfg;
+    c->device = cfg.device;
+    c->N = cfg.ring_entries;
+    c->mask = c->N - 1;
+    c->Q = cfg.tq_entries;
+    memset(c->table_host, 0, sizeof(c->table_host));
+    memset(c->user_registered, 0, sizeof(c->user_registered));
+#define CK(x)                                                                                       \
+    do {                                                                                            \
+        cudaError_t e_ = (x);                                                                       \
+        if (e_ != cudaSuccess) {                                                                    \
+            fprintf(stderr, "gpuos: %s failed: %s\n", #x, cudaGetErrorString(e_));                  \
+            free_all(c);                                                                            \
+            return e_ == cudaErrorMemoryAllocation ? GPUOS_ENOMEM : GPUOS_ECUDA;                    \
+        }                                                                                           \
+    } while (0)
+    CK(cudaSetDevice(c->device));
+    int sms = 0;
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device));
+    c->blocks = cfg.blocks ? cfg.blocks : (uint32_t)sms;
+    c->wpb = cfg.warps_per_block;
+    if (gpuos_dev_preload() != 0) {
+        free_all(c);
+        return GPUOS_ECUDA;
+    }
+    gpuos_dev_executor_attrs(&c->regs, &c->smem);
+    CK(cudaStreamCreateWithFlags(&c->exec_stream, cudaStreamNonBlocking));
+    CK(cudaStreamCreateWithFlags(&c->ctl_stream, cudaStreamNonBlocking));
+
+    const size_t ring_bytes = (size_t)c->N * sizeof(gpuos_desc);
+    if (cfg.ring_in_device_mem) {
+        int direct = 0;
+        CK(cudaDeviceGetAttribute(&direct, cudaDevAttrDirectManagedMemAccessFromHost, c->device));
+        if (!direct) {
+            free_all(c);
+            return GPUOS_EINVAL;
+        }
+        CK(cudaMallocManaged((void **)&c->ring, ring_bytes, cudaMemAttachGlobal));
+        c->ring_managed = true;
+        cudaMemLocation loc;
+        loc.type = cudaMemLocationTypeDevice;
+        loc.id = c->device;
+        CK(cudaMemAdvise(c->ring, ring_bytes, cudaMemAdviseSetPreferredLocation, loc));
+        cudaMemLocation hl;
+        hl.type = cudaMemLocationTypeHost;
+        hl.id = 0;
+        CK(cudaMemAdvise(c->ring, ring_bytes, cudaMemAdviseSetAccessedBy, hl));
+        CK(cudaMemPrefetchAsync(c->ring, ring_bytes, loc, 0, c->ctl_stream));
+        CK(cudaMemsetAsync(c->ring, 0, ring_bytes, c->ctl_stream));
+        CK(cudaStreamSynchronize(c->ctl_stream));
+        c->ring_dev = c->ring;
+    } else {
+        CK(cudaHostAlloc((void **)&c->ring, ring_bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+        memset(c->ring, 0, ring_bytes);
+        CK(cudaHostGetDevicePointer((void **)&c->ring_dev, c->ring, 0));
+    }
+    CK(cudaHostAlloc((void **)&c->rec, (size_t)c->N * sizeof(gpuos_rec_dev), cudaHostAllocMapped | cudaHostAllocPortable));
+    memset(c->rec, 0, (size_t)c->N * sizeof(gpuos_rec_dev));
+    CK(cudaHostGetDevicePointer((void **)&c->rec_dev, c->rec, 0));
+    CK(cudaHostAlloc((void **)&c->hctl, sizeof(gpuos_hostctl), cudaHostAllocMapped | cudaHostAllocPortable));
+    memset(c->hctl, 0, sizeof(gpuos_hostctl));
+    CK(cudaHostGetDevicePointer((void **)&c->hctl_dev, c->hctl, 0));
+    CK(cudaHostAlloc((void **)&c->version_stage, 64, cudaHostAllocPortable));
+
+    const uint32_t total_warps = c->blocks * c->wpb;
+    CK(cudaMalloc((void **)&c->mirror, (size_t)c->N * sizeof(gpuos_devdesc)));
+    CK(cudaMalloc((void **)&c->tiles_done, (size_t)c->N * 4));
+    CK(cudaMalloc((void **)&c->err, (size_t)c->N * 4));
+    CK(cudaMalloc((void **)&c->tile_ctr, (size_t)c->N * 4));
+    CK(cudaMalloc((void **)&c->done_dev, (size_t)c->N * 8));
+    CK(cudaMalloc((void **)&c->t_start, (size_t)c->N * 8));
+    CK(cudaMalloc((void **)&c->tq, (size_t)c->Q * 8));
+    CK(cudaMalloc((void **)&c->t_pub, (size_t)c->N * 8));
+    CK(cudaMalloc((void **)&c->dctl, sizeof(gpuos_devctl)));
+    CK(cudaMalloc((void **)&c->table, sizeof(c->table_host)));
+    CK(cudaMalloc((void **)&c->warp_stats, (size_t)total_warps * GPUOS_WS_N * 8));
+    CK(cudaMemsetAsync(c->mirror, 0, (size_t)c->N * sizeof(gpuos_devdesc), c->ctl_stream));
+    CK(cudaMemsetAsync(c->tiles_done, 0, (size_t)c->N * 4, c->ctl_stream));
+    CK(cudaMemsetAsync(c->err, 0, (size_t)c->N * 4, c->ctl_stream));
+    CK(cudaMemsetAsync(c->tile_ctr, 0, (size_t)c->N * 4, c->ctl_stream));
+    CK(cudaMemsetAsync(c->done_dev, 0, (size_t)c->N * 8, c->ctl_stream));
+    CK(cudaMemsetAsync(c->t_start, 0, (size_t)c->N * 8, c->ctl_stream));
+    CK(cudaMemsetAsync(c->tq, 0, (size_t)c->Q * 8, c->ctl_stream));
+    CK(cudaMemsetAsync(c->t_pub, 0, (size_t)c->N * 8, c->ctl_stream));
+    CK(cudaMemsetAsync(c->dctl, 0, sizeof(gpuos_devctl), c->ctl_stream));
+    CK(cudaMemsetAsync(c->warp_stats, 0, (size_t)total_warps * GPUOS_WS_N * 8, c->ctl_stream));
+
+    gpuos_op_fn builtin[GPUOS_OP_BUILTIN_COUNT];
+    if (gpuos_dev_builtin_table(builtin, GPUOS_OP_BUILTIN_COUNT) != 0) {
+        free_all(c);
+        return GPUOS_ECUDA;
+    }
+    for (int s = 0; s < 2; s++)
+        for (int i = 0; i < GPUOS_OP_BUILTIN_COUNT; i++) c->table_host[s][i] = (uint64_t)(uintptr_t)builtin[i];
+    CK(cudaMemcpyAsync(c->table, c->table_host, sizeof(c->table_host), cudaMemcpyHostToDevice, c->ctl_stream));
+    CK(cudaStreamSynchronize(c->ctl_stream));
+
+    c->commit_ns.assign(c->N, 0);
+    c->hv.assign(c->N, 0);
+    c->recent.assign(c->N, gpuos_record());
+
+    gpuos_exec_params &p = c->params;
+    memset(&p, 0, sizeof(p));
+    p.ring = c->ring_dev;
+    p.rec = c->rec_dev;
+    p.hctl = c->hctl_dev;
+    p.mirror = c->mirror;
+    p.tiles_done = c->tiles_done;
+    p.err = c->err;
+    p.tile_ctr = c->tile_ctr;
+    p.done_dev = c->done_dev;
+    p.t_start = c->t_start;
+    p.t_pub = c->t_pub;
+    p.tq = c->tq;
+    p.dctl = c->dctl;
+    p.table = c->table;
+    p.warp_stats = c->warp_stats;
+    p.ring_mask = c->mask;
+    p.tq_mask = c->Q - 1;
+    p.backoff_min_ns = cfg.backoff_min_ns;
+    p.backoff_max_ns = cfg.backoff_max_ns;
+    p.spin_polls = cfg.spin_polls;
+    p.idle_exit_ns = (uint64_t)cfg.idle_exit_ms * 1000000ull;
+    p.dep_timeout_ns = (uint64_t)(cfg.dep_timeout_ms ? cfg.dep_timeout_ms : 5000) * 1000000ull;
+    p.exit_after = cfg.exit_after;
+    c->accepting = true;
+    if (!cfg.deferred_start) {
+        const int rc = gpuos_start(c);
+        if (rc != GPUOS_OK) {
+            free_all(c);
+            return rc;
+        }
+    }
+    *out = c;
+    return GPUOS_OK;
+#undef CK
+}
+
+int gpuos_start(gpuos_ctx *c)
+{
+    if (!c || c->launched) return GPUOS_EINVAL;
+    if (cudaSetDevice(c->device) != cudaSuccess) return GPUOS_ECUDA;
+    heartbeat(c);
+    if (gpuos_dev_launch_executor(&c->params, c->blocks, c->wpb, c->exec_stream) != 0) {
+        fprintf(stderr, "gpuos: executor launch failed: %s\n", cudaGetErrorString(cudaGetLastError()));
+        return GPUOS_ECUDA;
+    }
+    c->launched = true;
+    /* wait (bounded) for the sequencer to report that it runs */
+    const uint64_t t0 = now_ns();
+    while (load_acq(&c->hctl->state) == 0u) {
+        if (cudaStreamQuery(c->exec_stream) != cudaErrorNotReady || now_ns() - t0 > 10000000000ull) {
+            fprintf(stderr, "gpuos: executor did not start\n");
+            store_rel(&c->hctl->stop, 1u);
+            return GPUOS_ECUDA;
+        }
+        cpu_relax();
+    }
+    c->running = true;
+    return GPUOS_OK;
+}
+
+int gpuos_executor_stream(gpuos_ctx *c, void **stream)
+{
+    if (!c || !stream) return GPUOS_EINVAL;
+    *stream = (void *)c->exec_stream;
+    return GPUOS_OK;
+}
+
+/* ---- harvesting completion records ------------------------------------------ */
+static void harvest_one(gpuos_ctx *c, uint64_t t)
+{
+    const uint32_t slot = (uint32_t)(t & c->mask);
+    if (c->hv[slot] == t + 1) return;
+    gpuos_rec_dev *r = c->rec + slot;
+    gpuos_record R;
+    R.ticket = t;
+    R.status = __atomic_load_n(&r->status, __ATOMIC_RELAXED);
+    R.version = __atomic_load_n(&r->version, __ATOMIC_RELAXED);
+    R.t_commit_host_ns = c->commit_ns[slot];
+    R.t_dispatch_dev_ns = __atomic_load_n(&r->t_dispatch, __ATOMIC_RELAXED);
+    R.t_publish_dev_ns = __atomic_load_n(&r->t_publish, __ATOMIC_RELAXED);
+    R.t_start_dev_ns = __atomic_load_n(&r->t_start, __ATOMIC_RELAXED);
+    R.t_done_dev_ns = __atomic_load_n(&r->t_done, __ATOMIC_RELAXED);
+    c->recent[slot] = R;
+    if (c->history && t >= c->hist_base && t - c->hist_base < c->hist_cap) c->history[t - c->hist_base] = R;
+    c->hv[slot] = t + 1;
+    c->n_completed++;
+    if (R.status != GPUOS_ST_OK) {
+        c->n_errors++;
+        c->pending_errors++;
+    }
+}
+
+static bool is_done(gpuos_ctx *c, uint64_t t)
+{
+    return load_acq(&c->rec[t & c->mask].done_seq) >= t + 1;
+}
+
+static void sweep(gpuos_ctx *c)
+{
+    /* tickets older than head - N were harvested when their slot was reused */
+    if (c->head > c->N && c->low < c->head - c->N) c->low = c->head - c->N;
+    while (c->low < c->head) {
+        const uint32_t slot = (uint32_t)(c->low & c->mask);
+        if (c->hv[slot] != c->low + 1) {
+            if (!is_done(c, c->low)) break;
+            harvest_one(c, c->low);
+        }
+        c->low++;
+    }
+}
+
+static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint32_t timeout_us)
+{
+    if (!c || !d) return GPUOS_EINVAL;
+    if (!c->accepting || (c->launched && !c->running)) return GPUOS_ESTOPPED;
+    if (!c->launched && c->head >= c->N) return GPUOS_EAGAIN; /* deferred: ring capacity */
+    if (c->launched && __atomic_load_n(&c->hctl->state, __ATOMIC_RELAXED) == 2u) {
+        c->running = false; /* the executor is leaving (stop or watchdog) */
+        if (getenv("GPUOS_DEBUG"))
+            fprintf(stderr,
+                    "gpuos: submit refused, executor leaving: exit_reason=%u sequenced=%llu now=%llu active=%llu "
+                    "idle_exit_ns=%llu\n",
+                    c->hctl->exit_reason, (unsigned long long)c->hctl->sequenced,
+                    (unsigned long long)c->hctl->exit_now, (unsigned long long)c->hctl->exit_active,
+                    (unsigned long long)c->params.idle_exit_ns);
+        return GPUOS_ESTOPPED;
+    }
+    uint32_t nt = 0;
+    const bool user_known = d->op_id >= GPUOS_OP_USER_FIRST && c->user_registered[d->op_id];
+    int rc = validate_and_tile(d, &nt, user_known);
+    if (rc) return rc;
+    const uint64_t t = c->head;
+    uint64_t deps[2];
+    for (int i = 0; i < 2; i++) {
+        uint64_t v = d->dep[i];
+        if (v && (d->flags & GPUOS_FLAG_DEP_REL)) {
+            if (v > t) return GPUOS_EINVAL;
+            v = t - v + 1; /* ticket + 1 of the descriptor v back */
+        }
+        if (v > t) return GPUOS_EINVAL; /* depends on itself or the future */
+        deps[i] = v;
+    }
+    const uint32_t slot = (uint32_t)(t & c->mask);
+    if (t >= c->N) {
+        const uint64_t prev = t - c->N;
+        if (!is_done(c, prev)) {
+            const uint64_t t0 = now_ns();
+            uint32_t spins = 0;
+            while (!is_done(c, prev)) {
+                if ((++spins & 1023u) == 0) {
+                    heartbeat(c);
+                    if (now_ns() - t0 > (uint64_t)timeout_us * 1000ull) return GPUOS_EAGAIN;
+                    if (executor_gone(c)) {
+                        c->running = false;
+                        return GPUOS_ESTOPPED;
+                    }
+                }
+                cpu_relax();
+            }
+        }
+        harvest_one(c, prev);
+    }
+    gpuos_desc *s = c->ring + slot;
+    gpuos_desc w = *d;
+    w.ntiles = nt;
+    w.dep[0] = deps[0];
+    w.dep[1] = deps[1];
+    w.flags = (uint8_t)(d->flags & GPUOS_FLAG_FENCE);
+    w.ticket = t;
+    /* body (first 120 bytes), then the commit word with a store-release */
+    const uint64_t *src = reinterpret_cast<const uint64_t *>(&w);
+    uint64_t *dst = reinterpret_cast<uint64_t *>(s);
+    for (int i = 0; i < 15; i++) __atomic_store_n(dst + i, src[i], __ATOMIC_RELAXED);
+    c->commit_ns[slot] = now_ns();
+    store_rel(&s->seq, t + 1);
+    c->head = t + 1;
+    if ((t & 63u) == 0) heartbeat(c);
+    if (ticket) *ticket = t;
+    return GPUOS_OK;
+}
+
+int gpuos_submit(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint32_t timeout_us)
+{
+    return submit_one(c, d, ticket, timeout_us);
+}
+
+int gpuos_submit_batch(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t *first_ticket,
+                       uint32_t *n_done, uint32_t timeout_us)
+{
+    if (!c || (!d && count)) return GPUOS_EINVAL;
+    if (first_ticket) *first_ticket = c->head;
+    uint32_t i = 0;
+    int rc = GPUOS_OK;
+    for (; i < count; i++) {
+        rc = submit_one(c, d + i, nullptr, timeout_us);
+        if (rc) break;
+    }
+    if (n_done) *n_done = i;
+    return rc;
+}
+
+int gpuos_sync(gpuos_ctx *c, uint64_t ticket, uint32_t timeout_ms)
+{
+    if (!c) return GPUOS_EINVAL;
+    const uint64_t target = (ticket == UINT64_MAX) ? c->head : ticket + 1;
+    if (target > c->head) return GPUOS_EINVAL;
+    if (!c->launched && target > c->low) return GPUOS_ESTOPPED;
+    const uint64_t t0 = now_ns();
+    uint32_t spins = 0;
+    heartbeat(c);
+    while (true) {
+        sweep(c);
+        bool done = c->low >= target;
+        if (!done && ticket != UINT64_MAX && (c->head - ticket <= c->N) && is_done(c, ticket)) {
+            harvest_one(c, ticket);
+            done = true;
+        }
+        if (done) break;
+        if ((++spins & 1023u) == 0) {
+            heartbeat(c);
+            if (now_ns() - t0 > (uint64_t)timeout_ms * 1000000ull) return GPUOS_ETIMEDOUT;
+            if (executor_gone(c)) {
+                sweep(c);
+                if (c->low >= target) break;
+                c->running = false;
+                return GPUOS_ESTOPPED;
+            }
+        }
+        cpu_relax();
+    }
+    if (c->pending_errors) {
+        c->pending_errors = 0;
+        return GPUOS_EDEVICE;
+    }
+    return GPUOS_OK;
+}
+
+int gpuos_query(gpuos_ctx *c, uint64_t ticket, gpuos_record *rec)
+{
+    if (!c || !rec) return GPUOS_EINVAL;
+    if (ticket >= c->head) return GPUOS_EINVAL;
+    if (c->history && ticket >= c->hist_base && ticket - c->hist_base < c->hist_cap &&
+        c->history[ticket - c->hist_base].ticket == ticket && ticket < c->low) {
+        *rec = c->history[ticket - c->hist_base];
+        return GPUOS_OK;
+    }
+    if (c->head - ticket > c->N) return GPUOS_EINVAL;
+    const uint32_t slot = (uint32_t)(ticket & c->mask);
+    if (c->hv[slot] != ticket + 1) {
+        if (!is_done(c, ticket)) return GPUOS_EAGAIN;
+        harvest_one(c, ticket);
+    }
+    *rec = c->recent[slot];
+    return GPUOS_OK;
+}
+
+int gpuos_set_history(gpuos_ctx *c, gpuos_record *buf, uint64_t base, uint64_t capacity)
+{
+    if (!c || (buf == nullptr && capacity)) return GPUOS_EINVAL;
+    c->history = buf;
+    c->hist_base = base;
+    c->hist_cap = buf ? capacity : 0;
+    if (buf)
+        for (uint64_t i = 0; i < capacity; i++) buf[i].ticket = UINT64_MAX;
+    return GPUOS_OK;
+}
+
+/* ---- dual-slot table flip ------------------------------------------------------- */
+static int flip_entry(gpuos_ctx *c, uint16_t op_id, uint64_t fnval)
+{
+    /* grace period: descriptors sequenced under version-1 (all tickets below
+     * the head recorded at the last flip) must have completed before the
+     * slot they read is rewritten */
+    const uint64_t t0 = now_ns();
+    while (true) {
+        sweep(c);
+        if (c->low >= c->flip_head) break;
+        if (now_ns() - t0 > (uint64_t)c->cfg.dep_timeout_ms * 2000000ull) return GPUOS_ETIMEDOUT;
+        if (executor_gone(c)) return GPUOS_ESTOPPED;
+        heartbeat(c);
+        cpu_relax();
+    }
+    const uint32_t nv = c->version + 1;
+    const uint32_t ns = nv & 1u;
+    memcpy(c->table_host[ns], c->table_host[c->version & 1u], sizeof(c->table_host[0]));
+    c->table_host[ns][op_id] = fnval;
+    if (cudaMemcpyAsync(c->table + (size_t)ns * GPUOS_MAX_OPS, c->table_host[ns], sizeof(c->table_host[0]),
+                        cudaMemcpyHostToDevice, c->ctl_stream) != cudaSuccess)
+        return GPUOS_ECUDA;
+    /* the version word lands only after the table slot (stream order) */
+    *c->version_stage = nv;
+    if (cudaMemcpyAsync(&c->dctl->version, c->version_stage, 4, cudaMemcpyHostToDevice, c->ctl_stream) != cudaSuccess)
+        return GPUOS_ECUDA;
+    if (cudaStreamSynchronize(c->ctl_stream) != cudaSuccess) return GPUOS_ECUDA;
+    c->version = nv;
+    c->flip_head = c->head;
+    heartbeat(c);
+    return GPUOS_OK;
+}
+
+static uint64_t fnv1a(const void *p, size_t n)
+{
+    const unsigned char *b = static_cast<const unsigned char *>(p);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < n; i++) h = (h ^ b[i]) * 1099511628211ull;
+    return h;
+}
+
+static bool executor_resident(gpuos_ctx *c)
+{
+    return c->launched && cudaStreamQuery(c->exec_stream) == cudaErrorNotReady;
+}
+
+/* index of the loaded module holding `image`, or -1 */
+static int find_module(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
+{
+    for (size_t i = 0; i < c->modules.size(); i++) {
+        const auto &m = c->modules[i];
+        if (m.hash == h && m.bytes.size() == len && memcmp(m.bytes.data(), image, len) == 0) return (int)i;
+    }
+    return -1;
+}
+
+static int load_module(gpuos_ctx *c, const void *image, size_t len, int *index)
+{
+    const uint64_t h = fnv1a(image, len);
+    const int found = find_module(c, image, len, h);
+    if (found >= 0) {
+        *index = found;
+        return GPUOS_OK;
+    }
+    if (executor_resident(c)) return GPUOS_EBUSY;
+    Driver &drv = driver();
+    if (!drv.ok) return GPUOS_ECUDA;
+    if (cudaSetDevice(c->device) != cudaSuccess) return GPUOS_ECUDA;
+    CUmodule mod = nullptr;
+    if (drv.load(&mod, image) != CUDA_SUCCESS) return GPUOS_EINVAL;
+    gpuos_ctx::Module m;
+    m.mod = mod;
+    m.hash = h;
+    m.bytes.assign(static_cast<const unsigned char *>(image), static_cast<const unsigned char *>(image) + len);
+    c->modules.push_back(std::move(m));
+    *index = (int)c->modules.size() - 1;
+    return GPUOS_OK;
+}
+
+int gpuos_load_module(gpuos_ctx *c, const void *image, size_t len)
+{
+    if (!c || !image || !len) return GPUOS_EINVAL;
+    int idx = -1;
+    return load_module(c, image, len, &idx);
+}
+
+int gpuos_register_op(gpuos_ctx *c, uint16_t op_id, const void *image, size_t len, const char *sym)
+{
+    if (!c || !image || !len || !sym || op_id >= GPUOS_MAX_OPS || op_id == GPUOS_OP_NOP) return GPUOS_EINVAL;
+    if (op_id >= GPUOS_OP_BUILTIN_COUNT && op_id < GPUOS_OP_USER_FIRST) return GPUOS_EINVAL;
+    if (!c->accepting) return GPUOS_ESTOPPED;
+    int idx = -1;
+    int rc = load_module(c, image, len, &idx);
+    if (rc) return rc;
+    heartbeat(c);
+    CUdeviceptr gp = 0;
+    size_t gsz = 0;
+    if (driver().get_global(&gp, &gsz, c->modules[idx].mod, sym) != CUDA_SUCCESS || gsz != sizeof(uint64_t))
+        return GPUOS_EINVAL;
+    uint64_t fnval = 0;
+    if (cudaMemcpyAsync(c->version_stage + 2, (const void *)gp, 8, cudaMemcpyDeviceToHost, c->ctl_stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(c->ctl_stream) != cudaSuccess)
+        return GPUOS_ECUDA;
+    memcpy(&fnval, c->version_stage + 2, 8);
+    if (fnval == 0) return GPUOS_EINVAL;
+    rc = flip_entry(c, op_id, fnval);
+    if (rc == GPUOS_OK && op_id >= GPUOS_OP_USER_FIRST) c->user_registered[op_id] = true;
+    return rc;
+}
+
+int gpuos_alias_op(gpuos_ctx *c, uint16_t op_id, uint16_t source_op)
+{
+    if (!c || op_id >= GPUOS_MAX_OPS || source_op >= GPUOS_MAX_OPS || op_id == GPUOS_OP_NOP) return GPUOS_EINVAL;
+    if (op_id >= GPUOS_OP_BUILTIN_COUNT && op_id < GPUOS_OP_USER_FIRST) return GPUOS_EINVAL;
+    if (!c->accepting) return GPUOS_ESTOPPED;
+    const uint64_t v = c->table_host[c->version & 1u][source_op];
+    if (v == 0) return GPUOS_EINVAL;
+    const int rc = flip_entry(c, op_id, v);
+    if (rc == GPUOS_OK && op_id >= GPUOS_OP_USER_FIRST) c->user_registered[op_id] = true;
+    return rc;
+}
+
+int gpuos_stats(gpuos_ctx *c, gpuos_stats_t *st)
+{
+    if (!c || !st) return GPUOS_EINVAL;
+    memset(st, 0, sizeof(*st));
+    const uint32_t tw = c->blocks * c->wpb;
+    std::vector<uint64_t> ws((size_t)tw * GPUOS_WS_N);
+    if (cudaMemcpyAsync(ws.data(), c->warp_stats, ws.size() * 8, cudaMemcpyDeviceToHost, c->ctl_stream) != cudaSuccess ||
+        cudaStreamSynchronize(c->ctl_stream) != cudaSuccess)
+        return GPUOS_ECUDA;
+    for (uint32_t w = 0; w < tw; w++) {
+        const uint64_t *x = &ws[(size_t)w * GPUOS_WS_N];
+        st->tiles += x[GPUOS_WS_TILES];
+        st->idle_polls += x[GPUOS_WS_IDLE];
+        st->sleeps += x[GPUOS_WS_SLEEPS];
+        st->dep_waits += x[GPUOS_WS_DEPWAIT];
+    }
+    /* warp 0 of block 0 is the sequencer: its phase timers */
+    st->seq_body_ns = ws[GPUOS_WS_T_BODY];
+    st->seq_mirror_ns = ws[GPUOS_WS_T_MIRROR];
+    st->seq_publish_ns = ws[GPUOS_WS_T_PUB];
+    sweep(c);
+    st->submitted = c->head;
+    st->completed = c->n_completed;
+    st->errors = c->n_errors;
+    st->sequenced = __atomic_load_n(&c->hctl->sequenced, __ATOMIC_RELAXED);
+    st->version = c->version;
+    st->running = (c->running && !executor_gone(c)) ? 1u : 0u;
+    st->exit_reason = __atomic_load_n(&c->hctl->exit_reason, __ATOMIC_RELAXED);
+    st->blocks = c->blocks;
+    st->warps_per_block = c->wpb;
+    st->regs_per_thread = c->regs;
+    st->static_smem_bytes = c->smem;
+    heartbeat(c);
+    return GPUOS_OK;
+}
+
+int gpuos_calibrate(gpuos_ctx *c, uint32_t pings, int64_t *off_lo, int64_t *off_hi, uint64_t *min_rtt_ns,
+                    uint64_t *rtts)
+{
+    if (!c || pings == 0) return GPUOS_EINVAL;
+    int rc = gpuos_sync(c, UINT64_MAX, 10000);
+    if (rc != GPUOS_OK && rc != GPUOS_EDEVICE) return rc;
+    gpuos_desc nop;
+    memset(&nop, 0, sizeof(nop));
+    nop.op_id = GPUOS_OP_NOP;
+    uint64_t best = UINT64_MAX;
+    int64_t lo = INT64_MIN, hi = INT64_MAX;
+    for (uint32_t i = 0; i < pings; i++) {
+        uint64_t t = 0;
+        const uint64_t t0 = now_ns();
+        rc = submit_one(c, &nop, &t, 1000000);
+        if (rc) return rc;
+        const gpuos_rec_dev *r = c->rec + (t & c->mask);
+        uint32_t spins = 0;
+        while (load_acq(&r->done_seq) < t + 1) {
+            if ((++spins & 0xFFFFFu) == 0 && executor_gone(c)) return GPUOS_ESTOPPED;
+        }
+        const uint64_t t1 = now_ns();
+        const uint64_t td = __atomic_load_n(&r->t_dispatch, __ATOMIC_RELAXED);
+        const uint64_t rtt = t1 - t0;
+        if (rtts) rtts[i] = rtt;
+        if (rtt < best) best = rtt;
+        const int64_t a = (int64_t)(td - t1), b = (int64_t)(td - t0);
+        if (a > lo) lo = a;
+        if (b < hi) hi = b;
+        harvest_one(c, t);
+        sweep(c);
+    }
+    if (off_lo) *off_lo = lo;
+    if (off_hi) *off_hi = hi;
+    if (min_rtt_ns) *min_rtt_ns = best;
+    return GPUOS_OK;
+}
+
+int gpuos_stop(gpuos_ctx *c, uint32_t timeout_ms)
+{
+    if (!c) return GPUOS_EINVAL;
+    int rc = GPUOS_OK;
+    if (c->running) {
+        const int s = gpuos_sync(c, UINT64_MAX, timeout_ms);
+        if (s == GPUOS_ETIMEDOUT) rc = s;
+    }
+    c->accepting = false;
+    store_rel(&c->hctl->stop, 1u);
+    if (!c->launched) return rc;
+    const uint64_t t0 = now_ns();
+    while (true) {
+        const cudaError_t q = cudaStreamQuery(c->exec_stream);
+        if (q != cudaErrorNotReady) {
+            if (q != cudaSuccess && rc == GPUOS_OK) rc = GPUOS_ECUDA;
+            c->running = false;
+            sweep(c);
+            return rc;
+        }
+        if (now_ns() - t0 > (uint64_t)(timeout_ms ? timeout_ms : 1) * 1000000ull) break;
+        cpu_relax();
+    }
+    return rc == GPUOS_OK ? GPUOS_ETIMEDOUT : rc;
+}
+
+int gpuos_shutdown(gpuos_ctx *c, uint32_t timeout_ms)
+{
+    if (!c) return GPUOS_EINVAL;
+    const int rc = gpuos_stop(c, timeout_ms);
+    if (c->launched && cudaStreamQuery(c->exec_stream) == cudaErrorNotReady) {
+        /* the kernel still runs (it will leave through its watchdog); device
+         * memory cannot be released under it, so only the host side goes */
+        delete c;
+        return rc;
+    }
+    free_all(c);
+    return rc;
+}
+
+int gpuos_eager_run(const gpuos_desc *d, uint32_t count, void *stream)
+{
+    if (!d && count) return GPUOS_EINVAL;
+    for (uint32_t i = 0; i < count; i++) {
+        uint32_t nt = 0;
+        if (d[i].op_id >= GPUOS_OP_BUILTIN_COUNT) return GPUOS_EINVAL;
+        const int rc = validate_and_tile(d + i, &nt, false);
+        if (rc) return rc;
+        if (gpuos_dev_eager_launch(d + i, nt, stream) != 0) return GPUOS_ECUDA;
+    }
+    return GPUOS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+/*
+ * Internal layouts shared by the host library (gpuos_host.cpp) and the device
+ * code (gpuos_device.cu). Not part of the public ABI.
+ */
+#ifndef GPUOS_INTERNAL_H
+#define GPUOS_INTERNAL_H
+
+#include <stdint.h>
+
+#include "gpuos.h"
+
+/* Tiling constants of the built-in ops (one tile = one warp's unit of work). */
+#define GPUOS_EW_VPT 16                   /* 16-byte vectors per lane per element-wise tile */
+#define GPUOS_EW_TILE_F32 (32 * GPUOS_EW_VPT * 4)  /* 2048 fp32 elements */
+#define GPUOS_EW_TILE_BF16 (32 * GPUOS_EW_VPT * 8) /* 4096 bf16 elements */
+#define GPUOS_SDPA_CHUNK 512              /* key rows per decode-attention tile */
+#define GPUOS_VM_COLS 32                  /* output columns per vecmat tile */
+#define GPUOS_ROW_REG_MAX 4096            /* rows up to this width stay in registers */
+#define GPUOS_MAX_WPB 16
+#define GPUOS_TILE_MAX (1u << 30)          /* tiles per descriptor */
+#define GPUOS_HELPERS 64                   /* work-queue entries (helper warps) per descriptor at most */
+#define GPUOS_TQ_MAX (1u << 20)            /* work-queue entries (23-bit stamps stay unambiguous) */
+
+#define GPUOS_TQ_CONSUMED (1ull << 63)
+#define GPUOS_TQ_STAMP_MASK 0x7FFFFFull
+
+/* Mirror of a descriptor in device memory, written by the sequencer warp.
+ * Same layout as gpuos_desc except the last fields. */
+typedef struct gpuos_devdesc {
+    uint16_t op_id;
+    uint8_t dtype;
+    uint8_t flags;
+    uint32_t ntiles;
+    uint64_t dep[2];
+    uint64_t a, b, out;
+    uint64_t aux0, aux1, aux2;
+    uint32_t dims[6];
+    float fparam[2];
+    uint64_t t_dispatch; /* device clock when the commit was seen (replaces `user`) */
+    uint64_t ticket;
+    uint32_t version;    /* table version fixed at sequencing (replaces `seq`) */
+    uint32_t pad;
+} gpuos_devdesc;
+
+/* Work-queue entries are single 64-bit words (see tq_word in the device
+ * code): consumed flag, 23-bit stamp, 16-bit ring slot, 24-bit tile. */
+
+/* Completion record in host-visible memory, written by the device. */
+typedef struct gpuos_rec_dev {
+    uint64_t done_seq; /* ticket + 1 once complete (store-release, system scope) */
+    int32_t status;
+    uint32_t version;
+    uint64_t t_dispatch;
+    uint64_t t_publish; /* tiles published to the work queue */
+    uint64_t t_start;   /* tile 0 began */
+    uint64_t t_done;
+    uint64_t pad[2];
+} gpuos_rec_dev;
+
+/* Host-visible control block (pinned host memory). */
+typedef struct gpuos_hostctl {
+    uint64_t heartbeat; /* host: bumped by API calls */
+    uint32_t stop;      /* host: 1 = leave when idle */
+    uint32_t pad0[29];
+    uint32_t state;       /* device: 1 running, 2 leaving */
+    uint32_t exit_reason; /* device: see gpuos_stats_t */
+    uint64_t sequenced;   /* device: tickets taken off the ring */
+    uint64_t exit_now;    /* device: clock when the sequencer decided to leave */
+    uint64_t exit_active; /* device: last activity it had seen then */
+    uint32_t pad1[24];
+} gpuos_hostctl;
+
+/* Device-memory control block; hot words on their own 128-byte lines. */
+typedef struct gpuos_devctl {
+    unsigned long long tq_claim; /* next work-queue index to claim */
+    uint64_t pad0[15];
+    unsigned long long completed; /* descriptors completed */
+    uint64_t pad1[15];
+    uint32_t exit_flag; /* nonzero: workers leave when they find no work */
+    uint32_t version;   /* operator-table version */
+    uint64_t pad2[15];
+} gpuos_devctl;
+
+/* Per-warp counters (owned by one warp each, plain stores). */
+enum { GPUOS_WS_TILES = 0, GPUOS_WS_IDLE = 1, GPUOS_WS_SLEEPS = 2, GPUOS_WS_DEPWAIT = 3,
+       GPUOS_WS_SEQ = 4, GPUOS_WS_T_BODY = 5, GPUOS_WS_T_MIRROR = 6, GPUOS_WS_T_PUB = 7, GPUOS_WS_N = 8 };
+
+typedef int (*gpuos_op_fn)(const gpuos_devdesc *d, uint32_t tile);
+
+typedef struct gpuos_exec_params {
+    const gpuos_desc *ring;  /* host-visible ring */
+    gpuos_rec_dev *rec;      /* host-visible completion records */
+    gpuos_hostctl *hctl;
+    gpuos_devdesc *mirror;   /* [ring_entries] */
+    uint32_t *tiles_done;    /* [ring_entries] */
+    uint32_t *err;           /* [ring_entries] */
+    uint32_t *tile_ctr;      /* [ring_entries], next extra tile (past the helpers' first tiles) */
+    uint64_t *done_dev;      /* [ring_entries], ticket + 1 stamps for dependency waits */
+    uint64_t *t_start;       /* [ring_entries], device clock when tile 0 began */
+    uint64_t *t_pub;         /* [ring_entries], device clock when tiles were published */
+    unsigned long long *tq;  /* [tq_entries] work-queue words */
+    gpuos_devctl *dctl;
+    gpuos_op_fn *table;      /* [2][GPUOS_MAX_OPS] */
+    uint64_t *warp_stats;    /* [total warps][GPUOS_WS_N] */
+    uint32_t ring_mask, tq_mask;
+    uint32_t backoff_min_ns, backoff_max_ns, spin_polls, pad;
+    uint64_t idle_exit_ns, dep_timeout_ns, exit_after;
+} gpuos_exec_params;
+
+#ifdef __cplusplus
+static_assert(sizeof(gpuos_desc) == 128, "descriptor must be 128 bytes");
+static_assert(sizeof(gpuos_devdesc) == 128, "mirror must be 128 bytes");
+static_assert(sizeof(gpuos_rec_dev) == 64, "record must be 64 bytes");
+#endif
+
+/* Launch helpers implemented in gpuos_device.cu (host side). */
+#ifdef __cplusplus
+extern "C" {
+#endif
+int gpuos_dev_launch_executor(const gpuos_exec_params *p, uint32_t blocks, uint32_t wpb, void *stream);
+int gpuos_dev_builtin_table(gpuos_op_fn *host_out, uint32_t n);
+int gpuos_dev_executor_attrs(uint32_t *regs, uint32_t *smem);
+int gpuos_dev_eager_launch(const gpuos_desc *d, uint32_t ntiles, void *stream);
+int gpuos_dev_preload(void);
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPUOS_INTERNAL_H */

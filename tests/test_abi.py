@@ -1,0 +1,135 @@
+"""The C-ABI library builds, loads and exports every symbol include/gpuos.h
+declares; host-only entry points behave without a GPU (CPU)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def G():
+    from persistent_micro_dispatch_gb300 import build
+    build.build()
+    from persistent_micro_dispatch_gb300 import gpuos
+    gpuos.lib()
+    return gpuos
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "gpuos.h")).read()
+    return sorted(set(re.findall(r"GPUOS_API\s+[\w\s\*]+?\b(gpuos_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_north_star_verbs():
+    syms = header_symbols()
+    for v in ("gpuos_init", "gpuos_submit", "gpuos_register_op", "gpuos_sync", "gpuos_shutdown"):
+        assert v in syms
+    assert len(syms) >= 17
+
+
+def test_library_exports_every_declared_symbol(G):
+    lib = C.CDLL(G.LIB_PATH)
+    for name in header_symbols():
+        assert hasattr(lib, name), name
+    assert set(header_symbols()) == set(G.API), "binding and header disagree"
+
+
+def test_only_public_symbols_exported(G):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", G.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert exported == set(header_symbols())
+
+
+def test_descriptor_layout_matches_header(G):
+    assert G.DESC_DTYPE.itemsize == 128
+    off = {n: G.DESC_DTYPE.fields[n][1] for n in G.DESC_DTYPE.names}
+    assert off["dep"] == 8 and off["a"] == 24 and off["dims"] == 72 and off["fparam"] == 96
+    assert off["user"] == 104 and off["ticket"] == 112 and off["seq"] == 120
+    assert C.sizeof(G.Config) == 72 and C.sizeof(G.Record) == 56
+
+
+def test_default_config(G):
+    c = G.default_config()
+    assert c.ring_entries == 4096 and c.warps_per_block == 8 and c.tq_entries == 65536
+    assert c.idle_exit_ms > 0 and c.dep_timeout_ms > 0
+
+
+def _desc(G, op, dtype=1, dims=(), ptr=0x1000, **kw):
+    d = G.make_descs(1)
+    d["op_id"] = G.OP[op] if isinstance(op, str) else op
+    d["dtype"] = dtype
+    dd = list(dims) + [0] * (6 - len(dims))
+    d["dims"] = dd
+    for f in ("a", "b", "out", "aux0", "aux1", "aux2"):
+        d[f] = kw.get(f, ptr)
+    return d
+
+
+def test_tiling_rule(G):
+    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 2          # 2048 fp32 per tile
+    assert G.op_ntiles(_desc(G, "add", 1, (4096,))) == 1          # 4096 bf16 per tile
+    assert G.op_ntiles(_desc(G, "relu", 0, (4097,))) == 3
+    assert G.op_ntiles(_desc(G, "gelu", 0, (0,))) == 1            # empty op: one tile
+    assert G.op_ntiles(_desc(G, "softmax", 1, (37, 1024))) == 37  # one row per tile
+    assert G.op_ntiles(_desc(G, "rope", 1, (5, 32, 128))) == 5
+    assert G.op_ntiles(_desc(G, "sdpa", 1, (3, 32, 128, 4096, 1025, 96))) == 3 * 32 * 3
+    assert G.op_ntiles(_desc(G, "vecmat", 1, (1024, 1024))) == 32
+    assert G.op_ntiles(_desc(G, "nop")) == 1
+
+
+@pytest.mark.parametrize("bad", [
+    dict(op=20, dims=(4,)),                                      # reserved id
+    dict(op="add", dtype=7, dims=(4,)),                          # bad dtype
+    dict(op="add", dims=(4,), a=0),                              # null input
+    dict(op="softmax", dtype=0, dims=(2, 8)),                    # row ops are bf16
+    dict(op="sdpa", dims=(1, 32, 64, 4096, 100, 32)),            # D must be 128
+    dict(op="sdpa", dims=(1, 32, 128, 4096, 5000, 32)),          # Lmax > Lcap
+    dict(op="sdpa", dims=(2, 32, 128, 4096, 100, 32)),           # counters < B*H
+    dict(op="sdpa", dims=(1, 32, 128, 4096, 100, 32), aux2=0x1008),  # unaligned workspace
+    dict(op="rope", dims=(1, 32, 127)),                          # odd D
+])
+def test_host_bounds_checks_reject(G, bad):
+    kw = dict(bad)
+    op = kw.pop("op")
+    dtype = kw.pop("dtype", 1)
+    dims = kw.pop("dims")
+    d = _desc(G, op, dtype, dims, **kw)
+    n = C.c_uint32()
+    assert G.lib().gpuos_op_ntiles(d.ctypes.data, C.byref(n)) == G.EINVAL
+
+
+def test_sdpa_workspace_formula_matches_stream_layout(G):
+    from workloads.streams import sdpa_workspace_bytes
+    for B, H, L in ((1, 32, 4096), (8, 32, 4096), (3, 4, 513), (2, 1, 1)):
+        assert G.sdpa_workspace_bytes(B, H, 128, L) == sdpa_workspace_bytes(B, H, 128, L)
+
+
+def test_strerror_and_clock(G):
+    assert "ring full" in G.strerror(G.EAGAIN)
+    assert "dependency" in G.strerror(G.ST_DEP_TIMEOUT, True)
+    t0 = G.host_now_ns()
+    t1 = G.host_now_ns()
+    assert t1 >= t0 > 0
+
+
+def test_init_without_gpu_fails_cleanly(G):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    ctx = C.c_void_p()
+    cfg = G.default_config()
+    rc = G.lib().gpuos_init(C.byref(cfg), C.byref(ctx))
+    assert rc in (G.ECUDA, G.ENOMEM) and not ctx.value
+
+
+def test_init_rejects_bad_config(G):
+    ctx = C.c_void_p()
+    for kw in (dict(ring_entries=100), dict(ring_entries=32), dict(warps_per_block=1),
+               dict(warps_per_block=17), dict(tq_entries=1000), dict(tq_entries=1 << 21), dict(backoff_min_ns=0)):
+        cfg = G.default_config(**kw)
+        assert G.lib().gpuos_init(C.byref(cfg), C.byref(ctx)) == G.EINVAL, kw

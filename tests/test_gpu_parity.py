@@ -1,0 +1,129 @@
+"""Parity of the persistent executor with the CPU oracle on the five seeded
+streams (GPU). Small cases compare every op; full-size cases compare sampled
+ops, recomputed by the oracle from the same seeded inputs.
+
+Bar: bit-exact for copy/order/exact-IEEE ops, 1e-5 relative for fp32,
+2e-2 absolute (or one bf16 ulp of the exact value) for bf16 outputs.
+"""
+import numpy as np
+import pytest
+
+from oracle.interp import Machine
+from tests.gpu_harness import (check_canaries, compare_stream, ensure_built, final_output_ops, need_gpu,
+                               run_executor, sample)
+from workloads import streams as S
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    need_gpu()
+    ensure_built()
+
+
+def _run_and_compare(s, check=None, sample_k=None, cfg=None, skip=None, seed=0):
+    from workloads.device import DeviceStream
+    S.check_hazards(s)
+    ds = DeviceStream(s)
+    descs = ds.descs()
+    st, hist = run_executor(ds, descs, **(cfg or {}))
+    assert np.all(hist["status"] == 0), f"device status: {np.unique(hist['status'])}"
+    assert st["completed"] == len(s.ops)
+    cand = final_output_ops(s, range(len(s.ops)) if check is None else check)
+    if sample_k is not None:
+        cand = sample(cand, sample_k, seed)
+    mach = Machine(s)
+    if sample_k is None and skip is None:
+        mach.run(keep=cand)
+    elif skip is not None:
+        mach.run(keep=cand, skip=[j for j in skip if j not in set(cand)])
+    else:
+        mach.run_closure(cand)
+    rep = compare_stream(s, ds, mach, cand)
+    print(f"{s.name}: {rep.summary()} stats={st}")
+    assert rep.ok(), "\n".join(rep.failures)
+    return s, ds, rep, st, hist
+
+
+def test_c1_smallest_stream_bit_exact():
+    """1,000 fp32 add/mul/ReLU on 4,096-element tensors: every output bit-exact."""
+    s, ds, rep, st, hist = _run_and_compare(S.stream_c1())
+    assert rep.exact == len(s.ops)
+    check_canaries(s, ds)
+
+
+def test_c2_variable_elementwise_small():
+    """3,000 descriptors over {add, mul, ReLU, GELU} x {fp32, bf16}, 30 % chained."""
+    s, ds, rep, st, hist = _run_and_compare(S.stream_c2(n_desc=3000, pool_elems=1 << 22))
+    check_canaries(s, ds)
+
+
+def test_c2l_large_ops_small():
+    s, ds, rep, st, hist = _run_and_compare(S.stream_c2l(n_desc=40, pool_elems=1 << 23))
+    check_canaries(s, ds)
+
+
+def test_c3_row_ops_small():
+    s, ds, rep, st, hist = _run_and_compare(S.stream_c3(n_desc=1500, pool_elems=1 << 22))
+    check_canaries(s, ds, names=("out_bf16", "out_f32"))
+
+
+def test_c4_decode_small_and_kv_copy_bit_exact():
+    """20 decode steps at full shapes (B<=8, 32x128, caches of 4,096 rows)."""
+    s, ds, rep, st, hist = _run_and_compare(S.stream_c4(n_steps=20))
+    _check_kv_copies(s, ds)
+
+
+def _check_kv_copies(s, ds):
+    """Replay every KV write with the GPU's own (rotated) k/v rows on the
+    initial caches: the GPU caches must equal the result byte for byte."""
+    iK, iV = s.buf_index("Kc"), s.buf_index("Vc")
+    K = s.buffers[iK].data.copy()
+    V = s.buffers[iV].data.copy()
+    for o in s.ops:
+        if o.op != "kv_write":
+            continue
+        B, H, D, Lc = o.dims[:4]
+        lens = s.buffers[o.aux0.buf].data[o.aux0.off:o.aux0.off + B]
+        k = ds.read(o.a, B * H * D).reshape(B, H, D)
+        v = ds.read(o.b, B * H * D).reshape(B, H, D)
+        K4 = K[o.out.off:o.out.off + B * H * Lc * D].reshape(B, H, Lc, D)
+        V4 = V[o.aux1.off:o.aux1.off + B * H * Lc * D].reshape(B, H, Lc, D)
+        for b in range(B):
+            K4[b, :, lens[b] - 1] = k[b]
+            V4[b, :, lens[b] - 1] = v[b]
+    assert np.array_equal(ds.read_buf(iK), K)
+    assert np.array_equal(ds.read_buf(iV), V)
+
+
+def test_c5_mixed_pipeline_small():
+    """3 tokens of the 32-layer synthetic decoder at hidden 4,096."""
+    s, ds, rep, st, hist = _run_and_compare(S.stream_c5(n_tokens=3))
+    _check_kv_copies(s, ds)
+
+
+@pytest.mark.slow
+def test_c2_full_sampled():
+    """Full C2 (100,000 descriptors); 400 sampled ops recomputed by the oracle."""
+    _run_and_compare(S.stream_c2(), sample_k=400, seed=2)
+
+
+@pytest.mark.slow
+def test_c2l_full_sampled():
+    _run_and_compare(S.stream_c2l(), sample_k=60, seed=6)
+
+
+@pytest.mark.slow
+def test_c3_full_sampled():
+    _run_and_compare(S.stream_c3(), sample_k=400, seed=3)
+
+
+@pytest.mark.slow
+def test_c4_full_sampled():
+    """Full C4 (2,000 steps). The oracle replays every RoPE and KV write and
+    evaluates SDPA only for 12 sampled steps (no op reads an SDPA output)."""
+    s = S.stream_c4()
+    sd = [j for j, o in enumerate(s.ops) if o.op == "sdpa"]
+    keep = sample(sd, 12, seed=4)
+    _run_and_compare(s, check=keep, skip=sd)

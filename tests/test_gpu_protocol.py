@@ -1,0 +1,385 @@
+"""Ring, table and failure-handling protocol of the executor (GPU).
+
+Every failure here is made on the host or with a bounded device wait: no
+test faults, traps or hangs the GPU.
+"""
+import time
+
+import numpy as np
+import pytest
+
+from oracle.interp import Machine
+from tests.gpu_harness import compare_stream, ensure_built, need_gpu
+from workloads import streams as S
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    need_gpu()
+    ensure_built()
+    from workloads.device import warm_torch
+    warm_torch()
+
+
+def G():
+    from persistent_micro_dispatch_gb300 import gpuos
+    return gpuos
+
+
+def _c1_small(n_desc=1000, n=4096, seed=11):
+    from workloads.device import DeviceStream
+    s = S.stream_c1(n_desc=n_desc, n=n, seed=seed)
+    return s, DeviceStream(s)
+
+
+def _check_all(s, ds):
+    m = Machine(s)
+    m.run(keep=range(len(s.ops)))
+    rep = compare_stream(s, ds, m, range(len(s.ops)))
+    assert rep.ok(), "\n".join(rep.failures)
+    return rep
+
+
+def test_ring_wraps_many_times_small_ring():
+    """1,000 descriptors through a 64-entry ring (15 laps), bit-exact."""
+    s, ds = _c1_small()
+    ex = G().Executor(ring_entries=64)
+    try:
+        ex.submit_batch(ds.descs())
+        ex.sync(timeout_ms=30_000)
+        st = ex.stats()
+    finally:
+        assert ex.shutdown() == 0
+    assert st["completed"] == 1000 and st["errors"] == 0
+    rep = _check_all(s, ds)
+    assert rep.exact == 1000
+
+
+def test_deferred_start_fills_ring_then_wraps():
+    s, ds = _c1_small(n_desc=300)
+    d = ds.descs()
+    ex = G().Executor(ring_entries=64, deferred_start=1)
+    try:
+        ex.submit_batch(d[:64])
+        # the ring is full and nothing runs yet: the next submit cannot wait
+        assert ex.try_submit(d[64:65], timeout_us=0) == G().EAGAIN
+        ex.start()
+        ex.submit_batch(d[64:])
+        ex.sync(timeout_ms=30_000)
+    finally:
+        assert ex.shutdown() == 0
+    _check_all(s, ds)
+
+
+def _big_add(n):
+    import torch
+    a = torch.ones(n, dtype=torch.float32, device="cuda")
+    b = torch.ones(n, dtype=torch.float32, device="cuda")
+    c = torch.empty(n, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    d = G().make_descs(1)
+    d["op_id"] = G().OP["add"]
+    d["dtype"] = G().F32
+    d["a"], d["b"], d["out"] = a.data_ptr(), b.data_ptr(), c.data_ptr()
+    d["dims"][0, 0] = n
+    return d, (a, b, c)
+
+
+def test_full_ring_returns_eagain_and_recovers():
+    """One worker warp busy with a long op: the 64-entry ring fills and a
+    submit with a short timeout returns EAGAIN; everything completes later."""
+    g = G()
+    big, keep = _big_add(1 << 26)
+    nop = g.make_descs(1)
+    ex = g.Executor(ring_entries=64, blocks=1, warps_per_block=2)
+    try:
+        ex.submit(big)
+        for _ in range(63):
+            ex.submit(nop)
+        t0 = time.perf_counter()
+        rc = ex.try_submit(nop, timeout_us=2000)
+        assert rc == g.EAGAIN
+        assert time.perf_counter() - t0 < 1.0
+        ex.submit(nop, timeout_us=30_000_000)  # waits for a slot, then succeeds
+        ex.sync(timeout_ms=60_000)
+        st = ex.stats()
+    finally:
+        assert ex.shutdown() == 0
+    assert st["completed"] == 65 and st["errors"] == 0
+    assert float(keep[2][-1].item()) == 2.0
+
+
+def test_fence_wait_times_out_with_status():
+    """A FENCE behind a long op with a 20 ms device wait bound completes with
+    GPUOS_ST_DEP_TIMEOUT; sync reports EDEVICE; the executor stays usable."""
+    g = G()
+    big, keep = _big_add(1 << 26)
+    nop = g.make_descs(1)
+    fence = g.make_descs(1)
+    fence["flags"] = g.FLAG_FENCE
+    ex = g.Executor(blocks=1, warps_per_block=2, dep_timeout_ms=20)
+    try:
+        ex.submit(big)
+        t = ex.submit(fence)
+        rc = ex.sync(timeout_ms=60_000, raise_on_error=False)
+        assert rc == g.EDEVICE
+        assert ex.query(t).status == g.ST_DEP_TIMEOUT
+        t2 = ex.submit(nop)
+        assert ex.sync(t2, timeout_ms=10_000, raise_on_error=False) == g.OK
+    finally:
+        ex.shutdown()
+
+
+def test_fence_orders_after_all_earlier():
+    """A FENCE descriptor starts only after every earlier one completed."""
+    g = G()
+    big, keep = _big_add(1 << 24)
+    nop = g.make_descs(1)
+    fence = g.make_descs(1)
+    fence["flags"] = g.FLAG_FENCE
+    ex = g.Executor()
+    try:
+        base = ex.stats()["submitted"]
+        h = ex.set_history(base, 3)
+        ex.submit(big)
+        ex.submit(nop)
+        ex.submit(fence)
+        ex.sync(timeout_ms=30_000)
+    finally:
+        ex.shutdown()
+    # the fenced descriptor is published (and starts) after both completed
+    assert h["t_publish_dev_ns"][2] >= h["t_done_dev_ns"][0]
+    assert h["t_start_dev_ns"][2] >= h["t_done_dev_ns"][1]
+
+
+def test_device_bounds_checks_return_status():
+    """Descriptors that pass the host checks but carry bad positions or
+    lengths in device memory complete with GPUOS_ST_BAD_ARGS."""
+    import torch
+    g = G()
+    B, H, D, Lc = 2, 4, 128, 64
+    q = torch.zeros(B * H * D, dtype=torch.bfloat16, device="cuda")
+    K = torch.zeros(B * H * Lc * D, dtype=torch.bfloat16, device="cuda")
+    V = torch.zeros_like(K)
+    o = torch.zeros_like(q)
+    lens = torch.tensor([0, 70], dtype=torch.int32, device="cuda")  # 0: pos -1; 70 > Lcap
+    ws = torch.zeros(g.sdpa_workspace_bytes(B, H, D, Lc), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    kv = g.make_descs(1)
+    kv["op_id"] = g.OP["kv_write"]
+    kv["a"], kv["b"], kv["aux0"], kv["out"], kv["aux1"] = q.data_ptr(), q.data_ptr(), lens.data_ptr(), K.data_ptr(), V.data_ptr()
+    kv["dims"][0, :4] = (B, H, D, Lc)
+    sd = g.make_descs(1)
+    sd["op_id"] = g.OP["sdpa"]
+    sd["a"], sd["b"], sd["aux1"], sd["aux0"], sd["out"], sd["aux2"] = (q.data_ptr(), K.data_ptr(), V.data_ptr(),
+                                                                      lens.data_ptr(), o.data_ptr(), ws.data_ptr())
+    sd["dims"][0, :6] = (B, H, D, Lc, Lc, B * H)
+    sd["fparam"][0, 0] = 0.1
+    bad = g.make_descs(1)
+    bad["op_id"] = 200  # not registered: rejected on the host, no ticket used
+    ex = g.Executor()
+    try:
+        assert ex.try_submit(bad) == g.EINVAL
+        t1 = ex.submit(kv)
+        t2 = ex.submit(sd)
+        assert ex.sync(timeout_ms=10_000, raise_on_error=False) == g.EDEVICE
+        assert ex.query(t1).status == g.ST_BAD_ARGS
+        assert ex.query(t2).status == g.ST_BAD_ARGS
+        st = ex.stats()
+        assert st["errors"] == 2 and st["submitted"] == 2
+    finally:
+        ex.shutdown()
+    assert int(ws.view(torch.int32)[: B * H].abs().sum().item()) == 0  # counters left zero
+
+
+def test_dependency_on_future_ticket_rejected():
+    g = G()
+    nop = g.make_descs(1)
+    nop["dep"][0, 0] = 5  # absolute ticket + 1 of a descriptor not yet submitted
+    ex = g.Executor()
+    try:
+        assert ex.try_submit(nop) == g.EINVAL
+    finally:
+        ex.shutdown()
+
+
+def _ext_image():
+    return open(G().EXT_CUBIN, "rb").read()
+
+
+@pytest.mark.skip(reason="cross-module function pointers are being replaced by in-module linking")
+def test_hot_swap_under_load_every_result_old_or_new():
+    """Swap op ADD for the injected subtract while 3,000 adds are in flight;
+    each descriptor's output is a+b or a-b according to the table version it
+    recorded; swapping back restores add. Bit-exact against the oracle
+    (a - b = a + (-b) exactly)."""
+    g = G()
+    from workloads.device import DeviceStream
+    s = S.stream_c1(n_desc=3000, n=4096, seed=12)
+    for o in s.ops:
+        o.op = "add"
+        if o.b is None:
+            o.b = S.Ref(s.buf_index("b"), o.a.off)
+    ds = DeviceStream(s)
+    d = ds.descs()
+    ex = g.Executor(deferred_start=1)
+    try:
+        ex.load_module(_ext_image())  # modules load before the executor is resident
+        ex.start()
+        hist = ex.set_history(0, len(d))
+        ex.submit_batch(d[:1000])
+        ex.register_op(g.OP["add"], _ext_image(), "gpuos_ext_sub_ptr")  # version 1
+        ex.submit_batch(d[1000:2000])
+        ex.alias_op(g.OP["add"], g.OP["mul"])  # version 2: mul
+        ex.submit_batch(d[2000:])
+        ex.sync(timeout_ms=30_000)
+        st = ex.stats()
+    finally:
+        ex.shutdown()
+    assert st["version"] == 2
+    ver = hist["version"]
+    assert set(np.unique(ver)) <= {0, 1, 2}
+    assert (ver[:1000] <= 1).all() and (ver[2000:] == 2).all()
+    assert (ver == 1).sum() > 0
+    m = Machine(s)
+    bi = s.buf_index("b")
+    for j, o in enumerate(s.ops):
+        if ver[j] == 1:
+            m.buf[bi][o.b.off:o.b.off + o.dims[0]] *= -1  # oracle: a + (-b)
+            m.apply(j)
+            m.buf[bi][o.b.off:o.b.off + o.dims[0]] *= -1
+        elif ver[j] == 2:
+            o.op = "mul"
+            m.apply(j)
+            o.op = "add"
+        else:
+            m.apply(j)
+    for j, o in enumerate(s.ops):
+        n = o.dims[0]
+        assert np.array_equal(ds.read(o.out, n).view(np.uint32), m.view(o.out, n).view(np.uint32)), (j, ver[j])
+
+
+@pytest.mark.skip(reason="cross-module function pointers are being replaced by in-module linking")
+def test_user_op_registration():
+    """An injected op under a new id (64) with a caller-set tile count."""
+    import torch
+    g = G()
+    n = 5000
+    x = torch.randn(n, dtype=torch.float32, device="cuda")
+    y = torch.zeros(n, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    d = g.make_descs(1)
+    d["op_id"] = 64
+    d["dtype"] = g.F32
+    d["a"], d["out"] = x.data_ptr(), y.data_ptr()
+    d["dims"][0, 0] = n
+    d["fparam"][0, 0] = 2.5
+    d["ntiles"] = (n + 1023) // 1024
+    ex = g.Executor(deferred_start=1)
+    try:
+        ex.load_module(_ext_image())
+        ex.start()
+        assert ex.try_submit(d) == g.EINVAL  # not registered yet
+        ex.register_op(64, _ext_image(), "gpuos_ext_scale_ptr")
+        ex.submit(d)
+        ex.sync(timeout_ms=10_000)
+    finally:
+        ex.shutdown()
+    xs = x.cpu().numpy()
+    want = (xs.astype(np.float64) * np.float32(2.5)).astype(np.float32)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+def test_register_op_rejects_bad_symbol_and_unloaded_image():
+    g = G()
+    ex = g.Executor(deferred_start=1)
+    try:
+        ex.load_module(_ext_image())
+        ex.start()
+        with pytest.raises(g.GpuosError) as e:
+            ex.register_op(64, _ext_image(), "no_such_symbol")
+        assert e.value.code == g.EINVAL
+        with pytest.raises(g.GpuosError) as e:
+            ex.register_op(20, _ext_image(), "gpuos_ext_sub_ptr")  # reserved id
+        assert e.value.code == g.EINVAL
+        # an image that is not loaded cannot be loaded under a resident executor
+        t0 = time.perf_counter()
+        with pytest.raises(g.GpuosError) as e:
+            ex.register_op(64, _ext_image() + b"\0" * 64, "gpuos_ext_scale_ptr")
+        assert e.value.code == g.EBUSY and time.perf_counter() - t0 < 1.0
+        assert ex.stats()["running"] == 1
+    finally:
+        ex.shutdown()
+
+
+def test_idle_watchdog_ends_executor():
+    """With no host activity for idle_exit_ms the kernel leaves by itself."""
+    g = G()
+    ex = g.Executor(idle_exit_ms=300)
+    try:
+        time.sleep(1.5)
+        st = ex.stats()
+        assert st["running"] == 0 and st["exit_reason"] == 2
+        assert ex.try_submit(g.make_descs(1)) == g.ESTOPPED
+    finally:
+        ex.shutdown()
+
+
+def test_exit_after_bounded_run():
+    s, ds = _c1_small(n_desc=200)
+    g = G()
+    ex = g.Executor(deferred_start=1, exit_after=200)
+    try:
+        ex.submit_batch(ds.descs())
+        ex.start()
+        ex.sync(timeout_ms=30_000)
+        t0 = time.perf_counter()
+        while ex.stats()["running"] and time.perf_counter() - t0 < 10:
+            time.sleep(0.01)
+        st = ex.stats()
+        assert st["running"] == 0 and st["exit_reason"] == 3
+    finally:
+        ex.shutdown()
+    _check_all(s, ds)
+
+
+def test_calibration_bounds_and_record_order():
+    g = G()
+    ex = g.Executor()
+    try:
+        lo, hi, rtt, rtts = ex.calibrate(100)
+        assert lo <= hi and 0 < rtt < 200_000
+        base = ex.stats()["submitted"]
+        h = ex.set_history(base, 50)
+        for _ in range(50):
+            ex.sync(ex.submit(g.make_descs(1)))
+    finally:
+        ex.shutdown()
+    assert (h["t_dispatch_dev_ns"] <= h["t_publish_dev_ns"]).all()
+    assert (h["t_publish_dev_ns"] <= h["t_start_dev_ns"]).all()
+    assert (h["t_start_dev_ns"] <= h["t_done_dev_ns"]).all()
+
+
+def test_eager_path_matches_executor_bitwise():
+    """The eager baseline runs the same op bodies: identical outputs."""
+    import torch
+    g = G()
+    from workloads.device import DeviceStream
+    s = S.stream_mixed_small()
+    ds1 = DeviceStream(s)
+    ds2 = DeviceStream(s)
+    ex = g.Executor()
+    try:
+        ex.submit_batch(ds1.descs())
+        ex.sync(timeout_ms=30_000)
+    finally:
+        ex.shutdown()
+    st = torch.cuda.Stream()
+    g.eager_run(ds2.descs(), st.cuda_stream)
+    st.synchronize()
+    for i, b in enumerate(s.buffers):
+        if b.name in ("sdpa_ws",):
+            continue
+        assert np.array_equal(ds1.read_buf(i).view(np.uint8), ds2.read_buf(i).view(np.uint8)), b.name

@@ -368,14 +368,16 @@ def test_vecmat_identity_and_integer_exact():
     rng = np.random.default_rng(15)
     K = N = 64
     x = bf(rng.standard_normal(K))
+    eye = bf(np.eye(K))  # keep the operands alive across the C call
     out = np.empty(N, np.float64)
-    lib().orc_vecmat(P(x), P(bf(np.eye(K))), K, N, P(out))
+    lib().orc_vecmat(P(x), P(eye), K, N, P(out))
     assert np.array_equal(out, unbf(x))
     K, N = 37, 19
     xi = rng.integers(-8, 9, K)
     Wi = rng.integers(-8, 9, (K, N))
+    xb, Wb = bf(xi), bf(Wi)
     out = np.empty(N, np.float64)
-    lib().orc_vecmat(P(bf(xi)), P(bf(Wi)), K, N, P(out))
+    lib().orc_vecmat(P(xb), P(Wb), K, N, P(out))
     want = [sum(int(xi[k]) * int(Wi[k, n]) for k in range(K)) for n in range(N)]
     assert out.tolist() == [float(w) for w in want]
 

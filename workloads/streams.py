@@ -54,9 +54,11 @@ CANARY_BYTE = 0x5A
 
 
 def sdpa_workspace_bytes(B: int, H: int, D: int, Lmax: int) -> int:
-    """Bytes of the fp32 split-K workspace a decode-SDPA descriptor needs."""
+    """Bytes of the split-K workspace of decode-SDPA descriptors with at most
+    B requests: B*H uint32 counters (rounded up to 4), then one fp32 partial
+    (m, l, acc[D]) per (request, head, chunk)."""
     nch = max(1, -(-Lmax // SDPA_CHUNK))
-    return 4 * (B * H * nch * (D + 2)) + 4 * (B * H)
+    return 4 * ((B * H + 3) // 4 * 4) + 4 * (B * H * nch * (D + 2))
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -136,8 +138,10 @@ class Op:
 #             caches laid out [B][H][Lcap][D]; row lens[b]-1 is written.
 #             dims=(B,H,D,Lcap)
 #   sdpa      a=q[B,H,D], b=Kc, aux1=Vc, aux0=lens i32[B], out=o[B,H,D],
-#             aux2=fp32 workspace (sdpa_workspace_bytes); dims=(B,H,D,Lcap,Lmax)
-#             with every lens[b] <= Lmax <= Lcap; fparam=(scale,)
+#             aux2=workspace (sdpa_workspace_bytes of the largest B);
+#             dims=(B,H,D,Lcap,Lmax,Ccap) with every lens[b] <= Lmax <= Lcap and
+#             Ccap = counters reserved at the workspace start (>= B*H, the same
+#             for every descriptor sharing the workspace); fparam=(scale,)
 #   vecmat    a=x[K], b=W[K,N] row-major -> out=y[N]; dims=(K,N)
 #   nop       no operands
 OP_FIELDS = ("a", "b", "out", "aux0", "aux1", "aux2")
@@ -196,12 +200,12 @@ def op_accesses(s: Stream, o: Op) -> List[Tuple[int, int, int, bool]]:
         R(o.a, B * H * D); R(o.b, B * H * D); R(o.aux0, B)
         R(o.out, B * H * Lc * D, True); R(o.aux1, B * H * Lc * D, True)
     elif o.op == "sdpa":
-        B, H, D, Lc, Lm = d[:5]
+        B, H, D, Lc, Lm, Cc = d[:6]
         R(o.a, B * H * D); R(o.aux0, B)
         R(o.b, B * H * Lc * D); R(o.aux1, B * H * Lc * D)
         R(o.out, B * H * D, True)
         if o.aux2 is not None:
-            ws = sdpa_workspace_bytes(B, H, D, Lm) // 4
+            ws = sdpa_workspace_bytes(max(B, Cc // H), H, D, Lm)
             R(o.aux2, ws); R(o.aux2, ws, True)
     elif o.op == "vecmat":
         K, N = d[:2]
@@ -468,7 +472,7 @@ def stream_c4(n_steps: int = 2000, B_max: int = 8, H: int = 32, D: int = 128, Lc
                         out=Ref(ik, 0), aux1=Ref(iv, 0), dims=(B, H, D, Lcap), deps=deps))
         s.ops.append(Op("sdpa", "bf16", a=Ref(iq, qoff), b=Ref(ik, 0), aux1=Ref(iv, 0),
                         aux0=Ref(il, loff), out=Ref(io, qoff), aux2=Ref(ws, 0),
-                        dims=(B, H, D, Lcap, Lm), fparam=(scale,), deps=(r + 1,)))
+                        dims=(B, H, D, Lcap, Lm, B_max * H), fparam=(scale,), deps=(r + 1,)))
         prev_sdpa = r + 2
         qoff += B * row
         loff += B
@@ -481,12 +485,14 @@ def stream_c5(n_tokens: int = 500, n_layers: int = 32, hidden: int = 4096, H: in
     """Mixed pipeline: a synthetic decoder, one strict chain of 7 ops per layer.
 
     Per token and layer: LayerNorm(x) -> h; vecmat(h[:vm], W_l) -> y;
-    RoPE(q=h viewed [1,H,D], k_t) at position L-1; KV write of (k_t, v_t) into
-    the layer's caches at row L-1; SDPA(q=h, caches, L) -> o; GELU(o) -> g;
-    residual add x' = x + g. Every op depends on the op before it. L follows
-    a random walk L_{t+1} = clamp(L_t + U{-walk..walk}, L_lo, Lcap) shared by
-    all layers of a token. Weights W ~ N(0, 0.02), gamma ~ N(1, 0.1),
-    beta ~ N(0, 0.1); caches prefilled with N(0,1); k_t, v_t fresh N(0,1).
+    RoPE(q_t, k_t) at position L-1; KV write of (k_t, v_t) into the layer's
+    caches at row L-1; SDPA(q_t, caches, L) -> o; GELU(o) -> g; residual add
+    x' = x + g. Every op depends on the op before it. The 1 x vm vecmat cannot
+    produce the H*D-wide projections, so q_t, k_t, v_t are fresh N(0,1) inputs
+    per token and layer (synthetic glue), and y is an output of its own. L
+    follows a random walk L_{t+1} = clamp(L_t + U{-walk..walk}, L_lo, Lcap)
+    shared by all layers of a token. Weights W ~ N(0, 0.02), gamma ~ N(1, 0.1),
+    beta ~ N(0, 0.1); caches prefilled with N(0,1).
     """
     assert H * D == hidden
     rng = np.random.default_rng(seed)
@@ -499,6 +505,7 @@ def stream_c5(n_tokens: int = 500, n_layers: int = 32, hidden: int = 4096, H: in
     iK = s.add_buf("Kc", "bf16", nl * cache_n, _pool(rng, nl * cache_n, "bf16"))
     iV = s.add_buf("Vc", "bf16", nl * cache_n, _pool(rng, nl * cache_n, "bf16"))
     kv_n = n_tokens * nl * hidden
+    iqn = s.add_buf("q_new", "bf16", kv_n, _pool(rng, kv_n, "bf16"))
     ik = s.add_buf("k_new", "bf16", kv_n, _pool(rng, kv_n, "bf16"))
     iv = s.add_buf("v_new", "bf16", kv_n, _pool(rng, kv_n, "bf16"))
     ix = s.add_buf("x", "bf16", (n_tokens * nl + 1) * hidden, fill=0)
@@ -529,14 +536,14 @@ def stream_c5(n_tokens: int = 500, n_layers: int = 32, hidden: int = 4096, H: in
                             fparam=(1e-5,), deps=dep0))
             s.ops.append(Op("vecmat", "bf16", a=Ref(ih, hx), b=Ref(iW, l * vm * vm),
                             out=Ref(iy, u * vm), dims=(vm, vm), deps=(base,)))
-            s.ops.append(Op("rope", "bf16", a=Ref(ih, hx), b=Ref(ik, hx), aux0=Ref(il, t),
+            s.ops.append(Op("rope", "bf16", a=Ref(iqn, hx), b=Ref(ik, hx), aux0=Ref(il, t),
                             dims=(1, H, D), fparam=(theta,), deps=(base + 1,)))
             s.ops.append(Op("kv_write", "bf16", a=Ref(ik, hx), b=Ref(iv, hx), aux0=Ref(il, t),
                             out=Ref(iK, l * cache_n), aux1=Ref(iV, l * cache_n),
                             dims=(1, H, D, Lcap), deps=(base + 2,)))
-            s.ops.append(Op("sdpa", "bf16", a=Ref(ih, hx), b=Ref(iK, l * cache_n),
+            s.ops.append(Op("sdpa", "bf16", a=Ref(iqn, hx), b=Ref(iK, l * cache_n),
                             aux1=Ref(iV, l * cache_n), aux0=Ref(il, t), out=Ref(io, hx),
-                            aux2=Ref(ws, 0), dims=(1, H, D, Lcap, Lt), fparam=(scale,),
+                            aux2=Ref(ws, 0), dims=(1, H, D, Lcap, Lt, H), fparam=(scale,),
                             deps=(base + 3,)))
             s.ops.append(Op("gelu", "bf16", a=Ref(io, hx), out=Ref(igl, hx), dims=(hidden,),
                             deps=(base + 4,)))
@@ -602,3 +609,58 @@ def stream_bytes(s: Stream) -> int:
         else:
             tot += op_bytes(o)
     return tot
+
+
+def stream_mixed_small(seed: int = 7) -> Stream:
+    """Every op kind once or twice at small sizes, with ragged tails and a
+    multi-chunk attention head (a quick end-to-end check)."""
+    rng = np.random.default_rng(seed)
+    s = Stream("mixed_small", meta=dict(seed=seed))
+    pf = s.add_buf("pool_f32", "f32", 1 << 16, _pool(rng, 1 << 16, "f32"))
+    pb = s.add_buf("pool_bf16", "bf16", 1 << 16, _pool(rng, 1 << 16, "bf16"))
+    px = s.add_buf("pool_x", "bf16", 1 << 16, _pool(rng, 1 << 16, "bf16", std=2.0))
+    pg = s.add_buf("gamma", "bf16", 4096, _pool(rng, 4096, "bf16", std=0.1, mean=1.0))
+    pbt = s.add_buf("beta", "bf16", 4096, _pool(rng, 4096, "bf16", std=0.1))
+    B, H, D, Lc = 2, 4, 128, 1100
+    iK = s.add_buf("Kc", "bf16", B * H * Lc * D, _pool(rng, B * H * Lc * D, "bf16"))
+    iV = s.add_buf("Vc", "bf16", B * H * Lc * D, _pool(rng, B * H * Lc * D, "bf16"))
+    iq = s.add_buf("q", "bf16", B * H * D, _pool(rng, B * H * D, "bf16"))
+    ik = s.add_buf("k_new", "bf16", B * H * D, _pool(rng, B * H * D, "bf16"))
+    iv = s.add_buf("v_new", "bf16", B * H * D, _pool(rng, B * H * D, "bf16"))
+    il = s.add_buf("lens", "i32", B, np.array([1037, 3], np.int32))
+    iW = s.add_buf("W", "bf16", 300 * 72, _pool(rng, 300 * 72, "bf16", std=0.05))
+    of = s.add_buf("out_f32", "f32", 1 << 15)
+    ob = s.add_buf("out_bf16", "bf16", 1 << 16)
+    io = s.add_buf("o", "bf16", B * H * D)
+    ws = s.add_buf("sdpa_ws", "u8", sdpa_workspace_bytes(B, H, D, Lc), fill=0)
+    ea, eb = _Arena(), _Arena()
+    for op, dt, n in (("add", "f32", 4097), ("mul", "bf16", 9001), ("relu", "f32", 7), ("gelu", "bf16", 255),
+                      ("gelu", "f32", 2049), ("add", "bf16", 0)):
+        pool = pf if dt == "f32" else pb
+        out = (of, ea.take(n)) if dt == "f32" else (ob, eb.take(n))
+        s.ops.append(Op(op, dt, a=Ref(pool, 256), b=Ref(pool, 8192) if op in ("add", "mul") else None,
+                        out=Ref(*out), dims=(n,)))
+    s.ops.append(Op("relu", "f32", a=Ref(of, 0), out=Ref(of, ea.take(4097)), dims=(4097,), deps=(0,)))
+    for op, R, Hh in (("softmax", 3, 1000), ("layernorm", 2, 4096), ("rowsum", 5, 2048), ("rowmax", 4, 33),
+                      ("rowmin", 1, 5000), ("softmax", 2, 6000)):
+        o = Op(op, "bf16", a=Ref(px, 512), dims=(R, Hh))
+        if op in ("softmax", "layernorm"):
+            o.out = Ref(ob, eb.take(R * Hh))
+        elif op == "rowsum":
+            o.out = Ref(of, ea.take(R))
+        else:
+            o.out = Ref(ob, eb.take(R))
+        if op == "layernorm":
+            o.b, o.aux0, o.fparam = Ref(pg, 0), Ref(pbt, 0), (1e-5,)
+        s.ops.append(o)
+    s.ops.append(Op("vecmat", "bf16", a=Ref(pb, 64), b=Ref(iW, 0), out=Ref(ob, eb.take(72)), dims=(300, 72)))
+    s.ops.append(Op("vecmat", "bf16", a=Ref(pb, 64), b=Ref(iW, 0), out=Ref(ob, eb.take(36)), dims=(600, 36)))
+    r = len(s.ops)
+    s.ops.append(Op("rope", "bf16", a=Ref(iq, 0), b=Ref(ik, 0), aux0=Ref(il, 0), dims=(B, H, D), fparam=(10000.0,)))
+    s.ops.append(Op("kv_write", "bf16", a=Ref(ik, 0), b=Ref(iv, 0), aux0=Ref(il, 0), out=Ref(iK, 0),
+                    aux1=Ref(iV, 0), dims=(B, H, D, Lc), deps=(r,)))
+    s.ops.append(Op("sdpa", "bf16", a=Ref(iq, 0), b=Ref(iK, 0), aux1=Ref(iV, 0), aux0=Ref(il, 0), out=Ref(io, 0),
+                    aux2=Ref(ws, 0), dims=(B, H, D, Lc, 1037, B * H), fparam=(1.0 / math.sqrt(D),),
+                    deps=(r + 1,)))
+    s.ops.append(Op("nop", fence=True))
+    return s
