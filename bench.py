@@ -225,7 +225,11 @@ def main():
     ap.add_argument("--no-eager", action="store_true")
     ap.add_argument("--profile-run", action="store_true",
                     help="one bounded executor run (ring filled before launch) for profilers; no JSON")
+    ap.add_argument("--profile-desc", type=int, default=0,
+                    help="profile run: descriptors (0 = the workload's own, capped at the ring size)")
+    ap.add_argument("--pool-log2", type=int, default=0, help="profile run: log2 of the input pool elements")
     ap.add_argument("--warps", type=int, default=0, help="executor warps per block (0 = default)")
+    ap.add_argument("--stage-bytes", type=int, default=16384, help="shared-memory staging per warp (0 = none)")
     args = ap.parse_args()
     os.environ.setdefault("GPUOS_DEBUG", "1")
     world, rank, local = dist_env()
@@ -243,10 +247,16 @@ def main():
     from workloads import streams as S
     from workloads.device import DeviceStream, warm_torch
 
-    cfg_kw = dict(device=local, idle_exit_ms=20000)
+    cfg_kw = dict(device=local, idle_exit_ms=20000, stage_bytes=args.stage_bytes)
     if args.warps:
         cfg_kw["warps_per_block"] = args.warps
-    s = make_stream(args.workload, args.tokens)
+    if args.profile_run and args.profile_desc and args.workload in ("c2", "c2l"):
+        kw = dict(n_desc=args.profile_desc)
+        if args.pool_log2:
+            kw["pool_elems"] = 1 << args.pool_log2
+        s = S.STREAMS[args.workload](**kw)
+    else:
+        s = make_stream(args.workload, args.tokens)
     n_ops = len(s.ops)
     step_bytes = S.stream_bytes(s)
     ds = DeviceStream(s, device=f"cuda:{local}")
@@ -302,12 +312,22 @@ def main():
     clocks.start()
     time.sleep(0.3)
     t0 = time.perf_counter()
+    h_marks = [G.host_now_ns()]
     ev0.record(xs)
+    h_marks.append(G.host_now_ns())
     ex.start()
+    h_marks.append(G.host_now_ns())
     ev1.record(xs)  # completes when the executor kernel ends
+    h_marks.append(G.host_now_ns())
     submit_ns = 0
-    for _ in range(args.steps):
+    for step in range(args.steps):
         a = time.perf_counter_ns()
+        if step == 0:
+            h_marks.append(G.host_now_ns())
+            st0 = ex.stats()
+            if not st0["running"]:
+                print(f"executor left before the first submit: host marks {np.diff(h_marks).tolist()} ns, "
+                      f"stats {st0}", file=sys.stderr, flush=True)
         ex.submit_batch(descs)
         submit_ns += time.perf_counter_ns() - a
         ex.sync(timeout_ms=600_000)
@@ -371,13 +391,13 @@ def main():
     if not args.no_eager:
         es = torch.cuda.Stream()
         for _ in range(max(1, args.warmup)):
-            G.eager_run(descs, es.cuda_stream)
+            G.eager_run(descs, es.cuda_stream, args.stage_bytes)
         es.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(es)
         for _ in range(args.steps):
-            G.eager_run(descs, es.cuda_stream)
+            G.eager_run(descs, es.cuda_stream, args.stage_bytes)
         e1.record(es)
         e1.synchronize()
         eg_ms = e0.elapsed_time(e1)
@@ -394,8 +414,10 @@ def main():
         h2d = sum(t.numel() for t in host_in)
         d2h = sum(t.numel() for t in host_out)
         cs = torch.cuda.Stream()
-        ex = G.Executor(**cfg_kw)
+        # device-wide synchronisation only while no executor is resident: a
+        # resident persistent kernel never lets it return
         torch.cuda.synchronize()
+        ex = G.Executor(**cfg_kw)
         barrier(world)
         a = time.perf_counter()
         for _ in range(args.steps):

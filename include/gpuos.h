@@ -69,6 +69,7 @@ extern "C" {
 #define GPUOS_ST_DEP_TIMEOUT 3   /* a dependency or fence wait ran out */
 #define GPUOS_ST_ABORTED 4       /* the executor was leaving */
 #define GPUOS_ST_BAD_DESC 5      /* ring slot did not hold the expected ticket */
+#define GPUOS_ST_COPY_TIMEOUT 6  /* a shared-memory staging copy did not land within its bound */
 
 /* ---- op ids (built-in operator library) --------------------------------- */
 enum {
@@ -139,7 +140,7 @@ typedef struct gpuos_desc {
 /* Executor / ring configuration. gpuos_default_config() fills defaults. */
 typedef struct gpuos_config {
     uint32_t ring_entries;    /* power of two in [64, 65536]; default 4096 (the page's default) */
-    uint32_t warps_per_block; /* 2..16; default 8 */
+    uint32_t warps_per_block; /* 2..16; default 12 */
     uint32_t blocks;          /* 0 = one block per SM */
     uint32_t backoff_min_ns;  /* first idle sleep; default 32 */
     uint32_t backoff_max_ns;  /* idle sleep cap; default 256 */
@@ -150,10 +151,14 @@ typedef struct gpuos_config {
                                     1: managed memory preferred on the device */
     int32_t device;           /* CUDA device ordinal; default 0 */
     uint64_t exit_after;      /* 0 = run until shutdown; n = leave once n descriptors completed */
-    uint32_t tq_entries;      /* work-queue entries, power of two in [1024, 2^20]; default 65536 */
+    uint32_t tq_entries;      /* work-queue entries: 0 (default) = 128 x ring_entries; else a power
+                                 of two above 64 x ring_entries, at most 2^30 */
     uint32_t deferred_start;  /* 1: gpuos_init does not launch; gpuos_start does (descriptors
                                  may be submitted before, up to ring_entries of them) */
-    uint32_t reserved[4];
+    uint32_t stage_bytes;     /* shared-memory staging per warp for bulk (TMA) copies: 0 = none
+                                 (register path; leaves shared memory to co-running kernels),
+                                 else a multiple of 1024 up to 24576; default 16384 */
+    uint32_t reserved[3];
 } gpuos_config;
 
 /* Completion record of one ticket (device clock = %globaltimer, host clock =
@@ -297,10 +302,12 @@ GPUOS_API int gpuos_op_ntiles(const gpuos_desc *d, uint32_t *ntiles);
 GPUOS_API size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, uint32_t Lmax);
 
 /* Eager baseline: launch the same op bodies as ordinary kernels, one
- * cudaLaunchKernel per descriptor, in order, on `stream` (a cudaStream_t; 0 =
- * legacy default). Deps are implied by stream order. Does not synchronize.
- * Errors: EINVAL (as gpuos_submit), ECUDA. */
-GPUOS_API int gpuos_eager_run(const gpuos_desc *d, uint32_t count, void *stream);
+ * cudaLaunchKernel per descriptor (one warp per tile, one warp per block), in
+ * order, on `stream` (a cudaStream_t; 0 = legacy default), with stage_bytes
+ * of shared-memory staging per warp as in gpuos_config. Deps are implied by
+ * stream order. Does not synchronize. Errors: EINVAL (as gpuos_submit),
+ * ECUDA. */
+GPUOS_API int gpuos_eager_run(const gpuos_desc *d, uint32_t count, uint32_t stage_bytes, void *stream);
 
 /* CLOCK_REALTIME in ns (the host clock of gpuos_record). */
 GPUOS_API uint64_t gpuos_host_now_ns(void);

@@ -110,6 +110,24 @@ DEV uint64_t globaltimer()
 }
 DEV uint32_t lane_id() { return threadIdx.x & 31u; }
 
+/* Elapsed-time accumulator for bounded waits. %globaltimer can read stale
+ * right after a launch and can jump when the driver resynchronises it, so a
+ * deadline adds up the deltas between consecutive checks, each clamped to
+ * 1 ms: one bad reading moves it by at most 1 ms. */
+struct Elapsed {
+    uint64_t last, acc;
+    __device__ __forceinline__ void start() { last = 0; acc = 0; }
+    __device__ __forceinline__ uint64_t tick(uint64_t now)
+    {
+        if (last != 0) {
+            uint64_t d = now - last;
+            acc += d > 1000000ull ? 1000000ull : d;
+        }
+        last = now;
+        return acc;
+    }
+};
+
 /* Idle backoff: spin for `spin` polls, then sleep min_ns << k up to max_ns. */
 DEV void backoff(uint32_t &polls, uint32_t spin, uint32_t min_ns, uint32_t max_ns, uint64_t *sleeps)
 {
@@ -168,6 +186,77 @@ DEV float warp_min(float v)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
+}
+
+/* ---------------------------------------------------------------------------
+ * Per-warp shared-memory staging. Dynamic shared memory of the executor (and
+ * of the eager kernel) starts with a 16-byte header {stride, stage_bytes},
+ * followed by one region per warp: {mbarrier, phase} and a staging buffer of
+ * stage_bytes (16-byte aligned). stage_bytes == 0 means "no staging": ops use
+ * their register path.
+ * ------------------------------------------------------------------------- */
+struct StageHdr {
+    uint32_t stride;      /* bytes between warp regions */
+    uint32_t stage_bytes; /* staging buffer per warp */
+    uint32_t pad[2];
+};
+struct WarpStage {
+    unsigned long long mbar; /* completion barrier of the warp's bulk copies */
+    uint32_t phase;          /* parity of the next phase to wait for */
+    uint32_t pad;
+};
+extern __shared__ __align__(16) unsigned char g_dyn_smem[];
+
+DEV StageHdr *stage_hdr() { return reinterpret_cast<StageHdr *>(g_dyn_smem); }
+DEV WarpStage *warp_stage()
+{
+    return reinterpret_cast<WarpStage *>(g_dyn_smem + 16 + (threadIdx.x >> 5) * stage_hdr()->stride);
+}
+DEV unsigned char *warp_stage_buf() { return reinterpret_cast<unsigned char *>(warp_stage()) + 16; }
+DEV uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+/* Lay out the header and every warp's barrier (all threads of the block). */
+DEV void stage_init(uint32_t stage_bytes)
+{
+    if (threadIdx.x == 0) {
+        stage_hdr()->stride = 16 + stage_bytes;
+        stage_hdr()->stage_bytes = stage_bytes;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31u) == 0) {
+        WarpStage *w = warp_stage();
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&w->mbar)) : "memory");
+        w->phase = 0;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+}
+
+/* Bulk-copy `bytes` (multiple of 16, 16-byte aligned ends) from global to the
+ * warp's shared buffer; completes on the warp's mbarrier (lane 0 only). */
+DEV void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes, unsigned long long *mbar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_addr(mbar)) : "memory");
+}
+DEV void mbar_expect(unsigned long long *mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(mbar)), "r"(bytes) : "memory");
+}
+/* Wait (bounded) for the phase of the given parity; false if the bound ran
+ * out. Every lane calls it. */
+DEV bool mbar_wait(unsigned long long *mbar, uint32_t parity)
+{
+    const uint32_t a = smem_addr(mbar);
+    for (uint32_t i = 0; i < (1u << 24); i++) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
 }
 
 /* ===========================================================================
@@ -266,11 +355,95 @@ DEV int ew_tile(const gpuos_devdesc *d, uint32_t tile)
     return GPUOS_ST_OK;
 }
 
+/* Element-wise tile through the warp's shared staging buffer: lane 0 issues
+ * one TMA bulk copy per operand and chunk (up to stage_bytes in flight per
+ * warp, no registers held), every lane waits on the warp's mbarrier, then
+ * computes from shared memory and stores 16-byte vectors. Used when every
+ * operand is 16-byte aligned; the ragged tail takes the scalar path. */
+template <int OP, bool BF>
+DEV int ew_tile_staged(const gpuos_devdesc *d, uint32_t tile, uint32_t stage_bytes)
+{
+    constexpr uint32_t VEC = BF ? 8 : 4;
+    constexpr uint32_t ES = BF ? 2 : 4;
+    constexpr uint32_t TILE = 32 * GPUOS_EW_VPT * VEC;
+    constexpr bool BIN = (OP == EW_ADD || OP == EW_MUL);
+    constexpr uint32_t NOPS = BIN ? 2 : 1;
+    const uint32_t lane = lane_id();
+    const uint64_t n = d->dims[0];
+    const uint64_t start = (uint64_t)tile * TILE;
+    if (start >= n) return GPUOS_ST_OK;
+    const uint32_t cnt = (uint32_t)((n - start) < TILE ? (n - start) : TILE);
+    const char *pa = reinterpret_cast<const char *>(d->a) + start * ES;
+    const char *pb = BIN ? reinterpret_cast<const char *>(d->b) + start * ES : pa;
+    char *po = reinterpret_cast<char *>(d->out) + start * ES;
+    const uint32_t nel = cnt / VEC * VEC;                      /* whole 16-byte vectors */
+    const uint32_t chunk = (stage_bytes / NOPS) / 16u * 16u / ES; /* elements per operand */
+    WarpStage *w = warp_stage();
+    unsigned char *sa = warp_stage_buf();
+    unsigned char *sb = sa + chunk * ES;
+    uint32_t phase = w->phase;
+    int32_t st = GPUOS_ST_OK;
+    for (uint32_t c0 = 0; c0 < nel; c0 += chunk) {
+        const uint32_t ce = (nel - c0) < chunk ? (nel - c0) : chunk;
+        const uint32_t bytes = ce * ES;
+        if (lane == 0) {
+            /* earlier generic reads of the buffer before the async writes */
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect(&w->mbar, bytes * NOPS);
+            bulk_g2s(sa, pa + (uint64_t)c0 * ES, bytes, &w->mbar);
+            if (BIN) bulk_g2s(sb, pb + (uint64_t)c0 * ES, bytes, &w->mbar);
+        }
+        if (!mbar_wait(&w->mbar, phase)) {
+            /* the copy did not land within the bound: wait once more (also
+             * bounded) so that no copy is left writing the buffer, then fail */
+            mbar_wait(&w->mbar, phase);
+            st = GPUOS_ST_COPY_TIMEOUT;
+            phase ^= 1u;
+            break;
+        }
+        phase ^= 1u;
+        const uint4 *va = reinterpret_cast<const uint4 *>(sa);
+        const uint4 *vb = reinterpret_cast<const uint4 *>(sb);
+        uint4 *vo = reinterpret_cast<uint4 *>(po + (uint64_t)c0 * ES);
+        const uint32_t nv = bytes / 16u;
+#pragma unroll 4
+        for (uint32_t v = lane; v < nv; v += 32) {
+            const uint4 x = va[v];
+            __stcg(vo + v, ew_vec<OP, BF>(x, BIN ? vb[v] : x));
+        }
+        __syncwarp();
+    }
+    if (lane == 0) w->phase = phase;
+    __syncwarp();
+    for (uint32_t i = nel + lane; i < cnt; i += 32) {
+        if (BF) {
+            const uint16_t *a16 = reinterpret_cast<const uint16_t *>(pa);
+            const uint16_t *b16 = reinterpret_cast<const uint16_t *>(pb);
+            reinterpret_cast<uint16_t *>(po)[i] = to_bf(ew1<OP>(bf1(a16[i]), bf1(b16[i])));
+        } else {
+            const float *a32 = reinterpret_cast<const float *>(pa);
+            const float *b32 = reinterpret_cast<const float *>(pb);
+            reinterpret_cast<float *>(po)[i] = ew1<OP>(a32[i], b32[i]);
+        }
+    }
+    return st;
+}
+
+template <int OP, bool BF>
+DEV int ew_pick(const gpuos_devdesc *d, uint32_t tile)
+{
+    const uint32_t sbytes = stage_hdr()->stage_bytes;
+    const bool bin = (OP == EW_ADD || OP == EW_MUL);
+    const uint64_t al = d->a | (bin ? d->b : 0) | d->out;
+    if (sbytes >= 2048 && (al & 15u) == 0) return ew_tile_staged<OP, BF>(d, tile, sbytes);
+    return ew_tile<OP, BF>(d, tile);
+}
+
 template <int OP>
 DEV int ew_dispatch(const gpuos_devdesc *d, uint32_t tile)
 {
-    if (d->dtype == GPUOS_BF16) return ew_tile<OP, true>(d, tile);
-    if (d->dtype == GPUOS_F32) return ew_tile<OP, false>(d, tile);
+    if (d->dtype == GPUOS_BF16) return ew_pick<OP, true>(d, tile);
+    if (d->dtype == GPUOS_F32) return ew_pick<OP, false>(d, tile);
     return GPUOS_ST_BAD_ARGS;
 }
 
@@ -792,14 +965,18 @@ __device__ gpuos_op_fn g_builtin_ops[GPUOS_OP_BUILTIN_COUNT] = {
  * Persistent executor
  * ======================================================================== */
 
-/* Work-queue entry word: [63] consumed, [62:40] stamp = (index + 1) mod 2^23,
- * [39:24] ring slot, [23:0] tile. One 64-bit word, so the claimer learns
- * everything with the acquire load that finds the entry published. */
-DEV uint64_t tq_word(uint64_t idx, uint32_t slot, uint32_t tile)
+/* Work-queue entry word: [63:24] stamp = (index + 1) mod 2^40, [23:8] ring
+ * slot, [7:0] helper index (the helper's first tile). One 64-bit word, so the
+ * claimer learns everything with the acquire load that finds it published.
+ * The queue holds more than GPUOS_HELPERS x ring_entries entries, so the
+ * entry a publication overwrites belongs to a ticket at least ring_entries
+ * older, which has completed; completion implies every helper entry of it
+ * was read. No producer-side check is needed. */
+DEV uint64_t tq_word(uint64_t idx, uint32_t slot, uint32_t helper)
 {
-    return (((idx + 1) & GPUOS_TQ_STAMP_MASK) << 40) | ((uint64_t)(slot & 0xFFFFu) << 24) | (tile & 0xFFFFFFu);
+    return (((idx + 1) & GPUOS_TQ_STAMP_MASK) << 24) | ((uint64_t)(slot & 0xFFFFu) << 8) | (helper & 0xFFu);
 }
-DEV bool tq_is(uint64_t w, uint64_t idx) { return ((w >> 40) & GPUOS_TQ_STAMP_MASK) == ((idx + 1) & GPUOS_TQ_STAMP_MASK); }
+DEV bool tq_is(uint64_t w, uint64_t idx) { return (w >> 24) == ((idx + 1) & GPUOS_TQ_STAMP_MASK); }
 
 DEV void fence_acq_rel_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
 
@@ -832,7 +1009,9 @@ DEV void set_exit(const gpuos_exec_params &p, uint32_t reason)
     st_relaxed_sys32(&p.hctl->state, 2u);
 }
 
-/* The sequencer warp: ring -> mirror + work queue. */
+/* The sequencer warp: ring -> mirror + work queue, up to 64 descriptors per
+ * batch (two ring slots per lane: slot s + lane and s + 32 + lane). */
+#define SEQ_SPL 2
 DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
 {
     const uint32_t lane = lane_id();
@@ -841,18 +1020,24 @@ DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
     uint64_t n_seq = 0, n_idle = 0, n_sleep = 0, t_body = 0, t_mirror = 0, t_pubs = 0;
     uint32_t polls = 0;
     uint64_t hb = ld_relaxed_sys(&p.hctl->heartbeat);
-    uint64_t t_active = globaltimer();
-    const uint32_t N = p.ring_mask + 1, Q = p.tq_mask + 1;
+    uint64_t t_active = 0;
+    Elapsed idle;
+    idle.start();
+    const uint32_t N = p.ring_mask + 1;
+    const uint32_t KMAX = N < 32u * SEQ_SPL ? N : 32u * SEQ_SPL;
     if (lane == 0) st_relaxed_sys32(&p.hctl->state, 1u);
 
     while (true) {
-        /* poll 32 consecutive slots, one per lane (relaxed; one fence below) */
-        const uint64_t my_t = s + lane;
-        const uint32_t my_slot = (uint32_t)(my_t & p.ring_mask);
-        const uint64_t seq = ld_relaxed_sys(&p.ring[my_slot].seq);
-        const uint32_t ready = __ballot_sync(0xFFFFFFFFu, seq == my_t + 1);
-        uint32_t k = (ready == 0xFFFFFFFFu) ? 32u : (uint32_t)(__ffs(~ready) - 1);
-        if (k > N) k = N;
+        /* poll 64 consecutive slots, two per lane (relaxed; one fence below) */
+        uint64_t rmask = 0;
+#pragma unroll
+        for (int h = 0; h < SEQ_SPL; h++) {
+            const uint64_t t = s + lane + 32u * h;
+            const uint64_t seq = ld_relaxed_sys(&p.ring[(uint32_t)(t & p.ring_mask)].seq);
+            rmask |= (uint64_t)__ballot_sync(0xFFFFFFFFu, seq == t + 1) << (32 * h);
+        }
+        uint32_t k = (rmask == ~0ull) ? 64u : (uint32_t)(__ffsll((long long)~rmask) - 1);
+        if (k > KMAX) k = KMAX;
         if (k == 0) {
             /* idle: stop flag, exit_after, watchdog */
             n_idle++;
@@ -865,9 +1050,10 @@ DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
                 const uint64_t h2 = ld_relaxed_sys(&p.hctl->heartbeat);
                 if (h2 != hb) {
                     hb = h2;
-                    t_active = now;
+                    idle.start();
                 }
-                if (p.idle_exit_ns && now - t_active > p.idle_exit_ns) reason = 2;
+                if (idle.tick(now) > p.idle_exit_ns && p.idle_exit_ns) reason = 2;
+                t_active = now - idle.acc;
                 reason = __shfl_sync(0xFFFFFFFFu, reason, 0);
                 if (reason) {
                     if (lane == 0) {
@@ -886,27 +1072,40 @@ DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
         polls = 0;
         /* the commits seen above happen-before everything below */
         fence_acq_rel_sys();
-        gpuos_desc dsc;
-        uint4 *dv = reinterpret_cast<uint4 *>(&dsc);
-        if (lane < k) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.ring + my_slot);
+        gpuos_desc dsc[SEQ_SPL];
 #pragma unroll
-            for (int i = 0; i < 8; i++) dv[i] = src[i];
+        for (int h = 0; h < SEQ_SPL; h++) {
+            const uint32_t pos = lane + 32u * h;
+            if (pos < k) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.ring + (uint32_t)((s + pos) & p.ring_mask));
+                uint4 *dv = reinterpret_cast<uint4 *>(&dsc[h]);
+#pragma unroll
+                for (int i = 0; i < 8; i++) dv[i] = src[i];
+            }
         }
         uint32_t version = 0;
         if (lane == 0) version = ld_acquire_gpu32(&p.dctl->version);
         version = __shfl_sync(0xFFFFFFFFu, version, 0);
         /* a FENCE descriptor must start a batch; cut the batch before it */
-        const uint32_t fmask = __ballot_sync(0xFFFFFFFFu, lane < k && (dsc.flags & GPUOS_FLAG_FENCE));
-        const uint32_t later = fmask & ~1u;
-        if (later) k = (uint32_t)(__ffs(later) - 1);
+        uint64_t fmask = 0;
+#pragma unroll
+        for (int h = 0; h < SEQ_SPL; h++) {
+            const uint32_t pos = lane + 32u * h;
+            fmask |= (uint64_t)__ballot_sync(0xFFFFFFFFu, pos < k && (dsc[h].flags & GPUOS_FLAG_FENCE)) << (32 * h);
+        }
+        const uint64_t later = fmask & ~1ull;
+        if (later) {
+            const uint32_t cut = (uint32_t)(__ffsll((long long)later) - 1);
+            if (cut < k) k = cut;
+        }
         uint32_t fence_status = GPUOS_ST_OK;
-        if (fmask & 1u) {
+        if (fmask & 1ull) {
             if (lane == 0) {
-                const uint64_t t0 = globaltimer();
+                Elapsed w;
+                w.start();
                 uint32_t fp = 0;
                 while (*reinterpret_cast<volatile unsigned long long *>(&p.dctl->completed) < s) {
-                    if (globaltimer() - t0 > p.dep_timeout_ns) {
+                    if (w.tick(globaltimer()) > p.dep_timeout_ns) {
                         fence_status = GPUOS_ST_DEP_TIMEOUT;
                         break;
                     }
@@ -919,75 +1118,88 @@ DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
         const uint64_t t_b = globaltimer();
 
         /* validate and mirror */
-        int32_t status = GPUOS_ST_OK;
-        uint32_t nt = 0;
-        if (lane < k) {
-            if (dsc.ticket != my_t) status = GPUOS_ST_BAD_DESC;
-            else if (dsc.op_id >= GPUOS_MAX_OPS) status = GPUOS_ST_BAD_OP;
-            else if (dsc.ntiles == 0 || dsc.ntiles > GPUOS_TILE_MAX) status = GPUOS_ST_BAD_ARGS;
-            if (lane == 0 && fence_status) status = (int32_t)fence_status;
-            if (status == GPUOS_ST_OK) {
-                /* one work-queue entry per helper warp (at most GPUOS_HELPERS);
-                 * helper h starts with tile h and takes later tiles from the
-                 * descriptor's tile counter */
-                nt = dsc.ntiles < GPUOS_HELPERS ? dsc.ntiles : GPUOS_HELPERS;
-                dsc.user = t_obs;                        /* -> t_dispatch */
-                dsc.seq = (uint64_t)version;             /* -> version, pad */
-                uint4 *mv = reinterpret_cast<uint4 *>(p.mirror + my_slot);
+        int32_t status[SEQ_SPL];
+        uint32_t nt[SEQ_SPL];
 #pragma unroll
-                for (int i = 0; i < 8; i++) __stcg(mv + i, dv[i]);
+        for (int h = 0; h < SEQ_SPL; h++) {
+            const uint32_t pos = lane + 32u * h;
+            const uint64_t my_t = s + pos;
+            status[h] = GPUOS_ST_OK;
+            nt[h] = 0;
+            if (pos < k) {
+                if (dsc[h].ticket != my_t) status[h] = GPUOS_ST_BAD_DESC;
+                else if (dsc[h].op_id >= GPUOS_MAX_OPS) status[h] = GPUOS_ST_BAD_OP;
+                else if (dsc[h].ntiles == 0 || dsc[h].ntiles > GPUOS_TILE_MAX) status[h] = GPUOS_ST_BAD_ARGS;
+                if (pos == 0 && fence_status) status[h] = (int32_t)fence_status;
+                if (status[h] == GPUOS_ST_OK) {
+                    /* one work-queue entry per helper warp (at most GPUOS_HELPERS);
+                     * helper i starts with tile i and takes later tiles from the
+                     * descriptor's tile counter */
+                    nt[h] = dsc[h].ntiles < GPUOS_HELPERS ? dsc[h].ntiles : GPUOS_HELPERS;
+                    dsc[h].user = t_obs;               /* -> t_dispatch */
+                    dsc[h].seq = (uint64_t)version;    /* -> version, pad */
+                    uint4 *mv = reinterpret_cast<uint4 *>(p.mirror + (uint32_t)(my_t & p.ring_mask));
+                    const uint4 *dv = reinterpret_cast<const uint4 *>(&dsc[h]);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) __stcg(mv + i, dv[i]);
+                }
             }
         }
         /* every lane's mirror writes happen-before every lane's fence */
         __syncwarp();
         __threadfence();
         const uint64_t t_m = globaltimer();
-        /* exclusive prefix of tile counts -> work-queue ranges */
-        uint32_t incl = nt;
+        /* exclusive prefix of entry counts in ticket order -> queue ranges */
+        uint32_t excl[SEQ_SPL];
+        uint32_t base = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= (uint32_t)o) incl += v;
+        for (int h = 0; h < SEQ_SPL; h++) {
+            uint32_t incl = nt[h];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= (uint32_t)o) incl += v;
+            }
+            excl[h] = base + incl - nt[h];
+            base += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
-        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-        const uint32_t excl = incl - nt;
-        /* entries j = 0 .. total-1 of the batch, spread over the lanes; the
-         * descriptor owning j is the last lane whose range starts at or
-         * before it (a 5-step search over the exclusive prefix) */
+        const uint32_t total = base;
+        const uint32_t total0 = __shfl_sync(0xFFFFFFFFu, excl[SEQ_SPL - 1], 0); /* start of second half */
+        /* entries j = 0 .. total-1 spread over the lanes; the owner of j is the
+         * last position whose range starts at or before it (a 5-step search
+         * inside the half that holds j) */
         for (uint32_t j0 = 0; j0 < total; j0 += 32) {
             const uint32_t j = j0 + lane;
+            const bool second = j >= total0;
             uint32_t i = 0;
 #pragma unroll
             for (int step = 16; step > 0; step >>= 1) {
                 const uint32_t cand = i + (uint32_t)step; /* <= 31 */
-                if (__shfl_sync(0xFFFFFFFFu, excl, cand) <= j) i = cand;
+                const uint32_t st0 = __shfl_sync(0xFFFFFFFFu, excl[0], cand);
+                const uint32_t st1 = __shfl_sync(0xFFFFFFFFu, excl[1], cand);
+                if ((second ? st1 : st0) <= j) i = cand;
             }
-            const uint32_t bi = __shfl_sync(0xFFFFFFFFu, excl, i);
-            const uint32_t sloti = (uint32_t)((s + i) & p.ring_mask);
+            /* both shuffles on every lane (a shuffle must not diverge) */
+            const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, excl[0], i);
+            const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, excl[1], i);
+            const uint32_t bi = second ? b1 : b0;
+            const uint32_t pos = i + (second ? 32u : 0u);
             if (j < total) {
-                const uint32_t t = j - bi;
                 const uint64_t idx = e + j;
-                unsigned long long *ent = p.tq + (idx & p.tq_mask);
-                if (idx >= Q) {
-                    /* the previous lap's entry must have been read by its claimer */
-                    uint32_t wp = 0;
-                    const uint64_t tw = globaltimer();
-                    while (true) {
-                        const uint64_t w = *reinterpret_cast<volatile unsigned long long *>(ent);
-                        if ((w & GPUOS_TQ_CONSUMED) && tq_is(w, idx - Q)) break;
-                        if (globaltimer() - tw > p.dep_timeout_ns) break; /* cannot happen: claims progress */
-                        backoff(wp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
-                    }
-                }
-                *reinterpret_cast<volatile unsigned long long *>(ent) = tq_word(idx, sloti, t);
+                *reinterpret_cast<volatile unsigned long long *>(p.tq + (idx & p.tq_mask)) =
+                    tq_word(idx, (uint32_t)((s + pos) & p.ring_mask), j - bi);
             }
         }
         const uint64_t t_pub = globaltimer();
-        if (lane < k && status == GPUOS_ST_OK)
-            *reinterpret_cast<volatile uint64_t *>(p.t_pub + my_slot) = t_pub;
-        /* descriptors that failed validation complete at once */
-        if (lane < k && status != GPUOS_ST_OK)
-            complete_desc(p, my_t, my_slot, status, version, t_obs);
+#pragma unroll
+        for (int h = 0; h < SEQ_SPL; h++) {
+            const uint32_t pos = lane + 32u * h;
+            const uint64_t my_t = s + pos;
+            const uint32_t slot = (uint32_t)(my_t & p.ring_mask);
+            if (pos < k && status[h] == GPUOS_ST_OK) *reinterpret_cast<volatile uint64_t *>(p.t_pub + slot) = t_pub;
+            /* descriptors that failed validation complete at once */
+            if (pos < k && status[h] != GPUOS_ST_OK) complete_desc(p, my_t, slot, status[h], version, t_obs);
+        }
         e += total;
         s += k;
         n_seq += k;
@@ -1003,7 +1215,7 @@ DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
             ws[GPUOS_WS_T_MIRROR] = t_mirror;
             ws[GPUOS_WS_T_PUB] = t_pubs;
         }
-        t_active = t_obs;
+        idle.start();
     }
     if (lane == 0) {
         ws[GPUOS_WS_SEQ] = n_seq;
@@ -1030,7 +1242,7 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         if (lane == 0) {
             while (true) {
                 w = ld_acquire_gpu(reinterpret_cast<const uint64_t *>(ent));
-                if (tq_is(w, e) && !(w & GPUOS_TQ_CONSUMED)) break;
+                if (tq_is(w, e)) break;
                 n_idle++;
                 if ((polls & 15u) == 0 && ld_relaxed_gpu32(&p.dctl->exit_flag)) {
                     leave = 1;
@@ -1038,15 +1250,14 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
                 }
                 backoff(polls, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
             }
-            if (!leave) *reinterpret_cast<volatile unsigned long long *>(ent) = w | GPUOS_TQ_CONSUMED;
         }
         leave = __shfl_sync(0xFFFFFFFFu, leave, 0);
         if (leave) break;
         w = __shfl_sync(0xFFFFFFFFu, w, 0);
         unsigned long long e_next = 0;
         if (lane == 0) e_next = atomicAdd(&p.dctl->tq_claim, 1ull); /* overlaps the tile */
-        const uint32_t slot = (uint32_t)((w >> 24) & 0xFFFFu);
-        uint32_t tile = (uint32_t)(w & 0xFFFFFFu); /* helper index = its first tile */
+        const uint32_t slot = (uint32_t)((w >> 8) & 0xFFFFu);
+        uint32_t tile = (uint32_t)(w & 0xFFu); /* helper index = its first tile */
         /* descriptor -> shared memory */
         reinterpret_cast<uint32_t *>(sd)[lane] = __ldcg(reinterpret_cast<const uint32_t *>(p.mirror + slot) + lane);
         __syncwarp();
@@ -1067,10 +1278,11 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
                 const uint64_t *stamp = p.done_dev + ((dep - 1) & p.ring_mask);
                 if (ld_acquire_gpu(stamp) >= dep) continue;
                 n_depw++;
-                const uint64_t t0 = globaltimer();
+                Elapsed w;
+                w.start();
                 uint32_t dp = 0;
                 while (ld_acquire_gpu(stamp) < dep) {
-                    if (globaltimer() - t0 > p.dep_timeout_ns) {
+                    if (w.tick(globaltimer()) > p.dep_timeout_ns) {
                         dstatus = GPUOS_ST_DEP_TIMEOUT;
                         break;
                     }
@@ -1087,44 +1299,47 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         __syncwarp();
         const gpuos_op_fn fn = reinterpret_cast<gpuos_op_fn>(__ldcg(
             reinterpret_cast<const unsigned long long *>(p.table) + (sd->version & 1u) * GPUOS_MAX_OPS + sd->op_id));
+        /* the helper's tiles: its first tile, then tiles from the descriptor's
+         * counter. Each next tile is claimed before the current one runs
+         * (the claim's latency overlaps the work), and the helper counts its
+         * tiles done only after its last claim: the descriptor cannot
+         * complete (and its counters be recycled) while a helper may still
+         * claim. */
+        int32_t status = dstatus;
+        uint32_t count = 0;
         while (true) {
-            /* claim the helper's next tile before this one is counted: the
-             * descriptor cannot complete (and its counters be recycled)
-             * while this warp still holds an uncounted tile */
             uint32_t next = ntiles;
             if (ntiles > helpers && lane == 0) next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
-            int32_t status = dstatus;
             if (status == GPUOS_ST_OK) {
                 if (fn == nullptr) status = GPUOS_ST_BAD_OP;
                 else status = fn(sd, tile);
             }
-            __syncwarp();
-            if (lane == 0) {
-                if (ntiles == 1) {
-                    /* sole tile: no counter round trip; the warp barrier above
-                     * orders every lane's writes before the completion releases */
-                    complete_desc(p, ticket, slot, status, sd->version, sd->t_dispatch);
-                } else {
-                    if (status) atomicCAS(p.err + slot, 0u, (uint32_t)status);
-                    __threadfence();
-                    const uint32_t old = atomicAdd(p.tiles_done + slot, 1u);
-                    if (old + 1 == ntiles) {
-                        __threadfence();
-                        const uint32_t st = ld_relaxed_gpu32(p.err + slot);
-                        complete_desc(p, ticket, slot, (int32_t)st, sd->version, sd->t_dispatch);
-                    }
-                }
-                n_tiles++;
-                if ((n_tiles & 63u) == 0) {
-                    ws[GPUOS_WS_TILES] = n_tiles;
-                    ws[GPUOS_WS_IDLE] = n_idle;
-                    ws[GPUOS_WS_SLEEPS] = n_sleep;
-                    ws[GPUOS_WS_DEPWAIT] = n_depw;
-                }
-            }
+            count++;
             next = __shfl_sync(0xFFFFFFFFu, next, 0);
             if (next >= ntiles) break;
             tile = next;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            if (ntiles == 1) {
+                /* sole tile: no counter round trip; the warp barrier above
+                 * orders every lane's writes before the completion releases */
+                complete_desc(p, ticket, slot, status, sd->version, sd->t_dispatch);
+            } else {
+                if (status) atomicCAS(p.err + slot, 0u, (uint32_t)status);
+                __threadfence();
+                const uint32_t old = atomicAdd(p.tiles_done + slot, count);
+                if (old + count == ntiles) {
+                    __threadfence();
+                    const uint32_t st = ld_relaxed_gpu32(p.err + slot);
+                    complete_desc(p, ticket, slot, (int32_t)st, sd->version, sd->t_dispatch);
+                }
+            }
+            n_tiles += count;
+            ws[GPUOS_WS_TILES] = n_tiles;
+            ws[GPUOS_WS_IDLE] = n_idle;
+            ws[GPUOS_WS_SLEEPS] = n_sleep;
+            ws[GPUOS_WS_DEPWAIT] = n_depw;
         }
         e = __shfl_sync(0xFFFFFFFFu, e_next, 0);
         __syncwarp();
@@ -1140,6 +1355,7 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
 extern "C" __global__ void __launch_bounds__(GPUOS_MAX_WPB * 32, 1) gpuos_executor_kernel(gpuos_exec_params p)
 {
     __shared__ __align__(16) gpuos_devdesc sdesc[GPUOS_MAX_WPB];
+    stage_init(p.stage_bytes);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
     if (blockIdx.x == 0 && warp == 0) sequencer(p, gw);
@@ -1172,9 +1388,10 @@ DEV int builtin_call(const gpuos_devdesc *d, uint32_t t)
 }
 
 #define EAGER_WPB 1
-extern "C" __global__ void __launch_bounds__(EAGER_WPB * 32) gpuos_eager_kernel(gpuos_devdesc d)
+extern "C" __global__ void __launch_bounds__(EAGER_WPB * 32) gpuos_eager_kernel(gpuos_devdesc d, uint32_t stage_bytes)
 {
     __shared__ __align__(16) gpuos_devdesc sd[EAGER_WPB];
+    stage_init(stage_bytes);
     const uint32_t warp = threadIdx.x >> 5;
     reinterpret_cast<uint32_t *>(&sd[warp])[lane_id()] = reinterpret_cast<const uint32_t *>(&d)[lane_id()];
     __syncwarp();
@@ -1185,9 +1402,15 @@ extern "C" __global__ void __launch_bounds__(EAGER_WPB * 32) gpuos_eager_kernel(
 /* ===========================================================================
  * Host-side launch helpers
  * ======================================================================== */
+extern "C" uint32_t gpuos_dev_dyn_smem(uint32_t wpb, uint32_t stage_bytes) { return 16u + wpb * (16u + stage_bytes); }
+
 extern "C" int gpuos_dev_launch_executor(const gpuos_exec_params *p, uint32_t blocks, uint32_t wpb, void *stream)
 {
-    gpuos_executor_kernel<<<blocks, wpb * 32, 0, (cudaStream_t)stream>>>(*p);
+    const uint32_t dyn = gpuos_dev_dyn_smem(wpb, p->stage_bytes);
+    if (cudaFuncSetAttribute(gpuos_executor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) !=
+        cudaSuccess)
+        return -1;
+    gpuos_executor_kernel<<<blocks, wpb * 32, dyn, (cudaStream_t)stream>>>(*p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -1214,13 +1437,21 @@ extern "C" int gpuos_dev_preload(void)
     return 0;
 }
 
-extern "C" int gpuos_dev_eager_launch(const gpuos_desc *d, uint32_t ntiles, void *stream)
+extern "C" int gpuos_dev_eager_launch(const gpuos_desc *d, uint32_t ntiles, uint32_t stage_bytes, void *stream)
 {
     gpuos_devdesc dd;
     static_assert(sizeof(dd) == sizeof(*d), "layout");
     memcpy(&dd, d, sizeof(dd));
     dd.ntiles = ntiles;
     const uint32_t grid = (ntiles + EAGER_WPB - 1) / EAGER_WPB;
-    gpuos_eager_kernel<<<grid, EAGER_WPB * 32, 0, (cudaStream_t)stream>>>(dd);
+    const uint32_t dyn = gpuos_dev_dyn_smem(EAGER_WPB, stage_bytes);
+    static uint32_t attr_set = 0;
+    if (dyn > attr_set) {
+        if (cudaFuncSetAttribute(gpuos_eager_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) !=
+            cudaSuccess)
+            return -1;
+        attr_set = dyn;
+    }
+    gpuos_eager_kernel<<<grid, EAGER_WPB * 32, dyn, (cudaStream_t)stream>>>(dd, stage_bytes);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

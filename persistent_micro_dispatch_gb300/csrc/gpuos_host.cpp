@@ -167,6 +167,7 @@ const char *gpuos_strerror(int code, int is_status)
         case GPUOS_ST_DEP_TIMEOUT: return "dependency or fence wait timed out";
         case GPUOS_ST_ABORTED: return "executor was leaving";
         case GPUOS_ST_BAD_DESC: return "ring slot did not hold the expected ticket";
+        case GPUOS_ST_COPY_TIMEOUT: return "a staging copy did not complete within its bound";
         default: return "unknown device status";
         }
     }
@@ -188,7 +189,7 @@ void gpuos_default_config(gpuos_config *c)
 {
     memset(c, 0, sizeof(*c));
     c->ring_entries = 4096;
-    c->warps_per_block = 8;
+    c->warps_per_block = 12;
     c->blocks = 0;
     c->backoff_min_ns = 32;
     c->backoff_max_ns = 256;
@@ -198,7 +199,8 @@ void gpuos_default_config(gpuos_config *c)
     c->ring_in_device_mem = 0;
     c->device = 0;
     c->exit_after = 0;
-    c->tq_entries = 65536;
+    c->tq_entries = 0; /* sized from ring_entries */
+    c->stage_bytes = 16384;
 }
 
 size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, uint32_t Lmax)
@@ -333,8 +335,14 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     else gpuos_default_config(&cfg);
     if (!is_pow2(cfg.ring_entries) || cfg.ring_entries < 64 || cfg.ring_entries > 65536) return GPUOS_EINVAL;
     if (cfg.warps_per_block < 2 || cfg.warps_per_block > GPUOS_MAX_WPB) return GPUOS_EINVAL;
-    if (!is_pow2(cfg.tq_entries) || cfg.tq_entries < 1024 || cfg.tq_entries > GPUOS_TQ_MAX) return GPUOS_EINVAL;
+    /* the work queue must hold more than GPUOS_HELPERS entries per ring slot
+     * (0 = the smallest such power of two) */
+    if (cfg.tq_entries == 0 && cfg.ring_entries <= 65536) cfg.tq_entries = 2u * GPUOS_HELPERS * cfg.ring_entries;
+    if (!is_pow2(cfg.tq_entries) || cfg.tq_entries > GPUOS_TQ_MAX ||
+        (uint64_t)cfg.tq_entries <= (uint64_t)GPUOS_HELPERS * cfg.ring_entries)
+        return GPUOS_EINVAL;
     if (cfg.backoff_min_ns == 0 || cfg.backoff_max_ns < cfg.backoff_min_ns) return GPUOS_EINVAL;
+    if ((cfg.stage_bytes & 1023u) || cfg.stage_bytes > 24576u) return GPUOS_EINVAL;
 
     gpuos_ctx *c = new (std::nothrow) gpuos_ctx();
     if (!c) return GPUOS_ENOMEM;
@@ -460,6 +468,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     p.backoff_min_ns = cfg.backoff_min_ns;
     p.backoff_max_ns = cfg.backoff_max_ns;
     p.spin_polls = cfg.spin_polls;
+    p.stage_bytes = cfg.stage_bytes;
     p.idle_exit_ns = (uint64_t)cfg.idle_exit_ms * 1000000ull;
     p.dep_timeout_ns = (uint64_t)(cfg.dep_timeout_ms ? cfg.dep_timeout_ms : 5000) * 1000000ull;
     p.exit_after = cfg.exit_after;
@@ -944,15 +953,16 @@ int gpuos_shutdown(gpuos_ctx *c, uint32_t timeout_ms)
     return rc;
 }
 
-int gpuos_eager_run(const gpuos_desc *d, uint32_t count, void *stream)
+int gpuos_eager_run(const gpuos_desc *d, uint32_t count, uint32_t stage_bytes, void *stream)
 {
     if (!d && count) return GPUOS_EINVAL;
+    if ((stage_bytes & 1023u) || stage_bytes > 24576u) return GPUOS_EINVAL;
     for (uint32_t i = 0; i < count; i++) {
         uint32_t nt = 0;
         if (d[i].op_id >= GPUOS_OP_BUILTIN_COUNT) return GPUOS_EINVAL;
         const int rc = validate_and_tile(d + i, &nt, false);
         if (rc) return rc;
-        if (gpuos_dev_eager_launch(d + i, nt, stream) != 0) return GPUOS_ECUDA;
+        if (gpuos_dev_eager_launch(d + i, nt, stage_bytes, stream) != 0) return GPUOS_ECUDA;
     }
     return GPUOS_OK;
 }

@@ -10,19 +10,17 @@
 #include "gpuos.h"
 
 /* Tiling constants of the built-in ops (one tile = one warp's unit of work). */
-#define GPUOS_EW_VPT 16                   /* 16-byte vectors per lane per element-wise tile */
-#define GPUOS_EW_TILE_F32 (32 * GPUOS_EW_VPT * 4)  /* 2048 fp32 elements */
-#define GPUOS_EW_TILE_BF16 (32 * GPUOS_EW_VPT * 8) /* 4096 bf16 elements */
+#define GPUOS_EW_VPT 32                   /* 16-byte vectors per lane per element-wise tile */
+#define GPUOS_EW_TILE_F32 (32 * GPUOS_EW_VPT * 4)  /* 4096 fp32 elements */
+#define GPUOS_EW_TILE_BF16 (32 * GPUOS_EW_VPT * 8) /* 8192 bf16 elements */
 #define GPUOS_SDPA_CHUNK 512              /* key rows per decode-attention tile */
 #define GPUOS_VM_COLS 32                  /* output columns per vecmat tile */
 #define GPUOS_ROW_REG_MAX 4096            /* rows up to this width stay in registers */
 #define GPUOS_MAX_WPB 16
 #define GPUOS_TILE_MAX (1u << 30)          /* tiles per descriptor */
 #define GPUOS_HELPERS 64                   /* work-queue entries (helper warps) per descriptor at most */
-#define GPUOS_TQ_MAX (1u << 20)            /* work-queue entries (23-bit stamps stay unambiguous) */
-
-#define GPUOS_TQ_CONSUMED (1ull << 63)
-#define GPUOS_TQ_STAMP_MASK 0x7FFFFFull
+#define GPUOS_TQ_MAX (1u << 30)            /* work-queue entries */
+#define GPUOS_TQ_STAMP_MASK 0xFFFFFFFFFFull /* 40-bit stamps */
 
 /* Mirror of a descriptor in device memory, written by the sequencer warp.
  * Same layout as gpuos_desc except the last fields. */
@@ -43,7 +41,7 @@ typedef struct gpuos_devdesc {
 } gpuos_devdesc;
 
 /* Work-queue entries are single 64-bit words (see tq_word in the device
- * code): consumed flag, 23-bit stamp, 16-bit ring slot, 24-bit tile. */
+ * code): 40-bit stamp, 16-bit ring slot, 8-bit helper index. */
 
 /* Completion record in host-visible memory, written by the device. */
 typedef struct gpuos_rec_dev {
@@ -103,7 +101,7 @@ typedef struct gpuos_exec_params {
     gpuos_op_fn *table;      /* [2][GPUOS_MAX_OPS] */
     uint64_t *warp_stats;    /* [total warps][GPUOS_WS_N] */
     uint32_t ring_mask, tq_mask;
-    uint32_t backoff_min_ns, backoff_max_ns, spin_polls, pad;
+    uint32_t backoff_min_ns, backoff_max_ns, spin_polls, stage_bytes;
     uint64_t idle_exit_ns, dep_timeout_ns, exit_after;
 } gpuos_exec_params;
 
@@ -120,7 +118,8 @@ extern "C" {
 int gpuos_dev_launch_executor(const gpuos_exec_params *p, uint32_t blocks, uint32_t wpb, void *stream);
 int gpuos_dev_builtin_table(gpuos_op_fn *host_out, uint32_t n);
 int gpuos_dev_executor_attrs(uint32_t *regs, uint32_t *smem);
-int gpuos_dev_eager_launch(const gpuos_desc *d, uint32_t ntiles, void *stream);
+int gpuos_dev_eager_launch(const gpuos_desc *d, uint32_t ntiles, uint32_t stage_bytes, void *stream);
+uint32_t gpuos_dev_dyn_smem(uint32_t wpb, uint32_t stage_bytes);
 int gpuos_dev_preload(void);
 #ifdef __cplusplus
 }

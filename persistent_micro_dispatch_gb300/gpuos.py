@@ -18,7 +18,7 @@ EXT_CUBIN = os.path.join(HERE, "gpuos_ext_ops.cubin")
 
 # ---- constants (mirror include/gpuos.h) --------------------------------------------
 OK, EINVAL, EAGAIN, ETIMEDOUT, EDEVICE, ECUDA, ESTOPPED, ENOMEM, EBUSY = 0, -1, -2, -3, -4, -5, -6, -7, -8
-ST_OK, ST_BAD_OP, ST_BAD_ARGS, ST_DEP_TIMEOUT, ST_ABORTED, ST_BAD_DESC = 0, 1, 2, 3, 4, 5
+ST_OK, ST_BAD_OP, ST_BAD_ARGS, ST_DEP_TIMEOUT, ST_ABORTED, ST_BAD_DESC, ST_COPY_TIMEOUT = 0, 1, 2, 3, 4, 5, 6
 OP = dict(nop=0, add=1, mul=2, relu=3, gelu=4, softmax=5, layernorm=6, rowsum=7, rowmax=8, rowmin=9,
           rope=10, kv_write=11, sdpa=12, vecmat=13)
 OP_USER_FIRST = 64
@@ -51,7 +51,8 @@ class Config(C.Structure):
                 ("backoff_min_ns", C.c_uint32), ("backoff_max_ns", C.c_uint32), ("spin_polls", C.c_uint32),
                 ("idle_exit_ms", C.c_uint32), ("dep_timeout_ms", C.c_uint32),
                 ("ring_in_device_mem", C.c_uint32), ("device", C.c_int32), ("exit_after", C.c_uint64),
-                ("tq_entries", C.c_uint32), ("deferred_start", C.c_uint32), ("reserved", C.c_uint32 * 4)]
+                ("tq_entries", C.c_uint32), ("deferred_start", C.c_uint32), ("stage_bytes", C.c_uint32),
+                ("reserved", C.c_uint32 * 3)]
 
 
 class Record(C.Structure):
@@ -96,7 +97,7 @@ API = {
     "gpuos_executor_stream": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p)]),
     "gpuos_op_ntiles": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint32)]),
     "gpuos_sdpa_workspace_bytes": (C.c_size_t, [C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint32]),
-    "gpuos_eager_run": (C.c_int, [C.c_void_p, C.c_uint32, C.c_void_p]),
+    "gpuos_eager_run": (C.c_int, [C.c_void_p, C.c_uint32, C.c_uint32, C.c_void_p]),
     "gpuos_host_now_ns": (C.c_uint64, []),
     "gpuos_strerror": (C.c_char_p, [C.c_int, C.c_int]),
 }
@@ -157,10 +158,11 @@ def host_now_ns() -> int:
     return int(lib().gpuos_host_now_ns())
 
 
-def eager_run(descs: np.ndarray, stream_ptr: int = 0) -> None:
+def eager_run(descs: np.ndarray, stream_ptr: int = 0, stage_bytes: int = 16384) -> None:
     """Launch each descriptor as its own kernel on ``stream_ptr`` (cudaStream_t)."""
     descs = np.ascontiguousarray(descs, dtype=DESC_DTYPE)
-    check(lib().gpuos_eager_run(descs.ctypes.data, len(descs), C.c_void_p(stream_ptr)), "gpuos_eager_run")
+    check(lib().gpuos_eager_run(descs.ctypes.data, len(descs), stage_bytes, C.c_void_p(stream_ptr)),
+          "gpuos_eager_run")
 
 
 def make_descs(n: int) -> np.ndarray:

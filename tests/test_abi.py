@@ -55,7 +55,7 @@ def test_descriptor_layout_matches_header(G):
 
 def test_default_config(G):
     c = G.default_config()
-    assert c.ring_entries == 4096 and c.warps_per_block == 8 and c.tq_entries == 65536
+    assert c.ring_entries == 4096 and c.warps_per_block == 12 and c.tq_entries == 0
     assert c.idle_exit_ms > 0 and c.dep_timeout_ms > 0
 
 
@@ -71,9 +71,9 @@ def _desc(G, op, dtype=1, dims=(), ptr=0x1000, **kw):
 
 
 def test_tiling_rule(G):
-    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 2          # 2048 fp32 per tile
-    assert G.op_ntiles(_desc(G, "add", 1, (4096,))) == 1          # 4096 bf16 per tile
-    assert G.op_ntiles(_desc(G, "relu", 0, (4097,))) == 3
+    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 1          # 4096 fp32 per tile
+    assert G.op_ntiles(_desc(G, "add", 1, (16384,))) == 2         # 8192 bf16 per tile
+    assert G.op_ntiles(_desc(G, "relu", 0, (8193,))) == 3
     assert G.op_ntiles(_desc(G, "gelu", 0, (0,))) == 1            # empty op: one tile
     assert G.op_ntiles(_desc(G, "softmax", 1, (37, 1024))) == 37  # one row per tile
     assert G.op_ntiles(_desc(G, "rope", 1, (5, 32, 128))) == 5
@@ -130,6 +130,7 @@ def test_init_without_gpu_fails_cleanly(G):
 def test_init_rejects_bad_config(G):
     ctx = C.c_void_p()
     for kw in (dict(ring_entries=100), dict(ring_entries=32), dict(warps_per_block=1),
-               dict(warps_per_block=17), dict(tq_entries=1000), dict(tq_entries=1 << 21), dict(backoff_min_ns=0)):
+               dict(warps_per_block=17), dict(tq_entries=1000), dict(tq_entries=1 << 18), dict(backoff_min_ns=0),
+               dict(stage_bytes=1000), dict(stage_bytes=32768)):
         cfg = G.default_config(**kw)
         assert G.lib().gpuos_init(C.byref(cfg), C.byref(ctx)) == G.EINVAL, kw

@@ -53,14 +53,19 @@ def test_c1_smallest_stream_bit_exact():
     check_canaries(s, ds)
 
 
-def test_c2_variable_elementwise_small():
-    """3,000 descriptors over {add, mul, ReLU, GELU} x {fp32, bf16}, 30 % chained."""
-    s, ds, rep, st, hist = _run_and_compare(S.stream_c2(n_desc=3000, pool_elems=1 << 22))
+@pytest.mark.parametrize("stage_bytes", [16384, 0])
+def test_c2_variable_elementwise_small(stage_bytes):
+    """3,000 descriptors over {add, mul, ReLU, GELU} x {fp32, bf16}, 30 % chained,
+    with shared-memory (TMA bulk copy) staging and with the register path."""
+    s, ds, rep, st, hist = _run_and_compare(S.stream_c2(n_desc=3000, pool_elems=1 << 22),
+                                            cfg=dict(stage_bytes=stage_bytes))
     check_canaries(s, ds)
 
 
-def test_c2l_large_ops_small():
-    s, ds, rep, st, hist = _run_and_compare(S.stream_c2l(n_desc=40, pool_elems=1 << 23))
+@pytest.mark.parametrize("stage_bytes", [16384, 0])
+def test_c2l_large_ops_small(stage_bytes):
+    s, ds, rep, st, hist = _run_and_compare(S.stream_c2l(n_desc=40, pool_elems=1 << 23),
+                                            cfg=dict(stage_bytes=stage_bytes))
     check_canaries(s, ds)
 
 

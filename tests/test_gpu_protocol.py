@@ -377,7 +377,7 @@ def test_eager_path_matches_executor_bitwise():
     finally:
         ex.shutdown()
     st = torch.cuda.Stream()
-    g.eager_run(ds2.descs(), st.cuda_stream)
+    g.eager_run(ds2.descs(), st.cuda_stream, stage_bytes=16384)
     st.synchronize()
     for i, b in enumerate(s.buffers):
         if b.name in ("sdpa_ws",):
