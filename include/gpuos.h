@@ -245,27 +245,32 @@ GPUOS_API int gpuos_query(gpuos_ctx *ctx, uint64_t ticket, gpuos_record *rec);
  * in caller memory (host), for latency statistics. buf may be NULL to stop. */
 GPUOS_API int gpuos_set_history(gpuos_ctx *ctx, gpuos_record *buf, uint64_t base, uint64_t capacity);
 
-/* Load a precompiled sm_103a cubin image into the context (driver API; the
- * bytes are copied). On this driver a module load waits for the device to go
- * idle, which a resident executor never does, so loading is allowed only
- * while the executor is not resident: before gpuos_start (deferred_start) or
- * after gpuos_stop. Loading an image already loaded is a no-op. Modules stay
- * loaded until gpuos_shutdown. Errors: EINVAL (not a loadable image), EBUSY
- * (executor resident), ECUDA. */
+/* Add an operator module: a relocatable sm_103a cubin (nvcc -cubin
+ * -rdc=true; the bytes are copied) that defines device functions with the op
+ * signature and `__device__` variables holding their addresses. At
+ * gpuos_start the library links every added module with its relocatable
+ * executor build (driver JIT linker) and launches the executor from the
+ * linked module: a device-function pointer is only callable inside the module
+ * that holds its code, and on this driver a module load waits for the device
+ * to go idle, which a resident executor never does. So modules are added
+ * before gpuos_start (deferred_start); adding an image already added is a
+ * no-op. Errors: EINVAL (does not link), EBUSY (executor already launched),
+ * ECUDA. */
 GPUOS_API int gpuos_load_module(gpuos_ctx *ctx, const void *image, size_t len);
 
 /* Runtime operator injection (§3 Q2 "3. Dynamic Operator Table", steps 3-5):
- * find the loaded module holding `image` (gpuos_load_module; loaded here if
- * the executor is not resident), read its `__device__` variable
- * `fnptr_symbol` holding the address of a device function with the op
- * signature, write it into the inactive table slot (a copy of the active one
- * with entry op_id replaced), then flip the version with a store-release.
- * Nothing stops: descriptors sequenced before the flip finish with the old
- * entry; later ones use the new one. Before a later flip reuses that slot the
- * call waits until every descriptor sequenced under the older version has
- * completed. The function must use at most the executor's registers per
- * thread (compile it with the same -maxrregcount). Errors: EINVAL, EBUSY
- * (image not loaded and executor resident), ECUDA, ETIMEDOUT. */
+ * for a module added with gpuos_load_module (and so linked into the running
+ * executor), read its `__device__` variable `fnptr_symbol` holding the
+ * address of a device function with the op signature, write it into the
+ * inactive table slot (a copy of the active one with entry op_id replaced),
+ * then flip the version with a store-release. Nothing stops: descriptors
+ * sequenced before the flip finish with the old entry; later ones use the new
+ * one. Before a later flip reuses that slot the call waits until every
+ * descriptor sequenced under the older version has completed. The function
+ * must use at most the executor's registers per thread (compile it with the
+ * same -maxrregcount). Errors: EINVAL (bad id or symbol, image does not
+ * link), EBUSY (image not added before the launch, or executor not yet
+ * launched), ECUDA, ETIMEDOUT. */
 GPUOS_API int gpuos_register_op(gpuos_ctx *ctx, uint16_t op_id, const void *image, size_t len,
                       const char *fnptr_symbol);
 

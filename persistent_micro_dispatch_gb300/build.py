@@ -21,6 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgpuos.so")
 EXT_CUBIN = os.path.join(HERE, "gpuos_ext_ops.cubin")
+# relocatable build of the executor: op modules are linked with it at run time
+EXEC_RDC = os.path.join(HERE, "gpuos_exec_rdc.cubin")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc")
@@ -74,19 +76,29 @@ def build(force: bool = False) -> str:
                 log = os.path.join(BUILD, src.replace(".cu", ".ptxas.txt"))
             jobs.append((cmd, log))
     ext_src = os.path.join(CSRC, "gpuos_ext_ops.cu")
+    dev_src = os.path.join(CSRC, "gpuos_device.cu")
+    if force or _stale(EXEC_RDC, [dev_src] + headers):
+        # every function of the relocatable build must fit the executor's
+        # per-thread register budget (launch bounds: 512 threads, 1 block/SM)
+        jobs.append(([NVCC] + ARCH + COMMON + ["-cubin", "-rdc=true", "-maxrregcount", "128", "-Xptxas", "-v",
+                                               dev_src, "-o", EXEC_RDC + ".tmp"],
+                     os.path.join(BUILD, "gpuos_exec_rdc.ptxas.txt")))
     with cf.ThreadPoolExecutor(max_workers=4) as ex:
         list(ex.map(lambda j: _run(*j), jobs))
+    if os.path.exists(EXEC_RDC + ".tmp"):
+        os.replace(EXEC_RDC + ".tmp", EXEC_RDC)
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + ".tmp"
         _run([NVCC] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"])
         os.replace(tmp, LIB)
-    # The injectable op module must not use more registers than the executor
-    # holds per thread: compile it with the executor's count as its cap.
+    # The example op module is a relocatable object (linked into the executor
+    # at run time); it must not use more registers than the executor holds
+    # per thread, so it is compiled with the executor's count as its cap.
     if os.path.exists(ext_src) and (force or _stale(EXT_CUBIN, [ext_src, LIB] + headers)):
         regs = executor_regs()
         tmp = EXT_CUBIN + ".tmp"
         log = os.path.join(BUILD, "gpuos_ext_ops.ptxas.txt")
-        _run([NVCC] + ARCH + COMMON + ["-cubin", "-maxrregcount", str(regs), "-Xptxas", "-v",
+        _run([NVCC] + ARCH + COMMON + ["-cubin", "-rdc=true", "-maxrregcount", str(regs), "-Xptxas", "-v",
                                       ext_src, "-o", tmp], log)
         os.replace(tmp, EXT_CUBIN)
     return LIB

@@ -1,15 +1,18 @@
 /*
- * Injectable operator module, compiled on its own to an sm_103a cubin and
- * loaded at run time by gpuos_register_op ("GPUOS: A GPU Operating System
- * Primitive for Transparent Operation Fusion", §3 Q2 "3. Dynamic Operator
- * Table", steps 2-5: load the module through the driver API, resolve the
- * symbol to a device-function pointer, write it into the inactive table
- * slot, flip the version).
+ * Example operator module, compiled on its own to a relocatable sm_103a cubin
+ * (nvcc -cubin -rdc=true) and handed to gpuos_load_module / gpuos_register_op
+ * ("GPUOS: A GPU Operating System Primitive for Transparent Operation
+ * Fusion", §3 Q2 "3. Dynamic Operator Table": load the operator through the
+ * driver API, resolve its symbol to a device-function pointer, write it into
+ * the inactive table slot, flip the version).
  *
- * Each op is exported as a __device__ variable holding the function's
- * address, which the host reads with cuModuleGetGlobal. The functions follow
- * the executor's op signature and must stay within its register budget (the
- * build compiles this file with the executor's register count as the cap).
+ * The library links this object with its relocatable executor build before
+ * the executor's launch, so the functions live in the executor's own module
+ * (a device-function pointer is only callable inside the module that holds
+ * its code). Each op is exported as a __device__ variable holding the
+ * function's address, read after linking with cuModuleGetGlobal. The
+ * functions follow the executor's op signature and stay within its register
+ * budget (the build caps them at the executor's register count).
  *
  *   gpuos_ext_sub   out = a - b, element-wise fp32/bf16, same tiling as the
  *                   built-in add (it can replace op 1 in a hot swap)
@@ -67,10 +70,3 @@ extern "C" __device__ __noinline__ int gpuos_ext_scale(const gpuos_devdesc *d, u
 extern "C" __device__ gpuos_op_fn gpuos_ext_sub_ptr = gpuos_ext_sub;
 extern "C" __device__ gpuos_op_fn gpuos_ext_scale_ptr = gpuos_ext_scale;
 
-/* Takes the functions' addresses inside a kernel, so that whole-program
- * compilation keeps their bodies; it is never launched. */
-extern "C" __global__ void gpuos_ext_keep(gpuos_op_fn *out)
-{
-    out[0] = gpuos_ext_sub;
-    out[1] = gpuos_ext_scale;
-}

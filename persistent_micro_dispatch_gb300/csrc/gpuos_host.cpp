@@ -21,6 +21,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <dlfcn.h>
+
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
@@ -28,6 +30,7 @@
 #include <cstring>
 #include <ctime>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "gpuos_internal.h"
@@ -38,11 +41,29 @@ namespace {
 typedef CUresult (*pfn_cuModuleLoadData)(CUmodule *, const void *);
 typedef CUresult (*pfn_cuModuleGetGlobal)(CUdeviceptr *, size_t *, CUmodule, const char *);
 typedef CUresult (*pfn_cuModuleUnload)(CUmodule);
+typedef CUresult (*pfn_cuModuleGetFunction)(CUfunction *, CUmodule, const char *);
+typedef CUresult (*pfn_cuLinkCreate)(unsigned int, CUjit_option *, void **, CUlinkState *);
+typedef CUresult (*pfn_cuLinkAddData)(CUlinkState, CUjitInputType, void *, size_t, const char *, unsigned int,
+                                      CUjit_option *, void **);
+typedef CUresult (*pfn_cuLinkComplete)(CUlinkState, void **, size_t *);
+typedef CUresult (*pfn_cuLinkDestroy)(CUlinkState);
+typedef CUresult (*pfn_cuFuncSetAttribute)(CUfunction, CUfunction_attribute, int);
+typedef CUresult (*pfn_cuFuncGetAttribute)(int *, CUfunction_attribute, CUfunction);
+typedef CUresult (*pfn_cuLaunchKernel)(CUfunction, unsigned int, unsigned int, unsigned int, unsigned int,
+                                       unsigned int, unsigned int, unsigned int, CUstream, void **, void **);
 
 struct Driver {
     pfn_cuModuleLoadData load = nullptr;
     pfn_cuModuleGetGlobal get_global = nullptr;
     pfn_cuModuleUnload unload = nullptr;
+    pfn_cuModuleGetFunction get_function = nullptr;
+    pfn_cuLinkCreate link_create = nullptr;
+    pfn_cuLinkAddData link_add = nullptr;
+    pfn_cuLinkComplete link_complete = nullptr;
+    pfn_cuLinkDestroy link_destroy = nullptr;
+    pfn_cuFuncSetAttribute func_set_attr = nullptr;
+    pfn_cuFuncGetAttribute func_get_attr = nullptr;
+    pfn_cuLaunchKernel launch = nullptr;
     bool ok = false;
 };
 
@@ -59,9 +80,73 @@ Driver &driver()
     if (!d.ok) {
         d.ok = resolve("cuModuleLoadData", (void **)&d.load) &&
                resolve("cuModuleGetGlobal", (void **)&d.get_global) &&
-               resolve("cuModuleUnload", (void **)&d.unload);
+               resolve("cuModuleUnload", (void **)&d.unload) &&
+               resolve("cuModuleGetFunction", (void **)&d.get_function) &&
+               resolve("cuLinkCreate", (void **)&d.link_create) &&
+               resolve("cuLinkAddData", (void **)&d.link_add) &&
+               resolve("cuLinkComplete", (void **)&d.link_complete) &&
+               resolve("cuLinkDestroy", (void **)&d.link_destroy) &&
+               resolve("cuFuncSetAttribute", (void **)&d.func_set_attr) &&
+               resolve("cuFuncGetAttribute", (void **)&d.func_get_attr) &&
+               resolve("cuLaunchKernel", (void **)&d.launch);
     }
     return d;
+}
+
+/* The relocatable build of the executor (gpuos_exec_rdc.cubin), read from
+ * the directory this library was loaded from. */
+const std::vector<unsigned char> &exec_rdc_image()
+{
+    static std::vector<unsigned char> img;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        Dl_info info;
+        if (dladdr((void *)&exec_rdc_image, &info) && info.dli_fname) {
+            std::string path(info.dli_fname);
+            const size_t cut = path.find_last_of('/');
+            path = (cut == std::string::npos ? std::string(".") : path.substr(0, cut)) + "/gpuos_exec_rdc.cubin";
+            FILE *f = fopen(path.c_str(), "rb");
+            if (f) {
+                fseek(f, 0, SEEK_END);
+                const long n = ftell(f);
+                fseek(f, 0, SEEK_SET);
+                if (n > 0) {
+                    img.resize((size_t)n);
+                    if (fread(img.data(), 1, (size_t)n, f) != (size_t)n) img.clear();
+                }
+                fclose(f);
+            }
+        }
+    }
+    return img;
+}
+
+/* Link the relocatable executor with the given relocatable op objects into
+ * one loadable image (driver JIT linker). Returns GPUOS_OK and the image. */
+int link_images(const std::vector<std::vector<unsigned char>> &objs, std::vector<unsigned char> *out)
+{
+    Driver &drv = driver();
+    if (!drv.ok) return GPUOS_ECUDA;
+    const std::vector<unsigned char> &exe = exec_rdc_image();
+    if (exe.empty()) return GPUOS_ECUDA;
+    CUlinkState st = nullptr;
+    if (drv.link_create(0, nullptr, nullptr, &st) != CUDA_SUCCESS) return GPUOS_ECUDA;
+    int rc = GPUOS_OK;
+    if (drv.link_add(st, CU_JIT_INPUT_CUBIN, (void *)exe.data(), exe.size(), "gpuos_exec", 0, nullptr, nullptr) !=
+        CUDA_SUCCESS)
+        rc = GPUOS_ECUDA;
+    for (size_t i = 0; rc == GPUOS_OK && i < objs.size(); i++) {
+        if (drv.link_add(st, CU_JIT_INPUT_CUBIN, (void *)objs[i].data(), objs[i].size(), "gpuos_op_module", 0,
+                         nullptr, nullptr) != CUDA_SUCCESS)
+            rc = GPUOS_EINVAL;
+    }
+    void *cubin = nullptr;
+    size_t n = 0;
+    if (rc == GPUOS_OK && drv.link_complete(st, &cubin, &n) != CUDA_SUCCESS) rc = GPUOS_EINVAL;
+    if (rc == GPUOS_OK) out->assign((unsigned char *)cubin, (unsigned char *)cubin + n);
+    drv.link_destroy(st);
+    return rc;
 }
 
 uint64_t now_ns()
@@ -136,11 +221,12 @@ struct gpuos_ctx {
     uint32_t version = 0;
     uint64_t flip_head = 0; /* head when the current version was published */
     struct Module {
-        CUmodule mod;
         uint64_t hash;
         std::vector<unsigned char> bytes;
     };
-    std::vector<Module> modules;
+    std::vector<Module> modules;  /* op objects linked into the executor */
+    CUmodule linked = nullptr;    /* executor + op objects, when modules exist */
+    CUfunction linked_exec = nullptr;
     uint32_t regs = 0, smem = 0;
     gpuos_exec_params params;
     bool accepting = false; /* submissions allowed (until stop) */
@@ -287,9 +373,8 @@ int gpuos_op_ntiles(const gpuos_desc *d, uint32_t *ntiles)
 
 static void free_all(gpuos_ctx *c)
 {
-    for (auto &m : c->modules) {
-        if (driver().ok) driver().unload(m.mod);
-    }
+    if (c->linked && driver().ok) driver().unload(c->linked);
+    c->linked = nullptr;
     c->modules.clear();
     if (c->ring) {
         if (c->ring_managed) cudaFree(c->ring);
@@ -485,12 +570,63 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
 #undef CK
 }
 
+/* With op modules loaded: link them with the relocatable executor, load the
+ * result, take the built-in table from it (function pointers are valid only
+ * inside the module that holds the code) and launch its executor. */
+static int launch_linked(gpuos_ctx *c)
+{
+    Driver &drv = driver();
+    std::vector<std::vector<unsigned char>> objs;
+    for (auto &m : c->modules) objs.push_back(m.bytes);
+    std::vector<unsigned char> img;
+    int rc = link_images(objs, &img);
+    if (rc) return rc;
+    if (drv.load(&c->linked, img.data()) != CUDA_SUCCESS) return GPUOS_ECUDA;
+    CUdeviceptr tab = 0;
+    size_t tsz = 0;
+    if (drv.get_global(&tab, &tsz, c->linked, "g_builtin_ops") != CUDA_SUCCESS ||
+        tsz != GPUOS_OP_BUILTIN_COUNT * sizeof(gpuos_op_fn))
+        return GPUOS_ECUDA;
+    uint64_t builtin[GPUOS_OP_BUILTIN_COUNT];
+    if (cudaMemcpy(builtin, (const void *)tab, sizeof(builtin), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GPUOS_ECUDA;
+    for (int sl = 0; sl < 2; sl++)
+        for (int i = 0; i < GPUOS_OP_BUILTIN_COUNT; i++) c->table_host[sl][i] = builtin[i];
+    if (cudaMemcpy(c->table, c->table_host, sizeof(c->table_host), cudaMemcpyHostToDevice) != cudaSuccess)
+        return GPUOS_ECUDA;
+    if (drv.get_function(&c->linked_exec, c->linked, "gpuos_executor_kernel") != CUDA_SUCCESS) return GPUOS_ECUDA;
+    /* every function of the executor and of the op modules was compiled with
+     * at most GPUOS_MAX_REGS registers; the linked kernel must hold that many
+     * per thread, or an indirect call could use registers it does not own */
+    int regs = 0;
+    if (drv.func_get_attr(&regs, CU_FUNC_ATTRIBUTE_NUM_REGS, c->linked_exec) != CUDA_SUCCESS) return GPUOS_ECUDA;
+    if (regs < GPUOS_MAX_REGS) {
+        fprintf(stderr, "gpuos: linked executor holds %d registers per thread, below %d\n", regs, GPUOS_MAX_REGS);
+        return GPUOS_EINVAL;
+    }
+    c->regs = (uint32_t)regs;
+    const uint32_t dyn = gpuos_dev_dyn_smem(c->wpb, c->params.stage_bytes);
+    if (drv.func_set_attr(c->linked_exec, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, (int)dyn) != CUDA_SUCCESS)
+        return GPUOS_ECUDA;
+    void *args[] = {&c->params};
+    if (drv.launch(c->linked_exec, c->blocks, 1, 1, c->wpb * 32, 1, 1, dyn, (CUstream)c->exec_stream, args,
+                   nullptr) != CUDA_SUCCESS)
+        return GPUOS_ECUDA;
+    return GPUOS_OK;
+}
+
 int gpuos_start(gpuos_ctx *c)
 {
     if (!c || c->launched) return GPUOS_EINVAL;
     if (cudaSetDevice(c->device) != cudaSuccess) return GPUOS_ECUDA;
     heartbeat(c);
-    if (gpuos_dev_launch_executor(&c->params, c->blocks, c->wpb, c->exec_stream) != 0) {
+    if (!c->modules.empty()) {
+        const int rc = launch_linked(c);
+        if (rc) {
+            fprintf(stderr, "gpuos: linked executor launch failed (%d)\n", rc);
+            return rc;
+        }
+    } else if (gpuos_dev_launch_executor(&c->params, c->blocks, c->wpb, c->exec_stream) != 0) {
         fprintf(stderr, "gpuos: executor launch failed: %s\n", cudaGetErrorString(cudaGetLastError()));
         return GPUOS_ECUDA;
     }
@@ -772,34 +908,23 @@ static int find_module(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
     return -1;
 }
 
-static int load_module(gpuos_ctx *c, const void *image, size_t len, int *index)
-{
-    const uint64_t h = fnv1a(image, len);
-    const int found = find_module(c, image, len, h);
-    if (found >= 0) {
-        *index = found;
-        return GPUOS_OK;
-    }
-    if (executor_resident(c)) return GPUOS_EBUSY;
-    Driver &drv = driver();
-    if (!drv.ok) return GPUOS_ECUDA;
-    if (cudaSetDevice(c->device) != cudaSuccess) return GPUOS_ECUDA;
-    CUmodule mod = nullptr;
-    if (drv.load(&mod, image) != CUDA_SUCCESS) return GPUOS_EINVAL;
-    gpuos_ctx::Module m;
-    m.mod = mod;
-    m.hash = h;
-    m.bytes.assign(static_cast<const unsigned char *>(image), static_cast<const unsigned char *>(image) + len);
-    c->modules.push_back(std::move(m));
-    *index = (int)c->modules.size() - 1;
-    return GPUOS_OK;
-}
-
 int gpuos_load_module(gpuos_ctx *c, const void *image, size_t len)
 {
     if (!c || !image || !len) return GPUOS_EINVAL;
-    int idx = -1;
-    return load_module(c, image, len, &idx);
+    const uint64_t h = fnv1a(image, len);
+    if (find_module(c, image, len, h) >= 0) return GPUOS_OK;
+    if (c->launched) return GPUOS_EBUSY; /* linked into the executor at gpuos_start */
+    /* check now that the object links with the executor */
+    std::vector<std::vector<unsigned char>> objs(1);
+    objs[0].assign((const unsigned char *)image, (const unsigned char *)image + len);
+    std::vector<unsigned char> img;
+    const int rc = link_images(objs, &img);
+    if (rc) return rc;
+    gpuos_ctx::Module m;
+    m.hash = h;
+    m.bytes = std::move(objs[0]);
+    c->modules.push_back(std::move(m));
+    return GPUOS_OK;
 }
 
 int gpuos_register_op(gpuos_ctx *c, uint16_t op_id, const void *image, size_t len, const char *sym)
@@ -807,13 +932,16 @@ int gpuos_register_op(gpuos_ctx *c, uint16_t op_id, const void *image, size_t le
     if (!c || !image || !len || !sym || op_id >= GPUOS_MAX_OPS || op_id == GPUOS_OP_NOP) return GPUOS_EINVAL;
     if (op_id >= GPUOS_OP_BUILTIN_COUNT && op_id < GPUOS_OP_USER_FIRST) return GPUOS_EINVAL;
     if (!c->accepting) return GPUOS_ESTOPPED;
-    int idx = -1;
-    int rc = load_module(c, image, len, &idx);
-    if (rc) return rc;
+    if (find_module(c, image, len, fnv1a(image, len)) < 0) {
+        /* not linked into the executor: only possible before the launch */
+        const int rc = gpuos_load_module(c, image, len);
+        if (rc) return rc;
+    }
+    if (!c->launched || !c->linked) return GPUOS_EBUSY; /* the swap needs the linked, running executor */
     heartbeat(c);
     CUdeviceptr gp = 0;
     size_t gsz = 0;
-    if (driver().get_global(&gp, &gsz, c->modules[idx].mod, sym) != CUDA_SUCCESS || gsz != sizeof(uint64_t))
+    if (driver().get_global(&gp, &gsz, c->linked, sym) != CUDA_SUCCESS || gsz != sizeof(uint64_t))
         return GPUOS_EINVAL;
     uint64_t fnval = 0;
     if (cudaMemcpyAsync(c->version_stage + 2, (const void *)gp, 8, cudaMemcpyDeviceToHost, c->ctl_stream) !=
@@ -822,7 +950,7 @@ int gpuos_register_op(gpuos_ctx *c, uint16_t op_id, const void *image, size_t le
         return GPUOS_ECUDA;
     memcpy(&fnval, c->version_stage + 2, 8);
     if (fnval == 0) return GPUOS_EINVAL;
-    rc = flip_entry(c, op_id, fnval);
+    const int rc = flip_entry(c, op_id, fnval);
     if (rc == GPUOS_OK && op_id >= GPUOS_OP_USER_FIRST) c->user_registered[op_id] = true;
     return rc;
 }

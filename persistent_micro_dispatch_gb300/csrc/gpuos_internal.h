@@ -17,6 +17,7 @@
 #define GPUOS_VM_COLS 32                  /* output columns per vecmat tile */
 #define GPUOS_ROW_REG_MAX 4096            /* rows up to this width stay in registers */
 #define GPUOS_MAX_WPB 16
+#define GPUOS_MAX_REGS 128 /* registers per thread: 65536 / (16 warps x 32) */
 #define GPUOS_TILE_MAX (1u << 30)          /* tiles per descriptor */
 #define GPUOS_HELPERS 64                   /* work-queue entries (helper warps) per descriptor at most */
 #define GPUOS_TQ_MAX (1u << 30)            /* work-queue entries */

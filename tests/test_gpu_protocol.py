@@ -209,7 +209,6 @@ def _ext_image():
     return open(G().EXT_CUBIN, "rb").read()
 
 
-@pytest.mark.skip(reason="cross-module function pointers are being replaced by in-module linking")
 def test_hot_swap_under_load_every_result_old_or_new():
     """Swap op ADD for the injected subtract while 3,000 adds are in flight;
     each descriptor's output is a+b or a-b according to the table version it
@@ -261,7 +260,6 @@ def test_hot_swap_under_load_every_result_old_or_new():
         assert np.array_equal(ds.read(o.out, n).view(np.uint32), m.view(o.out, n).view(np.uint32)), (j, ver[j])
 
 
-@pytest.mark.skip(reason="cross-module function pointers are being replaced by in-module linking")
 def test_user_op_registration():
     """An injected op under a new id (64) with a caller-set tile count."""
     import torch
