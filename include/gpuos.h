@@ -61,6 +61,7 @@ extern "C" {
 #define GPUOS_ESTOPPED (-6)  /* the executor is no longer running */
 #define GPUOS_ENOMEM (-7)
 #define GPUOS_EBUSY (-8)     /* needs the executor not resident (see gpuos_load_module) */
+#define GPUOS_ETOOBIG (-9)   /* sizes beyond a fixed limit (see gpuos_sdpa_noalloc) */
 
 /* ---- device status codes (gpuos_record.status) -------------------------- */
 #define GPUOS_ST_OK 0
@@ -313,6 +314,29 @@ GPUOS_API size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, 
  * stream order. Does not synchronize. Errors: EINVAL (as gpuos_submit),
  * ECUDA. */
 GPUOS_API int gpuos_eager_run(const gpuos_desc *d, uint32_t count, uint32_t stage_bytes, void *stream);
+
+/* Decode attention that allocates nothing. The method has no counterpart of
+ * this call; it exists for callers that cannot allocate device memory at the
+ * time they attend: code running beside a resident executor (cudaFree, and a
+ * cudaMalloc that must grow the heap, wait for an idle device, which a
+ * resident executor never gives) and code held to a memory budget fixed up
+ * front. It computes what GPUOS_OP_SDPA computes (same op body, one launch on
+ * `stream`, a cudaStream_t, 0 = legacy default) with inputs and output given
+ * as for that op: q[B][H][D], caches Kc/Vc [B][H][Lcap][D] bf16, lens i32[B]
+ * in device memory, out[B][H][D] bf16; all 16-byte aligned; D = 128. The
+ * split-K scratch is a fixed device array inside the library (about 1 MiB per
+ * device, held until the process exits) instead of a caller workspace; it
+ * bounds B * H <= 256 and Lmax <= 4096, and larger sizes return
+ * GPUOS_ETOOBIG. The first call on a device looks up the array's device
+ * address (make that call before any stream capture). Every call on a device
+ * shares the array and the call clears its counters first, so calls that
+ * overlap on the GPU (different streams, no ordering) race: order them.
+ * No allocation happens (no cudaMalloc, cudaFree or allocating library
+ * routine). Errors: EINVAL, ETOOBIG, ECUDA. Asynchronous: the caller
+ * synchronizes `stream`. */
+GPUOS_API int gpuos_sdpa_noalloc(const void *q, const void *Kc, const void *Vc, const int32_t *lens, void *out,
+                                 uint32_t B, uint32_t H, uint32_t D, uint32_t Lcap, uint32_t Lmax, float scale,
+                                 void *stream);
 
 /* CLOCK_REALTIME in ns (the host clock of gpuos_record). */
 GPUOS_API uint64_t gpuos_host_now_ns(void);

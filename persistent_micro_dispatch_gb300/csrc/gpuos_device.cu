@@ -1455,3 +1455,77 @@ extern "C" int gpuos_dev_eager_launch(const gpuos_desc *d, uint32_t ntiles, uint
     gpuos_eager_kernel<<<grid, EAGER_WPB * 32, dyn, (cudaStream_t)stream>>>(dd, stage_bytes);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
+
+/* ===========================================================================
+ * Decode attention that allocates nothing.
+ *
+ * Some callers cannot allocate device memory when they attend: a serving
+ * loop that runs beside a resident persistent executor (cudaFree, and a
+ * cudaMalloc that has to grow the heap, wait for the device to go idle, which
+ * a resident executor never does), and code that runs under a fixed memory
+ * budget reserved up front. gpuos_sdpa_noalloc gives them the split-K decode
+ * attention with its scratch in a file-scope device array of fixed size
+ * instead of a caller workspace. The caller still passes every input and the
+ * output.
+ * ======================================================================== */
+#define GPUOS_NOALLOC_MAX_BH 256u  /* requests x heads */
+#define GPUOS_NOALLOC_MAX_L 4096u  /* rows attended per request (8 chunks of 512) */
+#define GPUOS_NOALLOC_CTR_BYTES (4u * GPUOS_NOALLOC_MAX_BH)
+#define GPUOS_NOALLOC_BYTES \
+    (GPUOS_NOALLOC_CTR_BYTES + 4u * GPUOS_NOALLOC_MAX_BH * (GPUOS_NOALLOC_MAX_L / GPUOS_SDPA_CHUNK) * 130u)
+
+/* Shared by every call on a device and kept until the process exits. In host
+ * code this name is only a stand-in for the device array: never pass it to a
+ * kernel; use the address cudaGetSymbolAddress returns for the device. */
+static __device__ __align__(256) unsigned char g_sdpa_scratch[GPUOS_NOALLOC_BYTES];
+
+extern "C" __global__ void __launch_bounds__(32) gpuos_sdpa_noalloc_kernel(gpuos_devdesc d)
+{
+    __shared__ __align__(16) gpuos_devdesc sd;
+    reinterpret_cast<uint32_t *>(&sd)[lane_id()] = reinterpret_cast<const uint32_t *>(&d)[lane_id()];
+    __syncwarp();
+    if (blockIdx.x < sd.ntiles) (void)sdpa_tile(&sd, blockIdx.x);
+}
+
+extern "C" GPUOS_API int gpuos_sdpa_noalloc(const void *q, const void *Kc, const void *Vc, const int32_t *lens,
+                                            void *out, uint32_t B, uint32_t H, uint32_t D, uint32_t Lcap,
+                                            uint32_t Lmax, float scale, void *stream)
+{
+    if (!q || !Kc || !Vc || !lens || !out || B == 0 || H == 0 || D != 128 || Lcap == 0 || Lmax == 0 || Lmax > Lcap)
+        return GPUOS_EINVAL;
+    if (((uintptr_t)q | (uintptr_t)Kc | (uintptr_t)Vc | (uintptr_t)out) & 15u) return GPUOS_EINVAL;
+    if ((uint64_t)B * H > GPUOS_NOALLOC_MAX_BH || Lmax > GPUOS_NOALLOC_MAX_L) return GPUOS_ETOOBIG;
+    /* set-up, once per device with that device current: the device address of
+     * the scratch array (the first call on a device does this) */
+    static void *scratch[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GPUOS_ECUDA;
+    if (!scratch[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_sdpa_scratch) != cudaSuccess || !ptr) return GPUOS_ECUDA;
+        scratch[dev] = ptr;
+    }
+    /* the split-K counters must start at zero; the partials need no clearing */
+    if (cudaMemsetAsync(scratch[dev], 0, GPUOS_NOALLOC_CTR_BYTES, (cudaStream_t)stream) != cudaSuccess)
+        return GPUOS_ECUDA;
+    gpuos_devdesc d;
+    memset(&d, 0, sizeof(d));
+    d.op_id = GPUOS_OP_SDPA;
+    d.dtype = GPUOS_BF16;
+    d.a = (uint64_t)(uintptr_t)q;
+    d.b = (uint64_t)(uintptr_t)Kc;
+    d.aux1 = (uint64_t)(uintptr_t)Vc;
+    d.aux0 = (uint64_t)(uintptr_t)lens;
+    d.out = (uint64_t)(uintptr_t)out;
+    d.aux2 = (uint64_t)(uintptr_t)scratch[dev];
+    d.dims[0] = B;
+    d.dims[1] = H;
+    d.dims[2] = D;
+    d.dims[3] = Lcap;
+    d.dims[4] = Lmax;
+    d.dims[5] = GPUOS_NOALLOC_MAX_BH; /* counters reserved at the start of the array */
+    d.fparam[0] = scale;
+    d.ntiles = B * H * ((Lmax + GPUOS_SDPA_CHUNK - 1) / GPUOS_SDPA_CHUNK);
+    gpuos_sdpa_noalloc_kernel<<<d.ntiles, 32, 0, (cudaStream_t)stream>>>(d);
+    return cudaGetLastError() == cudaSuccess ? GPUOS_OK : GPUOS_ECUDA;
+}

@@ -267,6 +267,7 @@ const char *gpuos_strerror(int code, int is_status)
     case GPUOS_ESTOPPED: return "executor is not running";
     case GPUOS_ENOMEM: return "out of memory";
     case GPUOS_EBUSY: return "not allowed while the executor is resident (load modules before gpuos_start)";
+    case GPUOS_ETOOBIG: return "sizes exceed the fixed scratch of gpuos_sdpa_noalloc (B*H <= 256, Lmax <= 4096)";
     default: return "unknown error";
     }
 }

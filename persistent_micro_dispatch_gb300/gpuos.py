@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libgpuos.so")
 EXT_CUBIN = os.path.join(HERE, "gpuos_ext_ops.cubin")
 
 # ---- constants (mirror include/gpuos.h) --------------------------------------------
-OK, EINVAL, EAGAIN, ETIMEDOUT, EDEVICE, ECUDA, ESTOPPED, ENOMEM, EBUSY = 0, -1, -2, -3, -4, -5, -6, -7, -8
+OK, EINVAL, EAGAIN, ETIMEDOUT, EDEVICE, ECUDA, ESTOPPED, ENOMEM, EBUSY, ETOOBIG = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
 ST_OK, ST_BAD_OP, ST_BAD_ARGS, ST_DEP_TIMEOUT, ST_ABORTED, ST_BAD_DESC, ST_COPY_TIMEOUT = 0, 1, 2, 3, 4, 5, 6
 OP = dict(nop=0, add=1, mul=2, relu=3, gelu=4, softmax=5, layernorm=6, rowsum=7, rowmax=8, rowmin=9,
           rope=10, kv_write=11, sdpa=12, vecmat=13)
@@ -99,6 +99,8 @@ API = {
     "gpuos_sdpa_workspace_bytes": (C.c_size_t, [C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint32]),
     "gpuos_eager_run": (C.c_int, [C.c_void_p, C.c_uint32, C.c_uint32, C.c_void_p]),
     "gpuos_host_now_ns": (C.c_uint64, []),
+    "gpuos_sdpa_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32,
+                                     C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint32, C.c_float, C.c_void_p]),
     "gpuos_strerror": (C.c_char_p, [C.c_int, C.c_int]),
 }
 
@@ -163,6 +165,14 @@ def eager_run(descs: np.ndarray, stream_ptr: int = 0, stage_bytes: int = 16384) 
     descs = np.ascontiguousarray(descs, dtype=DESC_DTYPE)
     check(lib().gpuos_eager_run(descs.ctypes.data, len(descs), stage_bytes, C.c_void_p(stream_ptr)),
           "gpuos_eager_run")
+
+
+def sdpa_noalloc(q: int, Kc: int, Vc: int, lens: int, out: int, B: int, H: int, D: int, Lcap: int, Lmax: int,
+                 scale: float, stream_ptr: int = 0) -> int:
+    """Decode attention with the library's fixed scratch (device pointers in);
+    returns the raw return code."""
+    return lib().gpuos_sdpa_noalloc(C.c_void_p(q), C.c_void_p(Kc), C.c_void_p(Vc), C.c_void_p(lens), C.c_void_p(out),
+                                    B, H, D, Lcap, Lmax, scale, C.c_void_p(stream_ptr))
 
 
 def make_descs(n: int) -> np.ndarray:
