@@ -206,6 +206,74 @@ def run_reference(args, world, rank):
 
 
 # ---------------------------------------------------------------------------
+# co-running GEMM (hybrid execution: large GEMMs keep the normal launch path)
+# ---------------------------------------------------------------------------
+class Gemm:
+    """An 8192^3 bf16 torch.matmul looped on its own stream, operands
+    N(0, 0.02). Warmed up (its kernel loaded) before any executor is
+    resident."""
+
+    N = 8192
+
+    def __init__(self, device_index: int):
+        import torch
+        dev = f"cuda:{device_index}"
+        g = torch.Generator(device=dev).manual_seed(5)
+        self.a = (torch.randn(self.N, self.N, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        self.b = (torch.randn(self.N, self.N, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        self.c = torch.empty_like(self.a)
+        self.stream = torch.cuda.Stream()
+        with torch.cuda.stream(self.stream):
+            torch.matmul(self.a, self.b, out=self.c)
+        torch.cuda.synchronize()
+        self.events = []
+        self.alone_tflops = None
+
+    def flops(self, n):
+        return 2.0 * self.N ** 3 * n
+
+    def measure_alone(self, n):
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        with torch.cuda.stream(self.stream):
+            for _ in range(n):
+                torch.matmul(self.a, self.b, out=self.c)
+        e1.record(self.stream)
+        e1.synchronize()
+        return self.flops(n) / (e0.elapsed_time(e1) / 1e3) / 1e12
+
+    def enqueue(self, n):
+        import torch
+        first = torch.cuda.Event(enable_timing=True)
+        first.record(self.stream)
+        self.events = [first]
+        with torch.cuda.stream(self.stream):
+            for _ in range(n):
+                torch.matmul(self.a, self.b, out=self.c)
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(self.stream)
+                self.events.append(ev)
+
+    def progress(self):
+        return sum(1 for ev in self.events[1:] if ev.query())
+
+    def report(self, done_while_resident, kern_ms):
+        """TFLOP/s of the GEMMs that completed while the executor was
+        resident (a bounded wait lets the rest finish afterwards)."""
+        t0 = time.perf_counter()
+        while not self.events[-1].query() and time.perf_counter() - t0 < 120:
+            time.sleep(0.01)
+        out = {"alone_tflops": self.alone_tflops, "gemms_done_while_executor_resident": done_while_resident,
+               "gemms_enqueued": len(self.events) - 1, "executor_kernel_ms": kern_ms}
+        if done_while_resident:
+            ms = self.events[0].elapsed_time(self.events[done_while_resident])
+            out["corun_tflops"] = self.flops(done_while_resident) / (ms / 1e3) / 1e12
+            out["gemm_slowdown"] = out["alone_tflops"] / out["corun_tflops"]
+        return out
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def pct(x, q):
@@ -230,6 +298,11 @@ def main():
     ap.add_argument("--pool-log2", type=int, default=0, help="profile run: log2 of the input pool elements")
     ap.add_argument("--warps", type=int, default=0, help="executor warps per block (0 = default)")
     ap.add_argument("--stage-bytes", type=int, default=16384, help="shared-memory staging per warp (0 = none)")
+    ap.add_argument("--blocks", type=int, default=0, help="executor blocks (0 = one per SM)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the eager launches captured into a CUDA graph (replay, and re-capture per step)")
+    ap.add_argument("--corun-gemm", action="store_true",
+                    help="loop a normally launched 8192^3 bf16 GEMM on a second stream during the timed region")
     args = ap.parse_args()
     os.environ.setdefault("GPUOS_DEBUG", "1")
     world, rank, local = dist_env()
@@ -247,14 +320,18 @@ def main():
     from workloads import streams as S
     from workloads.device import DeviceStream, warm_torch
 
-    cfg_kw = dict(device=local, idle_exit_ms=20000, stage_bytes=args.stage_bytes)
+    cfg_kw = dict(device=local, idle_exit_ms=20000, stage_bytes=args.stage_bytes, blocks=args.blocks)
     if args.warps:
         cfg_kw["warps_per_block"] = args.warps
-    if args.profile_run and args.profile_desc and args.workload in ("c2", "c2l"):
+    if args.profile_run and args.profile_desc and args.workload in ("c2", "c2l", "c3"):
         kw = dict(n_desc=args.profile_desc)
         if args.pool_log2:
             kw["pool_elems"] = 1 << args.pool_log2
         s = S.STREAMS[args.workload](**kw)
+    elif args.profile_run and args.profile_desc and args.workload == "c4":
+        s = S.stream_c4(n_steps=max(1, args.profile_desc // 3))
+    elif args.profile_run and args.profile_desc and args.workload == "c5":
+        s = S.stream_c5(n_tokens=max(1, args.profile_desc // 224))
     else:
         s = make_stream(args.workload, args.tokens)
     n_ops = len(s.ops)
@@ -300,6 +377,11 @@ def main():
     if rc_sd != G.OK:
         print(f"warm-up executor shutdown: {G.strerror(rc_sd)}", file=sys.stderr)
 
+    gemm = None
+    if args.corun_gemm:
+        gemm = Gemm(local)
+        gemm.alone_tflops = gemm.measure_alone(20)
+
     # ---- timed region: one launch of the persistent executor, K steps
     ex = G.Executor(**cfg_kw, deferred_start=1)
     hist = ex.set_history(0, args.steps * n_ops)
@@ -312,25 +394,20 @@ def main():
     clocks.start()
     time.sleep(0.3)
     t0 = time.perf_counter()
-    h_marks = [G.host_now_ns()]
     ev0.record(xs)
-    h_marks.append(G.host_now_ns())
     ex.start()
-    h_marks.append(G.host_now_ns())
     ev1.record(xs)  # completes when the executor kernel ends
-    h_marks.append(G.host_now_ns())
+    if gemm is not None:
+        gemm.enqueue(40)
     submit_ns = 0
     for step in range(args.steps):
         a = time.perf_counter_ns()
-        if step == 0:
-            h_marks.append(G.host_now_ns())
-            st0 = ex.stats()
-            if not st0["running"]:
-                print(f"executor left before the first submit: host marks {np.diff(h_marks).tolist()} ns, "
-                      f"stats {st0}", file=sys.stderr, flush=True)
         ex.submit_batch(descs)
         submit_ns += time.perf_counter_ns() - a
         ex.sync(timeout_ms=600_000)
+    gemm_progress = None
+    if gemm is not None:
+        gemm_progress = gemm.progress()  # GEMMs finished while the executor was resident
     ex.stop()
     torch.cuda.synchronize()
     t1 = time.perf_counter()
@@ -353,6 +430,18 @@ def main():
     iso_dev_us = (ih["t_done_dev_ns"].astype(np.int64) - ih["t_dispatch_dev_ns"].astype(np.int64)) / 1e3
     busy_ns = int(h["t_done_dev_ns"].max()) - int(h["t_dispatch_dev_ns"].min()) if len(h) else 0
 
+    # per op kind: device time from tile-0 start to completion, and bandwidth
+    kinds = {}
+    if len(h):
+        opn = np.array([s.ops[int(t) % n_ops].op for t in h["ticket"]])
+        dur = (h["t_done_dev_ns"].astype(np.int64) - h["t_start_dev_ns"].astype(np.int64)) / 1e3
+        per_op_bytes = np.array([S.sdpa_bytes(o, s.buffers[o.aux0.buf].data[o.aux0.off:o.aux0.off + o.dims[0]])
+                                 if o.op == "sdpa" else S.op_bytes(o) for o in s.ops], dtype=np.float64)
+        byts = per_op_bytes[(h["ticket"] % n_ops).astype(np.int64)]
+        for k in sorted(set(opn.tolist())):
+            m = opn == k
+            kinds[k] = {"n": int(m.sum()), "dur_us_p50": float(np.median(dur[m])),
+                        "gbs_p50": float(np.median(byts[m] / np.maximum(dur[m], 1e-3) / 1e3))}
     peak, peak_kind = measured_peak_gbs()
     achieved = step_bytes * args.steps / (kern_ms / 1e3) / 1e9
     result = {
@@ -382,10 +471,14 @@ def main():
                      "kernel": "gpuos_executor_kernel", "kernel_ms": kern_ms,
                      "device_busy_ms": busy_ns / 1e6},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+        "op_kinds": kinds,
         "executor": {k: st[k] for k in ("tiles", "idle_polls", "sleeps", "dep_waits", "regs_per_thread",
                                         "static_smem_bytes", "seq_body_ns", "seq_mirror_ns", "seq_publish_ns")},
         "wall_s": wall,
     }
+
+    if gemm is not None:
+        result["corun_gemm"] = gemm.report(gemm_progress, kern_ms)
 
     # ---- eager baseline: same op bodies, one cudaLaunchKernel per descriptor
     if not args.no_eager:
@@ -403,6 +496,35 @@ def main():
         eg_ms = e0.elapsed_time(e1)
         result["eager"] = {"value": n_ops * args.steps / (eg_ms / 1e3), "unit": UNIT,
                            "ms_per_step": eg_ms / args.steps, "launches_per_step": n_ops}
+
+    # ---- CUDA Graphs baseline: the eager launches of one step captured once
+    # and replayed (stable shapes), and captured + instantiated anew every
+    # step (what shapes that change every step cost)
+    if args.graph:
+        gs = torch.cuda.Stream()
+        G.eager_run(descs, gs.cuda_stream, args.stage_bytes)  # kernel attributes set outside capture
+        gs.synchronize()
+        c0 = time.perf_counter()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            G.eager_run(descs, gs.cuda_stream, args.stage_bytes)
+        cap_s = time.perf_counter() - c0
+        graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(gs):
+            e0.record()
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record()
+        e1.synchronize()
+        rep_ms = e0.elapsed_time(e1) / args.steps
+        result["cuda_graph"] = {"replay_value": n_ops / (rep_ms / 1e3), "unit": UNIT, "replay_ms_per_step": rep_ms,
+                                "capture_instantiate_ms": cap_s * 1e3,
+                                "recapture_value": n_ops / (rep_ms / 1e3 + cap_s)}
+        del graph
+        torch.cuda.synchronize()
 
     # ---- end to end: host buffers, copies inside the timed region
     if not args.no_e2e:

@@ -93,7 +93,7 @@ enum {
     GPUOS_OP_SDPA = 12,     /* o = softmax(scale q.K^T) V over rows 0..lens[b]-1; a = q[B][H][D],
                                b = Kc, aux1 = Vc [B][H][Lcap][D], aux0 = lens, out = o[B][H][D],
                                aux2 = 16-byte aligned fp32 workspace: first round_up(Ccap, 4)
-                               uint32 counters, then B*H*ceil(Lmax/512) partials of D+2 floats
+                               uint32 counters, then B*H*ceil(Lmax/256) partials of D+2 floats
                                (gpuos_sdpa_workspace_bytes(Bcap, H, D, Lmax) with Ccap = Bcap*H);
                                the counters must be zero before first use and every descriptor
                                leaves them zero; descriptors sharing a workspace use one Ccap;
@@ -152,8 +152,8 @@ typedef struct gpuos_config {
                                     1: managed memory preferred on the device */
     int32_t device;           /* CUDA device ordinal; default 0 */
     uint64_t exit_after;      /* 0 = run until shutdown; n = leave once n descriptors completed */
-    uint32_t tq_entries;      /* work-queue entries: 0 (default) = 128 x ring_entries; else a power
-                                 of two above 64 x ring_entries, at most 2^30 */
+    uint32_t tq_entries;      /* work-queue entries: 0 (default) = 2048 x ring_entries; else a
+                                 power of two above 1024 x ring_entries, at most 2^30 */
     uint32_t deferred_start;  /* 1: gpuos_init does not launch; gpuos_start does (descriptors
                                  may be submitted before, up to ring_entries of them) */
     uint32_t stage_bytes;     /* shared-memory staging per warp for bulk (TMA) copies: 0 = none
@@ -171,7 +171,7 @@ typedef struct gpuos_record {
     uint64_t t_commit_host_ns;  /* host clock just before the commit store-release */
     uint64_t t_dispatch_dev_ns; /* when the executor saw the commit (picked it off the ring) */
     uint64_t t_publish_dev_ns;  /* when its tiles were published to the work queue */
-    uint64_t t_start_dev_ns;    /* when a warp began its tile 0 */
+    uint64_t t_start_dev_ns;    /* when a warp began its tile 0 (dependencies met) */
     uint64_t t_done_dev_ns;     /* when its last tile finished */
 } gpuos_record;
 
@@ -283,12 +283,14 @@ GPUOS_API int gpuos_alias_op(gpuos_ctx *ctx, uint16_t op_id, uint16_t source_op)
 /* Live counters (host and device). */
 GPUOS_API int gpuos_stats(gpuos_ctx *ctx, gpuos_stats_t *st);
 
-/* NOP ping-pong: `pings` round trips, each committing a NOP (host clock t0)
- * and spinning on its completion record (host clock t1). Since the device
- * picks the NOP up between t0 and t1, every ping bounds the offset
- * off = device clock - host clock to [t_dispatch - t1, t_dispatch - t0];
- * *off_lo / *off_hi receive the intersection over all pings and *min_rtt_ns
- * the smallest t1 - t0. rtts (may be NULL) receives every round trip. */
+/* NOP ping-pong: `pings` round trips. Each commits a NOP (host clock t0)
+ * and spins until the executor's echo of the time it saw the commit appears
+ * in the ticket's record (host clock t1; the echo is written the moment the
+ * commit is seen, before the descriptor is read). Since the device sees the
+ * commit between t0 and t1, every ping bounds off = device clock - host clock
+ * to [t_dispatch - t1, t_dispatch - t0]; *off_lo / *off_hi receive the
+ * intersection over all pings and *min_rtt_ns the smallest t1 - t0. rtts
+ * (may be NULL) receives every echo round trip. */
 GPUOS_API int gpuos_calibrate(gpuos_ctx *ctx, uint32_t pings, int64_t *off_lo, int64_t *off_hi,
                               uint64_t *min_rtt_ns, uint64_t *rtts);
 
@@ -324,7 +326,7 @@ GPUOS_API int gpuos_eager_run(const gpuos_desc *d, uint32_t count, uint32_t stag
  * `stream`, a cudaStream_t, 0 = legacy default) with inputs and output given
  * as for that op: q[B][H][D], caches Kc/Vc [B][H][Lcap][D] bf16, lens i32[B]
  * in device memory, out[B][H][D] bf16; all 16-byte aligned; D = 128. The
- * split-K scratch is a fixed device array inside the library (about 1 MiB per
+ * split-K scratch is a fixed device array inside the library (about 2 MiB per
  * device, held until the process exits) instead of a caller workspace; it
  * bounds B * H <= 256 and Lmax <= 4096, and larger sizes return
  * GPUOS_ETOOBIG. The first call on a device looks up the array's device

@@ -718,12 +718,15 @@ DEV int kv_tile(const gpuos_devdesc *d, uint32_t b)
     return GPUOS_ST_OK;
 }
 
-/* ---- decode SDPA: one (request, head, 512-row chunk) per tile -------------
+/* ---- decode SDPA: one (request, head, GPUOS_SDPA_CHUNK-row chunk) per tile --
  * Four 8-lane groups walk interleaved key rows; in a group lane li owns dims
- * [16 li, 16 li + 16) of q, K and V. Scores use exp2 with log2(e) folded into
- * the query scale; each group keeps an online-softmax state (m, l, acc),
+ * [8 li, 8 li + 8) and [64 + 8 li, 64 + 8 li + 8) of q, K and V (two 16-byte
+ * pieces 128 bytes apart, so a quarter-warp reads 128 contiguous bytes of a
+ * row: no shared-memory bank conflicts). Scores use exp2 with log2(e) folded
+ * into the query scale; each group keeps an online-softmax state (m, l, acc),
  * the four states merge by shuffles, and multi-chunk heads merge through the
- * workspace in the last chunk to finish. */
+ * workspace in the last chunk to finish. With shared-memory staging the K and
+ * V rows of the chunk arrive by TMA bulk copies, 32 rows of each per stage. */
 DEV void sdpa_merge(float &m, float &l, float *acc, float mo, float lo, const float *acco)
 {
     const float mn = fmaxf(m, mo);
@@ -732,6 +735,46 @@ DEV void sdpa_merge(float &m, float &l, float *acc, float mo, float lo, const fl
     l = l * a + lo * b;
 #pragma unroll
     for (int i = 0; i < 16; i++) acc[i] = acc[i] * a + acco[i] * b;
+    m = mn;
+}
+
+/* One online-softmax step over UK keys held as (k0,k1,v0,v1) pieces. */
+template <int UK>
+DEV void sdpa_step(const float *q, const uint4 (&kv)[UK][2], const uint4 (&vv)[UK][2], const bool *valid, float &m,
+                   float &l, float *acc)
+{
+    float sc[UK];
+#pragma unroll
+    for (int u = 0; u < UK; u++) {
+        float kf[16];
+        unpack8(kv[u][0], kf);
+        unpack8(kv[u][1], kf + 8);
+        float p = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; i++) p = fmaf(q[i], kf[i], p);
+        p += __shfl_xor_sync(0xFFFFFFFFu, p, 1);
+        p += __shfl_xor_sync(0xFFFFFFFFu, p, 2);
+        p += __shfl_xor_sync(0xFFFFFFFFu, p, 4);
+        sc[u] = valid[u] ? p : -INFINITY;
+    }
+    float mn = m;
+#pragma unroll
+    for (int u = 0; u < UK; u++) mn = fmaxf(mn, sc[u]);
+    const float mu = (mn == -INFINITY) ? 0.0f : mn;
+    const float corr = exp2f(m - mu);
+    l *= corr;
+#pragma unroll
+    for (int i = 0; i < 16; i++) acc[i] *= corr;
+#pragma unroll
+    for (int u = 0; u < UK; u++) {
+        const float p = exp2f(sc[u] - mu);
+        l += p;
+        float vf[16];
+        unpack8(vv[u][0], vf);
+        unpack8(vv[u][1], vf + 8);
+#pragma unroll
+        for (int i = 0; i < 16; i++) acc[i] = fmaf(p, vf[i], acc[i]);
+    }
     m = mn;
 }
 
@@ -754,69 +797,86 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
 
     float q[16];
     {
-        const uint4 *qp = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(d->a) + bh * 128) + 2 * li;
-        unpack8(__ldcg(qp), q);
-        unpack8(__ldcg(qp + 1), q + 8);
+        const uint16_t *qp = reinterpret_cast<const uint16_t *>(d->a) + bh * 128;
+        unpack8(__ldcg(reinterpret_cast<const uint4 *>(qp + 8 * li)), q);
+        unpack8(__ldcg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * li)), q + 8);
 #pragma unroll
         for (int i = 0; i < 16; i++) q[i] *= qs;
     }
-    const uint4 *Kp = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(d->b) + bh * Lcap * 128) + 2 * li;
-    const uint4 *Vp = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(d->aux1) + bh * Lcap * 128) + 2 * li;
+    const uint16_t *Kb = reinterpret_cast<const uint16_t *>(d->b) + bh * Lcap * 128;
+    const uint16_t *Vb = reinterpret_cast<const uint16_t *>(d->aux1) + bh * Lcap * 128;
     float m = -INFINITY, l = 0.0f, acc[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) acc[i] = 0.0f;
-
     constexpr int UK = 2; /* keys per group per step */
-    for (uint32_t tb = t0; tb < t1; tb += 4 * UK) {
-        uint4 kv[UK][2], vv[UK][2];
-        bool valid[UK];
-#pragma unroll
-        for (int u = 0; u < UK; u++) {
-            const uint32_t t = tb + g + 4 * u;
-            valid[u] = t < t1;
-            if (valid[u]) {
-                kv[u][0] = __ldcg(Kp + (uint64_t)t * 16);
-                kv[u][1] = __ldcg(Kp + (uint64_t)t * 16 + 1);
-                vv[u][0] = __ldcg(Vp + (uint64_t)t * 16);
-                vv[u][1] = __ldcg(Vp + (uint64_t)t * 16 + 1);
-            } else {
-                kv[u][0] = kv[u][1] = vv[u][0] = vv[u][1] = make_uint4(0, 0, 0, 0);
+    int32_t status = GPUOS_ST_OK;
+    const uint32_t sbytes = stage_hdr()->stage_bytes;
+    const uint32_t SUB = sbytes / 512u; /* key rows per stage: K and V, 256 bytes each */
+    if (SUB >= 8) {
+        WarpStage *w = warp_stage();
+        unsigned char *sK = warp_stage_buf();
+        unsigned char *sV = sK + SUB * 256u;
+        uint32_t phase = w->phase;
+        for (uint32_t tb = t0; tb < t1; tb += SUB) {
+            const uint32_t nk = (t1 - tb) < SUB ? (t1 - tb) : SUB;
+            const uint32_t bytes = nk * 256u;
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_expect(&w->mbar, 2u * bytes);
+                bulk_g2s(sK, Kb + (uint64_t)tb * 128, bytes, &w->mbar);
+                bulk_g2s(sV, Vb + (uint64_t)tb * 128, bytes, &w->mbar);
             }
+            if (!mbar_wait(&w->mbar, phase)) {
+                mbar_wait(&w->mbar, phase);
+                status = GPUOS_ST_COPY_TIMEOUT;
+                phase ^= 1u;
+                break;
+            }
+            phase ^= 1u;
+            for (uint32_t kk = 0; kk < nk; kk += 4 * UK) {
+                uint4 kv[UK][2], vv[UK][2];
+                bool valid[UK];
+#pragma unroll
+                for (int u = 0; u < UK; u++) {
+                    const uint32_t t = kk + g + 4 * u;
+                    valid[u] = t < nk;
+                    const uint32_t tt = valid[u] ? t : 0u;
+                    const uint4 *kr = reinterpret_cast<const uint4 *>(sK + tt * 256u) + li;
+                    const uint4 *vr = reinterpret_cast<const uint4 *>(sV + tt * 256u) + li;
+                    kv[u][0] = kr[0];
+                    kv[u][1] = kr[8];
+                    vv[u][0] = vr[0];
+                    vv[u][1] = vr[8];
+                }
+                sdpa_step<UK>(q, kv, vv, valid, m, l, acc);
+            }
+            __syncwarp();
         }
-        float sc[UK];
+        if (lane == 0) w->phase = phase;
+        __syncwarp();
+    } else {
+        for (uint32_t tb = t0; tb < t1; tb += 4 * UK) {
+            uint4 kv[UK][2], vv[UK][2];
+            bool valid[UK];
 #pragma unroll
-        for (int u = 0; u < UK; u++) {
-            float kf[16];
-            unpack8(kv[u][0], kf);
-            unpack8(kv[u][1], kf + 8);
-            float p = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; i++) p = fmaf(q[i], kf[i], p);
-            p += __shfl_xor_sync(0xFFFFFFFFu, p, 1);
-            p += __shfl_xor_sync(0xFFFFFFFFu, p, 2);
-            p += __shfl_xor_sync(0xFFFFFFFFu, p, 4);
-            sc[u] = valid[u] ? p : -INFINITY;
+            for (int u = 0; u < UK; u++) {
+                const uint32_t t = tb + g + 4 * u;
+                valid[u] = t < t1;
+                if (valid[u]) {
+                    const uint4 *kr = reinterpret_cast<const uint4 *>(Kb + (uint64_t)t * 128) + li;
+                    const uint4 *vr = reinterpret_cast<const uint4 *>(Vb + (uint64_t)t * 128) + li;
+                    kv[u][0] = __ldcg(kr);
+                    kv[u][1] = __ldcg(kr + 8);
+                    vv[u][0] = __ldcg(vr);
+                    vv[u][1] = __ldcg(vr + 8);
+                } else {
+                    kv[u][0] = kv[u][1] = vv[u][0] = vv[u][1] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            sdpa_step<UK>(q, kv, vv, valid, m, l, acc);
         }
-        float mn = m;
-#pragma unroll
-        for (int u = 0; u < UK; u++) mn = fmaxf(mn, sc[u]);
-        const float mu = (mn == -INFINITY) ? 0.0f : mn;
-        const float corr = exp2f(m - mu);
-        l *= corr;
-#pragma unroll
-        for (int i = 0; i < 16; i++) acc[i] *= corr;
-#pragma unroll
-        for (int u = 0; u < UK; u++) {
-            const float p = exp2f(sc[u] - mu);
-            l += p;
-            float vf[16];
-            unpack8(vv[u][0], vf);
-            unpack8(vv[u][1], vf + 8);
-#pragma unroll
-            for (int i = 0; i < 16; i++) acc[i] = fmaf(p, vf[i], acc[i]);
-        }
-        m = mn;
     }
+    if (status != GPUOS_ST_OK) return status;
     /* merge the four groups (lanes li, li+8, li+16, li+24) */
 #pragma unroll
     for (int o = 8; o <= 16; o <<= 1) {
@@ -834,9 +894,8 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
             float r[16];
 #pragma unroll
             for (int i = 0; i < 16; i++) r[i] = acc[i] * inv;
-            uint4 *op = reinterpret_cast<uint4 *>(o16) + 2 * li;
-            op[0] = pack8(r);
-            op[1] = pack8(r + 8);
+            reinterpret_cast<uint4 *>(o16 + 8 * li)[0] = pack8(r);
+            reinterpret_cast<uint4 *>(o16 + 64 + 8 * li)[0] = pack8(r + 8);
         }
         return GPUOS_ST_OK;
     }
@@ -847,7 +906,10 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
     float *part = ws + (bh * nch + c) * 130;
     if (g == 0) {
 #pragma unroll
-        for (int i = 0; i < 16; i++) __stcg(part + 2 + 16 * li + i, acc[i]);
+        for (int i = 0; i < 8; i++) {
+            __stcg(part + 2 + 8 * li + i, acc[i]);
+            __stcg(part + 2 + 64 + 8 * li + i, acc[8 + i]);
+        }
         if (li == 0) {
             __stcg(part, m);
             __stcg(part + 1, l);
@@ -867,10 +929,10 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
     float den = 0.0f, o4[4] = {0.f, 0.f, 0.f, 0.f};
     for (uint32_t k = 0; k < nchb; k++) {
         const float *pk = ws + (bh * nch + k) * 130;
-        const float w = exp2f(__ldcg(pk) - M);
-        den += __ldcg(pk + 1) * w;
+        const float wgt = exp2f(__ldcg(pk) - M);
+        den += __ldcg(pk + 1) * wgt;
 #pragma unroll
-        for (int i = 0; i < 4; i++) o4[i] += __ldcg(pk + 2 + 4 * lane + i) * w;
+        for (int i = 0; i < 4; i++) o4[i] += __ldcg(pk + 2 + 4 * lane + i) * wgt;
     }
     const float inv = 1.0f / den;
     uint2 st;
@@ -965,18 +1027,18 @@ __device__ gpuos_op_fn g_builtin_ops[GPUOS_OP_BUILTIN_COUNT] = {
  * Persistent executor
  * ======================================================================== */
 
-/* Work-queue entry word: [63:24] stamp = (index + 1) mod 2^40, [23:8] ring
- * slot, [7:0] helper index (the helper's first tile). One 64-bit word, so the
- * claimer learns everything with the acquire load that finds it published.
- * The queue holds more than GPUOS_HELPERS x ring_entries entries, so the
- * entry a publication overwrites belongs to a ticket at least ring_entries
- * older, which has completed; completion implies every helper entry of it
- * was read. No producer-side check is needed. */
+/* Work-queue entry word: [63:28] stamp = (index + 1) mod 2^36, [27:12] ring
+ * slot, [11:0] helper index (the helper's first tile). One 64-bit word, so
+ * the claimer learns everything with the acquire load that finds it
+ * published. The queue holds more than GPUOS_HELPERS x ring_entries entries,
+ * so the entry a publication overwrites belongs to a ticket at least
+ * ring_entries older, which has completed; completion implies every helper
+ * entry of it was read. No producer-side check is needed. */
 DEV uint64_t tq_word(uint64_t idx, uint32_t slot, uint32_t helper)
 {
-    return (((idx + 1) & GPUOS_TQ_STAMP_MASK) << 24) | ((uint64_t)(slot & 0xFFFFu) << 8) | (helper & 0xFFu);
+    return (((idx + 1) & GPUOS_TQ_STAMP_MASK) << 28) | ((uint64_t)(slot & 0xFFFFu) << 12) | (helper & 0xFFFu);
 }
-DEV bool tq_is(uint64_t w, uint64_t idx) { return (w >> 24) == ((idx + 1) & GPUOS_TQ_STAMP_MASK); }
+DEV bool tq_is(uint64_t w, uint64_t idx) { return (w >> 28) == ((idx + 1) & GPUOS_TQ_STAMP_MASK); }
 
 DEV void fence_acq_rel_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
 
@@ -1009,15 +1071,24 @@ DEV void set_exit(const gpuos_exec_params &p, uint32_t reason)
     st_relaxed_sys32(&p.hctl->state, 2u);
 }
 
+/* Helper warps per descriptor: one per tile up to GPUOS_HELPERS, except row
+ * ops, whose tiles (one row) are small: one helper per four rows. */
+DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles)
+{
+    uint32_t hlp = ntiles;
+    if (op_id >= GPUOS_OP_SOFTMAX && op_id <= GPUOS_OP_ROWMIN) hlp = (ntiles + 3u) / 4u;
+    return hlp < GPUOS_HELPERS ? hlp : GPUOS_HELPERS;
+}
+
 /* The sequencer warp: ring -> mirror + work queue, up to 64 descriptors per
  * batch (two ring slots per lane: slot s + lane and s + 32 + lane). */
 #define SEQ_SPL 2
-DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
+DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
 {
     const uint32_t lane = lane_id();
     uint64_t *ws = p.warp_stats + (uint64_t)gw * GPUOS_WS_N;
     uint64_t s = 0, e = 0;
-    uint64_t n_seq = 0, n_idle = 0, n_sleep = 0, t_body = 0, t_mirror = 0, t_pubs = 0;
+    uint64_t n_seq = 0, n_idle = 0, n_sleep = 0, t_body = 0, t_mirror = 0, t_pubs = 0, n_inline = 0;
     uint32_t polls = 0;
     uint64_t hb = ld_relaxed_sys(&p.hctl->heartbeat);
     uint64_t t_active = 0;
@@ -1070,6 +1141,14 @@ DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
         }
         const uint64_t t_obs = globaltimer();
         polls = 0;
+        /* echo the observation time into each record at once (a posted
+         * write): the host can time commit -> observe without waiting for
+         * the whole descriptor */
+#pragma unroll
+        for (int h = 0; h < SEQ_SPL; h++) {
+            const uint32_t pos = lane + 32u * h;
+            if (pos < k) st_relaxed_sys(&p.rec[(uint32_t)((s + pos) & p.ring_mask)].t_dispatch, t_obs);
+        }
         /* the commits seen above happen-before everything below */
         fence_acq_rel_sys();
         gpuos_desc dsc[SEQ_SPL];
@@ -1135,15 +1214,52 @@ DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
                     /* one work-queue entry per helper warp (at most GPUOS_HELPERS);
                      * helper i starts with tile i and takes later tiles from the
                      * descriptor's tile counter */
-                    nt[h] = dsc[h].ntiles < GPUOS_HELPERS ? dsc[h].ntiles : GPUOS_HELPERS;
-                    dsc[h].user = t_obs;               /* -> t_dispatch */
-                    dsc[h].seq = (uint64_t)version;    /* -> version, pad */
+                    nt[h] = helper_count(dsc[h].op_id, dsc[h].ntiles);
+                    dsc[h].user = t_obs;                                    /* -> t_dispatch */
+                    dsc[h].seq = (uint64_t)version | ((uint64_t)nt[h] << 32); /* -> version, helpers */
                     uint4 *mv = reinterpret_cast<uint4 *>(p.mirror + (uint32_t)(my_t & p.ring_mask));
                     const uint4 *dv = reinterpret_cast<const uint4 *>(&dsc[h]);
 #pragma unroll
                     for (int i = 0; i < 8; i++) __stcg(mv + i, dv[i]);
                 }
             }
+        }
+        /* An idle ring (a batch of one) and a dependency-free single-tile
+         * descriptor: the sequencer runs the tile itself, sparing the
+         * mirror -> work queue -> worker hop. */
+        uint32_t inl = 0;
+        if (lane == 0)
+            inl = (k == 1 && status[0] == GPUOS_ST_OK && dsc[0].ntiles == 1 && dsc[0].dep[0] == 0 &&
+                   dsc[0].dep[1] == 0) ? 1u : 0u;
+        inl = __shfl_sync(0xFFFFFFFFu, inl, 0);
+        if (inl) {
+            const uint32_t slot = (uint32_t)(s & p.ring_mask);
+            if (lane == 0) {
+                uint4 *sv = reinterpret_cast<uint4 *>(sd);
+                const uint4 *dv = reinterpret_cast<const uint4 *>(&dsc[0]);
+#pragma unroll
+                for (int i = 0; i < 8; i++) sv[i] = dv[i];
+                const uint64_t ts = globaltimer();
+                *reinterpret_cast<volatile uint64_t *>(p.t_pub + slot) = ts;
+                *reinterpret_cast<volatile uint64_t *>(p.t_start + slot) = ts;
+            }
+            __syncwarp();
+            const gpuos_op_fn fn = reinterpret_cast<gpuos_op_fn>(__ldcg(
+                reinterpret_cast<const unsigned long long *>(p.table) + (version & 1u) * GPUOS_MAX_OPS + sd->op_id));
+            int32_t st = GPUOS_ST_BAD_OP;
+            if (fn != nullptr) st = fn(sd, 0);
+            __syncwarp();
+            if (lane == 0) complete_desc(p, s, slot, st, version, t_obs);
+            s += 1;
+            n_seq += 1;
+            n_inline += 1;
+            if (lane == 0) {
+                st_relaxed_sys(&p.hctl->sequenced, s);
+                ws[GPUOS_WS_SEQ] = n_seq;
+                ws[GPUOS_WS_TILES] = n_inline;
+            }
+            idle.start();
+            continue;
         }
         /* every lane's mirror writes happen-before every lane's fence */
         __syncwarp();
@@ -1164,30 +1280,42 @@ DEV void sequencer(const gpuos_exec_params &p, uint32_t gw)
             base += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
         const uint32_t total = base;
-        const uint32_t total0 = __shfl_sync(0xFFFFFFFFu, excl[SEQ_SPL - 1], 0); /* start of second half */
-        /* entries j = 0 .. total-1 spread over the lanes; the owner of j is the
-         * last position whose range starts at or before it (a 5-step search
-         * inside the half that holds j) */
-        for (uint32_t j0 = 0; j0 < total; j0 += 32) {
-            const uint32_t j = j0 + lane;
-            const bool second = j >= total0;
-            uint32_t i = 0;
+        /* Publication. Each lane writes the first (up to 16) entries of its own
+         * descriptors; descriptors with more entries are finished by the
+         * whole warp, one after another. */
+        {
+            uint32_t most = nt[0] > nt[1] ? nt[0] : nt[1];
 #pragma unroll
-            for (int step = 16; step > 0; step >>= 1) {
-                const uint32_t cand = i + (uint32_t)step; /* <= 31 */
-                const uint32_t st0 = __shfl_sync(0xFFFFFFFFu, excl[0], cand);
-                const uint32_t st1 = __shfl_sync(0xFFFFFFFFu, excl[1], cand);
-                if ((second ? st1 : st0) <= j) i = cand;
+            for (int o = 16; o > 0; o >>= 1) most = max(most, __shfl_xor_sync(0xFFFFFFFFu, most, o));
+            const uint32_t jmax = most < 16u ? most : 16u;
+#pragma unroll
+            for (int h = 0; h < SEQ_SPL; h++) {
+                const uint32_t slot = (uint32_t)((s + lane + 32u * h) & p.ring_mask);
+                for (uint32_t j = 0; j < jmax; j++) {
+                    if (j < nt[h]) {
+                        const uint64_t idx = e + excl[h] + j;
+                        *reinterpret_cast<volatile unsigned long long *>(p.tq + (idx & p.tq_mask)) =
+                            tq_word(idx, slot, j);
+                    }
+                }
             }
-            /* both shuffles on every lane (a shuffle must not diverge) */
-            const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, excl[0], i);
-            const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, excl[1], i);
-            const uint32_t bi = second ? b1 : b0;
-            const uint32_t pos = i + (second ? 32u : 0u);
-            if (j < total) {
-                const uint64_t idx = e + j;
-                *reinterpret_cast<volatile unsigned long long *>(p.tq + (idx & p.tq_mask)) =
-                    tq_word(idx, (uint32_t)((s + pos) & p.ring_mask), j - bi);
+            if (most > 16u) {
+#pragma unroll
+                for (int h = 0; h < SEQ_SPL; h++) {
+                    uint32_t big = __ballot_sync(0xFFFFFFFFu, nt[h] > 16u);
+                    while (big) {
+                        const uint32_t i = (uint32_t)(__ffs(big) - 1);
+                        big &= big - 1;
+                        const uint32_t nti = __shfl_sync(0xFFFFFFFFu, nt[h], i);
+                        const uint32_t bi = __shfl_sync(0xFFFFFFFFu, excl[h], i);
+                        const uint32_t slot = (uint32_t)((s + i + 32u * h) & p.ring_mask);
+                        for (uint32_t j = 16u + lane; j < nti; j += 32) {
+                            const uint64_t idx = e + bi + j;
+                            *reinterpret_cast<volatile unsigned long long *>(p.tq + (idx & p.tq_mask)) =
+                                tq_word(idx, slot, j);
+                        }
+                    }
+                }
             }
         }
         const uint64_t t_pub = globaltimer();
@@ -1256,15 +1384,14 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         w = __shfl_sync(0xFFFFFFFFu, w, 0);
         unsigned long long e_next = 0;
         if (lane == 0) e_next = atomicAdd(&p.dctl->tq_claim, 1ull); /* overlaps the tile */
-        const uint32_t slot = (uint32_t)((w >> 8) & 0xFFFFu);
-        uint32_t tile = (uint32_t)(w & 0xFFu); /* helper index = its first tile */
+        const uint32_t slot = (uint32_t)((w >> 12) & 0xFFFFu);
+        uint32_t tile = (uint32_t)(w & 0xFFFu); /* helper index = its first tile */
         /* descriptor -> shared memory */
         reinterpret_cast<uint32_t *>(sd)[lane] = __ldcg(reinterpret_cast<const uint32_t *>(p.mirror + slot) + lane);
         __syncwarp();
         const uint64_t ticket = sd->ticket;
         const uint32_t ntiles = sd->ntiles;
-        const uint32_t helpers = ntiles < GPUOS_HELPERS ? ntiles : GPUOS_HELPERS;
-        if (lane == 0 && tile == 0) *reinterpret_cast<volatile uint64_t *>(p.t_start + slot) = globaltimer();
+        const uint32_t helpers = sd->pad; /* helper count fixed by the sequencer */
         int32_t dstatus = GPUOS_ST_OK;
         if (lane == 0) {
             for (int i = 0; i < 2; i++) {
@@ -1296,6 +1423,8 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
             }
         }
         dstatus = __shfl_sync(0xFFFFFFFFu, dstatus, 0);
+        /* tile 0 starts once its dependencies are met */
+        if (lane == 0 && tile == 0) *reinterpret_cast<volatile uint64_t *>(p.t_start + slot) = globaltimer();
         __syncwarp();
         const gpuos_op_fn fn = reinterpret_cast<gpuos_op_fn>(__ldcg(
             reinterpret_cast<const unsigned long long *>(p.table) + (sd->version & 1u) * GPUOS_MAX_OPS + sd->op_id));
@@ -1358,7 +1487,7 @@ extern "C" __global__ void __launch_bounds__(GPUOS_MAX_WPB * 32, 1) gpuos_execut
     stage_init(p.stage_bytes);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
-    if (blockIdx.x == 0 && warp == 0) sequencer(p, gw);
+    if (blockIdx.x == 0 && warp == 0) sequencer(p, &sdesc[0], gw);
     else worker(p, &sdesc[warp], gw);
 }
 
@@ -1482,6 +1611,7 @@ static __device__ __align__(256) unsigned char g_sdpa_scratch[GPUOS_NOALLOC_BYTE
 extern "C" __global__ void __launch_bounds__(32) gpuos_sdpa_noalloc_kernel(gpuos_devdesc d)
 {
     __shared__ __align__(16) gpuos_devdesc sd;
+    stage_init(0); /* the op body reads the staging header: none here (register path) */
     reinterpret_cast<uint32_t *>(&sd)[lane_id()] = reinterpret_cast<const uint32_t *>(&d)[lane_id()];
     __syncwarp();
     if (blockIdx.x < sd.ntiles) (void)sdpa_tile(&sd, blockIdx.x);
@@ -1526,6 +1656,6 @@ extern "C" GPUOS_API int gpuos_sdpa_noalloc(const void *q, const void *Kc, const
     d.dims[5] = GPUOS_NOALLOC_MAX_BH; /* counters reserved at the start of the array */
     d.fparam[0] = scale;
     d.ntiles = B * H * ((Lmax + GPUOS_SDPA_CHUNK - 1) / GPUOS_SDPA_CHUNK);
-    gpuos_sdpa_noalloc_kernel<<<d.ntiles, 32, 0, (cudaStream_t)stream>>>(d);
+    gpuos_sdpa_noalloc_kernel<<<d.ntiles, 32, gpuos_dev_dyn_smem(1, 0), (cudaStream_t)stream>>>(d);
     return cudaGetLastError() == cudaSuccess ? GPUOS_OK : GPUOS_ECUDA;
 }

@@ -749,6 +749,8 @@ static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint3
         harvest_one(c, prev);
     }
     gpuos_desc *s = c->ring + slot;
+    /* the device echoes its observation time here (see gpuos_calibrate) */
+    __atomic_store_n(&c->rec[slot].t_dispatch, (uint64_t)0, __ATOMIC_RELAXED);
     gpuos_desc w = *d;
     w.ntiles = nt;
     w.dep[0] = deps[0];
@@ -1022,11 +1024,16 @@ int gpuos_calibrate(gpuos_ctx *c, uint32_t pings, int64_t *off_lo, int64_t *off_
         if (rc) return rc;
         const gpuos_rec_dev *r = c->rec + (t & c->mask);
         uint32_t spins = 0;
-        while (load_acq(&r->done_seq) < t + 1) {
+        /* the sequencer echoes its observation time into the record as soon
+         * as it sees the commit: t0 <= observation <= t1 */
+        uint64_t td = 0;
+        while ((td = __atomic_load_n(&r->t_dispatch, __ATOMIC_ACQUIRE)) == 0) {
             if ((++spins & 0xFFFFFu) == 0 && executor_gone(c)) return GPUOS_ESTOPPED;
         }
         const uint64_t t1 = now_ns();
-        const uint64_t td = __atomic_load_n(&r->t_dispatch, __ATOMIC_RELAXED);
+        while (load_acq(&r->done_seq) < t + 1) {
+            if ((++spins & 0xFFFFFu) == 0 && executor_gone(c)) return GPUOS_ESTOPPED;
+        }
         const uint64_t rtt = t1 - t0;
         if (rtts) rtts[i] = rtt;
         if (rtt < best) best = rtt;

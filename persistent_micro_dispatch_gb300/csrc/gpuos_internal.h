@@ -13,15 +13,15 @@
 #define GPUOS_EW_VPT 32                   /* 16-byte vectors per lane per element-wise tile */
 #define GPUOS_EW_TILE_F32 (32 * GPUOS_EW_VPT * 4)  /* 4096 fp32 elements */
 #define GPUOS_EW_TILE_BF16 (32 * GPUOS_EW_VPT * 8) /* 8192 bf16 elements */
-#define GPUOS_SDPA_CHUNK 512              /* key rows per decode-attention tile */
+#define GPUOS_SDPA_CHUNK 256              /* key rows per decode-attention tile */
 #define GPUOS_VM_COLS 32                  /* output columns per vecmat tile */
 #define GPUOS_ROW_REG_MAX 4096            /* rows up to this width stay in registers */
 #define GPUOS_MAX_WPB 16
 #define GPUOS_MAX_REGS 128 /* registers per thread: 65536 / (16 warps x 32) */
 #define GPUOS_TILE_MAX (1u << 30)          /* tiles per descriptor */
-#define GPUOS_HELPERS 64                   /* work-queue entries (helper warps) per descriptor at most */
+#define GPUOS_HELPERS 1024                 /* work-queue entries (helper warps) per descriptor at most */
 #define GPUOS_TQ_MAX (1u << 30)            /* work-queue entries */
-#define GPUOS_TQ_STAMP_MASK 0xFFFFFFFFFFull /* 40-bit stamps */
+#define GPUOS_TQ_STAMP_MASK 0xFFFFFFFFFull /* 36-bit stamps */
 
 /* Mirror of a descriptor in device memory, written by the sequencer warp.
  * Same layout as gpuos_desc except the last fields. */
@@ -42,7 +42,7 @@ typedef struct gpuos_devdesc {
 } gpuos_devdesc;
 
 /* Work-queue entries are single 64-bit words (see tq_word in the device
- * code): 40-bit stamp, 16-bit ring slot, 8-bit helper index. */
+ * code): 36-bit stamp, 16-bit ring slot, 12-bit helper index. */
 
 /* Completion record in host-visible memory, written by the device. */
 typedef struct gpuos_rec_dev {

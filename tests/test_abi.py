@@ -77,7 +77,7 @@ def test_tiling_rule(G):
     assert G.op_ntiles(_desc(G, "gelu", 0, (0,))) == 1            # empty op: one tile
     assert G.op_ntiles(_desc(G, "softmax", 1, (37, 1024))) == 37  # one row per tile
     assert G.op_ntiles(_desc(G, "rope", 1, (5, 32, 128))) == 5
-    assert G.op_ntiles(_desc(G, "sdpa", 1, (3, 32, 128, 4096, 1025, 96))) == 3 * 32 * 3
+    assert G.op_ntiles(_desc(G, "sdpa", 1, (3, 32, 128, 4096, 1025, 96))) == 3 * 32 * 5  # 256-row chunks
     assert G.op_ntiles(_desc(G, "vecmat", 1, (1024, 1024))) == 32
     assert G.op_ntiles(_desc(G, "nop")) == 1
 

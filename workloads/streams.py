@@ -46,7 +46,7 @@ ALL_OPS = ELEMENTWISE + ROWOPS + ("rope", "kv_write", "sdpa", "vecmat", "nop")
 # positions; the CUDA path keeps one partial (m, l, acc[D]) per chunk in a
 # caller-provided fp32 workspace followed by one uint32 counter per
 # (request, head). The layout is part of the descriptor contract.
-SDPA_CHUNK = 512
+SDPA_CHUNK = 256
 
 # Canary byte written into every output arena before a run; bytes that no op
 # writes must still hold it afterwards.
