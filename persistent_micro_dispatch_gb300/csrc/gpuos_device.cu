@@ -1382,8 +1382,6 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         leave = __shfl_sync(0xFFFFFFFFu, leave, 0);
         if (leave) break;
         w = __shfl_sync(0xFFFFFFFFu, w, 0);
-        unsigned long long e_next = 0;
-        if (lane == 0) e_next = atomicAdd(&p.dctl->tq_claim, 1ull); /* overlaps the tile */
         const uint32_t slot = (uint32_t)((w >> 12) & 0xFFFFu);
         uint32_t tile = (uint32_t)(w & 0xFFFu); /* helper index = its first tile */
         /* descriptor -> shared memory */
@@ -1470,6 +1468,10 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
             ws[GPUOS_WS_SLEEPS] = n_sleep;
             ws[GPUOS_WS_DEPWAIT] = n_depw;
         }
+        /* claim the next entry only now: a claim held while this warp was
+         * busy would keep a published tile waiting behind this one */
+        unsigned long long e_next = 0;
+        if (lane == 0) e_next = atomicAdd(&p.dctl->tq_claim, 1ull);
         e = __shfl_sync(0xFFFFFFFFu, e_next, 0);
         __syncwarp();
     }
