@@ -117,12 +117,15 @@ void orc_relu(int dtype, const void *a, double *out, long n)
     }
 }
 
-/* GELU, exact form: c = x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)). */
+/* GELU, exact form: c = x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), evaluated
+ * as 0.5 x erfc(-x / sqrt 2) (the identity 1 + erf(z) = erfc(-z)), which
+ * keeps full relative accuracy for x < 0, where 1 + erf cancels to 0 in
+ * double below x = -8.3. */
 void orc_gelu(int dtype, const void *a, double *out, long n)
 {
     for (long i = 0; i < n; i++) {
         double x = load(dtype, a, i);
-        out[i] = 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+        out[i] = 0.5 * x * erfc(-x / sqrt(2.0));
     }
 }
 

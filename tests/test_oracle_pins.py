@@ -137,6 +137,18 @@ def test_gelu_odd_part_and_limits():
     assert -1e-20 < gb[2] <= 0.0 and gb[3] == 0.0
 
 
+def test_gelu_negative_tail_relative_accuracy():
+    """Deep in the negative tail GELU(x) = x Phi(x) is tiny but not zero; the
+    oracle must keep relative accuracy there (1 + erf cancels in double).
+    Reference: SciPy's normal CDF (ndtr), an independent library routine."""
+    sp = pytest.importorskip("scipy.special")
+    a = np.array([-4.0, -6.0, -8.0, -9.0, -10.0, -12.0, -20.0, -30.0], np.float32)
+    got = _ew("gelu", "f32", a)
+    want = a.astype(np.float64) * sp.ndtr(a.astype(np.float64))
+    assert np.all(want < 0)
+    assert np.max(np.abs(got / want - 1.0)) < 1e-12
+
+
 # ---- row ops -----------------------------------------------------------------------
 def _softmax(x, R, H):
     out = np.empty(R * H, np.float64)
