@@ -299,6 +299,8 @@ def main():
     ap.add_argument("--warps", type=int, default=0, help="executor warps per block (0 = default)")
     ap.add_argument("--stage-bytes", type=int, default=16384, help="shared-memory staging per warp (0 = none)")
     ap.add_argument("--blocks", type=int, default=0, help="executor blocks (0 = one per SM)")
+    ap.add_argument("--spin-polls", type=int, default=0, help="idle polls before backoff sleeps (0 = default)")
+    ap.add_argument("--backoff-max-ns", type=int, default=0, help="longest idle sleep (0 = default)")
     ap.add_argument("--graph", action="store_true",
                     help="also time the eager launches captured into a CUDA graph (replay, and re-capture per step)")
     ap.add_argument("--corun-gemm", action="store_true",
@@ -323,6 +325,10 @@ def main():
     cfg_kw = dict(device=local, idle_exit_ms=20000, stage_bytes=args.stage_bytes, blocks=args.blocks)
     if args.warps:
         cfg_kw["warps_per_block"] = args.warps
+    if args.spin_polls:
+        cfg_kw["spin_polls"] = args.spin_polls
+    if args.backoff_max_ns:
+        cfg_kw["backoff_max_ns"] = args.backoff_max_ns
     if args.profile_run and args.profile_desc and args.workload in ("c2", "c2l", "c3"):
         kw = dict(n_desc=args.profile_desc)
         if args.pool_log2:
@@ -416,6 +422,7 @@ def main():
     wall = t1 - t0
     kern_ms = ev0.elapsed_time(ev1)
     st = ex.stats()
+    tprof = ex.tile_profile()
     ex.shutdown()
     units, secs = aggregate(n_ops * args.steps, kern_ms / 1e3, world)
     value = units / secs
@@ -435,6 +442,19 @@ def main():
     if len(h):
         opn = np.array([s.ops[int(t) % n_ops].op for t in h["ticket"]])
         dur = (h["t_done_dev_ns"].astype(np.int64) - h["t_start_dev_ns"].astype(np.int64)) / 1e3
+        # dispatch gap of a dependent op: its last dependency done -> its tile 0 started
+        tix = h["ticket"].astype(np.int64)
+        jj = tix % n_ops
+        t_done = h["t_done_dev_ns"].astype(np.int64)
+        last_dep = np.full(len(h), -1, dtype=np.int64)
+        for k in range(2):
+            offk = np.array([(j - o.deps[k]) if len(o.deps) > k else 0 for j, o in enumerate(s.ops)],
+                            dtype=np.int64)[jj]
+            dep_t = tix - offk
+            idx = np.clip(np.searchsorted(tix, dep_t), 0, len(tix) - 1)
+            ok = (offk > 0) & (tix[idx] == dep_t)
+            last_dep = np.where(ok, np.maximum(last_dep, t_done[idx]), last_dep)
+        gap = np.where(last_dep >= 0, (h["t_start_dev_ns"].astype(np.int64) - last_dep) / 1e3, np.nan)
         per_op_bytes = np.array([S.sdpa_bytes(o, s.buffers[o.aux0.buf].data[o.aux0.off:o.aux0.off + o.dims[0]])
                                  if o.op == "sdpa" else S.op_bytes(o) for o in s.ops], dtype=np.float64)
         byts = per_op_bytes[(h["ticket"] % n_ops).astype(np.int64)]
@@ -442,6 +462,13 @@ def main():
             m = opn == k
             kinds[k] = {"n": int(m.sum()), "dur_us_p50": float(np.median(dur[m])),
                         "gbs_p50": float(np.median(byts[m] / np.maximum(dur[m], 1e-3) / 1e3))}
+            gk = gap[m & ~np.isnan(gap)]
+            if gk.size:
+                kinds[k]["dep_gap_us_p50"] = float(np.median(gk))
+            if k in tprof:  # mean device time per tile: in the op, finishing, waiting for inputs
+                tp = tprof[k]
+                kinds[k].update(tiles_per_op=tp["tiles"] / max(1, int(m.sum())), tile_body_us=tp["body_us"],
+                                tile_finish_us=tp["finish_us"], tile_dep_us=tp["dep_us"])
     peak, peak_kind = measured_peak_gbs()
     achieved = step_bytes * args.steps / (kern_ms / 1e3) / 1e9
     result = {

@@ -93,7 +93,8 @@ enum {
     GPUOS_OP_SDPA = 12,     /* o = softmax(scale q.K^T) V over rows 0..lens[b]-1; a = q[B][H][D],
                                b = Kc, aux1 = Vc [B][H][Lcap][D], aux0 = lens, out = o[B][H][D],
                                aux2 = 16-byte aligned fp32 workspace: first round_up(Ccap, 4)
-                               uint32 counters, then B*H*ceil(Lmax/256) partials of D+2 floats
+                               uint32 counters, then B*H*ceil(Lmax/32) partials of 132 floats
+                               {m, l, 2 pad, acc[128]}
                                (gpuos_sdpa_workspace_bytes(Bcap, H, D, Lmax) with Ccap = Bcap*H);
                                the counters must be zero before first use and every descriptor
                                leaves them zero; descriptors sharing a workspace use one Ccap;
@@ -196,6 +197,19 @@ typedef struct gpuos_stats_t {
     uint64_t seq_mirror_ns;  /* device: sequencer time mirroring + fencing */
     uint64_t seq_publish_ns; /* device: sequencer time publishing work-queue entries */
 } gpuos_stats_t;
+
+/* Where the executor's worker warps spent their time, per op id (device
+ * clock, summed over warps). Bucket b < GPUOS_OP_BUILTIN_COUNT is op id b;
+ * bucket GPUOS_OP_BUILTIN_COUNT gathers every user op id. */
+#define GPUOS_PROF_BUCKETS 16
+#define GPUOS_PROF_FIELDS 4
+typedef struct gpuos_tile_profile {
+    uint64_t tiles[GPUOS_PROF_BUCKETS];     /* tiles run */
+    uint64_t body_ns[GPUOS_PROF_BUCKETS];   /* inside the op's entry point */
+    uint64_t finish_ns[GPUOS_PROF_BUCKETS]; /* counting the helper's tiles and completing */
+    uint64_t dep_ns[GPUOS_PROF_BUCKETS];    /* from finding the work-queue entry to its
+                                               dependencies being met (mirror read included) */
+} gpuos_tile_profile;
 
 typedef struct gpuos_ctx gpuos_ctx;
 
@@ -302,11 +316,29 @@ GPUOS_API int gpuos_stop(gpuos_ctx *ctx, uint32_t timeout_ms);
 /* gpuos_stop, then free everything. The context is freed even on error. */
 GPUOS_API int gpuos_shutdown(gpuos_ctx *ctx, uint32_t timeout_ms);
 
-/* Host tiling rule of a built-in op (what ntiles the library will write). */
+/* Sum the worker warps' tile profiles (a snapshot; exact once the executor
+ * has left). Errors: EINVAL, ECUDA. */
+GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
+
+/* Host tiling rule of a built-in op (what ntiles the library will write);
+ * one tile is one warp's unit of work:
+ *   add/mul/relu/gelu  ceil(n / te), te the smallest power of two >= n / 16
+ *                      within [1024, 4096 (f32) or 8192 (bf16)] elements;
+ *                      the device splits n into ntiles ranges of
+ *                      round_up(ceil(n / ntiles), 256) elements
+ *   row ops            R (one row per tile)
+ *   rope, kv_write     B * ceil(H / 4) (one request, four heads per tile)
+ *   sdpa               B * H * ceil(Lmax / c), c = 256 key rows, halved down
+ *                      to 32 while B * H * ceil(Lmax / c) < 1536; a tile
+ *                      attends round_up(ceil(Lmax / chunks), 32) rows
+ *   vecmat             ceil(N / 8) (eight output columns per tile)
+ *   nop / empty op     1
+ * Returns GPUOS_EINVAL for a descriptor the library would reject. */
 GPUOS_API int gpuos_op_ntiles(const gpuos_desc *d, uint32_t *ntiles);
 
-/* Workspace bytes a decode-SDPA descriptor needs (fp32 partials of 512-row
- * chunks plus one counter per (b, h)). */
+/* Workspace bytes a decode-SDPA descriptor needs: one uint32 counter per
+ * (b, h), rounded up to 4, then fp32 partials for the finest split (32-row
+ * chunks). */
 GPUOS_API size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, uint32_t Lmax);
 
 /* Eager baseline: launch the same op bodies as ordinary kernels, one

@@ -79,8 +79,8 @@ def build(force: bool = False) -> str:
     dev_src = os.path.join(CSRC, "gpuos_device.cu")
     if force or _stale(EXEC_RDC, [dev_src] + headers):
         # every function of the relocatable build must fit the executor's
-        # per-thread register budget (launch bounds: 512 threads, 1 block/SM)
-        jobs.append(([NVCC] + ARCH + COMMON + ["-cubin", "-rdc=true", "-maxrregcount", "128", "-Xptxas", "-v",
+        # per-thread register budget (launch bounds: 384 threads, 1 block/SM)
+        jobs.append(([NVCC] + ARCH + COMMON + ["-cubin", "-rdc=true", "-maxrregcount", "168", "-Xptxas", "-v",
                                                dev_src, "-o", EXEC_RDC + ".tmp"],
                      os.path.join(BUILD, "gpuos_exec_rdc.ptxas.txt")))
     with cf.ThreadPoolExecutor(max_workers=4) as ex:
@@ -95,7 +95,7 @@ def build(force: bool = False) -> str:
     # at run time); it must not use more registers than the executor holds
     # per thread, so it is compiled with the executor's count as its cap.
     if os.path.exists(ext_src) and (force or _stale(EXT_CUBIN, [ext_src, LIB] + headers)):
-        regs = executor_regs()
+        regs = min(executor_regs(), 168)
         tmp = EXT_CUBIN + ".tmp"
         log = os.path.join(BUILD, "gpuos_ext_ops.ptxas.txt")
         _run([NVCC] + ARCH + COMMON + ["-cubin", "-rdc=true", "-maxrregcount", str(regs), "-Xptxas", "-v",

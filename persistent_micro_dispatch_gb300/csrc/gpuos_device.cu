@@ -64,6 +64,17 @@ DEV uint32_t ld_acquire_gpu32(const uint32_t *p)
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+/* Spin loops poll with relaxed loads (they read L2 and leave L1 alone) and
+ * take the acquire once, with a fence after the poll that succeeded: an
+ * acquire load also invalidates the SM's L1, and a spinning warp issuing one
+ * per poll would keep evicting the stack of the warp running an op on the
+ * same SM; a re-read would cost another L2 round trip. */
+DEV uint64_t ld_relaxed_gpu(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 DEV uint64_t ld_relaxed_sys(const uint64_t *p)
 {
     uint64_t v;
@@ -98,6 +109,25 @@ DEV void st_relaxed_sys32(uint32_t *p, uint32_t v)
 {
     asm volatile("st.relaxed.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+DEV void st_relaxed_gpu(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+/* Add with release (this thread's earlier writes) and acquire (the writes
+ * of every earlier adder) semantics at GPU scope; returns the old value. */
+DEV unsigned long long atom_add_acq_rel_gpu(unsigned long long *p, unsigned long long v)
+{
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+DEV uint32_t atom_add_acq_rel_gpu32(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 DEV void st_relaxed_gpu32(uint32_t *p, uint32_t v)
 {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -191,9 +221,10 @@ DEV float warp_min(float v)
 /* ---------------------------------------------------------------------------
  * Per-warp shared-memory staging. Dynamic shared memory of the executor (and
  * of the eager kernel) starts with a 16-byte header {stride, stage_bytes},
- * followed by one region per warp: {mbarrier, phase} and a staging buffer of
- * stage_bytes (16-byte aligned). stage_bytes == 0 means "no staging": ops use
- * their register path.
+ * followed by one region per warp: a 32-byte {mbarrier[2], phase[2]} block
+ * and a staging buffer of stage_bytes (16-byte aligned). Single-buffered ops
+ * use barrier 0 over the whole buffer; double-buffered ops use barrier i for
+ * half i. stage_bytes == 0 means "no staging": ops use their register path.
  * ------------------------------------------------------------------------- */
 struct StageHdr {
     uint32_t stride;      /* bytes between warp regions */
@@ -201,10 +232,11 @@ struct StageHdr {
     uint32_t pad[2];
 };
 struct WarpStage {
-    unsigned long long mbar; /* completion barrier of the warp's bulk copies */
-    uint32_t phase;          /* parity of the next phase to wait for */
-    uint32_t pad;
+    unsigned long long mbar[2]; /* completion barriers of the warp's bulk copies */
+    uint32_t phase[2];          /* parity of the next phase to wait for, per barrier */
+    uint32_t pad[2];
 };
+#define GPUOS_WARP_STAGE_HDR 32u
 extern __shared__ __align__(16) unsigned char g_dyn_smem[];
 
 DEV StageHdr *stage_hdr() { return reinterpret_cast<StageHdr *>(g_dyn_smem); }
@@ -212,21 +244,23 @@ DEV WarpStage *warp_stage()
 {
     return reinterpret_cast<WarpStage *>(g_dyn_smem + 16 + (threadIdx.x >> 5) * stage_hdr()->stride);
 }
-DEV unsigned char *warp_stage_buf() { return reinterpret_cast<unsigned char *>(warp_stage()) + 16; }
+DEV unsigned char *warp_stage_buf() { return reinterpret_cast<unsigned char *>(warp_stage()) + GPUOS_WARP_STAGE_HDR; }
 DEV uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-/* Lay out the header and every warp's barrier (all threads of the block). */
+/* Lay out the header and every warp's barriers (all threads of the block). */
 DEV void stage_init(uint32_t stage_bytes)
 {
     if (threadIdx.x == 0) {
-        stage_hdr()->stride = 16 + stage_bytes;
+        stage_hdr()->stride = GPUOS_WARP_STAGE_HDR + stage_bytes;
         stage_hdr()->stage_bytes = stage_bytes;
     }
     __syncthreads();
     if ((threadIdx.x & 31u) == 0) {
         WarpStage *w = warp_stage();
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&w->mbar)) : "memory");
-        w->phase = 0;
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&w->mbar[0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&w->mbar[1])) : "memory");
+        w->phase[0] = 0;
+        w->phase[1] = 0;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
@@ -269,6 +303,48 @@ DEV bool mbar_wait(unsigned long long *mbar, uint32_t parity)
 
 enum { EW_ADD = 0, EW_MUL = 1, EW_RELU = 2, EW_GELU = 3 };
 
+/* erfc(x) by the Chebyshev fit of Numerical Recipes (Press, Teukolsky,
+ * Vetterling, Flannery, 2nd ed., section 6.2, function erfcc): for z = |x|,
+ * t = 1 / (1 + z/2), erfc(z) = t exp(-z^2 + P(t)) with a degree-9 polynomial
+ * P, fractional error below 1.2e-7 for every z >= 0; erfc(-z) = 2 - erfc(z).
+ * No branch: one hardware reciprocal, one hardware exp2 and about fifteen
+ * multiply-adds per element, a fraction of a library erfc's code (the op
+ * bodies run from a cold instruction cache more often than not). */
+DEV float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+/* e^y as 2^(y log2 e): the product's rounding error is carried as a residual
+ * (one fma) and applied to first order, so the result keeps the accuracy of
+ * the hardware's ex2 (a few ulps) for |y| up to ~87. */
+DEV float exp_ex2(float y)
+{
+    const float t = y * 1.44269504f;
+    const float e = fmaf(y, 1.44269504f, -t) + y * 1.92596299e-8f;
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return fmaf(r, e * 0.693147181f, r);
+}
+DEV float erfc_nr(float x)
+{
+    const float z = fabsf(x);
+    const float t = rcp_approx(fmaf(0.5f, z, 1.0f));
+    float p = 0.17087277f;
+    p = fmaf(t, p, -0.82215223f);
+    p = fmaf(t, p, 1.48851587f);
+    p = fmaf(t, p, -1.13520398f);
+    p = fmaf(t, p, 0.27886807f);
+    p = fmaf(t, p, -0.18628806f);
+    p = fmaf(t, p, 0.09678418f);
+    p = fmaf(t, p, 0.37409196f);
+    p = fmaf(t, p, 1.00002368f);
+    p = fmaf(t, p, -1.26551223f);
+    const float r = t * exp_ex2(fmaf(-z, z, p));
+    return x >= 0.0f ? r : 2.0f - r;
+}
+
 template <int OP>
 DEV float ew1(float a, float b)
 {
@@ -278,7 +354,7 @@ DEV float ew1(float a, float b)
     /* GELU, exact form x * Phi(x) with Phi(x) = erfc(-x / sqrt 2) / 2: the
      * complementary error function keeps full relative accuracy for x < 0,
      * where 1 + erf(x / sqrt 2) would cancel */
-    return 0.5f * a * erfcf(-a * 0.70710678118654752f);
+    return 0.5f * a * erfc_nr(-a * 0.70710678118654752f);
 }
 
 template <int OP, bool BF>
@@ -301,19 +377,30 @@ DEV uint4 ew_vec(const uint4 &va, const uint4 &vb)
     }
 }
 
-/* Element-wise tile: 32 lanes x GPUOS_EW_VPT 16-byte vectors, in rounds of 8
- * independent vector loads per operand per lane. Unaligned operands take a
- * scalar path with the same arithmetic. */
+/* Elements per tile of an element-wise op. The host chose ntiles as
+ * ceil(n / te) for a te that is a multiple of GPUOS_EW_ALIGN; rounding
+ * ceil(n / ntiles) up to that multiple gives back a size no larger than te
+ * whose ntiles tiles cover n, so tile starts stay 16-byte aligned. */
+DEV uint32_t ew_tile_elems(uint64_t n, uint32_t ntiles)
+{
+    const uint64_t nt = ntiles ? ntiles : 1u;
+    const uint64_t per = (n + nt - 1) / nt;
+    return (uint32_t)((per + GPUOS_EW_ALIGN - 1) / GPUOS_EW_ALIGN * GPUOS_EW_ALIGN);
+}
+
+/* Element-wise tile: up to GPUOS_EW_VPT 16-byte vectors per lane, in rounds
+ * of 8 independent vector loads per operand per lane. Unaligned operands take
+ * a scalar path with the same arithmetic. */
 template <int OP, bool BF>
 DEV int ew_tile(const gpuos_devdesc *d, uint32_t tile)
 {
     constexpr uint32_t VEC = BF ? 8 : 4;
     constexpr uint32_t ES = BF ? 2 : 4;
-    constexpr uint32_t TILE = 32 * GPUOS_EW_VPT * VEC;
     constexpr bool BIN = (OP == EW_ADD || OP == EW_MUL);
-    constexpr int U = 8;
+    constexpr int U = (OP == EW_GELU) ? 2 : 8; /* GELU: short code, it is long per element */
     const uint32_t lane = lane_id();
     const uint64_t n = d->dims[0];
+    const uint32_t TILE = ew_tile_elems(n, d->ntiles);
     const uint64_t start = (uint64_t)tile * TILE;
     if (start >= n) return GPUOS_ST_OK;
     const uint32_t cnt = (uint32_t)((n - start) < TILE ? (n - start) : TILE);
@@ -365,11 +452,11 @@ DEV int ew_tile_staged(const gpuos_devdesc *d, uint32_t tile, uint32_t stage_byt
 {
     constexpr uint32_t VEC = BF ? 8 : 4;
     constexpr uint32_t ES = BF ? 2 : 4;
-    constexpr uint32_t TILE = 32 * GPUOS_EW_VPT * VEC;
     constexpr bool BIN = (OP == EW_ADD || OP == EW_MUL);
     constexpr uint32_t NOPS = BIN ? 2 : 1;
     const uint32_t lane = lane_id();
     const uint64_t n = d->dims[0];
+    const uint32_t TILE = ew_tile_elems(n, d->ntiles);
     const uint64_t start = (uint64_t)tile * TILE;
     if (start >= n) return GPUOS_ST_OK;
     const uint32_t cnt = (uint32_t)((n - start) < TILE ? (n - start) : TILE);
@@ -381,7 +468,7 @@ DEV int ew_tile_staged(const gpuos_devdesc *d, uint32_t tile, uint32_t stage_byt
     WarpStage *w = warp_stage();
     unsigned char *sa = warp_stage_buf();
     unsigned char *sb = sa + chunk * ES;
-    uint32_t phase = w->phase;
+    uint32_t phase = w->phase[0];
     int32_t st = GPUOS_ST_OK;
     for (uint32_t c0 = 0; c0 < nel; c0 += chunk) {
         const uint32_t ce = (nel - c0) < chunk ? (nel - c0) : chunk;
@@ -389,14 +476,14 @@ DEV int ew_tile_staged(const gpuos_devdesc *d, uint32_t tile, uint32_t stage_byt
         if (lane == 0) {
             /* earlier generic reads of the buffer before the async writes */
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_expect(&w->mbar, bytes * NOPS);
-            bulk_g2s(sa, pa + (uint64_t)c0 * ES, bytes, &w->mbar);
-            if (BIN) bulk_g2s(sb, pb + (uint64_t)c0 * ES, bytes, &w->mbar);
+            mbar_expect(&w->mbar[0], bytes * NOPS);
+            bulk_g2s(sa, pa + (uint64_t)c0 * ES, bytes, &w->mbar[0]);
+            if (BIN) bulk_g2s(sb, pb + (uint64_t)c0 * ES, bytes, &w->mbar[0]);
         }
-        if (!mbar_wait(&w->mbar, phase)) {
+        if (!mbar_wait(&w->mbar[0], phase)) {
             /* the copy did not land within the bound: wait once more (also
              * bounded) so that no copy is left writing the buffer, then fail */
-            mbar_wait(&w->mbar, phase);
+            mbar_wait(&w->mbar[0], phase);
             st = GPUOS_ST_COPY_TIMEOUT;
             phase ^= 1u;
             break;
@@ -406,14 +493,22 @@ DEV int ew_tile_staged(const gpuos_devdesc *d, uint32_t tile, uint32_t stage_byt
         const uint4 *vb = reinterpret_cast<const uint4 *>(sb);
         uint4 *vo = reinterpret_cast<uint4 *>(po + (uint64_t)c0 * ES);
         const uint32_t nv = bytes / 16u;
+        if (OP == EW_GELU) {
+#pragma unroll 1
+            for (uint32_t v = lane; v < nv; v += 32) {
+                const uint4 x = va[v];
+                __stcg(vo + v, ew_vec<OP, BF>(x, x));
+            }
+        } else {
 #pragma unroll 4
-        for (uint32_t v = lane; v < nv; v += 32) {
-            const uint4 x = va[v];
-            __stcg(vo + v, ew_vec<OP, BF>(x, BIN ? vb[v] : x));
+            for (uint32_t v = lane; v < nv; v += 32) {
+                const uint4 x = va[v];
+                __stcg(vo + v, ew_vec<OP, BF>(x, BIN ? vb[v] : x));
+            }
         }
         __syncwarp();
     }
-    if (lane == 0) w->phase = phase;
+    if (lane == 0) w->phase[0] = phase;
     __syncwarp();
     for (uint32_t i = nel + lane; i < cnt; i += 32) {
         if (BF) {
@@ -459,14 +554,32 @@ DEV int row_reg(const gpuos_devdesc *d, uint32_t row, uint32_t H)
     const uint32_t lane = lane_id();
     const uint32_t nv = H / 8;
     const uint4 *x = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)row * H);
+    /* LayerNorm: gamma and beta come into the warp's staging buffer by TMA
+     * bulk copies issued before the row is read, so their latency hides
+     * behind the row load and the two reductions */
+    const bool stg = (K == ROW_LN) && stage_hdr()->stage_bytes >= 4u * H;
+    WarpStage *w = warp_stage();
+    const uint4 *sgam = reinterpret_cast<const uint4 *>(warp_stage_buf());
+    const uint4 *sbet = sgam + nv;
+    if (stg && lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect(&w->mbar[0], 4u * H);
+        bulk_g2s(warp_stage_buf(), reinterpret_cast<const void *>(d->b), 2u * H, &w->mbar[0]);
+        bulk_g2s(warp_stage_buf() + 2u * H, reinterpret_cast<const void *>(d->aux0), 2u * H, &w->mbar[0]);
+    }
     uint4 r[J];
 #pragma unroll
     for (int j = 0; j < J; j++) {
         const uint32_t v = lane + 32u * j;
         if (v < nv) r[j] = __ldcg(x + v);
     }
+    /* reductions keep one accumulator per element of a vector: eight
+     * independent chains of J steps instead of one chain of 8 J */
     if (K == ROW_SUM || K == ROW_MAX || K == ROW_MIN) {
-        float acc = (K == ROW_SUM) ? 0.0f : (K == ROW_MAX ? -INFINITY : INFINITY);
+        const float init = (K == ROW_SUM) ? 0.0f : (K == ROW_MAX ? -INFINITY : INFINITY);
+        float a8[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) a8[i] = init;
 #pragma unroll
         for (int j = 0; j < J; j++) {
             const uint32_t v = lane + 32u * j;
@@ -475,11 +588,18 @@ DEV int row_reg(const gpuos_devdesc *d, uint32_t row, uint32_t H)
                 unpack8(r[j], f);
 #pragma unroll
                 for (int i = 0; i < 8; i++) {
-                    if (K == ROW_SUM) acc += f[i];
-                    else if (K == ROW_MAX) acc = fmaxf(acc, f[i]);
-                    else acc = fminf(acc, f[i]);
+                    if (K == ROW_SUM) a8[i] += f[i];
+                    else if (K == ROW_MAX) a8[i] = fmaxf(a8[i], f[i]);
+                    else a8[i] = fminf(a8[i], f[i]);
                 }
             }
+        }
+        float acc = a8[0];
+#pragma unroll
+        for (int i = 1; i < 8; i++) {
+            if (K == ROW_SUM) acc += a8[i];
+            else if (K == ROW_MAX) acc = fmaxf(acc, a8[i]);
+            else acc = fminf(acc, a8[i]);
         }
         if (K == ROW_SUM) acc = warp_sum(acc);
         else if (K == ROW_MAX) acc = warp_max(acc);
@@ -492,27 +612,37 @@ DEV int row_reg(const gpuos_devdesc *d, uint32_t row, uint32_t H)
     }
     uint4 *y = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(d->out) + (uint64_t)row * H);
     if (K == ROW_SOFTMAX) {
-        float m = -INFINITY;
+        float m8[8], s8[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            m8[i] = -INFINITY;
+            s8[i] = 0.0f;
+        }
 #pragma unroll
         for (int j = 0; j < J; j++) {
             if (lane + 32u * j < nv) {
                 float f[8];
                 unpack8(r[j], f);
 #pragma unroll
-                for (int i = 0; i < 8; i++) m = fmaxf(m, f[i]);
+                for (int i = 0; i < 8; i++) m8[i] = fmaxf(m8[i], f[i]);
             }
         }
+        float m = m8[0];
+#pragma unroll
+        for (int i = 1; i < 8; i++) m = fmaxf(m, m8[i]);
         m = warp_max(m);
+#pragma unroll
+        for (int j = 0; j < J; j++) {
+            if (lane + 32u * j < nv) {
+                float f[8];
+                unpack8(r[j], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) s8[i] += __expf(f[i] - m);
+            }
+        }
         float s = 0.0f;
 #pragma unroll
-        for (int j = 0; j < J; j++) {
-            if (lane + 32u * j < nv) {
-                float f[8];
-                unpack8(r[j], f);
-#pragma unroll
-                for (int i = 0; i < 8; i++) s += __expf(f[i] - m);
-            }
-        }
+        for (int i = 0; i < 8; i++) s += s8[i];
         const float inv = 1.0f / warp_sum(s);
 #pragma unroll
         for (int j = 0; j < J; j++) {
@@ -528,18 +658,25 @@ DEV int row_reg(const gpuos_devdesc *d, uint32_t row, uint32_t H)
         return GPUOS_ST_OK;
     }
     /* LayerNorm: biased variance, two passes over the registers. */
-    float s = 0.0f;
+    float s8[8], q8[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        s8[i] = 0.0f;
+        q8[i] = 0.0f;
+    }
 #pragma unroll
     for (int j = 0; j < J; j++) {
         if (lane + 32u * j < nv) {
             float f[8];
             unpack8(r[j], f);
 #pragma unroll
-            for (int i = 0; i < 8; i++) s += f[i];
+            for (int i = 0; i < 8; i++) s8[i] += f[i];
         }
     }
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) s += s8[i];
     const float mean = warp_sum(s) / (float)H;
-    float q = 0.0f;
 #pragma unroll
     for (int j = 0; j < J; j++) {
         if (lane + 32u * j < nv) {
@@ -548,26 +685,206 @@ DEV int row_reg(const gpuos_devdesc *d, uint32_t row, uint32_t H)
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 const float t = f[i] - mean;
-                q += t * t;
+                q8[i] = fmaf(t, t, q8[i]);
             }
         }
     }
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) q += q8[i];
     const float rstd = rsqrtf(warp_sum(q) / (float)H + d->fparam[0]);
     const uint4 *g = reinterpret_cast<const uint4 *>(d->b);
     const uint4 *bt = reinterpret_cast<const uint4 *>(d->aux0);
+    if (stg) {
+        const uint32_t ph = w->phase[0];
+        const bool ok = mbar_wait(&w->mbar[0], ph);
+        if (!ok) mbar_wait(&w->mbar[0], ph); /* leave no copy writing the buffer */
+        __syncwarp();
+        if (lane == 0) w->phase[0] = ph ^ 1u;
+        __syncwarp();
+        if (!ok) return GPUOS_ST_COPY_TIMEOUT;
+    }
 #pragma unroll
     for (int j = 0; j < J; j++) {
         const uint32_t v = lane + 32u * j;
         if (v < nv) {
             float f[8], gf[8], bf[8];
             unpack8(r[j], f);
-            unpack8(__ldcg(g + v), gf);
-            unpack8(__ldcg(bt + v), bf);
+            unpack8(stg ? sgam[v] : __ldcg(g + v), gf);
+            unpack8(stg ? sbet[v] : __ldcg(bt + v), bf);
 #pragma unroll
             for (int i = 0; i < 8; i++) f[i] = (f[i] - mean) * rstd * gf[i] + bf[i];
             __stcg(y + v, pack8(f));
         }
     }
+    __syncwarp(); /* every lane's reads of the buffer before it is reused */
+    return GPUOS_ST_OK;
+}
+
+/* Rows staged in the warp's shared buffer: the row (and LayerNorm's gamma
+ * and beta) arrive by TMA bulk copies and every pass is a rolled loop over
+ * shared memory, so the code a tile runs stays a few hundred instructions
+ * (the op bodies mostly run from a cold instruction cache). LayerNorm rows
+ * whose x, gamma and beta do not fit together keep x resident and stream
+ * gamma and beta through the rest of the buffer in column chunks. */
+DEV bool stage_wait0(WarpStage *w)
+{
+    const uint32_t ph = w->phase[0];
+    const bool ok = mbar_wait(&w->mbar[0], ph);
+    if (!ok) mbar_wait(&w->mbar[0], ph); /* leave no copy writing the buffer */
+    __syncwarp();
+    if (lane_id() == 0) w->phase[0] = ph ^ 1u;
+    __syncwarp();
+    return ok;
+}
+
+template <int K>
+DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
+{
+    const uint32_t lane = lane_id(), nv = H / 8;
+    WarpStage *w = warp_stage();
+    unsigned char *buf = warp_stage_buf();
+    const uint4 *sx = reinterpret_cast<const uint4 *>(buf);
+    const uint16_t *x = reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)row * H;
+    if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect(&w->mbar[0], 2u * H + (K == ROW_LN ? 4u * C : 0u));
+        bulk_g2s(buf, x, 2u * H, &w->mbar[0]);
+        if (K == ROW_LN) {
+            bulk_g2s(buf + 2u * H, reinterpret_cast<const void *>(d->b), 2u * C, &w->mbar[0]);
+            bulk_g2s(buf + 2u * H + 2u * C, reinterpret_cast<const void *>(d->aux0), 2u * C, &w->mbar[0]);
+        }
+    }
+    if (!stage_wait0(w)) return GPUOS_ST_COPY_TIMEOUT;
+    if (K == ROW_SUM || K == ROW_MAX || K == ROW_MIN) {
+        const float init = (K == ROW_SUM) ? 0.0f : (K == ROW_MAX ? -INFINITY : INFINITY);
+        float a8[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) a8[i] = init;
+#pragma unroll 2
+        for (uint32_t v = lane; v < nv; v += 32) {
+            float f[8];
+            unpack8(sx[v], f);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                if (K == ROW_SUM) a8[i] += f[i];
+                else if (K == ROW_MAX) a8[i] = fmaxf(a8[i], f[i]);
+                else a8[i] = fminf(a8[i], f[i]);
+            }
+        }
+        float acc = a8[0];
+#pragma unroll
+        for (int i = 1; i < 8; i++) {
+            if (K == ROW_SUM) acc += a8[i];
+            else if (K == ROW_MAX) acc = fmaxf(acc, a8[i]);
+            else acc = fminf(acc, a8[i]);
+        }
+        if (K == ROW_SUM) acc = warp_sum(acc);
+        else if (K == ROW_MAX) acc = warp_max(acc);
+        else acc = warp_min(acc);
+        if (lane == 0) {
+            if (K == ROW_SUM) reinterpret_cast<float *>(d->out)[row] = acc;
+            else reinterpret_cast<uint16_t *>(d->out)[row] = to_bf(acc);
+        }
+        __syncwarp();
+        return GPUOS_ST_OK;
+    }
+    uint4 *y = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(d->out) + (uint64_t)row * H);
+    if (K == ROW_SOFTMAX) {
+        float m = -INFINITY;
+#pragma unroll 2
+        for (uint32_t v = lane; v < nv; v += 32) {
+            float f[8];
+            unpack8(sx[v], f);
+#pragma unroll
+            for (int i = 0; i < 8; i++) m = fmaxf(m, f[i]);
+        }
+        m = warp_max(m);
+        float s8[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) s8[i] = 0.0f;
+#pragma unroll 2
+        for (uint32_t v = lane; v < nv; v += 32) {
+            float f[8];
+            unpack8(sx[v], f);
+#pragma unroll
+            for (int i = 0; i < 8; i++) s8[i] += __expf(f[i] - m);
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; i++) sum += s8[i];
+        const float inv = 1.0f / warp_sum(sum);
+#pragma unroll 2
+        for (uint32_t v = lane; v < nv; v += 32) {
+            float f[8];
+            unpack8(sx[v], f);
+#pragma unroll
+            for (int i = 0; i < 8; i++) f[i] = __expf(f[i] - m) * inv;
+            __stcg(y + v, pack8(f));
+        }
+        __syncwarp();
+        return GPUOS_ST_OK;
+    }
+    /* LayerNorm: biased variance, mean and variance in two passes */
+    float s8[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) s8[i] = 0.0f;
+#pragma unroll 2
+    for (uint32_t v = lane; v < nv; v += 32) {
+        float f[8];
+        unpack8(sx[v], f);
+#pragma unroll
+        for (int i = 0; i < 8; i++) s8[i] += f[i];
+    }
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) sum += s8[i];
+    const float mean = warp_sum(sum) / (float)H;
+#pragma unroll
+    for (int i = 0; i < 8; i++) s8[i] = 0.0f;
+#pragma unroll 2
+    for (uint32_t v = lane; v < nv; v += 32) {
+        float f[8];
+        unpack8(sx[v], f);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const float t = f[i] - mean;
+            s8[i] = fmaf(t, t, s8[i]);
+        }
+    }
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) q += s8[i];
+    const float rstd = rsqrtf(warp_sum(q) / (float)H + d->fparam[0]);
+    const uint4 *sg = sx + nv;
+    const uint32_t cv = C / 8; /* vectors per gamma/beta chunk */
+    for (uint32_t c0 = 0; c0 < nv; c0 += cv) {
+        if (c0 > 0) {
+            /* next chunk of gamma and beta, once every lane is done with this one */
+            __syncwarp();
+            const uint32_t cb = min(cv, nv - c0) * 16u;
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_expect(&w->mbar[0], 2u * cb);
+                bulk_g2s(buf + 2u * H, reinterpret_cast<const unsigned char *>(d->b) + c0 * 16u, cb, &w->mbar[0]);
+                bulk_g2s(buf + 2u * H + 2u * C, reinterpret_cast<const unsigned char *>(d->aux0) + c0 * 16u, cb,
+                         &w->mbar[0]);
+            }
+            if (!stage_wait0(w)) return GPUOS_ST_COPY_TIMEOUT;
+        }
+        const uint32_t ce = min(nv, c0 + cv);
+#pragma unroll 2
+        for (uint32_t v = c0 + lane; v < ce; v += 32) {
+            float f[8], gf[8], bf[8];
+            unpack8(sx[v], f);
+            unpack8(sg[v - c0], gf);
+            unpack8(sg[cv + v - c0], bf);
+#pragma unroll
+            for (int i = 0; i < 8; i++) f[i] = (f[i] - mean) * rstd * gf[i] + bf[i];
+            __stcg(y + v, pack8(f));
+        }
+    }
+    __syncwarp(); /* every lane's reads of the buffer before it is reused */
     return GPUOS_ST_OK;
 }
 
@@ -627,106 +944,195 @@ DEV int row_tile(const gpuos_devdesc *d, uint32_t row)
     const uint32_t R = d->dims[0], H = d->dims[1];
     if (row >= R) return GPUOS_ST_OK;
     if (H == 0) return GPUOS_ST_BAD_ARGS;
-    bool ok = H <= GPUOS_ROW_REG_MAX && (H & 7u) == 0 && (d->a & 15u) == 0;
+    bool ok = (H & 7u) == 0 && (d->a & 15u) == 0;
     if (K == ROW_SOFTMAX || K == ROW_LN) ok = ok && (d->out & 15u) == 0;
     if (K == ROW_LN) ok = ok && ((d->b | d->aux0) & 15u) == 0;
-    return ok ? row_reg<K>(d, row, H) : row_generic<K>(d, row, H);
+    if (!ok) return row_generic<K>(d, row, H);
+    /* staged: the row, plus (LayerNorm) gamma and beta in chunks of C
+     * columns, a multiple of 8 of at least 256 (or all H) */
+    const uint32_t sb = stage_hdr()->stage_bytes;
+    if (2u * H <= sb) {
+        uint32_t C = 0;
+        if (K == ROW_LN) {
+            C = ((sb - 2u * H) / 4u) & ~7u;
+            if (C > H) C = H;
+        }
+        if (K != ROW_LN || C == H || C >= 256u) return row_staged<K>(d, row, H, C);
+    }
+    return H <= GPUOS_ROW_REG_MAX ? row_reg<K>(d, row, H) : row_generic<K>(d, row, H);
 }
 
-/* ---- RoPE: one request (all heads of q and k) per tile -------------------- */
-DEV int rope_tile(const gpuos_devdesc *d, uint32_t b)
+/* ---- RoPE: one (request, group of GPUOS_HEAD_GROUP heads) per tile --------
+ * Pairs (i, i + D/2) of every q and k row of the group rotate by the angle
+ * pos * theta^(-2i/D). With D % 4 == 0 and 4-byte aligned rows, lane l owns
+ * the pairs of elements 2w and 2w + 1 for words w = l, l + 32 of a half-row:
+ * every load of the tile is issued before the first rotation. */
+/* sin and cos of x: Cody-Waite reduction by 2 pi (2 pi split in three parts,
+ * the first exact in 8 bits, so k * part is exact for |k| < 2^15) to
+ * r in [-pi, pi], then the hardware sin/cos, whose absolute error there is
+ * below 4e-7. */
+DEV void sincos_cw(float x, float *sn, float *cs)
+{
+    const float k = rintf(x * 0.159154943f);
+    float r = fmaf(-k, 6.28125f, x);
+    r = fmaf(-k, 1.935307169e-3f, r);
+    r = fmaf(-k, 1.025313168e-11f, r);
+    __sincosf(r, sn, cs);
+}
+
+DEV int rope_tile(const gpuos_devdesc *d, uint32_t tile)
 {
     const uint32_t B = d->dims[0], H = d->dims[1], D = d->dims[2];
+    if (H == 0 || D == 0 || (D & 1u) || D > 256) return GPUOS_ST_BAD_ARGS;
+    const uint32_t ng = (H + GPUOS_HEAD_GROUP - 1) / GPUOS_HEAD_GROUP;
+    const uint32_t b = tile / ng, h0 = (tile - b * ng) * GPUOS_HEAD_GROUP;
     if (b >= B) return GPUOS_ST_OK;
-    if (D == 0 || (D & 1u) || D > 256) return GPUOS_ST_BAD_ARGS;
+    const uint32_t nh = (H - h0) < GPUOS_HEAD_GROUP ? (H - h0) : GPUOS_HEAD_GROUP;
     const int32_t pos = __ldcg(reinterpret_cast<const int32_t *>(d->aux0) + b) - 1;
     if (pos < 0) return GPUOS_ST_BAD_ARGS;
     const uint32_t lane = lane_id(), half = D / 2;
-    const float theta = d->fparam[0];
-    float c[4], s[4];
+    /* theta^(-2i/D) = 2^(-(2i/D) log2 theta) */
+    const float l2t = log2f(d->fparam[0]) * (-2.0f / (float)D);
+    const uint64_t row0 = ((uint64_t)b * H + h0) * D; /* first element of the group */
+    if ((D & 3u) == 0 && ((d->a | d->b) & 3u) == 0) {
+        const uint32_t hw = half / 2; /* words per half-row, <= 64 */
+        float c[2][2], sn[2][2];
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const uint32_t i = lane + 32u * j;
-        c[j] = 1.0f;
-        s[j] = 0.0f;
-        if (i < half) {
-            const float inv = powf(theta, -(2.0f * (float)i) / (float)D);
-            sincosf((float)pos * inv, &s[j], &c[j]);
+        for (int j = 0; j < 2; j++) {
+            const uint32_t wd = lane + 32u * j;
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                c[j][e] = 1.0f;
+                sn[j][e] = 0.0f;
+                if (wd < hw) {
+                    float inv;
+                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(l2t * (float)(2u * wd + e)));
+                    sincos_cw((float)pos * inv, &sn[j][e], &c[j][e]);
+                }
+            }
         }
+        uint32_t x0[2][GPUOS_HEAD_GROUP][2], x1[2][GPUOS_HEAD_GROUP][2];
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+            const uint32_t *base = reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint16_t *>(
+                which ? d->b : d->a) + row0);
+#pragma unroll
+            for (int hh = 0; hh < GPUOS_HEAD_GROUP; hh++) {
+#pragma unroll
+                for (int j = 0; j < 2; j++) {
+                    const uint32_t wd = lane + 32u * j;
+                    if ((uint32_t)hh < nh && wd < hw) {
+                        x0[which][hh][j] = __ldcg(base + (uint64_t)hh * (D / 2) + wd);
+                        x1[which][hh][j] = __ldcg(base + (uint64_t)hh * (D / 2) + hw + wd);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+            uint32_t *base = reinterpret_cast<uint32_t *>(reinterpret_cast<uint16_t *>(which ? d->b : d->a) + row0);
+#pragma unroll
+            for (int hh = 0; hh < GPUOS_HEAD_GROUP; hh++) {
+#pragma unroll
+                for (int j = 0; j < 2; j++) {
+                    const uint32_t wd = lane + 32u * j;
+                    if ((uint32_t)hh < nh && wd < hw) {
+                        const uint32_t u0 = x0[which][hh][j], u1 = x1[which][hh][j];
+                        const float a0 = bf_lo(u0), a1 = bf_hi(u0), b0 = bf_lo(u1), b1 = bf_hi(u1);
+                        base[(uint64_t)hh * (D / 2) + wd] =
+                            pack_bf2(a0 * c[j][0] - b0 * sn[j][0], a1 * c[j][1] - b1 * sn[j][1]);
+                        base[(uint64_t)hh * (D / 2) + hw + wd] =
+                            pack_bf2(b0 * c[j][0] + a0 * sn[j][0], b1 * c[j][1] + a1 * sn[j][1]);
+                    }
+                }
+            }
+        }
+        return GPUOS_ST_OK;
     }
+    /* any even D or 2-byte alignment: one element pair per lane and step */
     for (int which = 0; which < 2; which++) {
-        uint16_t *base = reinterpret_cast<uint16_t *>(which ? d->b : d->a) + (uint64_t)b * H * D;
-        for (uint32_t h0 = 0; h0 < H; h0 += 4) {
-            float x0[4][4], x1[4][4];
-#pragma unroll
-            for (int hh = 0; hh < 4; hh++) {
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const uint32_t i = lane + 32u * j;
-                    if (h0 + hh < H && i < half) {
-                        const uint16_t *row = base + (uint64_t)(h0 + hh) * D;
-                        x0[hh][j] = bf1(__ldcg(row + i));
-                        x1[hh][j] = bf1(__ldcg(row + i + half));
-                    }
-                }
-            }
-#pragma unroll
-            for (int hh = 0; hh < 4; hh++) {
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const uint32_t i = lane + 32u * j;
-                    if (h0 + hh < H && i < half) {
-                        uint16_t *row = base + (uint64_t)(h0 + hh) * D;
-                        row[i] = to_bf(x0[hh][j] * c[j] - x1[hh][j] * s[j]);
-                        row[i + half] = to_bf(x1[hh][j] * c[j] + x0[hh][j] * s[j]);
-                    }
-                }
-            }
+        uint16_t *base = reinterpret_cast<uint16_t *>(which ? d->b : d->a) + row0;
+        for (uint32_t k = lane; k < nh * half; k += 32) {
+            const uint32_t hh = k / half, i = k - hh * half;
+            float sv, cv, inv;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(l2t * (float)i));
+            sincos_cw((float)pos * inv, &sv, &cv);
+            uint16_t *row = base + (uint64_t)hh * D;
+            const float a0 = bf1(__ldcg(row + i)), b0 = bf1(__ldcg(row + i + half));
+            row[i] = to_bf(a0 * cv - b0 * sv);
+            row[i + half] = to_bf(b0 * cv + a0 * sv);
         }
     }
     return GPUOS_ST_OK;
 }
 
-/* ---- KV-cache slot write: one request per tile, bit-exact copy ------------- */
-DEV int kv_tile(const gpuos_devdesc *d, uint32_t b)
+/* ---- KV-cache slot write: one (request, group of GPUOS_HEAD_GROUP heads) per
+ * tile, k and v rows of the group copied bit for bit into row lens[b] - 1 of
+ * each head's cache; up to 8 16-byte loads per lane in flight per round ---- */
+DEV int kv_tile(const gpuos_devdesc *d, uint32_t tile)
 {
     const uint32_t B = d->dims[0], H = d->dims[1], D = d->dims[2], Lcap = d->dims[3];
+    if (H == 0) return GPUOS_ST_BAD_ARGS;
+    const uint32_t ng = (H + GPUOS_HEAD_GROUP - 1) / GPUOS_HEAD_GROUP;
+    const uint32_t b = tile / ng, h0 = (tile - b * ng) * GPUOS_HEAD_GROUP;
     if (b >= B) return GPUOS_ST_OK;
+    const uint32_t nh = (H - h0) < GPUOS_HEAD_GROUP ? (H - h0) : GPUOS_HEAD_GROUP;
     const int32_t pos = __ldcg(reinterpret_cast<const int32_t *>(d->aux0) + b) - 1;
     if (pos < 0 || (uint32_t)pos >= Lcap) return GPUOS_ST_BAD_ARGS;
     const uint32_t lane = lane_id();
+    const uint64_t bh0 = (uint64_t)b * H + h0;
+    const uint16_t *src[2] = {reinterpret_cast<const uint16_t *>(d->a) + bh0 * D,
+                              reinterpret_cast<const uint16_t *>(d->b) + bh0 * D};
+    uint16_t *dst[2] = {reinterpret_cast<uint16_t *>(d->out) + (bh0 * Lcap + (uint64_t)pos) * D,
+                        reinterpret_cast<uint16_t *>(d->aux1) + (bh0 * Lcap + (uint64_t)pos) * D};
+    const uint64_t hstride = (uint64_t)Lcap * D; /* elements between heads in the cache */
+    if ((D & 7u) == 0 && ((d->a | d->b | d->out | d->aux1) & 15u) == 0) {
+        const uint32_t nvr = D / 8, per = nh * nvr, total = 2u * per;
+        constexpr int U = 8;
+        for (uint32_t i0 = 0; i0 < total; i0 += 32u * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const uint32_t i = i0 + 32u * u + lane;
+                if (i < total) {
+                    const uint32_t which = i >= per, r = i - which * per, h = r / nvr, e = r - h * nvr;
+                    v[u] = __ldcg(reinterpret_cast<const uint4 *>(src[which] + (uint64_t)h * D) + e);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const uint32_t i = i0 + 32u * u + lane;
+                if (i < total) {
+                    const uint32_t which = i >= per, r = i - which * per, h = r / nvr, e = r - h * nvr;
+                    __stcg(reinterpret_cast<uint4 *>(dst[which] + h * hstride) + e, v[u]);
+                }
+            }
+        }
+        return GPUOS_ST_OK;
+    }
     for (int which = 0; which < 2; which++) {
-        const uint16_t *src = reinterpret_cast<const uint16_t *>(which ? d->b : d->a) + (uint64_t)b * H * D;
-        uint16_t *dst = reinterpret_cast<uint16_t *>(which ? d->aux1 : d->out) +
-                        ((uint64_t)b * H * Lcap + (uint64_t)pos) * D;
-        const uint64_t hstride = (uint64_t)Lcap * D; /* elements between heads in the cache */
-        if ((D & 7u) == 0 && (((uintptr_t)src | (uintptr_t)dst) & 15u) == 0) {
-            const uint32_t nvr = D / 8, total = H * nvr;
-#pragma unroll 4
-            for (uint32_t i = lane; i < total; i += 32) {
-                const uint32_t h = i / nvr, v = i - h * nvr;
-                const uint4 val = __ldcg(reinterpret_cast<const uint4 *>(src + (uint64_t)h * D) + v);
-                __stcg(reinterpret_cast<uint4 *>(dst + h * hstride) + v, val);
-            }
-        } else {
-            for (uint32_t i = lane; i < H * D; i += 32) {
-                const uint32_t h = i / D, e = i - h * D;
-                dst[h * hstride + e] = src[(uint64_t)h * D + e];
-            }
+        for (uint32_t i = lane; i < nh * D; i += 32) {
+            const uint32_t h = i / D, e = i - h * D;
+            dst[which][h * hstride + e] = src[which][(uint64_t)h * D + e];
         }
     }
     return GPUOS_ST_OK;
 }
 
-/* ---- decode SDPA: one (request, head, GPUOS_SDPA_CHUNK-row chunk) per tile --
- * Four 8-lane groups walk interleaved key rows; in a group lane li owns dims
- * [8 li, 8 li + 8) and [64 + 8 li, 64 + 8 li + 8) of q, K and V (two 16-byte
- * pieces 128 bytes apart, so a quarter-warp reads 128 contiguous bytes of a
- * row: no shared-memory bank conflicts). Scores use exp2 with log2(e) folded
- * into the query scale; each group keeps an online-softmax state (m, l, acc),
- * the four states merge by shuffles, and multi-chunk heads merge through the
- * workspace in the last chunk to finish. With shared-memory staging the K and
- * V rows of the chunk arrive by TMA bulk copies, 32 rows of each per stage. */
+/* ---- decode SDPA: one (request, head, chunk of key rows) per tile ---------
+ * The host picks the number of chunks per head (chunks of 256 rows, halved
+ * down to 64 while the op has few tiles); the tile recovers the chunk length
+ * from Lmax and ntiles. Four 8-lane groups walk interleaved key rows; in a
+ * group lane li owns dims [8 li, 8 li + 8) and [64 + 8 li, 64 + 8 li + 8) of
+ * q, K and V (two 16-byte pieces 128 bytes apart, so a quarter-warp reads 128
+ * contiguous bytes of a row: no shared-memory bank conflicts). Scores use
+ * exp2 with log2(e) folded into the query scale; each group keeps an
+ * online-softmax state (m, l, acc), the four states merge by shuffles, and
+ * multi-chunk heads merge through the workspace in the last chunk to finish.
+ * With shared-memory staging the K and V rows arrive by TMA bulk copies into
+ * the two halves of the warp's buffer in turn (stage_bytes / 1024 rows of
+ * each per half), so the next rows load while the current ones are scored. */
+#define GPUOS_SDPA_PART 132 /* floats per partial: m, l, 2 pad, acc[128] (16-byte multiple) */
 DEV void sdpa_merge(float &m, float &l, float *acc, float mo, float lo, const float *acco)
 {
     const float mn = fmaxf(m, mo);
@@ -778,61 +1184,82 @@ DEV void sdpa_step(const float *q, const uint4 (&kv)[UK][2], const uint4 (&vv)[U
     m = mn;
 }
 
+/* Lane 0: bulk-copy key rows [tb, tb + nk) of K and V into half hb. */
+DEV void sdpa_issue(WarpStage *w, unsigned char *buf, uint32_t SUB, uint32_t hb, const uint16_t *Kb,
+                    const uint16_t *Vb, uint32_t tb, uint32_t nk)
+{
+    unsigned char *sK = buf + hb * SUB * 512u;
+    unsigned char *sV = sK + SUB * 256u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect(&w->mbar[hb], 2u * nk * 256u);
+    bulk_g2s(sK, Kb + (uint64_t)tb * 128, nk * 256u, &w->mbar[hb]);
+    bulk_g2s(sV, Vb + (uint64_t)tb * 128, nk * 256u, &w->mbar[hb]);
+}
+
 DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
 {
     const uint32_t B = d->dims[0], H = d->dims[1], D = d->dims[2], Lcap = d->dims[3], Lmax = d->dims[4];
-    if (D != 128 || Lmax == 0 || Lmax > Lcap || d->dims[5] < B * H) return GPUOS_ST_BAD_ARGS;
-    const uint32_t nch = (Lmax + GPUOS_SDPA_CHUNK - 1) / GPUOS_SDPA_CHUNK;
-    if (tile >= B * H * nch) return GPUOS_ST_OK;
+    const uint32_t BH = B * H;
+    if (D != 128 || BH == 0 || Lmax == 0 || Lmax > Lcap || d->dims[5] < BH) return GPUOS_ST_BAD_ARGS;
+    const uint32_t nch = d->ntiles / BH;
+    if (nch == 0) return GPUOS_ST_BAD_ARGS;
+    if (tile >= BH * nch) return GPUOS_ST_OK;
+    const uint32_t CH = ((Lmax + nch - 1) / nch + 31u) & ~31u; /* key rows per chunk */
     const uint32_t b = tile / (H * nch), rem = tile - b * H * nch, h = rem / nch, c = rem - h * nch;
-    const int32_t L = __ldcg(reinterpret_cast<const int32_t *>(d->aux0) + b);
-    if (L < 1 || (uint32_t)L > Lmax) return GPUOS_ST_BAD_ARGS;
-    const uint32_t nchb = ((uint32_t)L + GPUOS_SDPA_CHUNK - 1) / GPUOS_SDPA_CHUNK;
-    if (c >= nchb) return GPUOS_ST_OK;
-    const uint32_t t0 = c * GPUOS_SDPA_CHUNK;
-    const uint32_t t1 = min((uint32_t)L, t0 + GPUOS_SDPA_CHUNK);
     const uint32_t lane = lane_id(), g = lane >> 3, li = lane & 7u;
     const uint64_t bh = (uint64_t)b * H + h;
-    const float qs = d->fparam[0] * 1.4426950408889634f;
-
-    float q[16];
-    {
-        const uint16_t *qp = reinterpret_cast<const uint16_t *>(d->a) + bh * 128;
-        unpack8(__ldcg(reinterpret_cast<const uint4 *>(qp + 8 * li)), q);
-        unpack8(__ldcg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * li)), q + 8);
-#pragma unroll
-        for (int i = 0; i < 16; i++) q[i] *= qs;
-    }
+    /* the length and the query in one round trip, then the first copies */
+    const int32_t L = __ldcg(reinterpret_cast<const int32_t *>(d->aux0) + b);
+    const uint16_t *qp = reinterpret_cast<const uint16_t *>(d->a) + bh * 128;
+    const uint4 q0 = __ldcg(reinterpret_cast<const uint4 *>(qp + 8 * li));
+    const uint4 q1 = __ldcg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * li));
+    if (L < 1 || (uint32_t)L > Lmax) return GPUOS_ST_BAD_ARGS;
+    const uint32_t nchb = ((uint32_t)L + CH - 1) / CH;
+    if (c >= nchb) return GPUOS_ST_OK;
+    const uint32_t t0 = c * CH;
+    const uint32_t t1 = min((uint32_t)L, t0 + CH);
     const uint16_t *Kb = reinterpret_cast<const uint16_t *>(d->b) + bh * Lcap * 128;
     const uint16_t *Vb = reinterpret_cast<const uint16_t *>(d->aux1) + bh * Lcap * 128;
+    const uint32_t SUB = stage_hdr()->stage_bytes / 1024u; /* key rows per half: K and V, 256 bytes each */
+    const uint32_t nsub = SUB >= 8 ? (t1 - t0 + SUB - 1) / SUB : 0;
+    WarpStage *w = warp_stage();
+    unsigned char *buf = warp_stage_buf();
+    if (SUB >= 8 && lane == 0) {
+        sdpa_issue(w, buf, SUB, 0, Kb, Vb, t0, min(SUB, t1 - t0));
+        if (nsub > 1) sdpa_issue(w, buf, SUB, 1, Kb, Vb, t0 + SUB, min(SUB, t1 - t0 - SUB));
+    }
+    const float qs = d->fparam[0] * 1.4426950408889634f;
+    float q[16];
+    unpack8(q0, q);
+    unpack8(q1, q + 8);
+#pragma unroll
+    for (int i = 0; i < 16; i++) q[i] *= qs;
     float m = -INFINITY, l = 0.0f, acc[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) acc[i] = 0.0f;
     constexpr int UK = 2; /* keys per group per step */
     int32_t status = GPUOS_ST_OK;
-    const uint32_t sbytes = stage_hdr()->stage_bytes;
-    const uint32_t SUB = sbytes / 512u; /* key rows per stage: K and V, 256 bytes each */
     if (SUB >= 8) {
-        WarpStage *w = warp_stage();
-        unsigned char *sK = warp_stage_buf();
-        unsigned char *sV = sK + SUB * 256u;
-        uint32_t phase = w->phase;
-        for (uint32_t tb = t0; tb < t1; tb += SUB) {
-            const uint32_t nk = (t1 - tb) < SUB ? (t1 - tb) : SUB;
-            const uint32_t bytes = nk * 256u;
-            if (lane == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_expect(&w->mbar, 2u * bytes);
-                bulk_g2s(sK, Kb + (uint64_t)tb * 128, bytes, &w->mbar);
-                bulk_g2s(sV, Vb + (uint64_t)tb * 128, bytes, &w->mbar);
-            }
-            if (!mbar_wait(&w->mbar, phase)) {
-                mbar_wait(&w->mbar, phase);
+        uint32_t phs = w->phase[0] | (w->phase[1] << 1); /* bit hb: parity to wait for on half hb */
+        for (uint32_t sI = 0; sI < nsub; sI++) {
+            const uint32_t hb = sI & 1u;
+            const uint32_t tb = t0 + sI * SUB;
+            const uint32_t nk = min(SUB, t1 - tb);
+            if (!mbar_wait(&w->mbar[hb], (phs >> hb) & 1u)) {
+                /* leave no copy writing the buffer: wait once more (bounded)
+                 * on this half and on the other one if it has a copy out */
+                mbar_wait(&w->mbar[hb], (phs >> hb) & 1u);
+                phs ^= 1u << hb;
+                if (sI + 1 < nsub) {
+                    mbar_wait(&w->mbar[hb ^ 1u], (phs >> (hb ^ 1u)) & 1u);
+                    phs ^= 1u << (hb ^ 1u);
+                }
                 status = GPUOS_ST_COPY_TIMEOUT;
-                phase ^= 1u;
                 break;
             }
-            phase ^= 1u;
+            phs ^= 1u << hb;
+            const unsigned char *sK = buf + hb * SUB * 512u;
+            const unsigned char *sV = sK + SUB * 256u;
             for (uint32_t kk = 0; kk < nk; kk += 4 * UK) {
                 uint4 kv[UK][2], vv[UK][2];
                 bool valid[UK];
@@ -850,9 +1277,13 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
                 }
                 sdpa_step<UK>(q, kv, vv, valid, m, l, acc);
             }
-            __syncwarp();
+            __syncwarp(); /* every lane is done with half hb before it is refilled */
+            if (lane == 0 && sI + 2 < nsub) sdpa_issue(w, buf, SUB, hb, Kb, Vb, tb + 2 * SUB, min(SUB, t1 - tb - 2 * SUB));
         }
-        if (lane == 0) w->phase = phase;
+        if (lane == 0) {
+            w->phase[0] = phs & 1u;
+            w->phase[1] = (phs >> 1) & 1u;
+        }
         __syncwarp();
     } else {
         for (uint32_t tb = t0; tb < t1; tb += 4 * UK) {
@@ -899,51 +1330,103 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
         }
         return GPUOS_ST_OK;
     }
-    /* split-K: publish this chunk's (m, l, acc[128]) and let the last chunk merge */
-    /* workspace: ctr_cap uint32 counters (rounded up to 4), then partials */
+    /* split-K: publish this chunk's (m, l, acc[128]) and let the last chunk
+     * merge. Workspace: round_up(Ccap, 4) uint32 counters, then partials of
+     * GPUOS_SDPA_PART floats {m, l, -, -, acc[128]} */
     uint32_t *cnt = reinterpret_cast<uint32_t *>(d->aux2);
     float *ws = reinterpret_cast<float *>(d->aux2) + ((d->dims[5] + 3u) & ~3u);
-    float *part = ws + (bh * nch + c) * 130;
+    const uint64_t p0 = bh * nch;
+    float *part = ws + (p0 + c) * GPUOS_SDPA_PART;
     if (g == 0) {
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            __stcg(part + 2 + 8 * li + i, acc[i]);
-            __stcg(part + 2 + 64 + 8 * li + i, acc[8 + i]);
-        }
+        float4 *pa = reinterpret_cast<float4 *>(part + 4);
+        __stcg(pa + 2 * li, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        __stcg(pa + 2 * li + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+        __stcg(pa + 16 + 2 * li, make_float4(acc[8], acc[9], acc[10], acc[11]));
+        __stcg(pa + 16 + 2 * li + 1, make_float4(acc[12], acc[13], acc[14], acc[15]));
         if (li == 0) {
             __stcg(part, m);
             __stcg(part + 1, l);
         }
     }
     __syncwarp();
+    /* one acq_rel add: releases this chunk's partial (the warp barrier above
+     * orders the other lanes' stores before lane 0's), and the last chunk
+     * acquires every other chunk's */
     uint32_t last = 0;
-    if (lane == 0) {
-        __threadfence();
-        last = (atomicAdd(cnt + bh, 1u) == nchb - 1) ? 1u : 0u;
-        if (last) __threadfence();
-    }
+    if (lane == 0) last = (atom_add_acq_rel_gpu32(cnt + bh, 1u) == nchb - 1) ? 1u : 0u;
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     if (!last) return GPUOS_ST_OK;
-    float M = -INFINITY;
-    for (uint32_t k = 0; k < nchb; k++) M = fmaxf(M, __ldcg(ws + (bh * nch + k) * 130));
-    float den = 0.0f, o4[4] = {0.f, 0.f, 0.f, 0.f};
-    for (uint32_t k = 0; k < nchb; k++) {
-        const float *pk = ws + (bh * nch + k) * 130;
-        const float wgt = exp2f(__ldcg(pk) - M);
-        den += __ldcg(pk + 1) * wgt;
+    /* the merge, in batches of 16 chunks whose (m, l, acc slice) loads are
+     * all in flight together; a running maximum rescales earlier batches */
+    float M = -INFINITY, den = 0.0f;
+    float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (uint32_t k0 = 0; k0 < nchb; k0 += 16) {
+        float mk[16], lk[16];
+        float4 vk[16];
 #pragma unroll
-        for (int i = 0; i < 4; i++) o4[i] += __ldcg(pk + 2 + 4 * lane + i) * wgt;
+        for (int k = 0; k < 16; k++) {
+            const uint32_t kc = min(k0 + (uint32_t)k, nchb - 1); /* duplicates past the end weigh 0 below */
+            const float *pk = ws + (p0 + kc) * GPUOS_SDPA_PART;
+            mk[k] = __ldcg(pk);
+            lk[k] = __ldcg(pk + 1);
+            vk[k] = __ldcg(reinterpret_cast<const float4 *>(pk + 4) + lane);
+        }
+        float mb = M;
+#pragma unroll
+        for (int k = 0; k < 16; k++)
+            if (k0 + k < nchb) mb = fmaxf(mb, mk[k]);
+        const float sc = exp2f(M - mb); /* 0 on the first batch (M = -inf) */
+        den *= sc;
+        o4.x *= sc;
+        o4.y *= sc;
+        o4.z *= sc;
+        o4.w *= sc;
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+            const float wk = (k0 + k < nchb) ? exp2f(mk[k] - mb) : 0.0f;
+            den = fmaf(lk[k], wk, den);
+            o4.x = fmaf(vk[k].x, wk, o4.x);
+            o4.y = fmaf(vk[k].y, wk, o4.y);
+            o4.z = fmaf(vk[k].z, wk, o4.z);
+            o4.w = fmaf(vk[k].w, wk, o4.w);
+        }
+        M = mb;
     }
     const float inv = 1.0f / den;
     uint2 st;
-    st.x = pack_bf2(o4[0] * inv, o4[1] * inv);
-    st.y = pack_bf2(o4[2] * inv, o4[3] * inv);
+    st.x = pack_bf2(o4.x * inv, o4.y * inv);
+    st.y = pack_bf2(o4.z * inv, o4.w * inv);
     reinterpret_cast<uint2 *>(o16)[lane] = st;
     if (lane == 0) atomicExch(cnt + bh, 0u); /* leave the workspace zeroed */
     return GPUOS_ST_OK;
 }
 
-/* ---- vector-matrix product: GPUOS_VM_COLS output columns per tile --------- */
+/* ---- vector-matrix product: GPUOS_VM_COLS (8) output columns per tile ----
+ * y[n] = sum_k x[k] W[k][n], W row-major [K][N]. A tile owns 8 columns, one
+ * 16-byte piece of every row of W (the neighbouring tile reads the other
+ * half of each 32-byte sector at about the same time). Lane l sums rows
+ * k = l, l + 32, ...; the 32 partial sums then reduce by shuffles. With
+ * staging, blocks of R rows (their W pieces and x values) arrive by 16-byte
+ * cp.async copies into the two halves of the warp's buffer in turn, so the
+ * next block loads while the current one is summed and no registers are
+ * held by loads in flight. */
+DEV void cp_async16(void *sdst, const void *gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(sdst)), "l"(gsrc) : "memory");
+}
+DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+DEV void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+DEV void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+/* Every lane: copy rows [k0, k0 + nk) into a half: W pieces first (16 bytes
+ * per row), then the rows' x values (nk is a multiple of 8 here). */
+DEV void vm_issue(unsigned char *half, const uint16_t *x, const uint16_t *W, uint32_t N, uint32_t c0, uint32_t R,
+                  uint32_t k0, uint32_t nk, uint32_t lane)
+{
+    for (uint32_t r = lane; r < nk; r += 32) cp_async16(half + r * 16u, W + (uint64_t)(k0 + r) * N + c0);
+    for (uint32_t i = lane; i < nk / 8u; i += 32) cp_async16(half + R * 16u + i * 16u, x + k0 + 8u * i);
+}
+
 DEV int vecmat_tile(const gpuos_devdesc *d, uint32_t tile)
 {
     const uint32_t K = d->dims[0], N = d->dims[1];
@@ -953,52 +1436,86 @@ DEV int vecmat_tile(const gpuos_devdesc *d, uint32_t tile)
     const uint16_t *x = reinterpret_cast<const uint16_t *>(d->a);
     const uint16_t *W = reinterpret_cast<const uint16_t *>(d->b);
     uint16_t *y = reinterpret_cast<uint16_t *>(d->out);
-    const bool vec = (N & 7u) == 0 && ((d->b | d->out) & 15u) == 0;
-    if (vec) {
-        /* lane: 8 columns (cb = lane & 3) of rows k = g, g + 8, ... (g = lane >> 2) */
-        const uint32_t cb = lane & 3u, g = lane >> 2;
-        const uint32_t col = c0 + 8 * cb;
-        const bool active = col < N;
+    if ((N & 7u) == 0 && ((d->b | d->out) & 15u) == 0) {
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) acc[i] = 0.0f;
-        constexpr int UR = 4;
-        for (uint32_t k0 = 0; k0 < K; k0 += 8 * UR) {
-            uint4 w[UR];
-            float xv[UR];
+        const uint32_t sbytes = stage_hdr()->stage_bytes;
+        /* rows per half: W pieces (16 B) and x values (2 B), a multiple of 32 */
+        const uint32_t R = (sbytes / 2u / 18u) & ~31u;
+        /* x is copied in 16-byte pieces of 8 values: it must be 16-byte
+         * aligned, and with K % 8 == 0 (R being a multiple of 32) every
+         * block holds a whole number of pieces, so no copy reads past x[K-1] */
+        if (R >= 32 && (d->a & 15u) == 0 && (K & 7u) == 0) {
+            unsigned char *buf = warp_stage_buf();
+            const uint32_t nblk = (K + R - 1) / R;
+            const uint32_t hbytes = sbytes / 2u;
+            vm_issue(buf, x, W, N, c0, R, 0, min(R, K), lane);
+            cp_async_commit();
+            if (nblk > 1) vm_issue(buf + hbytes, x, W, N, c0, R, R, min(R, K - R), lane);
+            cp_async_commit();
+            for (uint32_t s = 0; s < nblk; s++) {
+                cp_async_wait1(); /* this lane's copies of block s have landed */
+                __syncwarp();     /* ... and every other lane's */
+                const unsigned char *hf = buf + (s & 1u) * hbytes;
+                const uint32_t nk = min(R, K - s * R);
+                const uint16_t *xs = reinterpret_cast<const uint16_t *>(hf + R * 16u);
+#pragma unroll 7
+                for (uint32_t r = lane; r < nk; r += 32) {
+                    float wf[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(hf + r * 16u), wf);
+                    const float xv = bf1(xs[r]);
 #pragma unroll
-            for (int u = 0; u < UR; u++) {
-                const uint32_t k = k0 + g + 8 * u;
-                if (active && k < K) {
-                    w[u] = __ldcg(reinterpret_cast<const uint4 *>(W + (uint64_t)k * N + col));
-                    xv[u] = bf1(__ldcg(x + k));
-                } else {
-                    w[u] = make_uint4(0, 0, 0, 0);
-                    xv[u] = 0.0f;
+                    for (int i = 0; i < 8; i++) acc[i] = fmaf(xv, wf[i], acc[i]);
                 }
+                __syncwarp(); /* every lane is done with this half before it is refilled */
+                if (s + 2 < nblk) vm_issue(buf + (s & 1u) * hbytes, x, W, N, c0, R, (s + 2) * R,
+                                           min(R, K - (s + 2) * R), lane);
+                cp_async_commit();
             }
+            cp_async_wait0();
+            __syncwarp();
+        } else {
+            constexpr int UR = 8;
+            for (uint32_t k0 = 0; k0 < K; k0 += 32 * UR) {
+                uint4 w[UR];
+                float xv[UR];
 #pragma unroll
-            for (int u = 0; u < UR; u++) {
-                float wf[8];
-                unpack8(w[u], wf);
+                for (int u = 0; u < UR; u++) {
+                    const uint32_t k = k0 + lane + 32 * u;
+                    if (k < K) {
+                        w[u] = __ldcg(reinterpret_cast<const uint4 *>(W + (uint64_t)k * N + c0));
+                        xv[u] = bf1(__ldcg(x + k));
+                    } else {
+                        w[u] = make_uint4(0, 0, 0, 0);
+                        xv[u] = 0.0f;
+                    }
+                }
 #pragma unroll
-                for (int i = 0; i < 8; i++) acc[i] = fmaf(xv[u], wf[i], acc[i]);
+                for (int u = 0; u < UR; u++) {
+                    float wf[8];
+                    unpack8(w[u], wf);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) acc[i] = fmaf(xv[u], wf[i], acc[i]);
+                }
             }
         }
 #pragma unroll
-        for (int o = 4; o <= 16; o <<= 1) {
+        for (int o = 1; o <= 16; o <<= 1) {
 #pragma unroll
             for (int i = 0; i < 8; i++) acc[i] += __shfl_xor_sync(0xFFFFFFFFu, acc[i], o);
         }
-        if (g == 0 && active) __stcg(reinterpret_cast<uint4 *>(y + col), pack8(acc));
+        if (lane == 0) __stcg(reinterpret_cast<uint4 *>(y + c0), pack8(acc));
         return GPUOS_ST_OK;
     }
-    const uint32_t col = c0 + lane;
-    if (col < N) {
-        float acc = 0.0f;
-        for (uint32_t k = 0; k < K; k++) acc = fmaf(bf1(__ldcg(x + k)), bf1(__ldcg(W + (uint64_t)k * N + col)), acc);
-        y[col] = to_bf(acc);
-    }
+    /* any N or alignment: lane (g, j) sums column c0 + j over rows g, g + 4, ... */
+    const uint32_t j = lane & 7u, g = lane >> 3, col = c0 + j;
+    float acc = 0.0f;
+    if (col < N)
+        for (uint32_t k = g; k < K; k += 4) acc = fmaf(bf1(__ldcg(x + k)), bf1(__ldcg(W + (uint64_t)k * N + col)), acc);
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 8);
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
+    if (g == 0 && col < N) y[col] = to_bf(acc);
     return GPUOS_ST_OK;
 }
 
@@ -1023,6 +1540,28 @@ __device__ gpuos_op_fn g_builtin_ops[GPUOS_OP_BUILTIN_COUNT] = {
     op_rowsum, op_rowmax, op_rowmin, op_rope, op_kv_write, op_sdpa, op_vecmat,
 };
 
+/* The body of built-in op `kind`, inlined (the eager kernel). */
+DEV int builtin_call(uint32_t kind, const gpuos_devdesc *d, uint32_t t)
+{
+    switch (kind) {
+    case GPUOS_OP_NOP: return GPUOS_ST_OK;
+    case GPUOS_OP_ADD: return ew_dispatch<EW_ADD>(d, t);
+    case GPUOS_OP_MUL: return ew_dispatch<EW_MUL>(d, t);
+    case GPUOS_OP_RELU: return ew_dispatch<EW_RELU>(d, t);
+    case GPUOS_OP_GELU: return ew_dispatch<EW_GELU>(d, t);
+    case GPUOS_OP_SOFTMAX: return row_tile<ROW_SOFTMAX>(d, t);
+    case GPUOS_OP_LAYERNORM: return row_tile<ROW_LN>(d, t);
+    case GPUOS_OP_ROWSUM: return row_tile<ROW_SUM>(d, t);
+    case GPUOS_OP_ROWMAX: return row_tile<ROW_MAX>(d, t);
+    case GPUOS_OP_ROWMIN: return row_tile<ROW_MIN>(d, t);
+    case GPUOS_OP_ROPE: return rope_tile(d, t);
+    case GPUOS_OP_KV_WRITE: return kv_tile(d, t);
+    case GPUOS_OP_SDPA: return sdpa_tile(d, t);
+    case GPUOS_OP_VECMAT: return vecmat_tile(d, t);
+    default: return GPUOS_ST_BAD_OP;
+    }
+}
+
 /* ===========================================================================
  * Persistent executor
  * ======================================================================== */
@@ -1042,24 +1581,33 @@ DEV bool tq_is(uint64_t w, uint64_t idx) { return (w >> 28) == ((idx + 1) & GPUO
 
 DEV void fence_acq_rel_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
 
-/* Complete one descriptor (single thread). */
-DEV void complete_desc(const gpuos_exec_params &p, uint64_t ticket, uint32_t slot, int32_t status,
-                       uint32_t version, uint64_t t_dispatch)
+/* Complete one descriptor (single thread). The device-memory done stamp
+ * that dependent tiles wait on is released first; the host-visible record
+ * (stores across NVLink-C2C, whose acknowledgements a release would have to
+ * wait for) is written after it. The record's t_dispatch was written by the
+ * sequencer when it saw the commit. */
+DEV void complete_desc(const gpuos_exec_params &p, uint64_t ticket, uint32_t slot, int32_t status, uint32_t version)
 {
     gpuos_rec_dev *r = p.rec + slot;
     const uint64_t t_done = globaltimer();
+    /* release the stamp first (the tiles' outputs: a sole tile's through the
+     * warp barrier before this call, other tiles' through their acq_rel
+     * counter adds, which this thread acquired); the slot's counters are
+     * reset after it: only a ticket ring_entries later reuses them, and the
+     * host frees the slot only after the record's release below */
+    st_release_gpu(p.done_dev + slot, ticket + 1);
+    st_relaxed_gpu32(p.err + slot, 0u);
+    st_relaxed_gpu(p.tiles_done + slot, 0ull);
+    st_relaxed_gpu32(p.tile_ctr + slot, 0u);
+    const uint64_t t_pub = *reinterpret_cast<volatile uint64_t *>(p.t_pub + slot);
+    const uint64_t t_start = *reinterpret_cast<volatile uint64_t *>(p.t_start + slot);
     st_relaxed_sys32(reinterpret_cast<uint32_t *>(&r->status), (uint32_t)status);
     st_relaxed_sys32(&r->version, version);
-    st_relaxed_sys(&r->t_dispatch, t_dispatch);
-    st_relaxed_sys(&r->t_publish, *reinterpret_cast<volatile uint64_t *>(p.t_pub + slot));
-    st_relaxed_sys(&r->t_start, *reinterpret_cast<volatile uint64_t *>(p.t_start + slot));
+    st_relaxed_sys(&r->t_publish, t_pub);
+    st_relaxed_sys(&r->t_start, t_start);
     st_relaxed_sys(&r->t_done, t_done);
-    st_relaxed_gpu32(p.err + slot, 0u);
-    st_relaxed_gpu32(p.tiles_done + slot, 0u);
-    st_relaxed_gpu32(p.tile_ctr + slot, 0u);
-    /* release: the record fields and the slot's counters before the stamps
-     * (the tiles' outputs were fenced before their counter increments) */
-    st_release_gpu(p.done_dev + slot, ticket + 1);
+    /* release: the record's fields before its done word (which also frees
+     * the ring slot for the host) */
     st_release_sys(&r->done_seq, ticket + 1);
     atomicAdd(&p.dctl->completed, 1ull);
 }
@@ -1083,9 +1631,10 @@ DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles)
 /* The sequencer warp: ring -> mirror + work queue, up to 64 descriptors per
  * batch (two ring slots per lane: slot s + lane and s + 32 + lane). */
 #define SEQ_SPL 2
-DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
+DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, unsigned long long *s_table)
 {
     const uint32_t lane = lane_id();
+    uint32_t cached_version = 0xFFFFFFFFu; /* version whose table slot s_table holds */
     uint64_t *ws = p.warp_stats + (uint64_t)gw * GPUOS_WS_N;
     uint64_t s = 0, e = 0;
     uint64_t n_seq = 0, n_idle = 0, n_sleep = 0, t_body = 0, t_mirror = 0, t_pubs = 0, n_inline = 0;
@@ -1165,6 +1714,16 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         uint32_t version = 0;
         if (lane == 0) version = ld_acquire_gpu32(&p.dctl->version);
         version = __shfl_sync(0xFFFFFFFFu, version, 0);
+        if (version != cached_version) {
+            /* a new version: copy its table slot (written before the flip
+             * the acquire above saw) into shared memory */
+            __syncwarp();
+            for (uint32_t i = lane; i < GPUOS_MAX_OPS; i += 32)
+                s_table[i] = __ldcg(reinterpret_cast<const unsigned long long *>(p.table) +
+                                    (version & 1u) * GPUOS_MAX_OPS + i);
+            __syncwarp();
+            cached_version = version;
+        }
         /* a FENCE descriptor must start a batch; cut the batch before it */
         uint64_t fmask = 0;
 #pragma unroll
@@ -1215,7 +1774,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
                      * helper i starts with tile i and takes later tiles from the
                      * descriptor's tile counter */
                     nt[h] = helper_count(dsc[h].op_id, dsc[h].ntiles);
-                    dsc[h].user = t_obs;                                    /* -> t_dispatch */
+                    dsc[h].user = s_table[dsc[h].op_id];                     /* -> fn */
                     dsc[h].seq = (uint64_t)version | ((uint64_t)nt[h] << 32); /* -> version, helpers */
                     uint4 *mv = reinterpret_cast<uint4 *>(p.mirror + (uint32_t)(my_t & p.ring_mask));
                     const uint4 *dv = reinterpret_cast<const uint4 *>(&dsc[h]);
@@ -1244,12 +1803,10 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
                 *reinterpret_cast<volatile uint64_t *>(p.t_start + slot) = ts;
             }
             __syncwarp();
-            const gpuos_op_fn fn = reinterpret_cast<gpuos_op_fn>(__ldcg(
-                reinterpret_cast<const unsigned long long *>(p.table) + (version & 1u) * GPUOS_MAX_OPS + sd->op_id));
-            int32_t st = GPUOS_ST_BAD_OP;
-            if (fn != nullptr) st = fn(sd, 0);
+            const gpuos_op_fn fn = reinterpret_cast<gpuos_op_fn>(sd->fn);
+            const int32_t st = fn ? fn(sd, 0) : GPUOS_ST_BAD_OP;
             __syncwarp();
-            if (lane == 0) complete_desc(p, s, slot, st, version, t_obs);
+            if (lane == 0) complete_desc(p, s, slot, st, version);
             s += 1;
             n_seq += 1;
             n_inline += 1;
@@ -1326,7 +1883,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
             const uint32_t slot = (uint32_t)(my_t & p.ring_mask);
             if (pos < k && status[h] == GPUOS_ST_OK) *reinterpret_cast<volatile uint64_t *>(p.t_pub + slot) = t_pub;
             /* descriptors that failed validation complete at once */
-            if (pos < k && status[h] != GPUOS_ST_OK) complete_desc(p, my_t, slot, status[h], version, t_obs);
+            if (pos < k && status[h] != GPUOS_ST_OK) complete_desc(p, my_t, slot, status[h], version);
         }
         e += total;
         s += k;
@@ -1353,10 +1910,11 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
 }
 
 /* A worker warp: claim a tile, wait for its dependencies, dispatch, count. */
-DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
+DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, uint64_t *sprof)
 {
     const uint32_t lane = lane_id();
     uint64_t *ws = p.warp_stats + (uint64_t)gw * GPUOS_WS_N;
+    uint64_t t_found = 0, t_deps = 0; /* lane 0: entry found, dependencies met */
     uint64_t n_tiles = 0, n_idle = 0, n_sleep = 0, n_depw = 0;
     const uint32_t N = p.ring_mask + 1;
     unsigned long long e = 0;
@@ -1369,8 +1927,12 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         uint64_t w = 0;
         if (lane == 0) {
             while (true) {
-                w = ld_acquire_gpu(reinterpret_cast<const uint64_t *>(ent));
-                if (tq_is(w, e)) break;
+                w = ld_relaxed_gpu(reinterpret_cast<const uint64_t *>(ent));
+                if (tq_is(w, e)) {
+                    fence_acq_rel_gpu(); /* the acquire, once */
+                    t_found = globaltimer();
+                    break;
+                }
                 n_idle++;
                 if ((polls & 15u) == 0 && ld_relaxed_gpu32(&p.dctl->exit_flag)) {
                     leave = 1;
@@ -1382,6 +1944,7 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         leave = __shfl_sync(0xFFFFFFFFu, leave, 0);
         if (leave) break;
         w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        __syncwarp(); /* lane 0's acquire before every lane's mirror read */
         const uint32_t slot = (uint32_t)((w >> 12) & 0xFFFFu);
         uint32_t tile = (uint32_t)(w & 0xFFFu); /* helper index = its first tile */
         /* descriptor -> shared memory */
@@ -1390,6 +1953,7 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         const uint64_t ticket = sd->ticket;
         const uint32_t ntiles = sd->ntiles;
         const uint32_t helpers = sd->pad; /* helper count fixed by the sequencer */
+        const gpuos_op_fn fn = reinterpret_cast<gpuos_op_fn>(sd->fn);
         int32_t dstatus = GPUOS_ST_OK;
         if (lane == 0) {
             for (int i = 0; i < 2; i++) {
@@ -1406,7 +1970,7 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
                 Elapsed w;
                 w.start();
                 uint32_t dp = 0;
-                while (ld_acquire_gpu(stamp) < dep) {
+                while (ld_relaxed_gpu(stamp) < dep) {
                     if (w.tick(globaltimer()) > p.dep_timeout_ns) {
                         dstatus = GPUOS_ST_DEP_TIMEOUT;
                         break;
@@ -1418,14 +1982,16 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
                     backoff(dp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
                 }
                 if (dstatus) break;
+                fence_acq_rel_gpu(); /* the acquire, once */
             }
         }
         dstatus = __shfl_sync(0xFFFFFFFFu, dstatus, 0);
         /* tile 0 starts once its dependencies are met */
-        if (lane == 0 && tile == 0) *reinterpret_cast<volatile uint64_t *>(p.t_start + slot) = globaltimer();
+        if (lane == 0) {
+            t_deps = globaltimer();
+            if (tile == 0) *reinterpret_cast<volatile uint64_t *>(p.t_start + slot) = t_deps;
+        }
         __syncwarp();
-        const gpuos_op_fn fn = reinterpret_cast<gpuos_op_fn>(__ldcg(
-            reinterpret_cast<const unsigned long long *>(p.table) + (sd->version & 1u) * GPUOS_MAX_OPS + sd->op_id));
         /* the helper's tiles: its first tile, then tiles from the descriptor's
          * counter. Each next tile is claimed before the current one runs
          * (the claim's latency overlaps the work), and the helper counts its
@@ -1448,19 +2014,35 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
         }
         __syncwarp();
         if (lane == 0) {
+            const uint64_t t_body = globaltimer();
             if (ntiles == 1) {
                 /* sole tile: no counter round trip; the warp barrier above
                  * orders every lane's writes before the completion releases */
-                complete_desc(p, ticket, slot, status, sd->version, sd->t_dispatch);
+                complete_desc(p, ticket, slot, status, sd->version);
             } else {
+                /* one acq_rel add per helper: its tiles' writes are released
+                 * to the last helper, which acquires every helper's; a failed
+                 * helper records its status first and counts itself in the
+                 * high word */
                 if (status) atomicCAS(p.err + slot, 0u, (uint32_t)status);
-                __threadfence();
-                const uint32_t old = atomicAdd(p.tiles_done + slot, count);
-                if (old + count == ntiles) {
-                    __threadfence();
-                    const uint32_t st = ld_relaxed_gpu32(p.err + slot);
-                    complete_desc(p, ticket, slot, (int32_t)st, sd->version, sd->t_dispatch);
+                const unsigned long long add = (unsigned long long)count | (status ? (1ull << 32) : 0ull);
+                const unsigned long long old = atom_add_acq_rel_gpu(p.tiles_done + slot, add);
+                if ((uint32_t)old + count == ntiles) {
+                    const bool failed = (old >> 32) != 0 || status != GPUOS_ST_OK;
+                    const int32_t st = failed ? (int32_t)ld_relaxed_gpu32(p.err + slot) : GPUOS_ST_OK;
+                    complete_desc(p, ticket, slot, st, sd->version);
                 }
+            }
+            /* tile profile: accumulated in shared memory, written through
+             * to the warp's row (stores only, no read round trip) */
+            const uint32_t bk = sd->op_id < GPUOS_OP_BUILTIN_COUNT ? sd->op_id : GPUOS_OP_BUILTIN_COUNT;
+            const uint64_t t_fin = globaltimer();
+            const uint64_t add[GPUOS_PROF_FIELDS] = {count, t_body - t_deps, t_fin - t_body, t_deps - t_found};
+#pragma unroll
+            for (int f = 0; f < GPUOS_PROF_FIELDS; f++) {
+                const uint64_t v = sprof[f * GPUOS_PROF_BUCKETS + bk] + add[f];
+                sprof[f * GPUOS_PROF_BUCKETS + bk] = v;
+                ws[GPUOS_WS_PROF + f * GPUOS_PROF_BUCKETS + bk] = v;
             }
             n_tiles += count;
             ws[GPUOS_WS_TILES] = n_tiles;
@@ -1486,38 +2068,20 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw)
 extern "C" __global__ void __launch_bounds__(GPUOS_MAX_WPB * 32, 1) gpuos_executor_kernel(gpuos_exec_params p)
 {
     __shared__ __align__(16) gpuos_devdesc sdesc[GPUOS_MAX_WPB];
-    stage_init(p.stage_bytes);
+    __shared__ unsigned long long s_table[GPUOS_MAX_OPS]; /* the sequencer's copy of one table slot */
+    __shared__ uint64_t s_prof[GPUOS_MAX_WPB][GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS]; /* tile profiles */
     const uint32_t warp = threadIdx.x >> 5;
+    for (uint32_t i = threadIdx.x & 31u; i < GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS; i += 32) s_prof[warp][i] = 0;
+    stage_init(p.stage_bytes); /* (its block barriers also order the clearing above) */
     const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
-    if (blockIdx.x == 0 && warp == 0) sequencer(p, &sdesc[0], gw);
-    else worker(p, &sdesc[warp], gw);
+    if (blockIdx.x == 0 && warp == 0) sequencer(p, &sdesc[0], gw, s_table);
+    else worker(p, &sdesc[warp], gw, s_prof[warp]);
 }
 
 /* ===========================================================================
  * Eager baseline: the same op bodies, one launch per descriptor, one warp
  * per tile, one warp per block (spreads a descriptor over many SMs).
  * ======================================================================== */
-DEV int builtin_call(const gpuos_devdesc *d, uint32_t t)
-{
-    switch (d->op_id) {
-    case GPUOS_OP_NOP: return GPUOS_ST_OK;
-    case GPUOS_OP_ADD: return ew_dispatch<EW_ADD>(d, t);
-    case GPUOS_OP_MUL: return ew_dispatch<EW_MUL>(d, t);
-    case GPUOS_OP_RELU: return ew_dispatch<EW_RELU>(d, t);
-    case GPUOS_OP_GELU: return ew_dispatch<EW_GELU>(d, t);
-    case GPUOS_OP_SOFTMAX: return row_tile<ROW_SOFTMAX>(d, t);
-    case GPUOS_OP_LAYERNORM: return row_tile<ROW_LN>(d, t);
-    case GPUOS_OP_ROWSUM: return row_tile<ROW_SUM>(d, t);
-    case GPUOS_OP_ROWMAX: return row_tile<ROW_MAX>(d, t);
-    case GPUOS_OP_ROWMIN: return row_tile<ROW_MIN>(d, t);
-    case GPUOS_OP_ROPE: return rope_tile(d, t);
-    case GPUOS_OP_KV_WRITE: return kv_tile(d, t);
-    case GPUOS_OP_SDPA: return sdpa_tile(d, t);
-    case GPUOS_OP_VECMAT: return vecmat_tile(d, t);
-    default: return GPUOS_ST_BAD_OP;
-    }
-}
-
 #define EAGER_WPB 1
 extern "C" __global__ void __launch_bounds__(EAGER_WPB * 32) gpuos_eager_kernel(gpuos_devdesc d, uint32_t stage_bytes)
 {
@@ -1527,13 +2091,16 @@ extern "C" __global__ void __launch_bounds__(EAGER_WPB * 32) gpuos_eager_kernel(
     reinterpret_cast<uint32_t *>(&sd[warp])[lane_id()] = reinterpret_cast<const uint32_t *>(&d)[lane_id()];
     __syncwarp();
     const uint32_t tile = blockIdx.x * EAGER_WPB + warp;
-    if (tile < sd[warp].ntiles) (void)builtin_call(&sd[warp], tile);
+    if (tile < sd[warp].ntiles) (void)builtin_call(sd[warp].op_id, &sd[warp], tile);
 }
 
 /* ===========================================================================
  * Host-side launch helpers
  * ======================================================================== */
-extern "C" uint32_t gpuos_dev_dyn_smem(uint32_t wpb, uint32_t stage_bytes) { return 16u + wpb * (16u + stage_bytes); }
+extern "C" uint32_t gpuos_dev_dyn_smem(uint32_t wpb, uint32_t stage_bytes)
+{
+    return 16u + wpb * (GPUOS_WARP_STAGE_HDR + stage_bytes);
+}
 
 extern "C" int gpuos_dev_launch_executor(const gpuos_exec_params *p, uint32_t blocks, uint32_t wpb, void *stream)
 {
@@ -1600,10 +2167,10 @@ extern "C" int gpuos_dev_eager_launch(const gpuos_desc *d, uint32_t ntiles, uint
  * output.
  * ======================================================================== */
 #define GPUOS_NOALLOC_MAX_BH 256u  /* requests x heads */
-#define GPUOS_NOALLOC_MAX_L 4096u  /* rows attended per request (8 chunks of 512) */
+#define GPUOS_NOALLOC_MAX_L 4096u  /* rows attended per request (16 chunks of 256) */
 #define GPUOS_NOALLOC_CTR_BYTES (4u * GPUOS_NOALLOC_MAX_BH)
 #define GPUOS_NOALLOC_BYTES \
-    (GPUOS_NOALLOC_CTR_BYTES + 4u * GPUOS_NOALLOC_MAX_BH * (GPUOS_NOALLOC_MAX_L / GPUOS_SDPA_CHUNK) * 130u)
+    (GPUOS_NOALLOC_CTR_BYTES + 4u * GPUOS_NOALLOC_MAX_BH * (GPUOS_NOALLOC_MAX_L / GPUOS_SDPA_CHUNK) * GPUOS_SDPA_PART)
 
 /* Shared by every call on a device and kept until the process exits. In host
  * code this name is only a stand-in for the device array: never pass it to a

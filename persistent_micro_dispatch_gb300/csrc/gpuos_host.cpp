@@ -195,7 +195,8 @@ struct gpuos_ctx {
     bool ring_managed = false;
     /* device memory */
     gpuos_devdesc *mirror = nullptr;
-    uint32_t *tiles_done = nullptr, *err = nullptr, *tile_ctr = nullptr;
+    unsigned long long *tiles_done = nullptr;
+    uint32_t *err = nullptr, *tile_ctr = nullptr;
     uint64_t *done_dev = nullptr;
     uint64_t *t_start = nullptr;
     unsigned long long *tq = nullptr;
@@ -292,15 +293,38 @@ void gpuos_default_config(gpuos_config *c)
 
 size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, uint32_t Lmax)
 {
-    uint64_t nch = (Lmax + GPUOS_SDPA_CHUNK - 1) / GPUOS_SDPA_CHUNK;
+    /* the host splits keys into chunks of GPUOS_SDPA_CHUNK_MIN rows at the finest */
+    uint64_t nch = (Lmax + GPUOS_SDPA_CHUNK_MIN - 1) / GPUOS_SDPA_CHUNK_MIN;
     if (nch == 0) nch = 1;
-    (void)D; /* partials hold D + 2 floats; D is fixed at 128 */
+    (void)D; /* partials hold 132 floats {m, l, 2 pad, acc[128]}; D is fixed at 128 */
     const uint64_t ctr = ((uint64_t)B * H + 3u) & ~3ull;
-    return (size_t)(4ull * ctr + 4ull * B * H * nch * 130ull);
+    return (size_t)(4ull * ctr + 4ull * B * H * nch * 132ull);
 }
 
 static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 static bool al16(uint64_t p) { return (p & 15u) == 0; }
+
+/* Element-wise tiles: the smallest power of two >= n / GPUOS_EW_SPLIT, kept
+ * within [GPUOS_EW_TILE_MIN, the largest tile]. Small ops spread over up to
+ * GPUOS_EW_SPLIT warps; large ones take full tiles. The device recovers the
+ * tile size from n and ntiles alone (round_up(ceil(n / ntiles), 256)). */
+static uint64_t ew_tiles(uint64_t n, uint64_t tile_max)
+{
+    uint64_t te = GPUOS_EW_TILE_MIN;
+    while (te < tile_max && te * GPUOS_EW_SPLIT < n) te <<= 1;
+    return ceil_div(n, te);
+}
+
+/* Decode-attention chunks: 256 key rows, halved (down to 32) while the op
+ * would have fewer than GPUOS_SDPA_SPLIT tiles, so that a small batch still
+ * spreads over most of the worker warps. The device recovers the chunk length from Lmax
+ * and ntiles (round_up(ceil(Lmax / nchunks), 32)). */
+static uint64_t sdpa_chunks(uint64_t BH, uint64_t Lmax)
+{
+    uint64_t c = GPUOS_SDPA_CHUNK;
+    while (c > GPUOS_SDPA_CHUNK_MIN && BH * ceil_div(Lmax, c) < GPUOS_SDPA_SPLIT) c >>= 1;
+    return ceil_div(Lmax, c);
+}
 
 /* Host-side validation (the page's "bounds checking") and tiling rule. */
 static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool user_op_known)
@@ -317,7 +341,7 @@ static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool use
         if (d->dtype != GPUOS_F32 && d->dtype != GPUOS_BF16) return GPUOS_EINVAL;
         const bool bin = d->op_id == GPUOS_OP_ADD || d->op_id == GPUOS_OP_MUL;
         if (m[0] && (!d->a || !d->out || (bin && !d->b))) return GPUOS_EINVAL;
-        nt = ceil_div(m[0], d->dtype == GPUOS_F32 ? GPUOS_EW_TILE_F32 : GPUOS_EW_TILE_BF16);
+        nt = ew_tiles(m[0], d->dtype == GPUOS_F32 ? GPUOS_EW_TILE_F32 : GPUOS_EW_TILE_BF16);
         break;
     }
     case GPUOS_OP_SOFTMAX:
@@ -333,12 +357,12 @@ static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool use
     case GPUOS_OP_ROPE:
         if (m[0] && (!d->a || !d->b || !d->aux0 || m[1] == 0 || m[2] == 0 || (m[2] & 1) || m[2] > 256))
             return GPUOS_EINVAL;
-        nt = m[0];
+        nt = (uint64_t)m[0] * ceil_div(m[1], GPUOS_HEAD_GROUP);
         break;
     case GPUOS_OP_KV_WRITE:
         if (m[0] && (!d->a || !d->b || !d->aux0 || !d->out || !d->aux1 || m[1] == 0 || m[2] == 0 || m[3] == 0))
             return GPUOS_EINVAL;
-        nt = m[0];
+        nt = (uint64_t)m[0] * ceil_div(m[1], GPUOS_HEAD_GROUP);
         break;
     case GPUOS_OP_SDPA:
         if (m[0]) {
@@ -347,7 +371,7 @@ static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool use
             if ((uint64_t)m[5] < (uint64_t)m[0] * m[1]) return GPUOS_EINVAL;
             if (!al16(d->a) || !al16(d->b) || !al16(d->aux1) || !al16(d->out) || !al16(d->aux2)) return GPUOS_EINVAL;
         }
-        nt = (uint64_t)m[0] * m[1] * ceil_div(m[4], GPUOS_SDPA_CHUNK);
+        nt = (uint64_t)m[0] * m[1] * sdpa_chunks((uint64_t)m[0] * m[1], m[4]);
         break;
     case GPUOS_OP_VECMAT:
         if (m[1] && (!d->a || !d->b || !d->out || m[0] == 0)) return GPUOS_EINVAL;
@@ -429,6 +453,10 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
         return GPUOS_EINVAL;
     if (cfg.backoff_min_ns == 0 || cfg.backoff_max_ns < cfg.backoff_min_ns) return GPUOS_EINVAL;
     if ((cfg.stage_bytes & 1023u) || cfg.stage_bytes > 24576u) return GPUOS_EINVAL;
+    /* every warp's staging region and the executor's static shared memory
+     * (descriptor copies, the sequencer's table copy, tile profiles) must fit
+     * the 227 KB a block can hold */
+    if (gpuos_dev_dyn_smem(cfg.warps_per_block, cfg.stage_bytes) + GPUOS_EXEC_STATIC_SMEM > 232448u) return GPUOS_EINVAL;
 
     gpuos_ctx *c = new (std::nothrow) gpuos_ctx();
     if (!c) return GPUOS_ENOMEM;
@@ -498,7 +526,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
 
     const uint32_t total_warps = c->blocks * c->wpb;
     CK(cudaMalloc((void **)&c->mirror, (size_t)c->N * sizeof(gpuos_devdesc)));
-    CK(cudaMalloc((void **)&c->tiles_done, (size_t)c->N * 4));
+    CK(cudaMalloc((void **)&c->tiles_done, (size_t)c->N * 8));
     CK(cudaMalloc((void **)&c->err, (size_t)c->N * 4));
     CK(cudaMalloc((void **)&c->tile_ctr, (size_t)c->N * 4));
     CK(cudaMalloc((void **)&c->done_dev, (size_t)c->N * 8));
@@ -509,7 +537,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     CK(cudaMalloc((void **)&c->table, sizeof(c->table_host)));
     CK(cudaMalloc((void **)&c->warp_stats, (size_t)total_warps * GPUOS_WS_N * 8));
     CK(cudaMemsetAsync(c->mirror, 0, (size_t)c->N * sizeof(gpuos_devdesc), c->ctl_stream));
-    CK(cudaMemsetAsync(c->tiles_done, 0, (size_t)c->N * 4, c->ctl_stream));
+    CK(cudaMemsetAsync(c->tiles_done, 0, (size_t)c->N * 8, c->ctl_stream));
     CK(cudaMemsetAsync(c->err, 0, (size_t)c->N * 4, c->ctl_stream));
     CK(cudaMemsetAsync(c->tile_ctr, 0, (size_t)c->N * 4, c->ctl_stream));
     CK(cudaMemsetAsync(c->done_dev, 0, (size_t)c->N * 8, c->ctl_stream));
@@ -1003,6 +1031,24 @@ int gpuos_stats(gpuos_ctx *c, gpuos_stats_t *st)
     st->regs_per_thread = c->regs;
     st->static_smem_bytes = c->smem;
     heartbeat(c);
+    return GPUOS_OK;
+}
+
+int gpuos_tile_profile_get(gpuos_ctx *c, gpuos_tile_profile *out)
+{
+    if (!c || !out) return GPUOS_EINVAL;
+    memset(out, 0, sizeof(*out));
+    const uint32_t tw = c->blocks * c->wpb;
+    std::vector<uint64_t> ws((size_t)tw * GPUOS_WS_N);
+    if (cudaMemcpyAsync(ws.data(), c->warp_stats, ws.size() * 8, cudaMemcpyDeviceToHost, c->ctl_stream) != cudaSuccess ||
+        cudaStreamSynchronize(c->ctl_stream) != cudaSuccess)
+        return GPUOS_ECUDA;
+    uint64_t *rows[GPUOS_PROF_FIELDS] = {out->tiles, out->body_ns, out->finish_ns, out->dep_ns};
+    for (uint32_t w = 0; w < tw; w++) {
+        const uint64_t *x = &ws[(size_t)w * GPUOS_WS_N + GPUOS_WS_PROF];
+        for (uint32_t f = 0; f < GPUOS_PROF_FIELDS; f++)
+            for (uint32_t b = 0; b < GPUOS_PROF_BUCKETS; b++) rows[f][b] += x[f * GPUOS_PROF_BUCKETS + b];
+    }
     return GPUOS_OK;
 }
 

@@ -10,14 +10,23 @@
 #include "gpuos.h"
 
 /* Tiling constants of the built-in ops (one tile = one warp's unit of work). */
-#define GPUOS_EW_VPT 32                   /* 16-byte vectors per lane per element-wise tile */
-#define GPUOS_EW_TILE_F32 (32 * GPUOS_EW_VPT * 4)  /* 4096 fp32 elements */
-#define GPUOS_EW_TILE_BF16 (32 * GPUOS_EW_VPT * 8) /* 8192 bf16 elements */
-#define GPUOS_SDPA_CHUNK 256              /* key rows per decode-attention tile */
-#define GPUOS_VM_COLS 32                  /* output columns per vecmat tile */
+#define GPUOS_EW_VPT 32                   /* 16-byte vectors per lane in the largest element-wise tile */
+#define GPUOS_EW_TILE_F32 (32 * GPUOS_EW_VPT * 4)  /* 4096 fp32 elements at most */
+#define GPUOS_EW_TILE_BF16 (32 * GPUOS_EW_VPT * 8) /* 8192 bf16 elements at most */
+#define GPUOS_EW_TILE_MIN 1024            /* smallest element-wise tile the host picks */
+#define GPUOS_EW_SPLIT 16                 /* element-wise ops aim at this many tiles */
+#define GPUOS_EW_ALIGN 256                /* element-wise tile sizes are multiples of this */
+#define GPUOS_SDPA_CHUNK 256              /* key rows per decode-attention tile at most */
+#define GPUOS_SDPA_CHUNK_MIN 32           /* ... and at least (workspace sizing) */
+#define GPUOS_SDPA_SPLIT 1536             /* attention aims at this many tiles */
+#define GPUOS_HEAD_GROUP 4                /* heads per RoPE / KV-write tile */
+#define GPUOS_VM_COLS 8                   /* output columns per vecmat tile (16 bytes of a row) */
 #define GPUOS_ROW_REG_MAX 4096            /* rows up to this width stay in registers */
-#define GPUOS_MAX_WPB 16
-#define GPUOS_MAX_REGS 128 /* registers per thread: 65536 / (16 warps x 32) */
+#define GPUOS_MAX_WPB 12
+/* static shared memory of the executor kernel: descriptor copies, the
+ * sequencer's table copy, per-warp tile profiles */
+#define GPUOS_EXEC_STATIC_SMEM (GPUOS_MAX_WPB * 128 + 256 * 8 + GPUOS_MAX_WPB * GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS * 8)
+#define GPUOS_MAX_REGS 168 /* registers per thread: 65536 / (12 warps x 32), in steps of 8 */
 #define GPUOS_TILE_MAX (1u << 30)          /* tiles per descriptor */
 #define GPUOS_HELPERS 1024                 /* work-queue entries (helper warps) per descriptor at most */
 #define GPUOS_TQ_MAX (1u << 30)            /* work-queue entries */
@@ -35,7 +44,7 @@ typedef struct gpuos_devdesc {
     uint64_t aux0, aux1, aux2;
     uint32_t dims[6];
     float fparam[2];
-    uint64_t t_dispatch; /* device clock when the commit was seen (replaces `user`) */
+    uint64_t fn;         /* op entry point, fixed with the version at sequencing (replaces `user`) */
     uint64_t ticket;
     uint32_t version;    /* table version fixed at sequencing (replaces `seq`) */
     uint32_t pad;
@@ -82,7 +91,10 @@ typedef struct gpuos_devctl {
 
 /* Per-warp counters (owned by one warp each, plain stores). */
 enum { GPUOS_WS_TILES = 0, GPUOS_WS_IDLE = 1, GPUOS_WS_SLEEPS = 2, GPUOS_WS_DEPWAIT = 3,
-       GPUOS_WS_SEQ = 4, GPUOS_WS_T_BODY = 5, GPUOS_WS_T_MIRROR = 6, GPUOS_WS_T_PUB = 7, GPUOS_WS_N = 8 };
+       GPUOS_WS_SEQ = 4, GPUOS_WS_T_BODY = 5, GPUOS_WS_T_MIRROR = 6, GPUOS_WS_T_PUB = 7,
+       /* tile profile: GPUOS_PROF_FIELDS rows of GPUOS_PROF_BUCKETS (op id, or the last
+        * bucket for user ops): tiles, body ns, finish ns, dependency ns */
+       GPUOS_WS_PROF = 8, GPUOS_WS_N = 8 + GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS };
 
 typedef int (*gpuos_op_fn)(const gpuos_devdesc *d, uint32_t tile);
 
@@ -91,7 +103,7 @@ typedef struct gpuos_exec_params {
     gpuos_rec_dev *rec;      /* host-visible completion records */
     gpuos_hostctl *hctl;
     gpuos_devdesc *mirror;   /* [ring_entries] */
-    uint32_t *tiles_done;    /* [ring_entries] */
+    unsigned long long *tiles_done; /* [ring_entries]: tiles done (low 32 bits), failed helpers (high 32) */
     uint32_t *err;           /* [ring_entries] */
     uint32_t *tile_ctr;      /* [ring_entries], next extra tile (past the helpers' first tiles) */
     uint64_t *done_dev;      /* [ring_entries], ticket + 1 stamps for dependency waits */

@@ -75,6 +75,14 @@ class Stats(C.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
 
 
+PROF_BUCKETS = 16
+
+
+class TileProfile(C.Structure):
+    _fields_ = [("tiles", C.c_uint64 * PROF_BUCKETS), ("body_ns", C.c_uint64 * PROF_BUCKETS),
+                ("finish_ns", C.c_uint64 * PROF_BUCKETS), ("dep_ns", C.c_uint64 * PROF_BUCKETS)]
+
+
 # every symbol include/gpuos.h declares
 API = {
     "gpuos_default_config": (None, [C.POINTER(Config)]),
@@ -89,6 +97,7 @@ API = {
     "gpuos_load_module": (C.c_int, [C.c_void_p, C.c_void_p, C.c_size_t]),
     "gpuos_alias_op": (C.c_int, [C.c_void_p, C.c_uint16, C.c_uint16]),
     "gpuos_stats": (C.c_int, [C.c_void_p, C.POINTER(Stats)]),
+    "gpuos_tile_profile_get": (C.c_int, [C.c_void_p, C.POINTER(TileProfile)]),
     "gpuos_calibrate": (C.c_int, [C.c_void_p, C.c_uint32, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
                                   C.POINTER(C.c_uint64), C.c_void_p]),
     "gpuos_shutdown": (C.c_int, [C.c_void_p, C.c_uint32]),
@@ -241,6 +250,22 @@ class Executor:
         check(lib().gpuos_alias_op(self._ctx, op_id, source_op), "gpuos_alias_op")
 
     # -- measurement -----------------------------------------------------------
+    def tile_profile(self) -> dict:
+        """Per op name: tiles run and the mean device time per tile (µs)
+        inside the op, finishing (counting, completing) and waiting for
+        dependencies; user ops share the bucket "user"."""
+        t = TileProfile()
+        check(lib().gpuos_tile_profile_get(self._ctx, C.byref(t)), "gpuos_tile_profile_get")
+        names = {v: k for k, v in OP.items()}
+        out = {}
+        for b in range(PROF_BUCKETS):
+            n = int(t.tiles[b])
+            if n == 0:
+                continue
+            out[names.get(b, "user")] = {"tiles": n, "body_us": t.body_ns[b] / n / 1e3,
+                                         "finish_us": t.finish_ns[b] / n / 1e3, "dep_us": t.dep_ns[b] / n / 1e3}
+        return out
+
     def stats(self) -> dict:
         s = Stats()
         check(lib().gpuos_stats(self._ctx, C.byref(s)), "gpuos_stats")

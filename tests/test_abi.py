@@ -71,15 +71,51 @@ def _desc(G, op, dtype=1, dims=(), ptr=0x1000, **kw):
 
 
 def test_tiling_rule(G):
-    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 1          # 4096 fp32 per tile
-    assert G.op_ntiles(_desc(G, "add", 1, (16384,))) == 2         # 8192 bf16 per tile
-    assert G.op_ntiles(_desc(G, "relu", 0, (8193,))) == 3
+    # element-wise: te = smallest power of two >= n/16 within [1024, 4096 | 8192]
+    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 4          # te 1024
+    assert G.op_ntiles(_desc(G, "add", 1, (16384,))) == 16        # te 1024
+    assert G.op_ntiles(_desc(G, "relu", 0, (8193,))) == 9         # te 1024
+    assert G.op_ntiles(_desc(G, "mul", 0, (1000,))) == 1
+    assert G.op_ntiles(_desc(G, "add", 0, (65536,))) == 16        # te 4096 (fp32 cap)
+    assert G.op_ntiles(_desc(G, "add", 0, (1 << 20,))) == 256     # te 4096
+    assert G.op_ntiles(_desc(G, "gelu", 1, (1 << 20,))) == 128    # te 8192 (bf16 cap)
+    assert G.op_ntiles(_desc(G, "gelu", 1, (40000,))) == 10       # te 4096 >= 40000/16
     assert G.op_ntiles(_desc(G, "gelu", 0, (0,))) == 1            # empty op: one tile
     assert G.op_ntiles(_desc(G, "softmax", 1, (37, 1024))) == 37  # one row per tile
-    assert G.op_ntiles(_desc(G, "rope", 1, (5, 32, 128))) == 5
-    assert G.op_ntiles(_desc(G, "sdpa", 1, (3, 32, 128, 4096, 1025, 96))) == 3 * 32 * 5  # 256-row chunks
-    assert G.op_ntiles(_desc(G, "vecmat", 1, (1024, 1024))) == 32
+    assert G.op_ntiles(_desc(G, "rope", 1, (5, 32, 128))) == 5 * 8  # four heads per tile
+    assert G.op_ntiles(_desc(G, "rope", 1, (2, 6, 64))) == 2 * 2
+    kv = _desc(G, "kv_write", 1, (3, 30, 128, 4096), out=0x2000, aux1=0x3000)
+    assert G.op_ntiles(kv) == 3 * 8
+    # attention: 96 (request, head) pairs x 1025 rows: 256- and 128-row chunks
+    # give 480 and 864 tiles (< 1536), 64-row chunks 1632: 17 per head
+    assert G.op_ntiles(_desc(G, "sdpa", 1, (3, 32, 128, 4096, 1025, 96))) == 96 * 17
+    assert G.op_ntiles(_desc(G, "sdpa", 1, (8, 32, 128, 4096, 4096, 256))) == 256 * 16  # 256-row chunks
+    assert G.op_ntiles(_desc(G, "sdpa", 1, (1, 32, 128, 4096, 2000, 32))) == 32 * 63   # 32-row chunks
+    assert G.op_ntiles(_desc(G, "vecmat", 1, (1024, 1024))) == 128
+    assert G.op_ntiles(_desc(G, "vecmat", 1, (1024, 1000))) == 125
     assert G.op_ntiles(_desc(G, "nop")) == 1
+
+
+def test_device_tile_ranges_cover_each_op(G):
+    """The device recovers the element-wise tile size and the attention chunk
+    length from the host's ntiles (the rule stated in gpuos.h); for every
+    size the ranges must cover the op, stay 16-byte aligned, fit the largest
+    tile, and (attention) use no more partials than the workspace holds."""
+    for dt, cap in ((0, 4096), (1, 8192)):
+        for n in [1, 255, 256, 257, 1023, 1024, 1025, 4095, 4096, 4097, 16383, 16385, 65535, 65536,
+                  65537, 100003, 1 << 20, (1 << 20) + 7, 3 * 8192 + 1]:
+            nt = G.op_ntiles(_desc(G, "add", dt, (n,)))
+            te = -(-(-(-n // nt)) // 256) * 256
+            assert te * nt >= n and te <= cap and te % 256 == 0, (dt, n, nt, te)
+            assert (nt - 1) * te < n  # no tile starts past the end
+    for B, H, L in ((1, 32, 1), (1, 32, 33), (1, 32, 2000), (3, 32, 1025), (8, 32, 4096), (2, 1, 4096),
+                    (1, 1, 100), (4, 8, 777)):
+        nt = G.op_ntiles(_desc(G, "sdpa", 1, (B, H, 128, 4096, L, B * H)))
+        assert nt % (B * H) == 0
+        nch = nt // (B * H)
+        ch = -(-(-(-L // nch)) // 32) * 32
+        assert ch * nch >= L and ch <= 256
+        assert nch <= -(-L // 32)  # within the workspace's partials
 
 
 @pytest.mark.parametrize("bad", [
@@ -130,7 +166,9 @@ def test_init_without_gpu_fails_cleanly(G):
 def test_init_rejects_bad_config(G):
     ctx = C.c_void_p()
     for kw in (dict(ring_entries=100), dict(ring_entries=32), dict(warps_per_block=1),
-               dict(warps_per_block=17), dict(tq_entries=1000), dict(tq_entries=1 << 18), dict(backoff_min_ns=0),
-               dict(stage_bytes=1000), dict(stage_bytes=32768)):
+               dict(tq_entries=1000), dict(tq_entries=1 << 18), dict(backoff_min_ns=0),
+               dict(stage_bytes=1000), dict(stage_bytes=32768),
+               dict(warps_per_block=13),                             # > 12 warps (168 registers each)
+               dict(warps_per_block=12, stage_bytes=24576)):  # 12 x 24 KB staging > 227 KB
         cfg = G.default_config(**kw)
         assert G.lib().gpuos_init(C.byref(cfg), C.byref(ctx)) == G.EINVAL, kw

@@ -83,29 +83,74 @@ def test_c4_decode_small_and_kv_copy_bit_exact():
 def _check_kv_copies(s, ds):
     """Replay every KV write with the GPU's own (rotated) k/v rows on the
     initial caches: the GPU caches must equal the result byte for byte."""
-    iK, iV = s.buf_index("Kc"), s.buf_index("Vc")
-    K = s.buffers[iK].data.copy()
-    V = s.buffers[iV].data.copy()
+    caches = {}
     for o in s.ops:
         if o.op != "kv_write":
             continue
+        for ref in (o.out, o.aux1):
+            if ref.buf not in caches:
+                caches[ref.buf] = s.buffers[ref.buf].data.copy()
         B, H, D, Lc = o.dims[:4]
         lens = s.buffers[o.aux0.buf].data[o.aux0.off:o.aux0.off + B]
         k = ds.read(o.a, B * H * D).reshape(B, H, D)
         v = ds.read(o.b, B * H * D).reshape(B, H, D)
-        K4 = K[o.out.off:o.out.off + B * H * Lc * D].reshape(B, H, Lc, D)
-        V4 = V[o.aux1.off:o.aux1.off + B * H * Lc * D].reshape(B, H, Lc, D)
+        K4 = caches[o.out.buf][o.out.off:o.out.off + B * H * Lc * D].reshape(B, H, Lc, D)
+        V4 = caches[o.aux1.buf][o.aux1.off:o.aux1.off + B * H * Lc * D].reshape(B, H, Lc, D)
         for b in range(B):
             K4[b, :, lens[b] - 1] = k[b]
             V4[b, :, lens[b] - 1] = v[b]
-    assert np.array_equal(ds.read_buf(iK), K)
-    assert np.array_equal(ds.read_buf(iV), V)
+    assert caches, "no KV write in the stream"
+    for i, want in caches.items():
+        assert np.array_equal(ds.read_buf(i), want), s.buffers[i].name
+
+
+@pytest.mark.parametrize("stage_bytes", [16384, 0])
+def test_mixed_small_every_op_kind(stage_bytes):
+    """Every op kind at small, ragged sizes (tails, 1-row and 8-column tiles,
+    ragged head groups, multi-chunk attention), staged and register paths."""
+    s, ds, rep, st, hist = _run_and_compare(S.stream_mixed_small(), cfg=dict(stage_bytes=stage_bytes))
+    _check_kv_copies(s, ds)
 
 
 def test_c5_mixed_pipeline_small():
     """3 tokens of the 32-layer synthetic decoder at hidden 4,096."""
     s, ds, rep, st, hist = _run_and_compare(S.stream_c5(n_tokens=3))
     _check_kv_copies(s, ds)
+
+
+def test_gelu_fp32_error_bound_sweep():
+    """The GPU's GELU evaluates erfc by the Numerical Recipes Chebyshev fit
+    (fractional error < 1.2e-7) in fp32. Over x in [-12, 12] (and special
+    values) its relative error against the oracle's double GELU must stay
+    within the fit's bound plus fp32 rounding, which grows with the
+    conditioning of erfc(|x|/sqrt 2), about x^2 ulps of the argument."""
+    from workloads.device import DeviceStream
+    n = (1 << 20) + 37
+    x = np.linspace(-12.0, 12.0, n - 37).astype(np.float32)
+    special = np.array([0.0, -0.0, 1e-30, -1e-30, 1e-7, -1e-7, 0.5, -0.5, 1.0, -1.0, 2.0, -2.0, 3.0, -3.0,
+                        0.4769363, -0.4769363, 5.0, -5.0, 8.0, -8.0, 10.0, -10.0, 12.0, -12.0, 0.70710678,
+                        -0.70710678, 1.4142135, -1.4142135, 2.5, -2.5, 6.0, -6.0, 4.0, -4.0, 1.5, -1.5,
+                        3.5], np.float32)
+    xs = np.concatenate([x, special])
+    s = S.Stream("gelu_sweep")
+    ia = s.add_buf("x", "f32", n, xs)
+    io = s.add_buf("out", "f32", n)
+    s.ops.append(S.Op("gelu", "f32", a=S.Ref(ia, 0), out=S.Ref(io, 0), dims=(n,)))
+    ds = DeviceStream(s)
+    st, hist = run_executor(ds, ds.descs())
+    assert np.all(hist["status"] == 0)
+    got = ds.read(S.Ref(io, 0), n).astype(np.float64)
+    mach = Machine(s)
+    mach.run(keep=[0])
+    ref = mach.exact[0]["out"]
+    xd = xs.astype(np.float64)
+    bound = (6e-7 + 1.2e-7 * xd * xd) * np.abs(ref) + 1e-37
+    err = np.abs(got - ref)
+    bad = np.nonzero(err > bound)[0]
+    assert bad.size == 0, [(float(xd[i]), float(got[i]), float(ref[i])) for i in bad[:5]]
+    # and the parity rule the streams use
+    rep = compare_stream(s, ds, mach, [0])
+    assert rep.ok(), "\n".join(rep.failures)
 
 
 @pytest.mark.slow

@@ -42,11 +42,11 @@ ELEMENTWISE = ("add", "mul", "relu", "gelu")
 ROWOPS = ("softmax", "layernorm", "rowsum", "rowmax", "rowmin")
 ALL_OPS = ELEMENTWISE + ROWOPS + ("rope", "kv_write", "sdpa", "vecmat", "nop")
 
-# Decode attention splits each (request, head) into chunks of this many key
-# positions; the CUDA path keeps one partial (m, l, acc[D]) per chunk in a
-# caller-provided fp32 workspace followed by one uint32 counter per
+# Decode attention splits each (request, head) into chunks of at least this
+# many key positions; the CUDA path keeps one partial (m, l, 2 pad, acc[D])
+# per chunk in a caller-provided fp32 workspace after one uint32 counter per
 # (request, head). The layout is part of the descriptor contract.
-SDPA_CHUNK = 256
+SDPA_CHUNK_MIN = 32
 
 # Canary byte written into every output arena before a run; bytes that no op
 # writes must still hold it afterwards.
@@ -56,9 +56,9 @@ CANARY_BYTE = 0x5A
 def sdpa_workspace_bytes(B: int, H: int, D: int, Lmax: int) -> int:
     """Bytes of the split-K workspace of decode-SDPA descriptors with at most
     B requests: B*H uint32 counters (rounded up to 4), then one fp32 partial
-    (m, l, acc[D]) per (request, head, chunk)."""
-    nch = max(1, -(-Lmax // SDPA_CHUNK))
-    return 4 * ((B * H + 3) // 4 * 4) + 4 * (B * H * nch * (D + 2))
+    (m, l, 2 pad, acc[D]) per (request, head, chunk) at the finest split."""
+    nch = max(1, -(-Lmax // SDPA_CHUNK_MIN))
+    return 4 * ((B * H + 3) // 4 * 4) + 4 * (B * H * nch * (D + 4))
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -662,5 +662,24 @@ def stream_mixed_small(seed: int = 7) -> Stream:
     s.ops.append(Op("sdpa", "bf16", a=Ref(iq, 0), b=Ref(iK, 0), aux1=Ref(iV, 0), aux0=Ref(il, 0), out=Ref(io, 0),
                     aux2=Ref(ws, 0), dims=(B, H, D, Lc, 1037, B * H), fparam=(1.0 / math.sqrt(D),),
                     deps=(r + 1,)))
+    # ragged head groups (6 = 4 + 2 and 5 = 4 + 1 heads), the element-pair
+    # RoPE and element KV paths (D = 66), and a vecmat whose last tile holds
+    # 8 of 16 columns, on the staged path (K % 8 == 0, aligned operands)
+    for tag, (Bx, Hx, Dx, Lcx, lens) in (("2", (2, 6, 66, 40, [40, 17])), ("3", (1, 5, 64, 16, [9]))):
+        nq = Bx * Hx * Dx
+        jq = s.add_buf("q" + tag, "bf16", nq, _pool(rng, nq, "bf16"))
+        jk = s.add_buf("k_new" + tag, "bf16", nq, _pool(rng, nq, "bf16"))
+        jv = s.add_buf("v_new" + tag, "bf16", nq, _pool(rng, nq, "bf16"))
+        nc = Bx * Hx * Lcx * Dx
+        jK = s.add_buf("Kc" + tag, "bf16", nc, _pool(rng, nc, "bf16"))
+        jV = s.add_buf("Vc" + tag, "bf16", nc, _pool(rng, nc, "bf16"))
+        jl = s.add_buf("lens" + tag, "i32", Bx, np.array(lens, np.int32))
+        r = len(s.ops)
+        s.ops.append(Op("rope", "bf16", a=Ref(jq, 0), b=Ref(jk, 0), aux0=Ref(jl, 0), dims=(Bx, Hx, Dx),
+                        fparam=(10000.0,)))
+        s.ops.append(Op("kv_write", "bf16", a=Ref(jk, 0), b=Ref(jv, 0), aux0=Ref(jl, 0), out=Ref(jK, 0),
+                        aux1=Ref(jV, 0), dims=(Bx, Hx, Dx, Lcx), deps=(r,)))
+    iW2 = s.add_buf("W2", "bf16", 1024 * 40, _pool(rng, 1024 * 40, "bf16", std=0.05))
+    s.ops.append(Op("vecmat", "bf16", a=Ref(pb, 1024), b=Ref(iW2, 0), out=Ref(ob, eb.take(40)), dims=(1024, 40)))
     s.ops.append(Op("nop", fence=True))
     return s
