@@ -301,6 +301,8 @@ def main():
     ap.add_argument("--blocks", type=int, default=0, help="executor blocks (0 = one per SM)")
     ap.add_argument("--spin-polls", type=int, default=0, help="idle polls before backoff sleeps (0 = default)")
     ap.add_argument("--backoff-max-ns", type=int, default=0, help="longest idle sleep (0 = default)")
+    ap.add_argument("--ring-device", action="store_true",
+                    help="ring in device memory (managed, host-accessible) instead of pinned host memory")
     ap.add_argument("--graph", action="store_true",
                     help="also time the eager launches captured into a CUDA graph (replay, and re-capture per step)")
     ap.add_argument("--corun-gemm", action="store_true",
@@ -329,6 +331,8 @@ def main():
         cfg_kw["spin_polls"] = args.spin_polls
     if args.backoff_max_ns:
         cfg_kw["backoff_max_ns"] = args.backoff_max_ns
+    if args.ring_device:
+        cfg_kw["ring_in_device_mem"] = 1
     if args.profile_run and args.profile_desc and args.workload in ("c2", "c2l", "c3"):
         kw = dict(n_desc=args.profile_desc)
         if args.pool_log2:

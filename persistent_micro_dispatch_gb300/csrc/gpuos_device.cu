@@ -1584,8 +1584,7 @@ DEV void fence_acq_rel_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); 
 /* Complete one descriptor (single thread). The device-memory done stamp
  * that dependent tiles wait on is released first; the host-visible record
  * (stores across NVLink-C2C, whose acknowledgements a release would have to
- * wait for) is written after it. The record's t_dispatch was written by the
- * sequencer when it saw the commit. */
+ * wait for) is written after it. */
 DEV void complete_desc(const gpuos_exec_params &p, uint64_t ticket, uint32_t slot, int32_t status, uint32_t version)
 {
     gpuos_rec_dev *r = p.rec + slot;
@@ -1601,8 +1600,10 @@ DEV void complete_desc(const gpuos_exec_params &p, uint64_t ticket, uint32_t slo
     st_relaxed_gpu32(p.tile_ctr + slot, 0u);
     const uint64_t t_pub = *reinterpret_cast<volatile uint64_t *>(p.t_pub + slot);
     const uint64_t t_start = *reinterpret_cast<volatile uint64_t *>(p.t_start + slot);
+    const uint64_t t_disp = *reinterpret_cast<volatile uint64_t *>(p.t_disp + slot);
     st_relaxed_sys32(reinterpret_cast<uint32_t *>(&r->status), (uint32_t)status);
     st_relaxed_sys32(&r->version, version);
+    st_relaxed_sys(&r->t_dispatch, t_disp);
     st_relaxed_sys(&r->t_publish, t_pub);
     st_relaxed_sys(&r->t_start, t_start);
     st_relaxed_sys(&r->t_done, t_done);
@@ -1647,15 +1648,19 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
     const uint32_t KMAX = N < 32u * SEQ_SPL ? N : 32u * SEQ_SPL;
     if (lane == 0) st_relaxed_sys32(&p.hctl->state, 1u);
 
+    /* commit words of slots s + lane + 32 h, polled ahead (relaxed; the
+     * batch's fence comes after they are seen): the poll for the next batch
+     * is issued before the current one is published, so its NVLink-C2C
+     * round trip overlaps the publication */
+    uint64_t seqv[SEQ_SPL];
+#pragma unroll
+    for (int h = 0; h < SEQ_SPL; h++)
+        seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
     while (true) {
-        /* poll 64 consecutive slots, two per lane (relaxed; one fence below) */
         uint64_t rmask = 0;
 #pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++) {
-            const uint64_t t = s + lane + 32u * h;
-            const uint64_t seq = ld_relaxed_sys(&p.ring[(uint32_t)(t & p.ring_mask)].seq);
-            rmask |= (uint64_t)__ballot_sync(0xFFFFFFFFu, seq == t + 1) << (32 * h);
-        }
+        for (int h = 0; h < SEQ_SPL; h++)
+            rmask |= (uint64_t)__ballot_sync(0xFFFFFFFFu, seqv[h] == s + lane + 32u * h + 1) << (32 * h);
         uint32_t k = (rmask == ~0ull) ? 64u : (uint32_t)(__ffsll((long long)~rmask) - 1);
         if (k > KMAX) k = KMAX;
         if (k == 0) {
@@ -1686,18 +1691,20 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                 }
             }
             backoff(polls, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+#pragma unroll
+            for (int h = 0; h < SEQ_SPL; h++)
+                seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
             continue;
         }
         const uint64_t t_obs = globaltimer();
         polls = 0;
-        /* echo the observation time into each record at once (a posted
-         * write): the host can time commit -> observe without waiting for
-         * the whole descriptor */
-#pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++) {
-            const uint32_t pos = lane + 32u * h;
-            if (pos < k) st_relaxed_sys(&p.rec[(uint32_t)((s + pos) & p.ring_mask)].t_dispatch, t_obs);
-        }
+        /* a lone descriptor's observation time goes to its record at once
+         * (a posted write): the host times commit -> observe and calibrates
+         * the clocks with it. Every record gets it again at completion,
+         * from t_disp (the mirror fence orders that store before the
+         * publication); a batch's early echo would make this batch's fence
+         * wait for 64 stores across NVLink-C2C. */
+        if (k == 1 && lane == 0) st_relaxed_sys(&p.rec[(uint32_t)(s & p.ring_mask)].t_dispatch, t_obs);
         /* the commits seen above happen-before everything below */
         fence_acq_rel_sys();
         gpuos_desc dsc[SEQ_SPL];
@@ -1765,6 +1772,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             status[h] = GPUOS_ST_OK;
             nt[h] = 0;
             if (pos < k) {
+                *reinterpret_cast<volatile uint64_t *>(p.t_disp + (uint32_t)(my_t & p.ring_mask)) = t_obs;
                 if (dsc[h].ticket != my_t) status[h] = GPUOS_ST_BAD_DESC;
                 else if (dsc[h].op_id >= GPUOS_MAX_OPS) status[h] = GPUOS_ST_BAD_OP;
                 else if (dsc[h].ntiles == 0 || dsc[h].ntiles > GPUOS_TILE_MAX) status[h] = GPUOS_ST_BAD_ARGS;
@@ -1816,12 +1824,19 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                 ws[GPUOS_WS_TILES] = n_inline;
             }
             idle.start();
+#pragma unroll
+            for (int h = 0; h < SEQ_SPL; h++)
+                seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
             continue;
         }
         /* every lane's mirror writes happen-before every lane's fence */
         __syncwarp();
         __threadfence();
         const uint64_t t_m = globaltimer();
+        /* the next batch's poll, in flight during the publication below */
+#pragma unroll
+        for (int h = 0; h < SEQ_SPL; h++)
+            seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + k + lane + 32u * h) & p.ring_mask)].seq);
         /* exclusive prefix of entry counts in ticket order -> queue ranges */
         uint32_t excl[SEQ_SPL];
         uint32_t base = 0;

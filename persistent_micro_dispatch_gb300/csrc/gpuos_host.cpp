@@ -201,6 +201,7 @@ struct gpuos_ctx {
     uint64_t *t_start = nullptr;
     unsigned long long *tq = nullptr;
     uint64_t *t_pub = nullptr;
+    uint64_t *t_disp = nullptr;
     gpuos_devctl *dctl = nullptr;
     gpuos_op_fn *table = nullptr;
     uint64_t *warp_stats = nullptr;
@@ -415,6 +416,7 @@ static void free_all(gpuos_ctx *c)
     cudaFree(c->done_dev);
     cudaFree(c->t_start);
     cudaFree(c->t_pub);
+    cudaFree(c->t_disp);
     cudaFree(c->tq);
     cudaFree(c->dctl);
     cudaFree(c->table);
@@ -533,6 +535,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     CK(cudaMalloc((void **)&c->t_start, (size_t)c->N * 8));
     CK(cudaMalloc((void **)&c->tq, (size_t)c->Q * 8));
     CK(cudaMalloc((void **)&c->t_pub, (size_t)c->N * 8));
+    CK(cudaMalloc((void **)&c->t_disp, (size_t)c->N * 8));
     CK(cudaMalloc((void **)&c->dctl, sizeof(gpuos_devctl)));
     CK(cudaMalloc((void **)&c->table, sizeof(c->table_host)));
     CK(cudaMalloc((void **)&c->warp_stats, (size_t)total_warps * GPUOS_WS_N * 8));
@@ -544,6 +547,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     CK(cudaMemsetAsync(c->t_start, 0, (size_t)c->N * 8, c->ctl_stream));
     CK(cudaMemsetAsync(c->tq, 0, (size_t)c->Q * 8, c->ctl_stream));
     CK(cudaMemsetAsync(c->t_pub, 0, (size_t)c->N * 8, c->ctl_stream));
+    CK(cudaMemsetAsync(c->t_disp, 0, (size_t)c->N * 8, c->ctl_stream));
     CK(cudaMemsetAsync(c->dctl, 0, sizeof(gpuos_devctl), c->ctl_stream));
     CK(cudaMemsetAsync(c->warp_stats, 0, (size_t)total_warps * GPUOS_WS_N * 8, c->ctl_stream));
 
@@ -573,6 +577,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     p.done_dev = c->done_dev;
     p.t_start = c->t_start;
     p.t_pub = c->t_pub;
+    p.t_disp = c->t_disp;
     p.tq = c->tq;
     p.dctl = c->dctl;
     p.table = c->table;

@@ -109,6 +109,7 @@ typedef struct gpuos_exec_params {
     uint64_t *done_dev;      /* [ring_entries], ticket + 1 stamps for dependency waits */
     uint64_t *t_start;       /* [ring_entries], device clock when tile 0 began */
     uint64_t *t_pub;         /* [ring_entries], device clock when tiles were published */
+    uint64_t *t_disp;        /* [ring_entries], device clock when the commit was seen */
     unsigned long long *tq;  /* [tq_entries] work-queue words */
     gpuos_devctl *dctl;
     gpuos_op_fn *table;      /* [2][GPUOS_MAX_OPS] */
