@@ -1620,13 +1620,15 @@ DEV void set_exit(const gpuos_exec_params &p, uint32_t reason)
     st_relaxed_sys32(&p.hctl->state, 2u);
 }
 
-/* Helper warps per descriptor: one per tile up to GPUOS_HELPERS, except row
- * ops, whose tiles (one row) are small: one helper per four rows. */
-DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles)
+/* Helper warps per descriptor: one per tile, except row ops, whose tiles
+ * (one row) are small: one helper per four rows; at most GPUOS_HELPERS and
+ * at most the executor's worker warps (more would only queue). */
+DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles, uint32_t workers)
 {
     uint32_t hlp = ntiles;
     if (op_id >= GPUOS_OP_SOFTMAX && op_id <= GPUOS_OP_ROWMIN) hlp = (ntiles + 3u) / 4u;
-    return hlp < GPUOS_HELPERS ? hlp : GPUOS_HELPERS;
+    const uint32_t cap = workers < GPUOS_HELPERS ? (workers ? workers : 1u) : GPUOS_HELPERS;
+    return hlp < cap ? hlp : cap;
 }
 
 /* The sequencer warp: ring -> mirror + work queue, up to 64 descriptors per
@@ -1781,7 +1783,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                     /* one work-queue entry per helper warp (at most GPUOS_HELPERS);
                      * helper i starts with tile i and takes later tiles from the
                      * descriptor's tile counter */
-                    nt[h] = helper_count(dsc[h].op_id, dsc[h].ntiles);
+                    nt[h] = helper_count(dsc[h].op_id, dsc[h].ntiles, p.workers);
                     dsc[h].user = s_table[dsc[h].op_id];                     /* -> fn */
                     dsc[h].seq = (uint64_t)version | ((uint64_t)nt[h] << 32); /* -> version, helpers */
                     uint4 *mv = reinterpret_cast<uint4 *>(p.mirror + (uint32_t)(my_t & p.ring_mask));

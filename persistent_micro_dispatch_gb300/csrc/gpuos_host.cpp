@@ -588,6 +588,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     p.backoff_max_ns = cfg.backoff_max_ns;
     p.spin_polls = cfg.spin_polls;
     p.stage_bytes = cfg.stage_bytes;
+    p.workers = c->blocks * c->wpb - 1;
     p.idle_exit_ns = (uint64_t)cfg.idle_exit_ms * 1000000ull;
     p.dep_timeout_ns = (uint64_t)(cfg.dep_timeout_ms ? cfg.dep_timeout_ms : 5000) * 1000000ull;
     p.exit_after = cfg.exit_after;

@@ -28,7 +28,7 @@
 #define GPUOS_EXEC_STATIC_SMEM (GPUOS_MAX_WPB * 128 + 256 * 8 + GPUOS_MAX_WPB * GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS * 8)
 #define GPUOS_MAX_REGS 168 /* registers per thread: 65536 / (12 warps x 32), in steps of 8 */
 #define GPUOS_TILE_MAX (1u << 30)          /* tiles per descriptor */
-#define GPUOS_HELPERS 1024                 /* work-queue entries (helper warps) per descriptor at most */
+#define GPUOS_HELPERS 2048                 /* work-queue entries (helper warps) per descriptor at most */
 #define GPUOS_TQ_MAX (1u << 30)            /* work-queue entries */
 #define GPUOS_TQ_STAMP_MASK 0xFFFFFFFFFull /* 36-bit stamps */
 
@@ -116,6 +116,7 @@ typedef struct gpuos_exec_params {
     uint64_t *warp_stats;    /* [total warps][GPUOS_WS_N] */
     uint32_t ring_mask, tq_mask;
     uint32_t backoff_min_ns, backoff_max_ns, spin_polls, stage_bytes;
+    uint32_t workers, pad_w;  /* worker warps (all warps but the sequencer) */
     uint64_t idle_exit_ns, dep_timeout_ns, exit_after;
 } gpuos_exec_params;
 
