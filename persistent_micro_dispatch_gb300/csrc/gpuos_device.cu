@@ -1981,13 +1981,28 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, uint
                     break;
                 }
                 if (ticket + 1 - dep >= N) continue; /* older than the ring window: done */
-                const uint64_t *stamp = p.done_dev + ((dep - 1) & p.ring_mask);
+                const uint32_t dslot = (uint32_t)((dep - 1) & p.ring_mask);
+                const uint64_t *stamp = p.done_dev + dslot;
                 if (ld_acquire_gpu(stamp) >= dep) continue;
                 n_depw++;
+                /* A split dependency is complete as soon as its tile counter
+                 * reaches its tile count: every helper's acq_rel add is in the
+                 * counter's release sequence, so acquiring the final value
+                 * acquires every tile's writes; the last helper's own round
+                 * trip and the stamp's release come later. The counter is
+                 * zero before the dependency's helpers count (the previous
+                 * user of the slot reset it before its record freed the ring
+                 * slot, which happens-before this descriptor was published)
+                 * and is reset only after the dependency completed, so a
+                 * match never comes early. Sole-tile dependencies never count
+                 * (ntiles 1): they are seen through the stamp. */
+                const uint32_t dnt = __ldcg(&p.mirror[dslot].ntiles);
+                const unsigned long long *dcnt = p.tiles_done + dslot;
                 Elapsed w;
                 w.start();
                 uint32_t dp = 0;
-                while (ld_relaxed_gpu(stamp) < dep) {
+                while (ld_relaxed_gpu(stamp) < dep &&
+                       (dnt < 2 || (uint32_t)ld_relaxed_gpu(reinterpret_cast<const uint64_t *>(dcnt)) != dnt)) {
                     if (w.tick(globaltimer()) > p.dep_timeout_ns) {
                         dstatus = GPUOS_ST_DEP_TIMEOUT;
                         break;

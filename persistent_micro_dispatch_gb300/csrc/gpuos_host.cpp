@@ -306,12 +306,15 @@ static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 static bool al16(uint64_t p) { return (p & 15u) == 0; }
 
 /* Element-wise tiles: the smallest power of two >= n / GPUOS_EW_SPLIT, kept
- * within [GPUOS_EW_TILE_MIN, the largest tile]. Small ops spread over up to
- * GPUOS_EW_SPLIT warps; large ones take full tiles. The device recovers the
- * tile size from n and ntiles alone (round_up(ceil(n / ntiles), 256)). */
-static uint64_t ew_tiles(uint64_t n, uint64_t tile_max)
+ * within [the op's smallest tile, the largest tile]. Large ops spread over
+ * up to GPUOS_EW_SPLIT warps per 16 tiles; small add/mul/ReLU ops stay one
+ * tile (a split costs a completion-counter round trip), small GELUs split
+ * down to 1,024 elements (their arithmetic, not their bytes, sets the time).
+ * The device recovers the tile size from n and ntiles alone
+ * (round_up(ceil(n / ntiles), 256)). */
+static uint64_t ew_tiles(uint64_t n, uint64_t tile_min, uint64_t tile_max)
 {
-    uint64_t te = GPUOS_EW_TILE_MIN;
+    uint64_t te = tile_min < tile_max ? tile_min : tile_max;
     while (te < tile_max && te * GPUOS_EW_SPLIT < n) te <<= 1;
     return ceil_div(n, te);
 }
@@ -342,7 +345,8 @@ static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool use
         if (d->dtype != GPUOS_F32 && d->dtype != GPUOS_BF16) return GPUOS_EINVAL;
         const bool bin = d->op_id == GPUOS_OP_ADD || d->op_id == GPUOS_OP_MUL;
         if (m[0] && (!d->a || !d->out || (bin && !d->b))) return GPUOS_EINVAL;
-        nt = ew_tiles(m[0], d->dtype == GPUOS_F32 ? GPUOS_EW_TILE_F32 : GPUOS_EW_TILE_BF16);
+        nt = ew_tiles(m[0], d->op_id == GPUOS_OP_GELU ? GPUOS_GELU_TILE_MIN : GPUOS_EW_TILE_MIN,
+                      d->dtype == GPUOS_F32 ? GPUOS_EW_TILE_F32 : GPUOS_EW_TILE_BF16);
         break;
     }
     case GPUOS_OP_SOFTMAX:

@@ -71,12 +71,15 @@ def _desc(G, op, dtype=1, dims=(), ptr=0x1000, **kw):
 
 
 def test_tiling_rule(G):
-    # element-wise: te = smallest power of two >= n/16 within [1024, 4096 | 8192]
-    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 4          # te 1024
-    assert G.op_ntiles(_desc(G, "add", 1, (16384,))) == 16        # te 1024
-    assert G.op_ntiles(_desc(G, "relu", 0, (8193,))) == 9         # te 1024
+    # element-wise: te = smallest power of two >= n/16 within [4096 (GELU 1024), 4096 | 8192]
+    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 1          # te 4096
+    assert G.op_ntiles(_desc(G, "gelu", 0, (4096,))) == 4         # te 1024
+    assert G.op_ntiles(_desc(G, "add", 1, (16384,))) == 4         # te 4096
+    assert G.op_ntiles(_desc(G, "gelu", 1, (16384,))) == 16       # te 1024
+    assert G.op_ntiles(_desc(G, "relu", 0, (8193,))) == 3         # te 4096
     assert G.op_ntiles(_desc(G, "mul", 0, (1000,))) == 1
     assert G.op_ntiles(_desc(G, "add", 0, (65536,))) == 16        # te 4096 (fp32 cap)
+    assert G.op_ntiles(_desc(G, "add", 1, (65536,))) == 16        # te 4096
     assert G.op_ntiles(_desc(G, "add", 0, (1 << 20,))) == 256     # te 4096
     assert G.op_ntiles(_desc(G, "gelu", 1, (1 << 20,))) == 128    # te 8192 (bf16 cap)
     assert G.op_ntiles(_desc(G, "gelu", 1, (40000,))) == 10       # te 4096 >= 40000/16
@@ -101,10 +104,10 @@ def test_device_tile_ranges_cover_each_op(G):
     length from the host's ntiles (the rule stated in gpuos.h); for every
     size the ranges must cover the op, stay 16-byte aligned, fit the largest
     tile, and (attention) use no more partials than the workspace holds."""
-    for dt, cap in ((0, 4096), (1, 8192)):
+    for (dt, cap), op in [(dc, o) for dc in ((0, 4096), (1, 8192)) for o in ("add", "gelu")]:
         for n in [1, 255, 256, 257, 1023, 1024, 1025, 4095, 4096, 4097, 16383, 16385, 65535, 65536,
                   65537, 100003, 1 << 20, (1 << 20) + 7, 3 * 8192 + 1]:
-            nt = G.op_ntiles(_desc(G, "add", dt, (n,)))
+            nt = G.op_ntiles(_desc(G, op, dt, (n,)))
             te = -(-(-(-n // nt)) // 256) * 256
             assert te * nt >= n and te <= cap and te % 256 == 0, (dt, n, nt, te)
             assert (nt - 1) * te < n  # no tile starts past the end
