@@ -280,6 +280,48 @@ def pct(x, q):
     return float(np.percentile(x, q)) if len(x) else None
 
 
+def producers_sweep(G, cfg_kw) -> int:
+    """Aggregate submission throughput of T concurrent host threads, each
+    committing NOP descriptors in batches of 16 through one ring (the page's
+    ring-contention question). The single-thread line without the
+    multi-producer path (plain SPSC ring) is the reference."""
+    import threading
+    per_thread = 20_000
+    batch = 16
+    nop = G.make_descs(batch)
+    rows = []
+    for T, mp in [(1, 0), (1, 1), (2, 1), (4, 1), (8, 1), (16, 1), (32, 1), (64, 1)]:
+        ex = G.Executor(**cfg_kw, multi_producer=mp)
+        try:
+            go = threading.Barrier(T + 1)
+
+            def work():
+                go.wait()
+                for _ in range(per_thread // batch):
+                    ex.submit_batch(nop)
+
+            th = [threading.Thread(target=work) for _ in range(T)]
+            for t in th:
+                t.start()
+            go.wait()
+            t0 = time.perf_counter()
+            for t in th:
+                t.join()
+            t_sub = time.perf_counter() - t0
+            ex.sync(timeout_ms=60_000)
+            t_all = time.perf_counter() - t0
+            st = ex.stats()
+        finally:
+            ex.shutdown()
+        n = T * (per_thread // batch) * batch
+        assert st["completed"] >= n, st
+        rows.append({"threads": T, "multi_producer": mp, "descriptors": n,
+                     "submit_per_s": n / t_sub, "complete_per_s": n / t_all})
+    print(json.dumps({"metric": "host submission throughput vs producer threads (NOP batches of 16)",
+                      "unit": "descriptors/s", "rows": rows}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -301,6 +343,9 @@ def main():
     ap.add_argument("--blocks", type=int, default=0, help="executor blocks (0 = one per SM)")
     ap.add_argument("--spin-polls", type=int, default=0, help="idle polls before backoff sleeps (0 = default)")
     ap.add_argument("--backoff-max-ns", type=int, default=0, help="longest idle sleep (0 = default)")
+    ap.add_argument("--producers-sweep", action="store_true",
+                    help="host-thread contention curve: T threads submitting NOP batches (multi_producer=1); "
+                         "prints its own JSON line")
     ap.add_argument("--ring-device", action="store_true",
                     help="ring in device memory (managed, host-accessible) instead of pinned host memory")
     ap.add_argument("--graph", action="store_true",
@@ -351,6 +396,8 @@ def main():
     warm_torch(f"cuda:{local}")
     torch.cuda.synchronize()
 
+    if args.producers_sweep:
+        return producers_sweep(G, cfg_kw)
     if args.profile_run:
         # bounded run with the ring filled before the single launch: the
         # kernel ends on its own after len(descs) completions (replayable)

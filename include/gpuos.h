@@ -62,6 +62,7 @@ extern "C" {
 #define GPUOS_ENOMEM (-7)
 #define GPUOS_EBUSY (-8)     /* needs the executor not resident (see gpuos_load_module) */
 #define GPUOS_ETOOBIG (-9)   /* sizes beyond a fixed limit (see gpuos_sdpa_noalloc) */
+#define GPUOS_ECOMPILE (-10) /* operator source did not compile (see gpuos_compile_op's log) */
 
 /* ---- device status codes (gpuos_record.status) -------------------------- */
 #define GPUOS_ST_OK 0
@@ -142,7 +143,7 @@ typedef struct gpuos_desc {
 /* Executor / ring configuration. gpuos_default_config() fills defaults. */
 typedef struct gpuos_config {
     uint32_t ring_entries;    /* power of two in [64, 65536]; default 4096 (the page's default) */
-    uint32_t warps_per_block; /* 2..16; default 12 */
+    uint32_t warps_per_block; /* 2..12; default 12 */
     uint32_t blocks;          /* 0 = one block per SM */
     uint32_t backoff_min_ns;  /* first idle sleep; default 32 */
     uint32_t backoff_max_ns;  /* idle sleep cap; default 256 */
@@ -153,14 +154,17 @@ typedef struct gpuos_config {
                                     1: managed memory preferred on the device */
     int32_t device;           /* CUDA device ordinal; default 0 */
     uint64_t exit_after;      /* 0 = run until shutdown; n = leave once n descriptors completed */
-    uint32_t tq_entries;      /* work-queue entries: 0 (default) = 2048 x ring_entries; else a
-                                 power of two above 1024 x ring_entries, at most 2^30 */
+    uint32_t tq_entries;      /* work-queue entries: 0 (default) = 4096 x ring_entries; else a
+                                 power of two above 2048 x ring_entries, at most 2^30 */
     uint32_t deferred_start;  /* 1: gpuos_init does not launch; gpuos_start does (descriptors
                                  may be submitted before, up to ring_entries of them) */
     uint32_t stage_bytes;     /* shared-memory staging per warp for bulk (TMA) copies: 0 = none
                                  (register path; leaves shared memory to co-running kernels),
                                  else a multiple of 1024 up to 24576; default 16384 */
-    uint32_t reserved[3];
+    uint32_t multi_producer;  /* 0 (default): one submitting thread (SPSC ring, no locks);
+                                 1: any number of host threads may call gpuos_submit /
+                                 gpuos_submit_batch concurrently (see gpuos_submit) */
+    uint32_t reserved[2];
 } gpuos_config;
 
 /* Completion record of one ticket (device clock = %globaltimer, host clock =
@@ -236,7 +240,18 @@ GPUOS_API int gpuos_executor_stream(gpuos_ctx *ctx, void **stream);
  * with store-release). Validates op_id, pointers, dims and deps on the host,
  * computes ntiles for built-in ops, waits up to timeout_us for a free slot
  * (EAGAIN after that, nothing submitted). *ticket (may be NULL) receives the
- * ticket. Errors: EINVAL, EAGAIN, ESTOPPED. */
+ * ticket. Errors: EINVAL, EAGAIN, ESTOPPED.
+ *
+ * With multi_producer = 1 several threads may submit at once (§3 Q3, ring
+ * contention with concurrent host threads): a submission first validates all
+ * its descriptors, waits up to timeout_us for room in the ring (EAGAIN,
+ * nothing submitted), then reserves consecutive tickets with one atomic add
+ * and commits them. A reserved ticket is always committed (the executor
+ * takes tickets in order, so an abandoned one would stall every later one):
+ * after the reservation the call waits for its slots without a timeout,
+ * returning ESTOPPED only if the executor has left. Tickets of different
+ * threads interleave; a GPUOS_FLAG_DEP_REL distance counts in that global
+ * order. The context must have been started (EINVAL otherwise). */
 GPUOS_API int gpuos_submit(gpuos_ctx *ctx, const gpuos_desc *d, uint64_t *ticket, uint32_t timeout_us);
 
 /* Submit count descriptors in order (same as count gpuos_submit calls);
@@ -272,6 +287,25 @@ GPUOS_API int gpuos_set_history(gpuos_ctx *ctx, gpuos_record *buf, uint64_t base
  * no-op. Errors: EINVAL (does not link), EBUSY (executor already launched),
  * ECUDA. */
 GPUOS_API int gpuos_load_module(gpuos_ctx *ctx, const void *image, size_t len);
+
+/* Run-time compilation of an operator (§3 Q2 "3. Dynamic Operator Table",
+ * step 1). source: CUDA C++ that defines a device operator
+ *     __device__ int my_op(const gpuos_devdesc *d, uint32_t tile) { ... }
+ * and exports it as  __device__ gpuos_op_fn my_op_ptr = my_op;
+ * The library prepends the operator ABI header (gpuos_op_header(): the
+ * 128-byte gpuos_devdesc seen by operators, gpuos_op_fn, status codes) and
+ * compiles with NVRTC (opened at run time) for sm_103a, relocatable, with
+ * the executor's per-thread register cap. On success *image (malloc'd; free
+ * with gpuos_free_image) and *size hold a cubin for gpuos_load_module /
+ * gpuos_register_op. log (may be NULL) receives NVRTC's log, truncated to
+ * log_cap bytes. name (may be NULL) names the source in that log. Runs on
+ * the CPU only; no context is needed. Errors: EINVAL, ECOMPILE (see log),
+ * ECUDA (NVRTC missing or failed), ENOMEM. */
+GPUOS_API int gpuos_compile_op(const char *source, const char *name, void **image, size_t *size, char *log,
+                               size_t log_cap);
+GPUOS_API void gpuos_free_image(void *image);
+/* The header text gpuos_compile_op puts before every operator source. */
+GPUOS_API const char *gpuos_op_header(void);
 
 /* Runtime operator injection (§3 Q2 "3. Dynamic Operator Table", steps 3-5):
  * for a module added with gpuos_load_module (and so linked into the running

@@ -28,7 +28,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc")
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-I" + INCLUDE, "-I" + CSRC]
 
-SOURCES = ["gpuos_device.cu", "gpuos_host.cpp"]
+SOURCES = ["gpuos_device.cu", "gpuos_host.cpp", "gpuos_nvrtc.cpp"]
 
 
 def _run(cmd, log=None):

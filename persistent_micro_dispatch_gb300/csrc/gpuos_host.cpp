@@ -29,6 +29,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <ctime>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -208,7 +209,9 @@ struct gpuos_ctx {
     uint32_t *version_stage = nullptr; /* pinned 4 bytes for version flips */
     cudaStream_t exec_stream = nullptr, ctl_stream = nullptr;
     /* host state */
-    uint64_t head = 0;     /* next ticket */
+    bool mp = false;       /* multi-producer submission */
+    std::mutex hmu;        /* (multi-producer) harvest state: low, hv, recent, history, counts */
+    uint64_t head = 0;     /* next ticket (reserved, with multiple producers) */
     uint64_t low = 0;      /* every ticket < low harvested */
     std::vector<uint64_t> commit_ns;
     std::vector<uint64_t> hv; /* per slot: ticket + 1 last harvested */
@@ -238,8 +241,23 @@ struct gpuos_ctx {
 
 static inline void heartbeat(gpuos_ctx *c)
 {
-    __atomic_store_n(&c->hctl->heartbeat, c->hctl->heartbeat + 1, __ATOMIC_RELAXED);
+    __atomic_fetch_add(&c->hctl->heartbeat, (uint64_t)1, __ATOMIC_RELAXED);
 }
+
+static inline uint64_t head_of(gpuos_ctx *c) { return __atomic_load_n(&c->head, __ATOMIC_ACQUIRE); }
+
+/* The harvest state's lock, taken only with multiple producers. */
+struct HarvestLock {
+    std::mutex *m;
+    explicit HarvestLock(gpuos_ctx *c) : m(c->mp ? &c->hmu : nullptr)
+    {
+        if (m) m->lock();
+    }
+    ~HarvestLock()
+    {
+        if (m) m->unlock();
+    }
+};
 
 extern "C" {
 
@@ -270,6 +288,7 @@ const char *gpuos_strerror(int code, int is_status)
     case GPUOS_ENOMEM: return "out of memory";
     case GPUOS_EBUSY: return "not allowed while the executor is resident (load modules before gpuos_start)";
     case GPUOS_ETOOBIG: return "sizes exceed the fixed scratch of gpuos_sdpa_noalloc (B*H <= 256, Lmax <= 4096)";
+    case GPUOS_ECOMPILE: return "operator source did not compile (see the compile log)";
     default: return "unknown error";
     }
 }
@@ -459,6 +478,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
         return GPUOS_EINVAL;
     if (cfg.backoff_min_ns == 0 || cfg.backoff_max_ns < cfg.backoff_min_ns) return GPUOS_EINVAL;
     if ((cfg.stage_bytes & 1023u) || cfg.stage_bytes > 24576u) return GPUOS_EINVAL;
+    if (cfg.multi_producer > 1u) return GPUOS_EINVAL;
     /* every warp's staging region and the executor's static shared memory
      * (descriptor copies, the sequencer's table copy, tile profiles) must fit
      * the 227 KB a block can hold */
@@ -467,6 +487,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     gpuos_ctx *c = new (std::nothrow) gpuos_ctx();
     if (!c) return GPUOS_ENOMEM;
     c->cfg = cfg;
+    c->mp = cfg.multi_producer != 0;
     c->device = cfg.device;
     c->N = cfg.ring_entries;
     c->mask = c->N - 1;
@@ -723,9 +744,11 @@ static bool is_done(gpuos_ctx *c, uint64_t t)
 
 static void sweep(gpuos_ctx *c)
 {
-    /* tickets older than head - N were harvested when their slot was reused */
-    if (c->head > c->N && c->low < c->head - c->N) c->low = c->head - c->N;
-    while (c->low < c->head) {
+    /* tickets older than head - N were harvested when their slot was reused
+     * (reserved tickets not yet committed are simply not done) */
+    const uint64_t head = head_of(c);
+    if (head > c->N && c->low < head - c->N) c->low = head - c->N;
+    while (c->low < head) {
         const uint32_t slot = (uint32_t)(c->low & c->mask);
         if (c->hv[slot] != c->low + 1) {
             if (!is_done(c, c->low)) break;
@@ -807,8 +830,98 @@ static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint3
     return GPUOS_OK;
 }
 
+/* Multiple producers: validate every descriptor, wait for room, reserve
+ * count consecutive tickets with one atomic add, then write and commit them
+ * (each slot once its previous ticket completed). */
+static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t *first_ticket,
+                     uint32_t *n_done, uint32_t timeout_us)
+{
+    if (n_done) *n_done = 0;
+    if (!c->launched) return GPUOS_EINVAL;
+    if (!c->accepting || !c->running) return GPUOS_ESTOPPED;
+    if (__atomic_load_n(&c->hctl->state, __ATOMIC_RELAXED) == 2u) {
+        c->running = false;
+        return GPUOS_ESTOPPED;
+    }
+    if (count == 0) return GPUOS_OK;
+    if (count > c->N) return GPUOS_EINVAL;
+    std::vector<uint32_t> nts(count);
+    const uint64_t h0 = head_of(c);
+    for (uint32_t i = 0; i < count; i++) {
+        const bool user_known = d[i].op_id >= GPUOS_OP_USER_FIRST && c->user_registered[d[i].op_id];
+        int rc = validate_and_tile(d + i, &nts[i], user_known);
+        if (rc) return rc;
+        /* the ticket will be >= h0 + i, so these bounds hold for it */
+        for (int k = 0; k < 2; k++)
+            if (d[i].dep[k] > h0 + i) return GPUOS_EINVAL;
+    }
+    /* room for the batch (other producers may take it first: then the
+     * reserved slots below are waited for) */
+    const uint64_t t_start = now_ns();
+    uint32_t spins = 0;
+    while (true) {
+        uint64_t low;
+        {
+            HarvestLock lk(c);
+            sweep(c);
+            low = c->low;
+        }
+        if (head_of(c) + count <= low + c->N) break;
+        if ((++spins & 255u) == 0) {
+            heartbeat(c);
+            if (now_ns() - t_start > (uint64_t)timeout_us * 1000ull) return GPUOS_EAGAIN;
+            if (executor_gone(c)) {
+                c->running = false;
+                return GPUOS_ESTOPPED;
+            }
+        }
+        cpu_relax();
+    }
+    const uint64_t t0 = __atomic_fetch_add(&c->head, (uint64_t)count, __ATOMIC_ACQ_REL);
+    if (first_ticket) *first_ticket = t0;
+    for (uint32_t i = 0; i < count; i++) {
+        const uint64_t t = t0 + i;
+        const uint32_t slot = (uint32_t)(t & c->mask);
+        if (t >= c->N) {
+            const uint64_t prev = t - c->N;
+            while (!is_done(c, prev)) {
+                if ((++spins & 1023u) == 0) {
+                    heartbeat(c);
+                    if (executor_gone(c)) {
+                        c->running = false;
+                        return GPUOS_ESTOPPED;
+                    }
+                }
+                cpu_relax();
+            }
+            HarvestLock lk(c);
+            harvest_one(c, prev);
+        }
+        gpuos_desc w = d[i];
+        w.ntiles = nts[i];
+        for (int k = 0; k < 2; k++)
+            if (w.dep[k] && (d[i].flags & GPUOS_FLAG_DEP_REL)) w.dep[k] = t - w.dep[k] + 1;
+        w.flags = (uint8_t)(d[i].flags & GPUOS_FLAG_FENCE);
+        w.ticket = t;
+        gpuos_desc *sl = c->ring + slot;
+        __atomic_store_n(&c->rec[slot].t_dispatch, (uint64_t)0, __ATOMIC_RELAXED);
+        const uint64_t *src = reinterpret_cast<const uint64_t *>(&w);
+        uint64_t *dst = reinterpret_cast<uint64_t *>(sl);
+        for (int q = 0; q < 15; q++) __atomic_store_n(dst + q, src[q], __ATOMIC_RELAXED);
+        c->commit_ns[slot] = now_ns();
+        store_rel(&sl->seq, t + 1);
+        if (n_done) *n_done = i + 1;
+    }
+    heartbeat(c);
+    return GPUOS_OK;
+}
+
 int gpuos_submit(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint32_t timeout_us)
 {
+    if (c && c->mp) {
+        if (!d) return GPUOS_EINVAL;
+        return submit_mp(c, d, 1, ticket, nullptr, timeout_us);
+    }
     return submit_one(c, d, ticket, timeout_us);
 }
 
@@ -816,6 +929,7 @@ int gpuos_submit_batch(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64
                        uint32_t *n_done, uint32_t timeout_us)
 {
     if (!c || (!d && count)) return GPUOS_EINVAL;
+    if (c->mp) return submit_mp(c, d, count, first_ticket, n_done, timeout_us);
     if (first_ticket) *first_ticket = c->head;
     uint32_t i = 0;
     int rc = GPUOS_OK;
@@ -830,24 +944,30 @@ int gpuos_submit_batch(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64
 int gpuos_sync(gpuos_ctx *c, uint64_t ticket, uint32_t timeout_ms)
 {
     if (!c) return GPUOS_EINVAL;
-    const uint64_t target = (ticket == UINT64_MAX) ? c->head : ticket + 1;
-    if (target > c->head) return GPUOS_EINVAL;
+    const uint64_t head = head_of(c);
+    const uint64_t target = (ticket == UINT64_MAX) ? head : ticket + 1;
+    if (target > head) return GPUOS_EINVAL;
     if (!c->launched && target > c->low) return GPUOS_ESTOPPED;
     const uint64_t t0 = now_ns();
     uint32_t spins = 0;
     heartbeat(c);
     while (true) {
-        sweep(c);
-        bool done = c->low >= target;
-        if (!done && ticket != UINT64_MAX && (c->head - ticket <= c->N) && is_done(c, ticket)) {
-            harvest_one(c, ticket);
-            done = true;
+        bool done;
+        {
+            HarvestLock lk(c);
+            sweep(c);
+            done = c->low >= target;
+            if (!done && ticket != UINT64_MAX && (head_of(c) - ticket <= c->N) && is_done(c, ticket)) {
+                harvest_one(c, ticket);
+                done = true;
+            }
         }
         if (done) break;
         if ((++spins & 1023u) == 0) {
             heartbeat(c);
             if (now_ns() - t0 > (uint64_t)timeout_ms * 1000000ull) return GPUOS_ETIMEDOUT;
             if (executor_gone(c)) {
+                HarvestLock lk(c);
                 sweep(c);
                 if (c->low >= target) break;
                 c->running = false;
@@ -856,6 +976,7 @@ int gpuos_sync(gpuos_ctx *c, uint64_t ticket, uint32_t timeout_ms)
         }
         cpu_relax();
     }
+    HarvestLock lk(c);
     if (c->pending_errors) {
         c->pending_errors = 0;
         return GPUOS_EDEVICE;
@@ -866,13 +987,14 @@ int gpuos_sync(gpuos_ctx *c, uint64_t ticket, uint32_t timeout_ms)
 int gpuos_query(gpuos_ctx *c, uint64_t ticket, gpuos_record *rec)
 {
     if (!c || !rec) return GPUOS_EINVAL;
-    if (ticket >= c->head) return GPUOS_EINVAL;
+    HarvestLock lk(c);
+    if (ticket >= head_of(c)) return GPUOS_EINVAL;
     if (c->history && ticket >= c->hist_base && ticket - c->hist_base < c->hist_cap &&
         c->history[ticket - c->hist_base].ticket == ticket && ticket < c->low) {
         *rec = c->history[ticket - c->hist_base];
         return GPUOS_OK;
     }
-    if (c->head - ticket > c->N) return GPUOS_EINVAL;
+    if (head_of(c) - ticket > c->N) return GPUOS_EINVAL;
     const uint32_t slot = (uint32_t)(ticket & c->mask);
     if (c->hv[slot] != ticket + 1) {
         if (!is_done(c, ticket)) return GPUOS_EAGAIN;
@@ -901,8 +1023,11 @@ static int flip_entry(gpuos_ctx *c, uint16_t op_id, uint64_t fnval)
      * slot they read is rewritten */
     const uint64_t t0 = now_ns();
     while (true) {
-        sweep(c);
-        if (c->low >= c->flip_head) break;
+        {
+            HarvestLock lk(c);
+            sweep(c);
+            if (c->low >= c->flip_head) break;
+        }
         if (now_ns() - t0 > (uint64_t)c->cfg.dep_timeout_ms * 2000000ull) return GPUOS_ETIMEDOUT;
         if (executor_gone(c)) return GPUOS_ESTOPPED;
         heartbeat(c);
@@ -921,7 +1046,7 @@ static int flip_entry(gpuos_ctx *c, uint16_t op_id, uint64_t fnval)
         return GPUOS_ECUDA;
     if (cudaStreamSynchronize(c->ctl_stream) != cudaSuccess) return GPUOS_ECUDA;
     c->version = nv;
-    c->flip_head = c->head;
+    c->flip_head = head_of(c);
     heartbeat(c);
     return GPUOS_OK;
 }
@@ -1028,10 +1153,13 @@ int gpuos_stats(gpuos_ctx *c, gpuos_stats_t *st)
     st->seq_body_ns = ws[GPUOS_WS_T_BODY];
     st->seq_mirror_ns = ws[GPUOS_WS_T_MIRROR];
     st->seq_publish_ns = ws[GPUOS_WS_T_PUB];
-    sweep(c);
-    st->submitted = c->head;
-    st->completed = c->n_completed;
-    st->errors = c->n_errors;
+    {
+        HarvestLock lk(c);
+        sweep(c);
+        st->completed = c->n_completed;
+        st->errors = c->n_errors;
+    }
+    st->submitted = head_of(c);
     st->sequenced = __atomic_load_n(&c->hctl->sequenced, __ATOMIC_RELAXED);
     st->version = c->version;
     st->running = (c->running && !executor_gone(c)) ? 1u : 0u;
@@ -1076,7 +1204,7 @@ int gpuos_calibrate(gpuos_ctx *c, uint32_t pings, int64_t *off_lo, int64_t *off_
     for (uint32_t i = 0; i < pings; i++) {
         uint64_t t = 0;
         const uint64_t t0 = now_ns();
-        rc = submit_one(c, &nop, &t, 1000000);
+        rc = gpuos_submit(c, &nop, &t, 1000000);
         if (rc) return rc;
         const gpuos_rec_dev *r = c->rec + (t & c->mask);
         uint32_t spins = 0;
@@ -1096,6 +1224,7 @@ int gpuos_calibrate(gpuos_ctx *c, uint32_t pings, int64_t *off_lo, int64_t *off_
         const int64_t a = (int64_t)(td - t1), b = (int64_t)(td - t0);
         if (a > lo) lo = a;
         if (b < hi) hi = b;
+        HarvestLock lk(c);
         harvest_one(c, t);
         sweep(c);
     }
@@ -1122,6 +1251,7 @@ int gpuos_stop(gpuos_ctx *c, uint32_t timeout_ms)
         if (q != cudaErrorNotReady) {
             if (q != cudaSuccess && rc == GPUOS_OK) rc = GPUOS_ECUDA;
             c->running = false;
+            HarvestLock lk(c);
             sweep(c);
             return rc;
         }

@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(HERE, "libgpuos.so")
 EXT_CUBIN = os.path.join(HERE, "gpuos_ext_ops.cubin")
 
 # ---- constants (mirror include/gpuos.h) --------------------------------------------
-OK, EINVAL, EAGAIN, ETIMEDOUT, EDEVICE, ECUDA, ESTOPPED, ENOMEM, EBUSY, ETOOBIG = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+OK, EINVAL, EAGAIN, ETIMEDOUT, EDEVICE, ECUDA, ESTOPPED, ENOMEM, EBUSY, ETOOBIG, ECOMPILE = \
+    0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10
 ST_OK, ST_BAD_OP, ST_BAD_ARGS, ST_DEP_TIMEOUT, ST_ABORTED, ST_BAD_DESC, ST_COPY_TIMEOUT = 0, 1, 2, 3, 4, 5, 6
 OP = dict(nop=0, add=1, mul=2, relu=3, gelu=4, softmax=5, layernorm=6, rowsum=7, rowmax=8, rowmin=9,
           rope=10, kv_write=11, sdpa=12, vecmat=13)
@@ -52,7 +53,7 @@ class Config(C.Structure):
                 ("idle_exit_ms", C.c_uint32), ("dep_timeout_ms", C.c_uint32),
                 ("ring_in_device_mem", C.c_uint32), ("device", C.c_int32), ("exit_after", C.c_uint64),
                 ("tq_entries", C.c_uint32), ("deferred_start", C.c_uint32), ("stage_bytes", C.c_uint32),
-                ("reserved", C.c_uint32 * 3)]
+                ("multi_producer", C.c_uint32), ("reserved", C.c_uint32 * 2)]
 
 
 class Record(C.Structure):
@@ -98,6 +99,10 @@ API = {
     "gpuos_alias_op": (C.c_int, [C.c_void_p, C.c_uint16, C.c_uint16]),
     "gpuos_stats": (C.c_int, [C.c_void_p, C.POINTER(Stats)]),
     "gpuos_tile_profile_get": (C.c_int, [C.c_void_p, C.POINTER(TileProfile)]),
+    "gpuos_compile_op": (C.c_int, [C.c_char_p, C.c_char_p, C.POINTER(C.c_void_p), C.POINTER(C.c_size_t),
+                                   C.c_char_p, C.c_size_t]),
+    "gpuos_free_image": (None, [C.c_void_p]),
+    "gpuos_op_header": (C.c_char_p, []),
     "gpuos_calibrate": (C.c_int, [C.c_void_p, C.c_uint32, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
                                   C.POINTER(C.c_uint64), C.c_void_p]),
     "gpuos_shutdown": (C.c_int, [C.c_void_p, C.c_uint32]),
@@ -182,6 +187,27 @@ def sdpa_noalloc(q: int, Kc: int, Vc: int, lens: int, out: int, B: int, H: int, 
     returns the raw return code."""
     return lib().gpuos_sdpa_noalloc(C.c_void_p(q), C.c_void_p(Kc), C.c_void_p(Vc), C.c_void_p(lens), C.c_void_p(out),
                                     B, H, D, Lcap, Lmax, scale, C.c_void_p(stream_ptr))
+
+
+def compile_op(source: str, name: str = "gpuos_op.cu") -> bytes:
+    """Compile operator source at run time (NVRTC) to a relocatable sm_103a
+    cubin for Executor.load_module / register_op. Raises GpuosError with the
+    compiler log on failure."""
+    img = C.c_void_p()
+    size = C.c_size_t()
+    log = C.create_string_buffer(16384)
+    rc = lib().gpuos_compile_op(source.encode(), name.encode(), C.byref(img), C.byref(size), log, len(log))
+    if rc != OK:
+        raise GpuosError("gpuos_compile_op: " + log.value.decode(errors="replace"), rc)
+    try:
+        return C.string_at(img.value, size.value)
+    finally:
+        lib().gpuos_free_image(img)
+
+
+def op_header() -> str:
+    """The operator ABI header compile_op puts before every source."""
+    return lib().gpuos_op_header().decode()
 
 
 def make_descs(n: int) -> np.ndarray:

@@ -381,3 +381,123 @@ def test_eager_path_matches_executor_bitwise():
         if b.name in ("sdpa_ws",):
             continue
         assert np.array_equal(ds1.read_buf(i).view(np.uint8), ds2.read_buf(i).view(np.uint8)), b.name
+
+
+def test_multi_producer_threads_share_the_ring():
+    """Eight host threads submit concurrently (multi_producer = 1) through a
+    256-entry ring (many laps): each thread's descriptors (C1 ops on its own
+    slice of the stream) get unique tickets, every op runs once, every
+    output is bit-exact, and the completion count matches."""
+    import threading
+    s, ds = _c1_small(n_desc=2000)
+    descs = ds.descs()
+    ex = G().Executor(ring_entries=256, multi_producer=1)
+    T = 8
+    firsts = [[] for _ in range(T)]
+    errors = []
+
+    def producer(k):
+        try:
+            mine = descs[k::T]
+            for i in range(0, len(mine), 5):  # batches of 5 and single submits
+                chunk = mine[i:i + 5]
+                if i % 2 == 0:
+                    firsts[k].append((ex.submit_batch(chunk), len(chunk)))
+                else:
+                    for d in chunk:
+                        firsts[k].append((ex.submit(d), 1))
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    try:
+        th = [threading.Thread(target=producer, args=(k,)) for k in range(T)]
+        for t in th:
+            t.start()
+        for t in th:
+            t.join(timeout=120)
+        assert not errors, errors
+        ex.sync(timeout_ms=60_000)
+        st = ex.stats()
+    finally:
+        assert ex.shutdown() == 0
+    tickets = sorted(t0 + j for f in firsts for (t0, n) in f for j in range(n))
+    assert tickets == list(range(len(descs)))  # unique, no gaps
+    assert st["completed"] == len(descs) and st["errors"] == 0 and st["submitted"] == len(descs)
+    rep = _check_all(s, ds)
+    assert rep.exact == len(descs)
+
+
+def test_multi_producer_needs_started_executor():
+    g = G()
+    ex = g.Executor(deferred_start=1, multi_producer=1)
+    try:
+        d = g.make_descs(1)
+        assert ex.try_submit(d) == g.EINVAL
+        ex.start()
+        assert ex.try_submit(d) == g.OK
+        ex.sync(timeout_ms=10_000)
+    finally:
+        assert ex.shutdown() == 0
+
+
+_NEG_SRC = r'''
+/* out[i] = -a[i] (fp32). Tiles split n like the built-in element-wise ops:
+ * ntiles ranges of round_up(ceil(n / ntiles), 256) elements, so the op can
+ * also stand in for a built-in id, whose tile count the library computes. */
+__device__ int op_neg(const gpuos_devdesc *d, uint32_t tile)
+{
+    const uint32_t n = d->dims[0], lane = threadIdx.x & 31u;
+    const uint32_t nt = d->ntiles ? d->ntiles : 1u;
+    const uint32_t te = ((n + nt - 1u) / nt + 255u) / 256u * 256u;
+    const float *a = reinterpret_cast<const float *>(d->a);
+    float *o = reinterpret_cast<float *>(d->out);
+    const unsigned long long start = (unsigned long long)tile * te;
+    const unsigned long long end = start + te < n ? start + te : n;
+    for (unsigned long long i = start + lane; i < end; i += 32) o[i] = -a[i];
+    return GPUOS_ST_OK;
+}
+__device__ gpuos_op_fn op_neg_ptr = op_neg;
+'''
+
+
+def test_runtime_compiled_op_injection():
+    """An op compiled at run time (NVRTC) is linked into the executor and
+    installed under a new id; results are bit-exact, and swapping the
+    built-in id 1 (add) to it later changes what id 1 computes. (Results are
+    read after shutdown: a pageable device-to-host copy on PyTorch's stream
+    waits while the executor is resident.)"""
+    import torch
+    g = G()
+    img = g.compile_op(_NEG_SRC, "neg.cu")
+    n = 10_000
+    x = torch.randn(n, dtype=torch.float32, device="cuda")
+    y = torch.zeros(n, dtype=torch.float32, device="cuda")
+    z1 = torch.zeros(n, dtype=torch.float32, device="cuda")
+    z2 = torch.zeros(n, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    d = g.make_descs(3)
+    d["op_id"] = [70, 1, 1]
+    d["dtype"] = g.F32
+    d["a"] = x.data_ptr()
+    d["b"] = x.data_ptr()
+    d["out"] = [y.data_ptr(), z1.data_ptr(), z2.data_ptr()]
+    d["dims"][:, 0] = n
+    d["ntiles"][0] = (n + 1023) // 1024
+    ex = g.Executor(deferred_start=1)
+    try:
+        ex.load_module(img)
+        ex.start()
+        ex.register_op(70, img, "op_neg_ptr")
+        ex.submit_batch(d[:2])
+        ex.sync(timeout_ms=10_000)
+        ex.register_op(1, img, "op_neg_ptr")  # now id 1 runs the compiled op
+        ex.submit(d[2:3])
+        ex.sync(timeout_ms=10_000)
+        st = ex.stats()
+    finally:
+        ex.shutdown()
+    assert st["errors"] == 0 and st["version"] == 2
+    xs = x.cpu().numpy()
+    assert np.array_equal(y.cpu().numpy(), -xs)
+    assert np.array_equal(z1.cpu().numpy(), xs + xs)  # id 1 was still add
+    assert np.array_equal(z2.cpu().numpy(), -xs)
