@@ -716,7 +716,12 @@ int gpuos_executor_stream(gpuos_ctx *c, void **stream)
 static void harvest_one(gpuos_ctx *c, uint64_t t)
 {
     const uint32_t slot = (uint32_t)(t & c->mask);
-    if (c->hv[slot] == t + 1) return;
+    uint64_t seen = __atomic_load_n(&c->hv[slot], __ATOMIC_ACQUIRE);
+    if (seen >= t + 1) return;
+    /* one harvester per ticket: a producer reusing the slot and a sweeping
+     * thread may reach the same ticket together */
+    if (!__atomic_compare_exchange_n(&c->hv[slot], &seen, t + 1, false, __ATOMIC_ACQ_REL, __ATOMIC_ACQUIRE))
+        return;
     gpuos_rec_dev *r = c->rec + slot;
     gpuos_record R;
     R.ticket = t;
@@ -729,11 +734,10 @@ static void harvest_one(gpuos_ctx *c, uint64_t t)
     R.t_done_dev_ns = __atomic_load_n(&r->t_done, __ATOMIC_RELAXED);
     c->recent[slot] = R;
     if (c->history && t >= c->hist_base && t - c->hist_base < c->hist_cap) c->history[t - c->hist_base] = R;
-    c->hv[slot] = t + 1;
-    c->n_completed++;
+    __atomic_fetch_add(&c->n_completed, (uint64_t)1, __ATOMIC_RELAXED);
     if (R.status != GPUOS_ST_OK) {
-        c->n_errors++;
-        c->pending_errors++;
+        __atomic_fetch_add(&c->n_errors, (uint64_t)1, __ATOMIC_RELAXED);
+        __atomic_fetch_add(&c->pending_errors, (uint64_t)1, __ATOMIC_RELAXED);
     }
 }
 
@@ -747,15 +751,17 @@ static void sweep(gpuos_ctx *c)
     /* tickets older than head - N were harvested when their slot was reused
      * (reserved tickets not yet committed are simply not done) */
     const uint64_t head = head_of(c);
-    if (head > c->N && c->low < head - c->N) c->low = head - c->N;
-    while (c->low < head) {
-        const uint32_t slot = (uint32_t)(c->low & c->mask);
-        if (c->hv[slot] != c->low + 1) {
-            if (!is_done(c, c->low)) break;
-            harvest_one(c, c->low);
+    if (head > c->N && c->low < head - c->N) __atomic_store_n(&c->low, head - c->N, __ATOMIC_RELEASE);
+    uint64_t low = c->low;
+    while (low < head) {
+        const uint32_t slot = (uint32_t)(low & c->mask);
+        if (__atomic_load_n(&c->hv[slot], __ATOMIC_ACQUIRE) < low + 1) {
+            if (!is_done(c, low)) break;
+            harvest_one(c, low);
         }
-        c->low++;
+        low++;
     }
+    __atomic_store_n(&c->low, low, __ATOMIC_RELEASE);
 }
 
 static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint32_t timeout_us)
@@ -860,13 +866,12 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
     const uint64_t t_start = now_ns();
     uint32_t spins = 0;
     while (true) {
-        uint64_t low;
-        {
-            HarvestLock lk(c);
+        if (head_of(c) + count <= __atomic_load_n(&c->low, __ATOMIC_ACQUIRE) + c->N) break;
+        if (c->hmu.try_lock()) { /* one producer advances the harvest; the others spin */
             sweep(c);
-            low = c->low;
+            c->hmu.unlock();
+            if (head_of(c) + count <= __atomic_load_n(&c->low, __ATOMIC_ACQUIRE) + c->N) break;
         }
-        if (head_of(c) + count <= low + c->N) break;
         if ((++spins & 255u) == 0) {
             heartbeat(c);
             if (now_ns() - t_start > (uint64_t)timeout_us * 1000ull) return GPUOS_EAGAIN;
@@ -894,8 +899,7 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
                 }
                 cpu_relax();
             }
-            HarvestLock lk(c);
-            harvest_one(c, prev);
+            harvest_one(c, prev); /* lock-free: one harvester per ticket */
         }
         gpuos_desc w = d[i];
         w.ntiles = nts[i];
@@ -977,10 +981,7 @@ int gpuos_sync(gpuos_ctx *c, uint64_t ticket, uint32_t timeout_ms)
         cpu_relax();
     }
     HarvestLock lk(c);
-    if (c->pending_errors) {
-        c->pending_errors = 0;
-        return GPUOS_EDEVICE;
-    }
+    if (__atomic_exchange_n(&c->pending_errors, (uint64_t)0, __ATOMIC_ACQ_REL)) return GPUOS_EDEVICE;
     return GPUOS_OK;
 }
 
@@ -1156,8 +1157,8 @@ int gpuos_stats(gpuos_ctx *c, gpuos_stats_t *st)
     {
         HarvestLock lk(c);
         sweep(c);
-        st->completed = c->n_completed;
-        st->errors = c->n_errors;
+        st->completed = __atomic_load_n(&c->n_completed, __ATOMIC_RELAXED);
+        st->errors = __atomic_load_n(&c->n_errors, __ATOMIC_RELAXED);
     }
     st->submitted = head_of(c);
     st->sequenced = __atomic_load_n(&c->hctl->sequenced, __ATOMIC_RELAXED);
