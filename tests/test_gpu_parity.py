@@ -177,3 +177,43 @@ def test_c4_full_sampled():
     sd = [j for j, o in enumerate(s.ops) if o.op == "sdpa"]
     keep = sample(sd, 12, seed=4)
     _run_and_compare(s, check=keep, skip=sd)
+
+
+@pytest.mark.slow
+def test_largest_elementwise_op_sampled():
+    """One bf16 add of 2^31 + 1000 elements (three 4 GiB tensors): 64-bit
+    element offsets past 2^32 bytes, 262,145 tiles over the capped helper
+    count and the tile counter. Windows at the start, around 2^31 and at
+    the ragged end are compared with the oracle's add on the same windows;
+    the executor runs alone on this descriptor."""
+    import torch
+    from oracle.interp import lib as orc_lib
+    from persistent_micro_dispatch_gb300 import gpuos as G
+    n = (1 << 31) + 1000
+    g = torch.Generator(device="cuda").manual_seed(31)
+    a = torch.randn(n, device="cuda", generator=g, dtype=torch.bfloat16)
+    b = torch.randn(n, device="cuda", generator=g, dtype=torch.bfloat16)
+    out = torch.full((n,), 7.0, device="cuda", dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    d = G.make_descs(1)
+    d["op_id"] = G.OP["add"]
+    d["dtype"] = G.BF16
+    d["a"], d["b"], d["out"] = a.data_ptr(), b.data_ptr(), out.data_ptr()
+    d["dims"][0, 0] = n
+    ex = G.Executor()
+    try:
+        ex.submit(d)
+        ex.sync(timeout_ms=120_000)
+    finally:
+        assert ex.shutdown() == G.OK
+    L = orc_lib()
+    for lo in (0, 1 << 20, (1 << 31) - 4096, 1 << 31, n - 5000):
+        hi = min(n, lo + 8192)
+        av = a[lo:hi].view(torch.int16).cpu().numpy().view(np.uint16).copy()
+        bv = b[lo:hi].view(torch.int16).cpu().numpy().view(np.uint16).copy()
+        got = out[lo:hi].view(torch.int16).cpu().numpy().view(np.uint16)
+        exact = np.empty(hi - lo, np.float64)
+        want = np.empty(hi - lo, np.uint16)
+        L.orc_add(1, av.ctypes.data, bv.ctypes.data, exact.ctypes.data, hi - lo)
+        L.orc_store(1, exact.ctypes.data, want.ctypes.data, hi - lo)
+        assert np.array_equal(got, want), (lo, int(np.count_nonzero(got != want)))
