@@ -572,8 +572,20 @@ def main():
         e1.record(es)
         e1.synchronize()
         eg_ms = e0.elapsed_time(e1)
+        # isolated latency, measured like the executor's isolated round trip:
+        # the same sampled ops, one launch each, then a wait for it (host clock)
+        eg_rtt = []
+        for j in iso_idx:
+            d1 = descs[j:j + 1].copy()
+            d1["dep"] = 0
+            t0 = G.host_now_ns()
+            G.eager_run(d1, es.cuda_stream, args.stage_bytes)
+            es.synchronize()
+            eg_rtt.append(G.host_now_ns() - t0)
         result["eager"] = {"value": n_ops * args.steps / (eg_ms / 1e3), "unit": UNIT,
-                           "ms_per_step": eg_ms / args.steps, "launches_per_step": n_ops}
+                           "ms_per_step": eg_ms / args.steps, "launches_per_step": n_ops,
+                           "isolated_roundtrip_p50": pct(np.array(eg_rtt) / 1e3, 50),
+                           "isolated_roundtrip_p99": pct(np.array(eg_rtt) / 1e3, 99)}
 
     # ---- CUDA Graphs baseline: the eager launches of one step captured once
     # and replayed (stable shapes), and captured + instantiated anew every
