@@ -24,7 +24,7 @@ def header_symbols():
     return sorted(set(re.findall(r"GPUOS_API\s+[\w\s\*]+?\b(gpuos_\w+)\s*\(", txt)))
 
 
-def test_header_declares_the_north_star_verbs():
+def test_header_declares_the_ring_protocol_verbs():
     syms = header_symbols()
     for v in ("gpuos_init", "gpuos_submit", "gpuos_register_op", "gpuos_sync", "gpuos_shutdown"):
         assert v in syms
