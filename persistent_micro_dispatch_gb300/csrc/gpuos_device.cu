@@ -1641,6 +1641,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
     uint64_t *ws = p.warp_stats + (uint64_t)gw * GPUOS_WS_N;
     uint64_t s = 0, e = 0;
     uint64_t n_seq = 0, n_idle = 0, n_sleep = 0, t_body = 0, t_mirror = 0, t_pubs = 0, n_inline = 0;
+    uint32_t n_batches = 0;
     uint32_t polls = 0;
     uint64_t hb = ld_relaxed_sys(&p.hctl->heartbeat);
     uint64_t t_active = 0;
@@ -1667,7 +1668,9 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         if (k > KMAX) k = KMAX;
         if (k == 0) {
             /* idle: stop flag, exit_after, watchdog */
-            n_idle++;
+            if (n_idle++ == 0 || polls == 0) {
+                if (lane == 0) st_relaxed_sys(&p.hctl->sequenced, s);
+            }
             if ((polls & 31u) == 0) {
                 uint32_t reason = 0;
                 if (ld_relaxed_sys32(&p.hctl->stop)) reason = 1;
@@ -1909,7 +1912,11 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         t_mirror += t_m - t_b;
         t_pubs += t_pub - t_m;
         if (lane == 0) {
-            st_relaxed_sys(&p.hctl->sequenced, s);
+            /* the host-visible count (statistics and diagnostics only) goes
+             * out every 16th batch and when the ring runs dry: a store
+             * across NVLink-C2C per batch would make the next batch's
+             * system-scope fence wait for its acknowledgement */
+            if ((++n_batches & 15u) == 0) st_relaxed_sys(&p.hctl->sequenced, s);
             ws[GPUOS_WS_SEQ] = n_seq;
             ws[GPUOS_WS_IDLE] = n_idle;
             ws[GPUOS_WS_SLEEPS] = n_sleep;
