@@ -197,8 +197,8 @@ typedef struct gpuos_stats_t {
     uint32_t regs_per_thread; /* of the executor kernel */
     uint32_t static_smem_bytes;
     uint32_t reserved;
-    uint64_t seq_body_ns;    /* device: sequencer time reading descriptors (after seeing commits) */
-    uint64_t seq_mirror_ns;  /* device: sequencer time mirroring + fencing */
+    uint64_t seq_body_ns;    /* device: sequencer time reading, validating and mirroring descriptors */
+    uint64_t seq_mirror_ns;  /* device: sequencer time in the fence after mirroring */
     uint64_t seq_publish_ns; /* device: sequencer time publishing work-queue entries */
 } gpuos_stats_t;
 

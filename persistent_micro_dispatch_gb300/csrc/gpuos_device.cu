@@ -1631,9 +1631,11 @@ DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles, uint32_t workers)
     return hlp < cap ? hlp : cap;
 }
 
-/* The sequencer warp: ring -> mirror + work queue, up to 64 descriptors per
- * batch (two ring slots per lane: slot s + lane and s + 32 + lane). */
-#define SEQ_SPL 2
+/* The sequencer warp: ring -> mirror + work queue, up to 128 descriptors per
+ * batch (four ring slots per lane: slot s + lane + 32 h). */
+#define SEQ_SPL 2    /* ring slots per lane in one half of a batch (64 descriptors) */
+#define SEQ_HALVES 2 /* halves per batch */
+#define SEQ_POLL (SEQ_SPL * SEQ_HALVES)
 DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, unsigned long long *s_table)
 {
     const uint32_t lane = lane_id();
@@ -1648,23 +1650,32 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
     Elapsed idle;
     idle.start();
     const uint32_t N = p.ring_mask + 1;
-    const uint32_t KMAX = N < 32u * SEQ_SPL ? N : 32u * SEQ_SPL;
+    const uint32_t KMAX = N < 32u * SEQ_POLL ? N : 32u * SEQ_POLL;
     if (lane == 0) st_relaxed_sys32(&p.hctl->state, 1u);
 
-    /* commit words of slots s + lane + 32 h, polled ahead (relaxed; the
-     * batch's fence comes after they are seen): the poll for the next batch
-     * is issued before the current one is published, so its NVLink-C2C
-     * round trip overlaps the publication */
-    uint64_t seqv[SEQ_SPL];
+    /* commit words of slots s + lane + 32 h (h < SEQ_POLL), polled ahead
+     * (relaxed; the batch's fence comes after they are seen): the poll for
+     * the next batch is issued before the current one is published, so its
+     * NVLink-C2C round trip overlaps the publication. A batch of up to 128
+     * descriptors is read and mirrored in halves of 64 (two per lane) under
+     * one acquire fence, one mirror fence and one publication. */
+    uint64_t seqv[SEQ_POLL];
 #pragma unroll
-    for (int h = 0; h < SEQ_SPL; h++)
+    for (int h = 0; h < SEQ_POLL; h++)
         seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
     while (true) {
-        uint64_t rmask = 0;
+        uint64_t rm[SEQ_HALVES];
 #pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++)
-            rmask |= (uint64_t)__ballot_sync(0xFFFFFFFFu, seqv[h] == s + lane + 32u * h + 1) << (32 * h);
-        uint32_t k = (rmask == ~0ull) ? 64u : (uint32_t)(__ffsll((long long)~rmask) - 1);
+        for (int q = 0; q < SEQ_HALVES; q++) {
+            rm[q] = 0;
+#pragma unroll
+            for (int h = 0; h < SEQ_SPL; h++) {
+                const uint32_t pos = lane + 32u * (SEQ_SPL * q + h);
+                rm[q] |= (uint64_t)__ballot_sync(0xFFFFFFFFu, seqv[SEQ_SPL * q + h] == s + pos + 1) << (32 * h);
+            }
+        }
+        uint32_t k = (rm[0] != ~0ull) ? (uint32_t)(__ffsll((long long)~rm[0]) - 1)
+                                      : 64u + ((rm[1] == ~0ull) ? 64u : (uint32_t)(__ffsll((long long)~rm[1]) - 1));
         if (k > KMAX) k = KMAX;
         if (k == 0) {
             /* idle: stop flag, exit_after, watchdog */
@@ -1697,7 +1708,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             }
             backoff(polls, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
 #pragma unroll
-            for (int h = 0; h < SEQ_SPL; h++)
+            for (int h = 0; h < SEQ_POLL; h++)
                 seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
             continue;
         }
@@ -1708,97 +1719,110 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
          * the clocks with it. Every record gets it again at completion,
          * from t_disp (the mirror fence orders that store before the
          * publication); a batch's early echo would make this batch's fence
-         * wait for 64 stores across NVLink-C2C. */
+         * wait for its stores across NVLink-C2C. */
         if (k == 1 && lane == 0) st_relaxed_sys(&p.rec[(uint32_t)(s & p.ring_mask)].t_dispatch, t_obs);
         /* the commits seen above happen-before everything below */
         fence_acq_rel_sys();
-        gpuos_desc dsc[SEQ_SPL];
-#pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++) {
-            const uint32_t pos = lane + 32u * h;
-            if (pos < k) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.ring + (uint32_t)((s + pos) & p.ring_mask));
-                uint4 *dv = reinterpret_cast<uint4 *>(&dsc[h]);
-#pragma unroll
-                for (int i = 0; i < 8; i++) dv[i] = src[i];
-            }
-        }
         uint32_t version = 0;
-        if (lane == 0) version = ld_acquire_gpu32(&p.dctl->version);
-        version = __shfl_sync(0xFFFFFFFFu, version, 0);
-        if (version != cached_version) {
-            /* a new version: copy its table slot (written before the flip
-             * the acquire above saw) into shared memory */
-            __syncwarp();
-            for (uint32_t i = lane; i < GPUOS_MAX_OPS; i += 32)
-                s_table[i] = __ldcg(reinterpret_cast<const unsigned long long *>(p.table) +
-                                    (version & 1u) * GPUOS_MAX_OPS + i);
-            __syncwarp();
-            cached_version = version;
-        }
-        /* a FENCE descriptor must start a batch; cut the batch before it */
-        uint64_t fmask = 0;
+        int32_t status[SEQ_POLL];
+        uint32_t nt[SEQ_POLL];
 #pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++) {
-            const uint32_t pos = lane + 32u * h;
-            fmask |= (uint64_t)__ballot_sync(0xFFFFFFFFu, pos < k && (dsc[h].flags & GPUOS_FLAG_FENCE)) << (32 * h);
-        }
-        const uint64_t later = fmask & ~1ull;
-        if (later) {
-            const uint32_t cut = (uint32_t)(__ffsll((long long)later) - 1);
-            if (cut < k) k = cut;
-        }
-        uint32_t fence_status = GPUOS_ST_OK;
-        if (fmask & 1ull) {
-            if (lane == 0) {
-                Elapsed w;
-                w.start();
-                uint32_t fp = 0;
-                while (*reinterpret_cast<volatile unsigned long long *>(&p.dctl->completed) < s) {
-                    if (w.tick(globaltimer()) > p.dep_timeout_ns) {
-                        fence_status = GPUOS_ST_DEP_TIMEOUT;
-                        break;
-                    }
-                    backoff(fp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
-                }
-                __threadfence();
-            }
-            fence_status = __shfl_sync(0xFFFFFFFFu, fence_status, 0);
-        }
-        const uint64_t t_b = globaltimer();
-
-        /* validate and mirror */
-        int32_t status[SEQ_SPL];
-        uint32_t nt[SEQ_SPL];
-#pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++) {
-            const uint32_t pos = lane + 32u * h;
-            const uint64_t my_t = s + pos;
+        for (int h = 0; h < SEQ_POLL; h++) {
             status[h] = GPUOS_ST_OK;
             nt[h] = 0;
-            if (pos < k) {
-                *reinterpret_cast<volatile uint64_t *>(p.t_disp + (uint32_t)(my_t & p.ring_mask)) = t_obs;
-                if (dsc[h].ticket != my_t) status[h] = GPUOS_ST_BAD_DESC;
-                else if (dsc[h].op_id >= GPUOS_MAX_OPS) status[h] = GPUOS_ST_BAD_OP;
-                else if (dsc[h].ntiles == 0 || dsc[h].ntiles > GPUOS_TILE_MAX) status[h] = GPUOS_ST_BAD_ARGS;
-                if (pos == 0 && fence_status) status[h] = (int32_t)fence_status;
-                if (status[h] == GPUOS_ST_OK) {
-                    /* one work-queue entry per helper warp (at most GPUOS_HELPERS);
-                     * helper i starts with tile i and takes later tiles from the
-                     * descriptor's tile counter */
-                    nt[h] = helper_count(dsc[h].op_id, dsc[h].ntiles, p.workers);
-                    dsc[h].user = s_table[dsc[h].op_id];                     /* -> fn */
-                    dsc[h].seq = (uint64_t)version | ((uint64_t)nt[h] << 32); /* -> version, helpers */
-                    uint4 *mv = reinterpret_cast<uint4 *>(p.mirror + (uint32_t)(my_t & p.ring_mask));
-                    const uint4 *dv = reinterpret_cast<const uint4 *>(&dsc[h]);
+        }
+        gpuos_desc dsc[SEQ_SPL];
 #pragma unroll
-                    for (int i = 0; i < 8; i++) __stcg(mv + i, dv[i]);
+        for (int q = 0; q < SEQ_HALVES; q++) {
+            const uint32_t base = 64u * q;
+            if (base >= k) break; /* k is warp-uniform */
+#pragma unroll
+            for (int h = 0; h < SEQ_SPL; h++) {
+                const uint32_t pos = base + lane + 32u * h;
+                if (pos < k) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.ring + (uint32_t)((s + pos) & p.ring_mask));
+                    uint4 *dv = reinterpret_cast<uint4 *>(&dsc[h]);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) dv[i] = src[i];
+                }
+            }
+            if (q == 0) {
+                if (lane == 0) version = ld_acquire_gpu32(&p.dctl->version);
+                version = __shfl_sync(0xFFFFFFFFu, version, 0);
+                if (version != cached_version) {
+                    /* a new version: copy its table slot (written before the
+                     * flip the acquire above saw) into shared memory */
+                    __syncwarp();
+                    for (uint32_t i = lane; i < GPUOS_MAX_OPS; i += 32)
+                        s_table[i] = __ldcg(reinterpret_cast<const unsigned long long *>(p.table) +
+                                            (version & 1u) * GPUOS_MAX_OPS + i);
+                    __syncwarp();
+                    cached_version = version;
+                }
+            }
+            /* a FENCE descriptor must start a batch; cut the batch before it */
+            uint64_t fmask = 0;
+#pragma unroll
+            for (int h = 0; h < SEQ_SPL; h++) {
+                const uint32_t pos = base + lane + 32u * h;
+                fmask |= (uint64_t)__ballot_sync(0xFFFFFFFFu, pos < k && (dsc[h].flags & GPUOS_FLAG_FENCE))
+                         << (32 * h);
+            }
+            const uint64_t later = (q == 0) ? (fmask & ~1ull) : fmask;
+            if (later) {
+                const uint32_t cut = base + (uint32_t)(__ffsll((long long)later) - 1);
+                if (cut < k) k = cut;
+            }
+            uint32_t fence_status = GPUOS_ST_OK;
+            if (q == 0 && (fmask & 1ull)) {
+                if (lane == 0) {
+                    Elapsed w;
+                    w.start();
+                    uint32_t fp = 0;
+                    while (*reinterpret_cast<volatile unsigned long long *>(&p.dctl->completed) < s) {
+                        if (w.tick(globaltimer()) > p.dep_timeout_ns) {
+                            fence_status = GPUOS_ST_DEP_TIMEOUT;
+                            break;
+                        }
+                        backoff(fp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+                    }
+                    __threadfence();
+                }
+                fence_status = __shfl_sync(0xFFFFFFFFu, fence_status, 0);
+            }
+            /* validate and mirror */
+#pragma unroll
+            for (int h = 0; h < SEQ_SPL; h++) {
+                const uint32_t pos = base + lane + 32u * h;
+                const uint64_t my_t = s + pos;
+                if (pos < k) {
+                    int32_t st = GPUOS_ST_OK;
+                    *reinterpret_cast<volatile uint64_t *>(p.t_disp + (uint32_t)(my_t & p.ring_mask)) = t_obs;
+                    if (dsc[h].ticket != my_t) st = GPUOS_ST_BAD_DESC;
+                    else if (dsc[h].op_id >= GPUOS_MAX_OPS) st = GPUOS_ST_BAD_OP;
+                    else if (dsc[h].ntiles == 0 || dsc[h].ntiles > GPUOS_TILE_MAX) st = GPUOS_ST_BAD_ARGS;
+                    if (pos == 0 && fence_status) st = (int32_t)fence_status;
+                    status[SEQ_SPL * q + h] = st;
+                    if (st == GPUOS_ST_OK) {
+                        /* one work-queue entry per helper warp (at most
+                         * GPUOS_HELPERS); helper i starts with tile i and takes
+                         * later tiles from the descriptor's tile counter */
+                        const uint32_t hc = helper_count(dsc[h].op_id, dsc[h].ntiles, p.workers);
+                        nt[SEQ_SPL * q + h] = hc;
+                        dsc[h].user = s_table[dsc[h].op_id];                 /* -> fn */
+                        dsc[h].seq = (uint64_t)version | ((uint64_t)hc << 32); /* -> version, helpers */
+                        uint4 *mv = reinterpret_cast<uint4 *>(p.mirror + (uint32_t)(my_t & p.ring_mask));
+                        const uint4 *dv = reinterpret_cast<const uint4 *>(&dsc[h]);
+#pragma unroll
+                        for (int i = 0; i < 8; i++) __stcg(mv + i, dv[i]);
+                    }
                 }
             }
         }
+        const uint64_t t_b = globaltimer();
         /* An idle ring (a batch of one) and a dependency-free single-tile
          * descriptor: the sequencer runs the tile itself, sparing the
-         * mirror -> work queue -> worker hop. */
+         * mirror -> work queue -> worker hop. (k == 1: dsc[0] holds it.) */
         uint32_t inl = 0;
         if (lane == 0)
             inl = (k == 1 && status[0] == GPUOS_ST_OK && dsc[0].ntiles == 1 && dsc[0].dep[0] == 0 &&
@@ -1830,7 +1854,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             }
             idle.start();
 #pragma unroll
-            for (int h = 0; h < SEQ_SPL; h++)
+            for (int h = 0; h < SEQ_POLL; h++)
                 seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
             continue;
         }
@@ -1840,13 +1864,14 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         const uint64_t t_m = globaltimer();
         /* the next batch's poll, in flight during the publication below */
 #pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++)
+        for (int h = 0; h < SEQ_POLL; h++)
             seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + k + lane + 32u * h) & p.ring_mask)].seq);
-        /* exclusive prefix of entry counts in ticket order -> queue ranges */
-        uint32_t excl[SEQ_SPL];
+        /* exclusive prefix of entry counts in ticket order -> queue ranges
+         * (position lane + 32 h for h < SEQ_POLL) */
+        uint32_t excl[SEQ_POLL];
         uint32_t base = 0;
 #pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++) {
+        for (int h = 0; h < SEQ_POLL; h++) {
             uint32_t incl = nt[h];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -1861,12 +1886,14 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
          * descriptors; descriptors with more entries are finished by the
          * whole warp, one after another. */
         {
-            uint32_t most = nt[0] > nt[1] ? nt[0] : nt[1];
+            uint32_t most = 0;
+#pragma unroll
+            for (int h = 0; h < SEQ_POLL; h++) most = nt[h] > most ? nt[h] : most;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) most = max(most, __shfl_xor_sync(0xFFFFFFFFu, most, o));
             const uint32_t jmax = most < 16u ? most : 16u;
 #pragma unroll
-            for (int h = 0; h < SEQ_SPL; h++) {
+            for (int h = 0; h < SEQ_POLL; h++) {
                 const uint32_t slot = (uint32_t)((s + lane + 32u * h) & p.ring_mask);
                 for (uint32_t j = 0; j < jmax; j++) {
                     if (j < nt[h]) {
@@ -1878,7 +1905,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             }
             if (most > 16u) {
 #pragma unroll
-                for (int h = 0; h < SEQ_SPL; h++) {
+                for (int h = 0; h < SEQ_POLL; h++) {
                     uint32_t big = __ballot_sync(0xFFFFFFFFu, nt[h] > 16u);
                     while (big) {
                         const uint32_t i = (uint32_t)(__ffs(big) - 1);
@@ -1897,7 +1924,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         }
         const uint64_t t_pub = globaltimer();
 #pragma unroll
-        for (int h = 0; h < SEQ_SPL; h++) {
+        for (int h = 0; h < SEQ_POLL; h++) {
             const uint32_t pos = lane + 32u * h;
             const uint64_t my_t = s + pos;
             const uint32_t slot = (uint32_t)(my_t & p.ring_mask);
