@@ -551,7 +551,7 @@ def main():
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
         "op_kinds": kinds,
         "executor": {k: st[k] for k in ("tiles", "idle_polls", "sleeps", "dep_waits", "regs_per_thread",
-                                        "static_smem_bytes", "seq_body_ns", "seq_mirror_ns", "seq_publish_ns")},
+                                        "static_smem_bytes", "seq_body_ns", "seq_mirror_ns", "seq_publish_ns", "seq_batches", "host_wait_ns")},
         "wall_s": wall,
     }
 

@@ -144,7 +144,8 @@ typedef struct gpuos_desc {
 typedef struct gpuos_config {
     uint32_t ring_entries;    /* power of two in [64, 65536]; default 4096 (the page's default) */
     uint32_t warps_per_block; /* 2..12; default 12 */
-    uint32_t blocks;          /* 0 = one block per SM */
+    uint32_t blocks;          /* 0 = one block per SM; block 0 holds only the sequencer warp
+                                 (when blocks > 1) */
     uint32_t backoff_min_ns;  /* first idle sleep; default 32 */
     uint32_t backoff_max_ns;  /* idle sleep cap; default 256 */
     uint32_t spin_polls;      /* polls of pure spinning before backing off; default 4096 */
@@ -200,6 +201,9 @@ typedef struct gpuos_stats_t {
     uint64_t seq_body_ns;    /* device: sequencer time reading, validating and mirroring descriptors */
     uint64_t seq_mirror_ns;  /* device: sequencer time in the fence after mirroring */
     uint64_t seq_publish_ns; /* device: sequencer time publishing work-queue entries */
+    uint64_t seq_batches;    /* device: batches the sequencer took off the ring (lone descriptors
+                                it ran itself not counted) */
+    uint64_t host_wait_ns;   /* host: time submitting threads waited for a free ring slot */
 } gpuos_stats_t;
 
 /* Where the executor's worker warps spent their time, per op id (device
@@ -338,7 +342,8 @@ GPUOS_API int gpuos_stats(gpuos_ctx *ctx, gpuos_stats_t *st);
  * commit between t0 and t1, every ping bounds off = device clock - host clock
  * to [t_dispatch - t1, t_dispatch - t0]; *off_lo / *off_hi receive the
  * intersection over all pings and *min_rtt_ns the smallest t1 - t0. rtts
- * (may be NULL) receives every echo round trip. */
+ * (may be NULL) receives every echo round trip. It first waits for every
+ * submitted ticket; no other thread may submit while it runs. */
 GPUOS_API int gpuos_calibrate(gpuos_ctx *ctx, uint32_t pings, int64_t *off_lo, int64_t *off_hi,
                               uint64_t *min_rtt_ns, uint64_t *rtts);
 

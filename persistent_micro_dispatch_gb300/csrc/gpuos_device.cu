@@ -1884,8 +1884,13 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         const uint32_t total = base;
         /* Publication. Each lane writes the first (up to 16) entries of its own
          * descriptors; descriptors with more entries are finished by the
-         * whole warp, one after another. */
+         * whole warp, one after another. Entry j of a descriptor whose first
+         * entry has index i0 is tq_word(i0 + j, slot, j) = W0 + j * TQ_STEP
+         * with W0 = tq_word(i0, slot, 0): the stamp field takes the carry-free
+         * (mod 2^64) sum and the helper field j < 4096 never carries. The
+         * queue index is taken modulo 2^32 (the queue is smaller). */
         {
+            constexpr uint64_t TQ_STEP = (1ull << 28) + 1ull;
             uint32_t most = 0;
 #pragma unroll
             for (int h = 0; h < SEQ_POLL; h++) most = nt[h] > most ? nt[h] : most;
@@ -1895,12 +1900,15 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
 #pragma unroll
             for (int h = 0; h < SEQ_POLL; h++) {
                 const uint32_t slot = (uint32_t)((s + lane + 32u * h) & p.ring_mask);
+                const uint64_t i0 = e + excl[h];
+                const uint32_t q0 = (uint32_t)i0;
+                uint64_t wd = tq_word(i0, slot, 0);
+                const uint32_t nj = nt[h] < jmax ? nt[h] : jmax;
+#pragma unroll 4
                 for (uint32_t j = 0; j < jmax; j++) {
-                    if (j < nt[h]) {
-                        const uint64_t idx = e + excl[h] + j;
-                        *reinterpret_cast<volatile unsigned long long *>(p.tq + (idx & p.tq_mask)) =
-                            tq_word(idx, slot, j);
-                    }
+                    if (j < nj)
+                        *reinterpret_cast<volatile unsigned long long *>(p.tq + ((q0 + j) & p.tq_mask)) = wd;
+                    wd += TQ_STEP;
                 }
             }
             if (most > 16u) {
@@ -1913,10 +1921,12 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                         const uint32_t nti = __shfl_sync(0xFFFFFFFFu, nt[h], i);
                         const uint32_t bi = __shfl_sync(0xFFFFFFFFu, excl[h], i);
                         const uint32_t slot = (uint32_t)((s + i + 32u * h) & p.ring_mask);
+                        const uint64_t i0 = e + bi;
+                        const uint32_t q0 = (uint32_t)i0;
+                        uint64_t wd = tq_word(i0, slot, 0) + (uint64_t)(16u + lane) * TQ_STEP;
                         for (uint32_t j = 16u + lane; j < nti; j += 32) {
-                            const uint64_t idx = e + bi + j;
-                            *reinterpret_cast<volatile unsigned long long *>(p.tq + (idx & p.tq_mask)) =
-                                tq_word(idx, slot, j);
+                            *reinterpret_cast<volatile unsigned long long *>(p.tq + ((q0 + j) & p.tq_mask)) = wd;
+                            wd += 32ull * TQ_STEP;
                         }
                     }
                 }
@@ -1950,6 +1960,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             ws[GPUOS_WS_T_BODY] = t_body;
             ws[GPUOS_WS_T_MIRROR] = t_mirror;
             ws[GPUOS_WS_T_PUB] = t_pubs;
+            ws[GPUOS_WS_BATCHES] = n_batches;
         }
         idle.start();
     }
@@ -2140,8 +2151,11 @@ extern "C" __global__ void __launch_bounds__(GPUOS_MAX_WPB * 32, 1) gpuos_execut
     for (uint32_t i = threadIdx.x & 31u; i < GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS; i += 32) s_prof[warp][i] = 0;
     stage_init(p.stage_bytes); /* (its block barriers also order the clearing above) */
     const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
+    /* Block 0 is the sequencer's alone (unless it is the only block): worker
+     * warps beside it would share its issue slots and load/store pipe, and
+     * the sequencer's batch time sets the executor's dispatch rate. */
     if (blockIdx.x == 0 && warp == 0) sequencer(p, &sdesc[0], gw, s_table);
-    else worker(p, &sdesc[warp], gw, s_prof[warp]);
+    else if (blockIdx.x != 0 || gridDim.x == 1) worker(p, &sdesc[warp], gw, s_prof[warp]);
 }
 
 /* ===========================================================================

@@ -219,6 +219,7 @@ struct gpuos_ctx {
     gpuos_record *history = nullptr;
     uint64_t hist_base = 0, hist_cap = 0;
     uint64_t n_completed = 0, n_errors = 0;
+    uint64_t host_wait_ns = 0; /* submitters' time waiting for a free slot */
     uint64_t pending_errors = 0; /* errors harvested since the last sync report */
     /* operator table shadow */
     uint64_t table_host[2][GPUOS_MAX_OPS];
@@ -613,7 +614,8 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     p.backoff_max_ns = cfg.backoff_max_ns;
     p.spin_polls = cfg.spin_polls;
     p.stage_bytes = cfg.stage_bytes;
-    p.workers = c->blocks * c->wpb - 1;
+    /* worker warps: block 0 holds only the sequencer (when there are others) */
+    p.workers = c->blocks > 1 ? (c->blocks - 1) * c->wpb : c->wpb - 1;
     p.idle_exit_ns = (uint64_t)cfg.idle_exit_ms * 1000000ull;
     p.dep_timeout_ns = (uint64_t)(cfg.dep_timeout_ms ? cfg.dep_timeout_ms : 5000) * 1000000ull;
     p.exit_after = cfg.exit_after;
@@ -812,12 +814,11 @@ static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint3
                 }
                 cpu_relax();
             }
+            __atomic_fetch_add(&c->host_wait_ns, now_ns() - t0, __ATOMIC_RELAXED);
         }
         harvest_one(c, prev);
     }
     gpuos_desc *s = c->ring + slot;
-    /* the device echoes its observation time here (see gpuos_calibrate) */
-    __atomic_store_n(&c->rec[slot].t_dispatch, (uint64_t)0, __ATOMIC_RELAXED);
     gpuos_desc w = *d;
     w.ntiles = nt;
     w.dep[0] = deps[0];
@@ -882,6 +883,7 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
         }
         cpu_relax();
     }
+    if (spins) __atomic_fetch_add(&c->host_wait_ns, now_ns() - t_start, __ATOMIC_RELAXED);
     const uint64_t t0 = __atomic_fetch_add(&c->head, (uint64_t)count, __ATOMIC_ACQ_REL);
     if (first_ticket) *first_ticket = t0;
     for (uint32_t i = 0; i < count; i++) {
@@ -908,7 +910,6 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
         w.flags = (uint8_t)(d[i].flags & GPUOS_FLAG_FENCE);
         w.ticket = t;
         gpuos_desc *sl = c->ring + slot;
-        __atomic_store_n(&c->rec[slot].t_dispatch, (uint64_t)0, __ATOMIC_RELAXED);
         const uint64_t *src = reinterpret_cast<const uint64_t *>(&w);
         uint64_t *dst = reinterpret_cast<uint64_t *>(sl);
         for (int q = 0; q < 15; q++) __atomic_store_n(dst + q, src[q], __ATOMIC_RELAXED);
@@ -1154,6 +1155,8 @@ int gpuos_stats(gpuos_ctx *c, gpuos_stats_t *st)
     st->seq_body_ns = ws[GPUOS_WS_T_BODY];
     st->seq_mirror_ns = ws[GPUOS_WS_T_MIRROR];
     st->seq_publish_ns = ws[GPUOS_WS_T_PUB];
+    st->seq_batches = ws[GPUOS_WS_BATCHES];
+    st->host_wait_ns = __atomic_load_n(&c->host_wait_ns, __ATOMIC_RELAXED);
     {
         HarvestLock lk(c);
         sweep(c);
@@ -1204,6 +1207,12 @@ int gpuos_calibrate(gpuos_ctx *c, uint32_t pings, int64_t *off_lo, int64_t *off_
     int64_t lo = INT64_MIN, hi = INT64_MAX;
     for (uint32_t i = 0; i < pings; i++) {
         uint64_t t = 0;
+        /* every earlier ticket has completed and been harvested (the sync
+         * above, and each ping below waits for its own completion), so no
+         * completion rewrites this record any more: clear the field the
+         * sequencer echoes its observation time into (it still holds the
+         * previous ticket's) */
+        __atomic_store_n(&c->rec[head_of(c) & c->mask].t_dispatch, (uint64_t)0, __ATOMIC_RELAXED);
         const uint64_t t0 = now_ns();
         rc = gpuos_submit(c, &nop, &t, 1000000);
         if (rc) return rc;

@@ -93,9 +93,10 @@ typedef struct gpuos_devctl {
 /* Per-warp counters (owned by one warp each, plain stores). */
 enum { GPUOS_WS_TILES = 0, GPUOS_WS_IDLE = 1, GPUOS_WS_SLEEPS = 2, GPUOS_WS_DEPWAIT = 3,
        GPUOS_WS_SEQ = 4, GPUOS_WS_T_BODY = 5, GPUOS_WS_T_MIRROR = 6, GPUOS_WS_T_PUB = 7,
+       GPUOS_WS_BATCHES = 8,
        /* tile profile: GPUOS_PROF_FIELDS rows of GPUOS_PROF_BUCKETS (op id, or the last
         * bucket for user ops): tiles, body ns, finish ns, dependency ns */
-       GPUOS_WS_PROF = 8, GPUOS_WS_N = 8 + GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS };
+       GPUOS_WS_PROF = 9, GPUOS_WS_N = 9 + GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS };
 
 typedef int (*gpuos_op_fn)(const gpuos_devdesc *d, uint32_t tile);
 

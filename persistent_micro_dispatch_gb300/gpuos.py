@@ -70,7 +70,8 @@ class Stats(C.Structure):
                 ("running", C.c_uint32), ("exit_reason", C.c_uint32), ("blocks", C.c_uint32),
                 ("warps_per_block", C.c_uint32), ("regs_per_thread", C.c_uint32),
                 ("static_smem_bytes", C.c_uint32), ("reserved", C.c_uint32),
-                ("seq_body_ns", C.c_uint64), ("seq_mirror_ns", C.c_uint64), ("seq_publish_ns", C.c_uint64)]
+                ("seq_body_ns", C.c_uint64), ("seq_mirror_ns", C.c_uint64), ("seq_publish_ns", C.c_uint64),
+                ("seq_batches", C.c_uint64), ("host_wait_ns", C.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
@@ -258,7 +259,10 @@ class Executor:
         return r
 
     def set_history(self, base: int, capacity: int) -> np.ndarray:
-        self._hist = np.zeros(capacity, dtype=RECORD_DTYPE)
+        # written once per completion while descriptors stream in: touch every
+        # page now (a lazily mapped zero page faults on its first write)
+        self._hist = np.empty(capacity, dtype=RECORD_DTYPE)
+        self._hist.view(np.uint8)[:] = 0
         check(lib().gpuos_set_history(self._ctx, self._hist.ctypes.data, base, capacity), "gpuos_set_history")
         return self._hist
 
