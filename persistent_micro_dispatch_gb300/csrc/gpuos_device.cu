@@ -1731,6 +1731,18 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             status[h] = GPUOS_ST_OK;
             nt[h] = 0;
         }
+        /* the second half's bodies start towards L2 now (coherent with the
+         * host's writes): their NVLink-C2C round trip overlaps the first
+         * half's */
+#pragma unroll
+        for (int h = 0; h < SEQ_SPL; h++) {
+            const uint32_t pos = 64u + lane + 32u * h;
+            if (pos < k) {
+                const char *src = reinterpret_cast<const char *>(p.ring + (uint32_t)((s + pos) & p.ring_mask));
+#pragma unroll
+                for (int i = 0; i < 4; i++) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 32 * i));
+            }
+        }
         gpuos_desc dsc[SEQ_SPL];
 #pragma unroll
         for (int q = 0; q < SEQ_HALVES; q++) {
