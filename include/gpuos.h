@@ -368,9 +368,11 @@ GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
  *                      round_up(ceil(n / ntiles), 256) elements
  *   row ops            R (one row per tile)
  *   rope, kv_write     B * ceil(H / 4) (one request, four heads per tile)
- *   sdpa               B * H * ceil(Lmax / c), c = 256 key rows, halved down
- *                      to 32 while B * H * ceil(Lmax / c) < 1536; a tile
- *                      attends round_up(ceil(Lmax / chunks), 32) rows
+ *   sdpa               B * H * ceil(Lmax / c), c = round_up(ceil(Lmax / w), 32)
+ *                      key rows (at least 32), w = floor(1536 / (B * H)) or 1
+ *                      if B * H >= 1536: at most 1536 tiles (or B * H), one
+ *                      wave on the default executor; a tile attends
+ *                      round_up(ceil(Lmax / chunks), 32) rows
  *   vecmat             ceil(N / 8) (eight output columns per tile)
  *   nop / empty op     1
  * Returns GPUOS_EINVAL for a descriptor the library would reject. */

@@ -339,15 +339,20 @@ static uint64_t ew_tiles(uint64_t n, uint64_t tile_min, uint64_t tile_max)
     return ceil_div(n, te);
 }
 
-/* Decode-attention chunks: 256 key rows, halved (down to 32) while the op
- * would have fewer than GPUOS_SDPA_SPLIT tiles, so that a small batch still
- * spreads over most of the worker warps. The device recovers the chunk length from Lmax
- * and ntiles (round_up(ceil(Lmax / nchunks), 32)). */
+/* Decode-attention chunks: every (b, h) pair's keys are cut into at most
+ * floor(GPUOS_SDPA_SPLIT / (B * H)) chunks (at least one) of equal length,
+ * a multiple of 32 rows: the op has at most GPUOS_SDPA_SPLIT tiles (or B * H),
+ * all of which the default executor runs at once. A second, partial wave of
+ * tiles would leave most warps idle while it runs. The device recovers the
+ * chunk length from Lmax and ntiles: round_up(ceil(Lmax / nchunks), 32),
+ * which is at most the length chosen here, with no chunk starting past
+ * Lmax. */
 static uint64_t sdpa_chunks(uint64_t BH, uint64_t Lmax)
 {
-    uint64_t c = GPUOS_SDPA_CHUNK;
-    while (c > GPUOS_SDPA_CHUNK_MIN && BH * ceil_div(Lmax, c) < GPUOS_SDPA_SPLIT) c >>= 1;
-    return ceil_div(Lmax, c);
+    const uint64_t want = BH < GPUOS_SDPA_SPLIT ? GPUOS_SDPA_SPLIT / BH : 1;
+    uint64_t ch = (ceil_div(Lmax, want) + 31) & ~31ull;
+    if (ch < GPUOS_SDPA_CHUNK_MIN) ch = GPUOS_SDPA_CHUNK_MIN;
+    return ceil_div(Lmax, ch);
 }
 
 /* Host-side validation (the page's "bounds checking") and tiling rule. */

@@ -17,9 +17,9 @@
 #define GPUOS_GELU_TILE_MIN 1024          /* ... and GELU tile (more arithmetic per element) */
 #define GPUOS_EW_SPLIT 16                 /* element-wise ops aim at this many tiles */
 #define GPUOS_EW_ALIGN 256                /* element-wise tile sizes are multiples of this */
-#define GPUOS_SDPA_CHUNK 256              /* key rows per decode-attention tile at most */
-#define GPUOS_SDPA_CHUNK_MIN 32           /* ... and at least (workspace sizing) */
-#define GPUOS_SDPA_SPLIT 1536             /* attention aims at this many tiles */
+#define GPUOS_SDPA_CHUNK 256              /* key rows per tile of the allocation-free attention */
+#define GPUOS_SDPA_CHUNK_MIN 32           /* key rows per decode-attention tile at least (workspace sizing) */
+#define GPUOS_SDPA_SPLIT 1536             /* decode-attention tiles at most (unless B * H is more) */
 #define GPUOS_HEAD_GROUP 4                /* heads per RoPE / KV-write tile */
 #define GPUOS_VM_COLS 8                   /* output columns per vecmat tile (16 bytes of a row) */
 #define GPUOS_ROW_REG_MAX 4096            /* rows up to this width stay in registers */
