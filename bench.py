@@ -112,6 +112,40 @@ class ClockSampler:
         return out
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per descriptor of
+# the executor kernel, from one ncu capture of a bounded run of each stream
+# (``--profile-run --profile-desc N``: the stream's first N descriptors in the
+# ring before the single launch), and the digest of the device sources the
+# capture was taken on. A launch's traffic is that figure times the
+# descriptors it processed, reported only while the sources are unchanged.
+TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
+                   "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
+TRAFFIC = {
+    "c2": dict(bytes=249_449_728, descs=4096, sources="b6db7b5a084e60fd"),
+    "c2l": dict(bytes=996_640_000, descs=400, sources="b6db7b5a084e60fd"),
+    "c4": dict(bytes=30_830_919_000, descs=600, sources="b6db7b5a084e60fd"),
+    "c5": dict(bytes=493_404_160, descs=224, sources="b6db7b5a084e60fd"),
+}
+
+
+def sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def launch_traffic(workload: str, descs: int):
+    """DRAM bytes of one executor launch that processed `descs` descriptors,
+    scaled from the stream's capture; None once the kernel has changed."""
+    t = TRAFFIC.get(workload)
+    if t is None or sources_digest() != t["sources"]:
+        return None
+    return t["bytes"] / t["descs"] * descs
+
+
 def measured_peak_gbs():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -545,7 +579,8 @@ def main():
         },
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak, "traffic": launch_traffic(args.workload, n_ops * args.steps),
+                     "peak_kind": peak_kind,
                      "kernel": "gpuos_executor_kernel", "kernel_ms": kern_ms,
                      "device_busy_ms": busy_ns / 1e6},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},

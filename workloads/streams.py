@@ -384,7 +384,7 @@ def stream_c2l(n_desc: int = 4000, pool_elems: int = 1 << 27, seed: int = 6) -> 
     return stream_elementwise("c2l", n_desc, 65536, 1 << 20, 0.0, pool_elems, seed)
 
 
-def stream_c3(n_desc: int = 50_000, pool_elems: int = 1 << 26, seed: int = 3,
+def stream_c3(n_desc: int = 50_000, pool_elems: int = 1 << 27, seed: int = 3,
               hiddens: Sequence[int] = (1024, 2048, 4096), max_rows: int = 64) -> Stream:
     """Row-op stream: softmax, LayerNorm, row sum/max/min over bf16 [R, H].
 
