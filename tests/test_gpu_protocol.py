@@ -154,6 +154,35 @@ def test_fence_orders_after_all_earlier():
     assert h["t_start_dev_ns"][2] >= h["t_done_dev_ns"][1]
 
 
+def test_fence_cuts_batches_at_any_position():
+    """FENCE descriptors anywhere in a full ring (the sequencer takes up to 128
+    descriptors a batch, read in two halves of 64): each one is published and
+    starts only after every earlier descriptor completed, including at the
+    half and batch boundaries."""
+    g = G()
+    big, keep = _big_add(1 << 20)
+    n = 300
+    d = g.make_descs(n)
+    d[:] = big[0]
+    fences = [1, 63, 64, 65, 127, 128, 129, 191, 192, 255, 299]
+    for i in fences:
+        d["flags"][i] = g.FLAG_FENCE
+    ex = g.Executor(ring_entries=512, deferred_start=1)
+    try:
+        h = ex.set_history(0, n)
+        ex.submit_batch(d)
+        ex.start()
+        ex.sync(timeout_ms=30_000)
+    finally:
+        assert ex.shutdown() == 0
+    assert (h["status"] == 0).all() and (h["ticket"] == np.arange(n)).all()
+    done = h["t_done_dev_ns"]
+    for i in fences:
+        assert h["t_publish_dev_ns"][i] >= done[:i].max(), i
+        assert h["t_start_dev_ns"][i] >= done[:i].max(), i
+    assert bool((keep[2] == 2.0).all())
+
+
 def test_device_bounds_checks_return_status():
     """Descriptors that pass the host checks but carry bad positions or
     lengths in device memory complete with GPUOS_ST_BAD_ARGS."""
