@@ -121,10 +121,11 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
                    "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
 TRAFFIC = {
-    "c2": dict(bytes=249_449_728, descs=4096, sources="b6db7b5a084e60fd"),
-    "c2l": dict(bytes=996_640_000, descs=400, sources="b6db7b5a084e60fd"),
-    "c4": dict(bytes=30_830_919_000, descs=600, sources="b6db7b5a084e60fd"),
-    "c5": dict(bytes=493_404_160, descs=224, sources="b6db7b5a084e60fd"),
+    "c2": dict(bytes=249_464_832, descs=4096, sources="5daa6d1650495ac2"),
+    "c2l": dict(bytes=998_394_368, descs=400, sources="5daa6d1650495ac2"),
+    "c3": dict(bytes=400_407_296, descs=2048, sources="5daa6d1650495ac2"),
+    "c4": dict(bytes=30_850_434_000, descs=600, sources="5daa6d1650495ac2"),
+    "c5": dict(bytes=493_723_136, descs=224, sources="5daa6d1650495ac2"),
 }
 
 

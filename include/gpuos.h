@@ -176,7 +176,8 @@ typedef struct gpuos_record {
     uint32_t version;           /* operator-table version the descriptor ran with */
     uint64_t t_commit_host_ns;  /* host clock just before the commit store-release */
     uint64_t t_dispatch_dev_ns; /* when the executor saw the commit (picked it off the ring) */
-    uint64_t t_publish_dev_ns;  /* when its tiles were published to the work queue */
+    uint64_t t_publish_dev_ns;  /* when its batch was handed to the work queue (just before
+                                   its entries were written) */
     uint64_t t_start_dev_ns;    /* when a warp began its tile 0 (dependencies met) */
     uint64_t t_done_dev_ns;     /* when its last tile finished */
 } gpuos_record;

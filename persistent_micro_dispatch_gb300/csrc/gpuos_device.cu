@@ -1870,6 +1870,14 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                 seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
             continue;
         }
+        /* the batch's publication time, stored before the fence below like
+         * the mirror writes: a worker that finds an entry of the batch (and
+         * so may complete its descriptor) sees it */
+#pragma unroll
+        for (int h = 0; h < SEQ_POLL; h++) {
+            const uint32_t pos = lane + 32u * h;
+            if (pos < k) *reinterpret_cast<volatile uint64_t *>(p.t_pub + (uint32_t)((s + pos) & p.ring_mask)) = t_b;
+        }
         /* every lane's mirror writes happen-before every lane's fence */
         __syncwarp();
         __threadfence();
@@ -1950,7 +1958,6 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             const uint32_t pos = lane + 32u * h;
             const uint64_t my_t = s + pos;
             const uint32_t slot = (uint32_t)(my_t & p.ring_mask);
-            if (pos < k && status[h] == GPUOS_ST_OK) *reinterpret_cast<volatile uint64_t *>(p.t_pub + slot) = t_pub;
             /* descriptors that failed validation complete at once */
             if (pos < k && status[h] != GPUOS_ST_OK) complete_desc(p, my_t, slot, status[h], version);
         }
