@@ -1,0 +1,132 @@
+"""The comparison rules the GPU parity tests apply (CPU). Candidate results
+are held on the host: the oracle's own final buffers, which must pass, and
+copies of them with one planted error each, which must fail (bit-exact ops
+by one bit, tolerance ops just past their bound) or pass (just inside it)."""
+import numpy as np
+import pytest
+
+from oracle.interp import Machine
+from tests.gpu_harness import final_output_ops
+from tests.parity import Report, compare_op
+from workloads import streams as S
+
+
+@pytest.fixture(scope="module")
+def state():
+    s = S.stream_mixed_small()
+    m = Machine(s)
+    m.run(keep=range(len(s.ops)))
+    return s, m
+
+
+class HostCandidate:
+    """Candidate results on the host (a copy of the oracle's final buffers)."""
+
+    def __init__(self, m):
+        self.buf = [b.copy() for b in m.buf]
+
+    def read(self, ref, n):
+        return self.buf[ref.buf][ref.off:ref.off + n].copy()
+
+
+def _compare(s, m, cand, idx):
+    rep = Report()
+    for j in idx:
+        compare_op(rep, s, j, cand.read, m)
+    return rep
+
+
+def _first(s, pred):
+    idx = final_output_ops(s, range(len(s.ops)))
+    return next(j for j in idx if pred(s.ops[j]))
+
+
+def _set_bf16(cand, ref, k, value):
+    cand.buf[ref.buf][ref.off + k] = S.f32_to_bf16_bits(np.array([value], np.float32))[0]
+
+
+def test_oracle_results_pass_against_themselves(state):
+    s, m = state
+    idx = final_output_ops(s, range(len(s.ops)))
+    rep = _compare(s, m, HostCandidate(m), idx)
+    assert rep.ok(), rep.failures
+    assert rep.exact > 0 and rep.tol > 0
+
+
+def test_bit_exact_op_rejects_one_flipped_bit(state):
+    s, m = state
+    j = _first(s, lambda o: o.op == "add" and o.dtype == "f32" and o.dims[0] > 0)
+    cand = HostCandidate(m)
+    o = s.ops[j]
+    cand.buf[o.out.buf].view(np.uint32)[o.out.off + 5] ^= 1
+    rep = _compare(s, m, cand, [j])
+    assert not rep.ok() and "bit-exact" in rep.failures[0]
+
+
+def test_bf16_tolerance_is_two_hundredths_absolute(state):
+    s, m = state
+    j = _first(s, lambda o: o.op == "softmax")
+    o = s.ops[j]
+    r = m.exact[j]["out"]
+    k = int(np.argmin(np.abs(r)))  # a small value: its bf16 ulp is far below 2e-2
+    for delta, ok in ((0.012, True), (0.03, False)):
+        cand = HostCandidate(m)
+        _set_bf16(cand, o.out, k, r[k] + delta)
+        assert _compare(s, m, cand, [j]).ok() == ok, delta
+
+
+def test_bf16_tolerance_widens_to_one_ulp_for_large_values():
+    # exact values just above grid points of magnitude 5 and 10 (bf16 ulp
+    # 2^-5 and 2^-4): the grid neighbour above is more than 2e-2 but at
+    # most one ulp away and passes; two steps below fails
+    from tests.parity import check_bf16
+    o = S.Op("layernorm")
+    r = np.array([5.001, -10.002, 0.25])
+    ulp = np.array([2.0 ** -5, 2.0 ** -4, 2.0 ** -9])
+    near = np.array([5.0 + ulp[0], -10.0 - ulp[1], 0.25 + 0.015])
+    far = np.array([5.0 - 2 * ulp[0], -10.0 + 2 * ulp[1], 0.25])
+    bits = lambda v: S.f32_to_bf16_bits(v.astype(np.float32))
+    assert (np.abs(near - r)[:2] > 2e-2).all() and (np.abs(near - r)[:2] <= ulp[:2]).all()
+    rep = Report()
+    assert check_bf16(rep, 0, o, bits(near), r)
+    assert rep.ulp_branch == 2
+    assert not check_bf16(Report(), 0, o, bits(far), r)
+
+
+def test_fp32_tolerance_is_relative(state):
+    s, m = state
+    j = _first(s, lambda o: o.op == "gelu" and o.dtype == "f32")
+    o = s.ops[j]
+    r = m.exact[j]["out"]
+    k = int(np.argmax(np.abs(r)))
+    for rel, ok in ((5e-6, True), (3e-5, False)):
+        cand = HostCandidate(m)
+        cand.buf[o.out.buf][o.out.off + k] = np.float32(r[k] * (1 + rel))
+        assert _compare(s, m, cand, [j]).ok() == ok, rel
+
+
+def test_kv_cache_rows_are_compared_bit_exactly(state):
+    s, m = state
+    j = _first(s, lambda o: o.op == "kv_write" and o.dims[2] == 128)
+    o = s.ops[j]
+    B, H, D, Lc = o.dims[:4]
+    p = int(m.view(o.aux0, B)[0]) - 1
+    cand = HostCandidate(m)
+    cand.buf[o.out.buf][o.out.off + p * D + 3] ^= 1  # (b=0, h=0) row, one bit of one element
+    assert not _compare(s, m, cand, [j]).ok()
+
+
+def test_row_max_is_exact_and_row_sum_within_bound(state):
+    s, m = state
+    j = _first(s, lambda o: o.op == "rowmax")
+    o = s.ops[j]
+    cand = HostCandidate(m)
+    cand.buf[o.out.buf][o.out.off] ^= 1
+    assert not _compare(s, m, cand, [j]).ok()
+    j = _first(s, lambda o: o.op == "rowsum")
+    o = s.ops[j]
+    r = m.exact[j]["out"]
+    for delta, ok in ((0.015, True), (0.05, False)):
+        cand = HostCandidate(m)
+        cand.buf[o.out.buf][o.out.off] = np.float32(r[0] + delta)
+        assert _compare(s, m, cand, [j]).ok() == ok, delta
