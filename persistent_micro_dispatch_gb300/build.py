@@ -1,7 +1,7 @@
 """Build the C-ABI library ``libgpuos.so`` (and the injectable op cubin) in-tree.
 
 Only sm_103a is targeted. nvcc cross-compiles without a GPU, so this runs on
-any machine with CUDA 13; the GPU machine rebuilds for its own host architecture.
+any machine with CUDA 13; each machine rebuilds it for its own host architecture.
 Translation units compile in parallel; the whole build takes well under a
 minute.
 """
