@@ -130,3 +130,51 @@ def test_row_max_is_exact_and_row_sum_within_bound(state):
         cand = HostCandidate(m)
         cand.buf[o.out.buf][o.out.off] = np.float32(r[0] + delta)
         assert _compare(s, m, cand, [j]).ok() == ok, delta
+
+
+def _chain_stream():
+    """bf16 GELU feeding a bf16 add (the add's input comes from an op whose
+    own result is only within tolerance)."""
+    rng = np.random.default_rng(21)
+    s = S.Stream("chain")
+    n = 512
+    ix = s.add_buf("x", "bf16", n, S.f32_to_bf16_bits(rng.standard_normal(n, dtype=np.float32)))
+    iy = s.add_buf("y", "bf16", n, S.f32_to_bf16_bits(rng.standard_normal(n, dtype=np.float32)))
+    ig = s.add_buf("g", "bf16", n)
+    iz = s.add_buf("z", "bf16", n)
+    s.ops.append(S.Op("gelu", "bf16", a=S.Ref(ix), out=S.Ref(ig), dims=(n,)))
+    s.ops.append(S.Op("add", "bf16", a=S.Ref(ig), b=S.Ref(iy), out=S.Ref(iz), dims=(n,), deps=(0,)))
+    S.check_hazards(s)
+    return s
+
+
+def test_rounding_carried_along_a_chain_is_allowed_and_errors_are_not():
+    s = _chain_stream()
+    m = Machine(s)
+    m.run(keep=range(len(s.ops)))
+    f32 = lambda bits: S.bf16_bits_to_f32(bits)  # noqa: E731
+    g_ref, y, z_ref = s.ops[1].a, s.ops[1].b, s.ops[1].out
+    # a candidate whose GELU rounded one element the other way (one bf16
+    # ulp, within tolerance), and whose add is exact on that input
+    exact = m.exact[0]["out"]
+    yv = f32(m.buf[y.buf])
+    for k in np.argsort(-np.abs(exact)):
+        if abs(exact[k]) >= 2.0:  # keep the bf16 ulp <= 2^-7
+            continue
+        cand = HostCandidate(m)
+        g = cand.buf[g_ref.buf]
+        gk = float(f32(g[k:k + 1])[0])
+        # the grid neighbour on the other side of the exact value (within one ulp)
+        g[k] = g[k] + 1 if (exact[k] > gk) == (gk >= 0) else g[k] - 1
+        z = S.f32_to_bf16_bits(f32(g) + yv)
+        if z[k] != m.buf[z_ref.buf][k]:  # the perturbation reaches the add's result
+            break
+    assert z[k] != m.buf[z_ref.buf][k]
+    assert abs(float(f32(g[k:k + 1])[0]) - exact[k]) <= 2.0 ** -7
+    cand.buf[z_ref.buf][:] = z
+    rep = _compare(s, m, cand, [0, 1])
+    assert rep.ok(), rep.failures
+    # the same candidate with a wrong sum on another element
+    k2 = (k + 7) % z.size
+    cand.buf[z_ref.buf][k2] = S.f32_to_bf16_bits(np.array([float(f32(z[k2:k2 + 1])[0]) + 0.1], np.float32))[0]
+    assert not _compare(s, m, cand, [0, 1]).ok()
