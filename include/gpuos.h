@@ -222,23 +222,32 @@ typedef struct gpuos_tile_profile {
 
 typedef struct gpuos_ctx gpuos_ctx;
 
-/* Fill *cfg with defaults. */
+/* Fill *cfg with defaults. Source: GPUOS page, §3 Q2 "1. Ring Buffer
+ * Communication Channel" (4096 ring entries by default) and "2. Persistent
+ * Kernel Executor" (one block per SM; spin under load, exponential backoff
+ * when idle). */
 GPUOS_API void gpuos_default_config(gpuos_config *cfg);
 
 /* Allocate the ring, completion records and operator table, fill both table
  * slots with the built-in ops (version 0) and launch the executor once on a
  * non-blocking stream (grid = blocks, block = 32 * warps_per_block). *out
- * receives the context. Errors: EINVAL (bad config), ECUDA, ENOMEM. */
+ * receives the context. Errors: EINVAL (bad config), ECUDA, ENOMEM.
+ * Source: GPUOS page, §1 and §3 Q2 "2. Persistent Kernel Executor" (the
+ * persistent kernel is launched once when the process starts, one block per
+ * SM) with the ring of "1. Ring Buffer Communication Channel" and the table
+ * of "3. Dynamic Operator Table"; the name gpuos_init is this library's. */
 GPUOS_API int gpuos_init(const gpuos_config *cfg, gpuos_ctx **out);
 
 /* Launch the executor of a context made with deferred_start (once). Lets a
  * caller fill the ring first (a bounded, replayable run for profilers) or put
  * the single launch inside a timed region. Errors: EINVAL (already started),
- * ECUDA. */
+ * ECUDA. Source: the single launch of GPUOS page §3 Q2 "2. Persistent Kernel
+ * Executor", split from gpuos_init; the page has no separate start step. */
 GPUOS_API int gpuos_start(gpuos_ctx *ctx);
 
 /* The non-blocking stream the executor runs on (a cudaStream_t), so callers
- * can bracket the kernel with CUDA events. */
+ * can bracket the kernel with CUDA events. Measurement only; the page has no
+ * counterpart. */
 GPUOS_API int gpuos_executor_stream(gpuos_ctx *ctx, void **stream);
 
 /* Submit one descriptor (§3 Q2 ring protocol: acquire slot, write, commit
@@ -261,26 +270,40 @@ GPUOS_API int gpuos_submit(gpuos_ctx *ctx, const gpuos_desc *d, uint64_t *ticket
 
 /* Submit count descriptors in order (same as count gpuos_submit calls);
  * *first_ticket receives the first ticket. Stops at the first failure and
- * returns its code; *n_done (may be NULL) receives how many were submitted. */
+ * returns its code; *n_done (may be NULL) receives how many were submitted.
+ * Source: the host half of GPUOS page §3 Q2 "1. Ring Buffer Communication
+ * Channel" (acquire slot, write, commit with a store-release), once per
+ * descriptor. With one producer the call writes the bodies of a run of
+ * consecutive descriptors, then one release fence, then their commit words:
+ * every commit still follows its own body, as the protocol requires. */
 GPUOS_API int gpuos_submit_batch(gpuos_ctx *ctx, const gpuos_desc *d, uint32_t count, uint64_t *first_ticket,
                        uint32_t *n_done, uint32_t timeout_us);
 
 /* Wait until `ticket` (or, with ticket == UINT64_MAX, everything submitted so
- * far) has completed, up to timeout_ms. Returns EDEVICE if any descriptor
+ * far) has completed, up to timeout_ms. Source: the device's "release slot"
+ * step of GPUOS page §3 Q2 "1. Ring Buffer Communication Channel" is a
+ * store-release of the ticket's completion record, which this call reads
+ * with load-acquire; the name gpuos_sync is this library's. Returns EDEVICE if any descriptor
  * harvested by this call completed with a nonzero status, ETIMEDOUT on
  * timeout, ESTOPPED if the executor left with work outstanding. */
 GPUOS_API int gpuos_sync(gpuos_ctx *ctx, uint64_t ticket, uint32_t timeout_ms);
 
 /* Completion record of a finished ticket still in the history window (the
  * last `ring_entries` tickets, or the whole run with gpuos_set_history).
- * Errors: EAGAIN (not finished yet), EINVAL (outside the window). */
+ * Errors: EAGAIN (not finished yet), EINVAL (outside the window). Source:
+ * the completion ("release slot") of GPUOS page §3 Q2 "1. Ring Buffer
+ * Communication Channel", with the timestamps the latency breakdown of §3 Q3
+ * needs. */
 GPUOS_API int gpuos_query(gpuos_ctx *ctx, uint64_t ticket, gpuos_record *rec);
 
 /* Keep every harvested completion record of tickets [base, base + capacity)
- * in caller memory (host), for latency statistics. buf may be NULL to stop. */
+ * in caller memory (host), for latency statistics (GPUOS page §3 Q3, latency
+ * breakdown). buf may be NULL to stop. */
 GPUOS_API int gpuos_set_history(gpuos_ctx *ctx, gpuos_record *buf, uint64_t base, uint64_t capacity);
 
-/* Add an operator module: a relocatable sm_103a cubin (nvcc -cubin
+/* Source: GPUOS page §3 Q2 "3. Dynamic Operator Table", step (2): load the
+ * operator's module through the CUDA Driver API.
+ * Add an operator module: a relocatable sm_103a cubin (nvcc -cubin
  * -rdc=true; the bytes are copied) that defines device functions with the op
  * signature and `__device__` variables holding their addresses. At
  * gpuos_start the library links every added module with its relocatable
@@ -328,15 +351,22 @@ GPUOS_API const char *gpuos_op_header(void);
 GPUOS_API int gpuos_register_op(gpuos_ctx *ctx, uint16_t op_id, const void *image, size_t len,
                       const char *fnptr_symbol);
 
-/* Point op_id back at a built-in op or an earlier registered function:
+/* Source: GPUOS page §3 Q2 "3. Dynamic Operator Table", steps (4) and (5)
+ * (write the inactive slot, flip the version counter), with an entry that is
+ * already in the table.
+ * Point op_id back at a built-in op or an earlier registered function:
  * `source_op` names the entry to copy from the active table. Same flip and
  * grace-period protocol as gpuos_register_op. */
 GPUOS_API int gpuos_alias_op(gpuos_ctx *ctx, uint16_t op_id, uint16_t source_op);
 
-/* Live counters (host and device). */
+/* Live counters (host and device): polls, sleeps, tiles, sequencer phase
+ * times. Measurement only (the poll loop and backoff of GPUOS page §3 Q2
+ * "2. Persistent Kernel Executor"); the page has no counterpart. */
 GPUOS_API int gpuos_stats(gpuos_ctx *ctx, gpuos_stats_t *st);
 
-/* NOP ping-pong: `pings` round trips. Each commits a NOP (host clock t0)
+/* Source: measurement of the dispatch latency of GPUOS page §3 Q3 (latency
+ * breakdown: ~100 ns dispatch); the page has no calibration step.
+ * NOP ping-pong: `pings` round trips. Each commits a NOP (host clock t0)
  * and spins until the executor's echo of the time it saw the commit appears
  * in the ticket's record (host clock t1; the echo is written the moment the
  * commit is seen, before the descriptor is read). Since the device sees the
@@ -350,17 +380,25 @@ GPUOS_API int gpuos_calibrate(gpuos_ctx *ctx, uint32_t pings, int64_t *off_lo, i
 
 /* Drain (wait for everything submitted, up to timeout_ms), set the stop flag
  * and wait (up to timeout_ms) for the executor kernel to end; the context
- * stays valid (stats, queries) but accepts no more work. */
+ * stays valid (stats, queries) but accepts no more work. Source: none; the
+ * executor of GPUOS page §3 Q2 "2. Persistent Kernel Executor" never exits
+ * while the process lives, and this call is how a process ends it. */
 GPUOS_API int gpuos_stop(gpuos_ctx *ctx, uint32_t timeout_ms);
 
-/* gpuos_stop, then free everything. The context is freed even on error. */
+/* gpuos_stop, then free everything. The context is freed even on error.
+ * Source: none on the page (see gpuos_stop); the name gpuos_shutdown is this
+ * library's. */
 GPUOS_API int gpuos_shutdown(gpuos_ctx *ctx, uint32_t timeout_ms);
 
 /* Sum the worker warps' tile profiles (a snapshot; exact once the executor
- * has left). Errors: EINVAL, ECUDA. */
+ * has left). Errors: EINVAL, ECUDA. Measurement only (where per-op time goes,
+ * GPUOS page §3 Q3 latency breakdown); the page has no counterpart. */
 GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
 
-/* Host tiling rule of a built-in op (what ntiles the library will write);
+/* Source: the page's executor runs one descriptor per warp (GPUOS page §3 Q2
+ * "2. Persistent Kernel Executor"); its §4 critique notes the missing
+ * multi-block cooperation, which this split into warp tiles supplies.
+ * Host tiling rule of a built-in op (what ntiles the library will write);
  * one tile is one warp's unit of work:
  *   add/mul/relu/gelu  ceil(n / te), te the smallest power of two >= n / 16
  *                      within [4096 (GELU: 1024), 4096 (f32) or 8192 (bf16)]
@@ -379,12 +417,16 @@ GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
  * Returns GPUOS_EINVAL for a descriptor the library would reject. */
 GPUOS_API int gpuos_op_ntiles(const gpuos_desc *d, uint32_t *ntiles);
 
-/* Workspace bytes a decode-SDPA descriptor needs: one uint32 counter per
+/* Source: the SDPA op of GPUOS page §3 Q2, operator library (attention);
+ * the page gives no workspace, which the split-K form here needs.
+ * Workspace bytes a decode-SDPA descriptor needs: one uint32 counter per
  * (b, h), rounded up to 4, then fp32 partials for the finest split (32-row
  * chunks). */
 GPUOS_API size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, uint32_t Lmax);
 
-/* Eager baseline: launch the same op bodies as ordinary kernels, one
+/* Source: the eager baseline of GPUOS page §3 Q3 (Table 2, latency
+ * breakdown: one kernel launch per operation).
+ * Eager baseline: launch the same op bodies as ordinary kernels, one
  * cudaLaunchKernel per descriptor (one warp per tile, one warp per block), in
  * order, on `stream` (a cudaStream_t; 0 = legacy default), with stage_bytes
  * of shared-memory staging per warp as in gpuos_config. Deps are implied by
@@ -400,7 +442,11 @@ GPUOS_API int gpuos_eager_run(const gpuos_desc *d, uint32_t count, uint32_t stag
  * front. It computes what GPUOS_OP_SDPA computes (same op body, one launch on
  * `stream`, a cudaStream_t, 0 = legacy default) with inputs and output given
  * as for that op: q[B][H][D], caches Kc/Vc [B][H][Lcap][D] bf16, lens i32[B]
- * in device memory, out[B][H][D] bf16; all 16-byte aligned; D = 128. The
+ * in device memory, out[B][H][D] bf16; all 16-byte aligned; D = 128. Every
+ * lens[b] must lie in [1, Lmax]: the lengths stay in device memory, which the
+ * call does not read on the host, so a request whose length is outside that
+ * range is not detected; its heads' outputs are left unwritten and the call
+ * still returns GPUOS_OK. The
  * split-K scratch is a fixed device array inside the library (about 2 MiB per
  * device, held until the process exits) instead of a caller workspace; it
  * bounds B * H <= 256 and Lmax <= 4096, and larger sizes return
@@ -415,10 +461,12 @@ GPUOS_API int gpuos_sdpa_noalloc(const void *q, const void *Kc, const void *Vc, 
                                  uint32_t B, uint32_t H, uint32_t D, uint32_t Lcap, uint32_t Lmax, float scale,
                                  void *stream);
 
-/* CLOCK_REALTIME in ns (the host clock of gpuos_record). */
+/* CLOCK_REALTIME in ns (the host clock of gpuos_record). Measurement only;
+ * the page has no counterpart. */
 GPUOS_API uint64_t gpuos_host_now_ns(void);
 
-/* Text for a return code or, with is_status != 0, a device status. */
+/* Text for a return code or, with is_status != 0, a device status. The page
+ * has no counterpart. */
 GPUOS_API const char *gpuos_strerror(int code, int is_status);
 
 #ifdef __cplusplus

@@ -13,6 +13,14 @@ a first-order bound of that input difference carried through the op
 (|d(a+b)| <= |da|+|db|, |d(ab)| <= |da||b|+|db||a|, |dGELU| <= 1.13|dx|,
 the LayerNorm, softmax, vecmat and attention bounds in propagated_bound) is
 added to its tolerance. The expected value is always the oracle's.
+
+Widening is allowed only from producers that were themselves compared, and
+passed, in the same report, and only for inputs read as they stood when the
+consumer ran: if a differing input range has a writer that was not compared
+(or failed), or a writer after the consumer that the reader cannot undo, the
+consumer fails ("widening from an unchecked producer"). A reader (the
+``gpu_read`` callable) may expose ``timed(buf) -> bool`` to say that it
+returns a buffer as it stood right after the op being compared.
 """
 from __future__ import annotations
 
@@ -45,6 +53,7 @@ class Report:
         self.failures = []
         self.max_abs = 0.0
         self.max_rel = 0.0
+        self.passed = set()  # ops compared in this report without a failure
 
     def fail(self, j, o, msg):
         if len(self.failures) < 20:
@@ -69,38 +78,80 @@ def written_buffers(s: Stream) -> set:
 
 
 _BUCKET = 1 << 16
+_BIG = 8  # writes spanning more buckets than this are listed per buffer
+
+
+def _write_index(s: Stream):
+    """(buckets, big): small writes by (buffer, 64 K-element bucket), and
+    writes spanning more than _BIG buckets by buffer; entries (lo, hi, op)."""
+    idx = getattr(s, "_wr_index", None)
+    if idx is None:
+        buckets, big = {}, {}
+        for i, o in enumerate(s.ops):
+            for (bb, l2, h2, w) in op_accesses(s, o):
+                if not w:
+                    continue
+                k0, k1 = l2 // _BUCKET, (h2 - 1) // _BUCKET
+                if k1 - k0 > _BIG:
+                    big.setdefault(bb, []).append((l2, h2, i))
+                else:
+                    for k in range(k0, k1 + 1):
+                        buckets.setdefault((bb, k), []).append((l2, h2, i))
+        idx = s._wr_index = (buckets, big)
+    return idx
+
+
+def _overlapping_writes(s: Stream, b: int, lo: int, hi: int):
+    buckets, big = _write_index(s)
+    for (l2, h2, i) in big.get(b, ()):
+        if l2 < hi and lo < h2:
+            yield i
+    for k in range(lo // _BUCKET, (hi - 1) // _BUCKET + 1):
+        for (l2, h2, i) in buckets.get((b, k), ()):
+            if l2 < hi and lo < h2:
+                yield i
 
 
 def written_before(s: Stream, b: int, lo: int, hi: int, j: int) -> bool:
     """Does some op i < j write an element of [lo, hi) of buffer b?"""
-    idx = getattr(s, "_wr_index", None)
-    if idx is None:
-        idx = {}
-        for i, o in enumerate(s.ops):
-            for (bb, l2, h2, w) in op_accesses(s, o):
-                if w:
-                    for k in range(l2 // _BUCKET, (h2 - 1) // _BUCKET + 1):
-                        idx.setdefault((bb, k), []).append((l2, h2, i))
-        s._wr_index = idx
-    for k in range(lo // _BUCKET, (hi - 1) // _BUCKET + 1):
-        for (l2, h2, i) in idx.get((b, k), ()):
-            if i < j and l2 < hi and lo < h2:
-                return True
-    return False
+    return any(i < j for i in _overlapping_writes(s, b, lo, hi))
 
 
-def _inputs_identical(s: Stream, o: Op, gpu_read, mach) -> bool:
-    """Are every input range's bytes the same on the GPU and in the oracle?
-    Inputs no earlier op wrote are identical by construction (the seeded
-    inputs); others are compared as they stand after the run."""
+def writers_of(s: Stream, b: int, lo: int, hi: int) -> list:
+    """Every op that writes an element of [lo, hi) of buffer b, in order."""
+    return sorted(set(_overlapping_writes(s, b, lo, hi)))
+
+
+def _differing_inputs(s: Stream, o: Op, gpu_read, mach) -> list:
+    """Input ranges (buf, lo, hi) whose bytes differ between the GPU and the
+    oracle. Inputs no earlier op wrote are identical by construction (the
+    seeded inputs); others are compared as the reader returns them."""
     j = mach._op_index[id(o)]
+    diff = []
     for (b, lo, hi, w) in op_accesses(s, o):
         if w or not written_before(s, b, lo, hi, j):
             continue
         g = gpu_read(Ref(b, lo), hi - lo)
         r = mach.buf[b][lo:hi]
         if not np.array_equal(g.view(np.uint8), r.view(np.uint8)):
-            return False
+            diff.append((b, lo, hi))
+    return diff
+
+
+def _widening_sources_ok(rep: Report, s: Stream, j: int, o: Op, diff: list, gpu_read) -> bool:
+    """Every differing input of op j must come from producers compared (and
+    passed) in this report, read as it stood when op j ran."""
+    timed = getattr(gpu_read, "timed", None)
+    for (b, lo, hi) in diff:
+        for i in writers_of(s, b, lo, hi):
+            if i < j and i not in rep.passed:
+                rep.fail(j, o, f"widening from an unchecked producer: op {i} ({s.ops[i].op}) "
+                               f"writes buffer {s.buffers[b].name}")
+                return False
+            if i > j and not (timed is not None and timed(b)):
+                rep.fail(j, o, f"widening from an unchecked producer: input buffer {s.buffers[b].name} "
+                               f"is rewritten after the op by op {i} ({s.ops[i].op})")
+                return False
     return True
 
 
@@ -215,6 +266,15 @@ def mach_index(mach, o):
 
 
 def compare_op(rep: Report, s: Stream, j: int, gpu_read, mach) -> None:
+    """Compare op j (see _compare_op_body); record it as passed when it added
+    no failure."""
+    before = len(rep.failures)
+    _compare_op_body(rep, s, j, gpu_read, mach)
+    if len(rep.failures) == before:
+        rep.passed.add(j)
+
+
+def _compare_op_body(rep: Report, s: Stream, j: int, gpu_read, mach) -> None:
     """Compare op j's outputs on the GPU (read via gpu_read(ref, n)) with the
     oracle machine state after it applied op j (exact results in mach.exact[j]).
 
@@ -231,7 +291,10 @@ def compare_op(rep: Report, s: Stream, j: int, gpu_read, mach) -> None:
     if o.op == "nop":
         rep.exact += 1
         return
-    same_in = _inputs_identical(s, o, gpu_read, mach)
+    diff = _differing_inputs(s, o, gpu_read, mach)
+    same_in = not diff
+    if not same_in and not _widening_sources_ok(rep, s, j, o, diff, gpu_read):
+        return
     extra = 0.0 if same_in else propagated_bound(s, o, gpu_read, mach)
     if o.op in ("add", "mul", "relu", "gelu"):
         n = d[0]

@@ -9,8 +9,8 @@ import numpy as np
 import pytest
 
 from oracle.interp import Machine
-from tests.gpu_harness import (check_canaries, compare_stream, ensure_built, final_output_ops, need_gpu,
-                               run_executor, sample)
+from tests.gpu_harness import (check_canaries, check_kv_copies, compare_in_order, compare_stream, ensure_built,
+                               final_output_ops, need_gpu, run_executor, sample)
 from workloads import streams as S
 
 pytestmark = pytest.mark.gpu
@@ -23,6 +23,10 @@ def _setup():
 
 
 def _run_and_compare(s, check=None, sample_k=None, cfg=None, skip=None, seed=0):
+    """Run the stream on the executor, then compare with the oracle op by op
+    (each op against the GPU's result as it stood right after it). check /
+    sample_k pick target ops (the oracle then applies them and what they
+    depend on, and checks every comparable op it applies)."""
     from workloads.device import DeviceStream
     S.check_hazards(s)
     ds = DeviceStream(s)
@@ -30,17 +34,10 @@ def _run_and_compare(s, check=None, sample_k=None, cfg=None, skip=None, seed=0):
     st, hist = run_executor(ds, descs, **(cfg or {}))
     assert np.all(hist["status"] == 0), f"device status: {np.unique(hist['status'])}"
     assert st["completed"] == len(s.ops)
-    cand = final_output_ops(s, range(len(s.ops)) if check is None else check)
+    targets = check
     if sample_k is not None:
-        cand = sample(cand, sample_k, seed)
-    mach = Machine(s)
-    if sample_k is None and skip is None:
-        mach.run(keep=cand)
-    elif skip is not None:
-        mach.run(keep=cand, skip=[j for j in skip if j not in set(cand)])
-    else:
-        mach.run_closure(cand)
-    rep = compare_stream(s, ds, mach, cand)
+        targets = sample(final_output_ops(s, range(len(s.ops))), sample_k, seed)
+    rep, mach = compare_in_order(s, ds, targets=targets, skip=skip or ())
     print(f"{s.name}: {rep.summary()} stats={st}")
     assert rep.ok(), "\n".join(rep.failures)
     return s, ds, rep, st, hist
@@ -77,31 +74,7 @@ def test_c3_row_ops_small():
 def test_c4_decode_small_and_kv_copy_bit_exact():
     """20 decode steps at full shapes (B<=8, 32x128, caches of 4,096 rows)."""
     s, ds, rep, st, hist = _run_and_compare(S.stream_c4(n_steps=20))
-    _check_kv_copies(s, ds)
-
-
-def _check_kv_copies(s, ds):
-    """Replay every KV write with the GPU's own (rotated) k/v rows on the
-    initial caches: the GPU caches must equal the result byte for byte."""
-    caches = {}
-    for o in s.ops:
-        if o.op != "kv_write":
-            continue
-        for ref in (o.out, o.aux1):
-            if ref.buf not in caches:
-                caches[ref.buf] = s.buffers[ref.buf].data.copy()
-        B, H, D, Lc = o.dims[:4]
-        lens = s.buffers[o.aux0.buf].data[o.aux0.off:o.aux0.off + B]
-        k = ds.read(o.a, B * H * D).reshape(B, H, D)
-        v = ds.read(o.b, B * H * D).reshape(B, H, D)
-        K4 = caches[o.out.buf][o.out.off:o.out.off + B * H * Lc * D].reshape(B, H, Lc, D)
-        V4 = caches[o.aux1.buf][o.aux1.off:o.aux1.off + B * H * Lc * D].reshape(B, H, Lc, D)
-        for b in range(B):
-            K4[b, :, lens[b] - 1] = k[b]
-            V4[b, :, lens[b] - 1] = v[b]
-    assert caches, "no KV write in the stream"
-    for i, want in caches.items():
-        assert np.array_equal(ds.read_buf(i), want), s.buffers[i].name
+    check_kv_copies(s, ds)
 
 
 @pytest.mark.parametrize("stage_bytes", [16384, 0])
@@ -109,13 +82,13 @@ def test_mixed_small_every_op_kind(stage_bytes):
     """Every op kind at small, ragged sizes (tails, 1-row and 8-column tiles,
     ragged head groups, multi-chunk attention), staged and register paths."""
     s, ds, rep, st, hist = _run_and_compare(S.stream_mixed_small(), cfg=dict(stage_bytes=stage_bytes))
-    _check_kv_copies(s, ds)
+    check_kv_copies(s, ds)
 
 
 def test_c5_mixed_pipeline_small():
     """3 tokens of the 32-layer synthetic decoder at hidden 4,096."""
     s, ds, rep, st, hist = _run_and_compare(S.stream_c5(n_tokens=3))
-    _check_kv_copies(s, ds)
+    check_kv_copies(s, ds)
 
 
 def test_gelu_fp32_error_bound_sweep():

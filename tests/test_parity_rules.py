@@ -178,3 +178,90 @@ def test_rounding_carried_along_a_chain_is_allowed_and_errors_are_not():
     k2 = (k + 7) % z.size
     cand.buf[z_ref.buf][k2] = S.f32_to_bf16_bits(np.array([float(f32(z[k2:k2 + 1])[0]) + 0.1], np.float32))[0]
     assert not _compare(s, m, cand, [0, 1]).ok()
+
+
+# ---- widening only from checked producers ------------------------------------------
+class HostDS:
+    """Host stand-in for a device stream: reads from given final buffers."""
+
+    def __init__(self, s, bufs):
+        self.s, self.buf = s, bufs
+
+    def read(self, ref, n, dtype=None):
+        v = self.buf[ref.buf]
+        if dtype is not None:
+            v = v.view(S.NPTYPE[dtype])
+        return v[ref.off:ref.off + n].copy()
+
+
+def _perturbed_chain_candidate():
+    """The chain stream with a candidate whose GELU result is one bf16 ulp
+    off on one element (within tolerance) and whose add is exact on it."""
+    s = _chain_stream()
+    m = Machine(s)
+    m.run(keep=range(len(s.ops)))
+    f32 = S.bf16_bits_to_f32
+    g_ref, y, z_ref = s.ops[1].a, s.ops[1].b, s.ops[1].out
+    cand = HostCandidate(m)
+    g = cand.buf[g_ref.buf]
+    exact = m.exact[0]["out"]
+    k = int(np.argmin(np.abs(np.abs(exact) - 0.5)))
+    gk = float(f32(g[k:k + 1])[0])
+    g[k] = g[k] + 1 if (exact[k] > gk) == (gk >= 0) else g[k] - 1
+    cand.buf[z_ref.buf][:] = S.f32_to_bf16_bits(f32(g) + f32(m.buf[y.buf]))
+    return s, m, cand
+
+
+def test_widening_needs_the_producer_checked_first():
+    s, m, cand = _perturbed_chain_candidate()
+    rep = _compare(s, m, cand, [1])  # the consumer alone
+    assert not rep.ok() and "widening from an unchecked producer" in rep.failures[0]
+    rep = _compare(s, m, cand, [0, 1])  # producer first
+    assert rep.ok(), rep.failures
+
+
+def test_widening_from_a_failed_producer_is_refused():
+    s, m, cand = _perturbed_chain_candidate()
+    g_ref = s.ops[0].out
+    cand.buf[g_ref.buf][3] ^= 0x0100  # the producer itself now fails
+    rep = _compare(s, m, cand, [0, 1])
+    assert len(rep.failures) >= 2 and any("unchecked producer" in f for f in rep.failures)
+
+
+def test_widening_from_an_input_rewritten_later_is_refused():
+    """op 1 reads g after op 0 wrote it; op 2 rewrites g. At the end g no
+    longer holds what op 1 read, so op 1 cannot widen from it."""
+    rng = np.random.default_rng(5)
+    s = S.Stream("rewrite")
+    n = 256
+    ix = s.add_buf("x", "bf16", n, S.f32_to_bf16_bits(rng.standard_normal(n, dtype=np.float32)))
+    iy = s.add_buf("y", "bf16", n, S.f32_to_bf16_bits(rng.standard_normal(n, dtype=np.float32)))
+    ig = s.add_buf("g", "bf16", n)
+    iz = s.add_buf("z", "bf16", n)
+    s.ops.append(S.Op("gelu", "bf16", a=S.Ref(ix), out=S.Ref(ig), dims=(n,)))
+    s.ops.append(S.Op("add", "bf16", a=S.Ref(ig), b=S.Ref(iy), out=S.Ref(iz), dims=(n,), deps=(0,)))
+    s.ops.append(S.Op("relu", "bf16", a=S.Ref(iy), out=S.Ref(ig), dims=(n,), deps=(1,)))
+    S.check_hazards(s)
+    full = Machine(s)
+    full.run()
+    bufs = [b.copy() for b in full.buf]
+    bufs[iy][0] ^= 1  # differs from the oracle on an input op 1 reads...
+    bufs[ig][0] ^= 1  # ...and on the rewritten buffer
+    from tests.gpu_harness import compare_in_order
+    rep, _ = compare_in_order(s, HostDS(s, bufs), targets=[1])
+    assert not rep.ok()
+
+
+@pytest.mark.parametrize("make", [S.stream_mixed_small, lambda: S.stream_c4(n_steps=3),
+                                  lambda: S.stream_c5(n_tokens=1, n_layers=2)])
+def test_in_order_comparison_passes_the_oracle_own_results(make):
+    """Op by op against the GPU's result as it stood right after the op: the
+    oracle's own final buffers, given as the candidate, pass every op (KV
+    caches rebuilt from the candidate's k/v rows)."""
+    from tests.gpu_harness import compare_in_order
+    s = make()
+    full = Machine(s)
+    full.run()
+    rep, _ = compare_in_order(s, HostDS(s, [b.copy() for b in full.buf]))
+    assert rep.ok(), rep.failures
+    assert rep.checked >= len([o for o in s.ops if o.op != "nop"]) // 2

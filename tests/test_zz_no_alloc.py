@@ -6,8 +6,9 @@ comes) or under a memory budget fixed up front cannot hand the attention a
 freshly allocated workspace. This entry point keeps its split-K scratch in a
 fixed array inside the library. The test calls it twice in a row through the
 C ABI and checks each output against the workspace-based entry point
-(gpuos_eager_run with a GPUOS_OP_SDPA descriptor), within the bf16 rule the
-parity tests use; it also checks the size limit.
+(gpuos_eager_run with a GPUOS_OP_SDPA descriptor) and against the CPU
+oracle's decode attention, within the bf16 rule the parity tests use; it also
+checks the size limit.
 """
 import numpy as np
 import pytest
@@ -22,6 +23,20 @@ def _bf16_f64(t):
     import torch
     return t.view(torch.int16).cpu().numpy().view(np.uint16).astype(np.uint32).__lshift__(16).view(np.float32) \
         .astype(np.float64)
+
+
+def _oracle_sdpa(q, K, V, lens_list, B, H, D, Lcap, scale):
+    """The oracle's decode attention (double, unrounded) on host copies."""
+    import torch
+    from oracle.interp import lib as orc_lib
+    bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16).copy()  # noqa: E731
+    qh, Kh, Vh = bits(q), bits(K), bits(V)
+    lens = np.array(lens_list, np.int32)
+    out = np.empty(B * H * D, np.float64)
+    rc = orc_lib().orc_sdpa(qh.ctypes.data, Kh.ctypes.data, Vh.ctypes.data, lens.ctypes.data, B, H, D, Lcap,
+                            float(scale), out.ctypes.data)
+    assert rc == 0
+    return out
 
 
 def _workspace_path(G, q, K, V, lens, out, ws, B, H, D, Lcap, Lmax, scale, stream):
@@ -63,7 +78,11 @@ def test_sdpa_noalloc_matches_workspace_path_on_two_calls():
         st.synchronize()
         r = _bf16_f64(ref)
         x = _bf16_f64(got)
+        # against the workspace-based entry point
         assert np.all(np.abs(x - r) <= np.maximum(2e-2, ulp_bf16(r))), np.abs(x - r).max()
+        # against the oracle's exact value
+        exact = _oracle_sdpa(q, K, V, lens_list, B, H, D, Lcap, scale)
+        assert np.all(np.abs(x - exact) <= np.maximum(2e-2, ulp_bf16(exact))), np.abs(x - exact).max()
 
 
 def test_sdpa_noalloc_rejects_sizes_beyond_its_scratch():

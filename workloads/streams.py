@@ -67,8 +67,14 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     Used only to build bf16 *inputs* from float32 normal draws. Inputs are
     finite, so NaN handling is not needed here.
     """
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    # in 32-bit arithmetic: for a finite binary32 pattern (at most 0xFF7FFFFF)
+    # adding at most 0x8000 cannot wrap
+    r = u >> np.uint32(16)
+    r &= np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
     return r.astype(np.uint16)
 
 
