@@ -24,6 +24,7 @@
 #include <dlfcn.h>
 
 #include <atomic>
+#include <cstddef>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -157,14 +158,9 @@ uint64_t now_ns()
     return (uint64_t)ts.tv_sec * 1000000000ull + (uint64_t)ts.tv_nsec;
 }
 
-inline void cpu_relax()
-{
-#if defined(__aarch64__)
-    asm volatile("yield" ::: "memory");
-#else
-    std::atomic_signal_fence(std::memory_order_seq_cst);
-#endif
-}
+/* A spin-wait step: a compiler barrier, so every poll reloads memory (no
+ * architecture-specific hint, the same code on every host). */
+inline void cpu_relax() { std::atomic_signal_fence(std::memory_order_seq_cst); }
 
 template <typename T>
 T load_acq(const T *p)
@@ -725,10 +721,15 @@ static void harvest_one(gpuos_ctx *c, uint64_t t)
     const uint32_t slot = (uint32_t)(t & c->mask);
     uint64_t seen = __atomic_load_n(&c->hv[slot], __ATOMIC_ACQUIRE);
     if (seen >= t + 1) return;
-    /* one harvester per ticket: a producer reusing the slot and a sweeping
-     * thread may reach the same ticket together */
-    if (!__atomic_compare_exchange_n(&c->hv[slot], &seen, t + 1, false, __ATOMIC_ACQ_REL, __ATOMIC_ACQUIRE))
-        return;
+    /* one harvester per ticket: with several producers, a producer reusing
+     * the slot and a sweeping thread may reach the same ticket together; a
+     * single-producer context harvests from one thread */
+    if (c->mp) {
+        if (!__atomic_compare_exchange_n(&c->hv[slot], &seen, t + 1, false, __ATOMIC_ACQ_REL, __ATOMIC_ACQUIRE))
+            return;
+    } else {
+        __atomic_store_n(&c->hv[slot], t + 1, __ATOMIC_RELAXED);
+    }
     gpuos_rec_dev *r = c->rec + slot;
     gpuos_record R;
     R.ticket = t;
@@ -741,7 +742,10 @@ static void harvest_one(gpuos_ctx *c, uint64_t t)
     R.t_done_dev_ns = __atomic_load_n(&r->t_done, __ATOMIC_RELAXED);
     c->recent[slot] = R;
     if (c->history && t >= c->hist_base && t - c->hist_base < c->hist_cap) c->history[t - c->hist_base] = R;
-    __atomic_fetch_add(&c->n_completed, (uint64_t)1, __ATOMIC_RELAXED);
+    if (c->mp)
+        __atomic_fetch_add(&c->n_completed, (uint64_t)1, __ATOMIC_RELAXED);
+    else
+        __atomic_store_n(&c->n_completed, __atomic_load_n(&c->n_completed, __ATOMIC_RELAXED) + 1, __ATOMIC_RELAXED);
     if (R.status != GPUOS_ST_OK) {
         __atomic_fetch_add(&c->n_errors, (uint64_t)1, __ATOMIC_RELAXED);
         __atomic_fetch_add(&c->pending_errors, (uint64_t)1, __ATOMIC_RELAXED);
@@ -840,6 +844,106 @@ static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint3
     if ((t & 63u) == 0) heartbeat(c);
     if (ticket) *ticket = t;
     return GPUOS_OK;
+}
+
+/* Single producer, a run of descriptors. Up to GPUOS_COMMIT_RUN at a time:
+ * each is validated and tiled, takes its slot (once the slot's previous
+ * ticket has completed) and has its body written; then one release fence
+ * and the commit words of the whole run. Every commit word still follows
+ * its own body (the fence orders all of the run's bodies before any of its
+ * commits), which is all the device's acquire relies on; the run shares one
+ * host commit timestamp, taken before the fence (so at or before every
+ * commit of the run). Stops at the first failure, after committing what was
+ * written before it. */
+#define GPUOS_COMMIT_RUN 64u
+static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint32_t *n_done, uint32_t timeout_us)
+{
+    if (!c->accepting || (c->launched && !c->running)) return GPUOS_ESTOPPED;
+    if (c->launched && __atomic_load_n(&c->hctl->state, __ATOMIC_RELAXED) == 2u) {
+        c->running = false;
+        return GPUOS_ESTOPPED;
+    }
+    uint32_t done = 0;
+    int rc = GPUOS_OK;
+    while (done < count && rc == GPUOS_OK) {
+        const uint32_t m = count - done < GPUOS_COMMIT_RUN ? count - done : GPUOS_COMMIT_RUN;
+        const uint64_t t0 = c->head;
+        uint32_t k = 0;
+        for (; k < m; k++) {
+            const gpuos_desc *di = d + done + k;
+            const uint64_t t = t0 + k;
+            if (!c->launched && t >= c->N) {
+                rc = GPUOS_EAGAIN; /* deferred start: ring capacity */
+                break;
+            }
+            uint32_t nt = 0;
+            const bool user_known = di->op_id >= GPUOS_OP_USER_FIRST && c->user_registered[di->op_id];
+            rc = validate_and_tile(di, &nt, user_known);
+            if (rc) break;
+            uint64_t deps[2];
+            for (int q = 0; q < 2 && rc == GPUOS_OK; q++) {
+                uint64_t v = di->dep[q];
+                if (v && (di->flags & GPUOS_FLAG_DEP_REL)) {
+                    if (v > t) rc = GPUOS_EINVAL;
+                    v = t - v + 1;
+                }
+                if (v > t) rc = GPUOS_EINVAL;
+                deps[q] = v;
+            }
+            if (rc) break;
+            const uint32_t slot = (uint32_t)(t & c->mask);
+            if (t >= c->N) {
+                const uint64_t prev = t - c->N;
+                if (!is_done(c, prev)) {
+                    const uint64_t w0 = now_ns();
+                    uint32_t spins = 0;
+                    while (!is_done(c, prev)) {
+                        if ((++spins & 1023u) == 0) {
+                            heartbeat(c);
+                            if (now_ns() - w0 > (uint64_t)timeout_us * 1000ull) {
+                                rc = GPUOS_EAGAIN;
+                                break;
+                            }
+                            if (executor_gone(c)) {
+                                c->running = false;
+                                rc = GPUOS_ESTOPPED;
+                                break;
+                            }
+                        }
+                        cpu_relax();
+                    }
+                    __atomic_fetch_add(&c->host_wait_ns, now_ns() - w0, __ATOMIC_RELAXED);
+                    if (rc) break;
+                }
+                harvest_one(c, prev);
+            }
+            gpuos_desc w = *di;
+            w.ntiles = nt;
+            w.dep[0] = deps[0];
+            w.dep[1] = deps[1];
+            w.flags = (uint8_t)(di->flags & GPUOS_FLAG_FENCE);
+            w.ticket = t;
+            /* the body: the slot's previous descriptor completed, so the
+             * device no longer reads it; nothing reads the new body before
+             * its commit word */
+            memcpy(c->ring + slot, &w, offsetof(gpuos_desc, seq));
+        }
+        if (k) {
+            const uint64_t stamp = now_ns();
+            __atomic_thread_fence(__ATOMIC_RELEASE);
+            for (uint32_t q = 0; q < k; q++) {
+                const uint64_t t = t0 + q;
+                const uint32_t slot = (uint32_t)(t & c->mask);
+                c->commit_ns[slot] = stamp;
+                __atomic_store_n(&c->ring[slot].seq, t + 1, __ATOMIC_RELAXED);
+            }
+            __atomic_store_n(&c->head, t0 + k, __ATOMIC_RELEASE);
+            done += k;
+        }
+        heartbeat(c);
+    }
+    if (n_done) *n_done = done;
+    return rc;
 }
 
 /* Multiple producers: validate every descriptor, wait for room, reserve
@@ -941,14 +1045,16 @@ int gpuos_submit_batch(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64
     if (!c || (!d && count)) return GPUOS_EINVAL;
     if (c->mp) return submit_mp(c, d, count, first_ticket, n_done, timeout_us);
     if (first_ticket) *first_ticket = c->head;
-    uint32_t i = 0;
-    int rc = GPUOS_OK;
-    for (; i < count; i++) {
-        rc = submit_one(c, d + i, nullptr, timeout_us);
-        if (rc) break;
+    if (count == 0) {
+        if (n_done) *n_done = 0;
+        return GPUOS_OK;
     }
-    if (n_done) *n_done = i;
-    return rc;
+    if (count == 1) {
+        const int rc = submit_one(c, d, nullptr, timeout_us);
+        if (n_done) *n_done = rc == GPUOS_OK ? 1u : 0u;
+        return rc;
+    }
+    return submit_run_spsc(c, d, count, n_done, timeout_us);
 }
 
 int gpuos_sync(gpuos_ctx *c, uint64_t ticket, uint32_t timeout_ms)
