@@ -147,7 +147,9 @@ typedef struct gpuos_config {
     uint32_t blocks;          /* 0 = one block per SM; block 0 holds only the sequencer warp
                                  (when blocks > 1) */
     uint32_t backoff_min_ns;  /* first idle sleep; default 32 */
-    uint32_t backoff_max_ns;  /* idle sleep cap; default 256 */
+    uint32_t backoff_max_ns;  /* idle sleep cap of worker warps waiting for work; default 8000
+                                 (the sequencers' ring poll and dependency waits sleep at
+                                 most 256 ns, or this if smaller) */
     uint32_t spin_polls;      /* polls of pure spinning before backing off; default 4096 */
     uint32_t idle_exit_ms;    /* leave after this long with no host activity; 0 = never; default 10000 */
     uint32_t dep_timeout_ms;  /* bound of every device-side wait; default 5000 */
@@ -165,7 +167,12 @@ typedef struct gpuos_config {
     uint32_t multi_producer;  /* 0 (default): one submitting thread (SPSC ring, no locks);
                                  1: any number of host threads may call gpuos_submit /
                                  gpuos_submit_batch concurrently (see gpuos_submit) */
-    uint32_t reserved[2];
+    uint32_t sequencers;      /* warps of block 0 that take descriptors off the ring, 1..4
+                                 (and below warps_per_block when blocks == 1); 0 = default:
+                                 4 with more than one block, else 1. Tickets are cut into
+                                 windows of 128 (or ring_entries, if smaller), taken in turn;
+                                 work-queue space is still given out in ticket order */
+    uint32_t reserved;
 } gpuos_config;
 
 /* Completion record of one ticket (device clock = %globaltimer, host clock =
@@ -305,15 +312,24 @@ GPUOS_API int gpuos_set_history(gpuos_ctx *ctx, gpuos_record *buf, uint64_t base
  * operator's module through the CUDA Driver API.
  * Add an operator module: a relocatable sm_103a cubin (nvcc -cubin
  * -rdc=true; the bytes are copied) that defines device functions with the op
- * signature and `__device__` variables holding their addresses. At
- * gpuos_start the library links every added module with its relocatable
+ * signature and `__device__` variables holding their addresses. A
+ * device-function pointer is only callable inside the module that holds its
+ * code, so the library links every added module with its relocatable
  * executor build (driver JIT linker) and launches the executor from the
- * linked module: a device-function pointer is only callable inside the module
- * that holds its code, and on this driver a module load waits for the device
- * to go idle, which a resident executor never does. So modules are added
- * before gpuos_start (deferred_start); adding an image already added is a
- * no-op. Errors: EINVAL (does not link), EBUSY (executor already launched),
- * ECUDA. */
+ * linked module. Before gpuos_start (deferred_start) the module is linked at
+ * the launch. With the executor running, the call hands off (a module load
+ * waits for the device to go idle, which a resident executor never does):
+ * every submitted descriptor completes, the executor leaves, the module set
+ * is linked again and the executor is launched from it, continuing at the
+ * next ticket with the ring, the completion records and every operator
+ * binding carried over (the table is rebuilt with the new module's
+ * addresses). The hand-off takes milliseconds; descriptors submitted after
+ * it run on the new kernel, none is lost or run twice. It needs a
+ * single-producer context (EBUSY with multi_producer = 1), and per-warp
+ * counters of gpuos_stats restart with the new kernel. Adding an image
+ * already added is a no-op. Errors: EINVAL (does not link), EBUSY, ESTOPPED,
+ * ETIMEDOUT, ECUDA (the context accepts no more work after a failed
+ * hand-off). */
 GPUOS_API int gpuos_load_module(gpuos_ctx *ctx, const void *image, size_t len);
 
 /* Run-time compilation of an operator (§3 Q2 "3. Dynamic Operator Table",
@@ -345,9 +361,10 @@ GPUOS_API const char *gpuos_op_header(void);
  * one. Before a later flip reuses that slot the call waits until every
  * descriptor sequenced under the older version has completed. The function
  * must use at most the executor's registers per thread (compile it with the
- * same -maxrregcount). Errors: EINVAL (bad id or symbol, image does not
- * link), EBUSY (image not added before the launch, or executor not yet
- * launched), ECUDA, ETIMEDOUT. */
+ * same -maxrregcount). An image not yet added is added first with
+ * gpuos_load_module (a hand-off if the executor runs). Errors: EINVAL (bad id
+ * or symbol, image does not link), EBUSY (executor not yet launched, or a
+ * hand-off with several producers), ECUDA, ETIMEDOUT. */
 GPUOS_API int gpuos_register_op(gpuos_ctx *ctx, uint16_t op_id, const void *image, size_t len,
                       const char *fnptr_symbol);
 

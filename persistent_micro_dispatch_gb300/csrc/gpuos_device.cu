@@ -158,7 +158,15 @@ struct Elapsed {
     }
 };
 
-/* Idle backoff: spin for `spin` polls, then sleep min_ns << k up to max_ns. */
+/* Idle backoff: spin for `spin` polls, then sleep min_ns << k up to max_ns.
+ * Workers waiting for work sleep up to the configured cap (power when the
+ * ring stays empty); the sequencers' ring poll and the waits on a dependency
+ * or a fence, which sit on the dispatch path, sleep at most
+ * GPUOS_SHORT_SLEEP_NS. */
+DEV uint32_t short_cap(const gpuos_exec_params &p)
+{
+    return p.backoff_max_ns < GPUOS_SHORT_SLEEP_NS ? p.backoff_max_ns : GPUOS_SHORT_SLEEP_NS;
+}
 DEV void backoff(uint32_t &polls, uint32_t spin, uint32_t min_ns, uint32_t max_ns, uint64_t *sleeps)
 {
     if (polls < spin) {
@@ -1631,12 +1639,49 @@ DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles, uint32_t workers)
     return hlp < cap ? hlp : cap;
 }
 
-/* The sequencer warp: ring -> mirror + work queue, up to 128 descriptors per
- * batch (four ring slots per lane: slot s + lane + 32 h). */
+/* Work-queue reservation shared by the sequencer warps of block 0 (shared
+ * memory). Work-queue space is given out in ticket order: the warp whose
+ * batch starts at ticket pub_next takes tq_head, advances it by the batch's
+ * entries and passes the turn on. Workers claim entries in queue order, so
+ * an entry of a descriptor is never queued behind the entries of a later
+ * descriptor that may wait for it (with several sequencers, a later window
+ * may be ready first). */
+struct SeqBaton {
+    unsigned long long pub_next; /* first ticket whose entries are not reserved yet */
+    unsigned long long tq_head;  /* next free work-queue index */
+};
+
+/* Lane 0: wait (bounded) for the turn of the batch starting at ticket s. */
+DEV bool baton_wait(volatile SeqBaton *b, uint64_t s, uint64_t bound_ns)
+{
+    Elapsed w;
+    w.start();
+    uint32_t n = 0;
+    while (b->pub_next != s) {
+        if ((++n & 63u) == 0 && w.tick(globaltimer()) > bound_ns) return false;
+    }
+    __threadfence_block(); /* the previous holder's tq_head before it */
+    return true;
+}
+
+/* Lane 0: pass the turn on to the batch starting at ticket `next`. */
+DEV void baton_pass(volatile SeqBaton *b, uint64_t next)
+{
+    __threadfence_block(); /* tq_head before the turn moves */
+    b->pub_next = next;
+}
+
+/* A sequencer warp: ring -> mirror + work queue, up to 128 descriptors per
+ * batch (four ring slots per lane: slot s + lane + 32 h). With S sequencer
+ * warps, tickets are cut into windows of 128 (or the ring size, if smaller)
+ * and warp sq takes windows sq, sq + S, sq + 2S, ...: reading, checking and
+ * mirroring descriptors run in parallel; only the reservation of
+ * work-queue space follows ticket order (SeqBaton). */
 #define SEQ_SPL 2    /* ring slots per lane in one half of a batch (64 descriptors) */
 #define SEQ_HALVES 2 /* halves per batch */
 #define SEQ_POLL (SEQ_SPL * SEQ_HALVES)
-DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, unsigned long long *s_table)
+DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, unsigned long long *s_table,
+                   uint32_t sq, uint32_t S, SeqBaton *baton)
 {
     const uint32_t lane = lane_id();
     uint32_t cached_version = 0xFFFFFFFFu; /* version whose table slot s_table holds */
@@ -1650,8 +1695,13 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
     Elapsed idle;
     idle.start();
     const uint32_t N = p.ring_mask + 1;
-    const uint32_t KMAX = N < 32u * SEQ_POLL ? N : 32u * SEQ_POLL;
-    if (lane == 0) st_relaxed_sys32(&p.hctl->state, 1u);
+    const uint32_t WIN = N < 32u * SEQ_POLL ? N : 32u * SEQ_POLL; /* window of tickets, and batch limit */
+    const uint64_t WSKIP = (uint64_t)WIN * (S - 1);               /* other sequencers' windows */
+    s = p.ticket_base + (uint64_t)WIN * sq;
+    e = p.tq_base;
+    uint64_t wend = s + WIN;
+    volatile SeqBaton *vb = baton;
+    if (lane == 0 && sq == 0) st_relaxed_sys32(&p.hctl->state, 1u);
 
     /* commit words of slots s + lane + 32 h (h < SEQ_POLL), polled ahead
      * (relaxed; the batch's fence comes after they are seen): the poll for
@@ -1676,14 +1726,17 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         }
         uint32_t k = (rm[0] != ~0ull) ? (uint32_t)(__ffsll((long long)~rm[0]) - 1)
                                       : 64u + ((rm[1] == ~0ull) ? 64u : (uint32_t)(__ffsll((long long)~rm[1]) - 1));
-        if (k > KMAX) k = KMAX;
+        if (k > wend - s) k = (uint32_t)(wend - s);
         if (k == 0) {
             /* idle: stop flag, exit_after, watchdog */
             if (n_idle++ == 0 || polls == 0) {
-                if (lane == 0) st_relaxed_sys(&p.hctl->sequenced, s);
+                if (lane == 0 && sq == 0) st_relaxed_sys(&p.hctl->sequenced, s);
             }
             if ((polls & 31u) == 0) {
                 uint32_t reason = 0;
+                /* another sequencer decided to leave: follow it */
+                const uint32_t follow = S > 1 ? ld_relaxed_gpu32(&p.dctl->exit_flag) : 0u;
+                if (__shfl_sync(0xFFFFFFFFu, follow, 0)) break;
                 if (ld_relaxed_sys32(&p.hctl->stop)) reason = 1;
                 if (p.exit_after && *reinterpret_cast<volatile unsigned long long *>(&p.dctl->completed) >= p.exit_after)
                     reason = 3;
@@ -1706,7 +1759,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                     break;
                 }
             }
-            backoff(polls, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+            backoff(polls, p.spin_polls, p.backoff_min_ns, short_cap(p), &n_sleep);
 #pragma unroll
             for (int h = 0; h < SEQ_POLL; h++)
                 seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
@@ -1796,7 +1849,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                             fence_status = GPUOS_ST_DEP_TIMEOUT;
                             break;
                         }
-                        backoff(fp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+                        backoff(fp, p.spin_polls, p.backoff_min_ns, short_cap(p), &n_sleep);
                     }
                     __threadfence();
                 }
@@ -1842,6 +1895,16 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         inl = __shfl_sync(0xFFFFFFFFu, inl, 0);
         if (inl) {
             const uint32_t slot = (uint32_t)(s & p.ring_mask);
+            if (S > 1) {
+                /* no work-queue space, but the turn passes through it */
+                uint32_t ok = 1;
+                if (lane == 0) {
+                    ok = baton_wait(vb, s, p.dep_timeout_ns) ? 1u : 0u;
+                    if (ok) baton_pass(vb, s + 1);
+                    else set_exit(p, 4u);
+                }
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+            }
             if (lane == 0) {
                 uint4 *sv = reinterpret_cast<uint4 *>(sd);
                 const uint4 *dv = reinterpret_cast<const uint4 *>(&dsc[0]);
@@ -1857,10 +1920,16 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             __syncwarp();
             if (lane == 0) complete_desc(p, s, slot, st, version);
             s += 1;
+            if (S == 1) {
+                wend = s + WIN; /* one sequencer: batches start anywhere */
+            } else if (s == wend) {
+                s += WSKIP;
+                wend = s + WIN;
+            }
             n_seq += 1;
             n_inline += 1;
             if (lane == 0) {
-                st_relaxed_sys(&p.hctl->sequenced, s);
+                if (sq == 0) st_relaxed_sys(&p.hctl->sequenced, s);
                 ws[GPUOS_WS_SEQ] = n_seq;
                 ws[GPUOS_WS_TILES] = n_inline;
             }
@@ -1882,10 +1951,18 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         __syncwarp();
         __threadfence();
         const uint64_t t_m = globaltimer();
+        /* where the next batch starts (this window, or this warp's next one) */
+        uint64_t s_next = s + k, wend_next = wend;
+        if (S == 1) {
+            wend_next = s_next + WIN; /* one sequencer: batches start anywhere */
+        } else if (s_next == wend) {
+            s_next += WSKIP;
+            wend_next = s_next + WIN;
+        }
         /* the next batch's poll, in flight during the publication below */
 #pragma unroll
         for (int h = 0; h < SEQ_POLL; h++)
-            seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + k + lane + 32u * h) & p.ring_mask)].seq);
+            seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s_next + lane + 32u * h) & p.ring_mask)].seq);
         /* exclusive prefix of entry counts in ticket order -> queue ranges
          * (position lane + 32 h for h < SEQ_POLL) */
         uint32_t excl[SEQ_POLL];
@@ -1902,6 +1979,23 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             base += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
         const uint32_t total = base;
+        if (S > 1) {
+            /* this batch's turn to reserve work-queue space */
+            uint32_t ok = 1;
+            unsigned long long e0 = 0;
+            if (lane == 0) {
+                ok = baton_wait(vb, s, p.dep_timeout_ns) ? 1u : 0u;
+                if (ok) {
+                    e0 = vb->tq_head;
+                    vb->tq_head = e0 + total;
+                    baton_pass(vb, s + k);
+                } else {
+                    set_exit(p, 4u);
+                }
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+            e = __shfl_sync(0xFFFFFFFFu, e0, 0);
+        }
         /* Publication. Each lane writes the first (up to 16) entries of its own
          * descriptors; descriptors with more entries are finished by the
          * whole warp, one after another. Entry j of a descriptor whose first
@@ -1962,7 +2056,8 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             if (pos < k && status[h] != GPUOS_ST_OK) complete_desc(p, my_t, slot, status[h], version);
         }
         e += total;
-        s += k;
+        s = s_next;
+        wend = wend_next;
         n_seq += k;
         t_body += t_b - t_obs;
         t_mirror += t_m - t_b;
@@ -1972,7 +2067,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
              * out every 16th batch and when the ring runs dry: a store
              * across NVLink-C2C per batch would make the next batch's
              * system-scope fence wait for its acknowledgement */
-            if ((++n_batches & 15u) == 0) st_relaxed_sys(&p.hctl->sequenced, s);
+            if ((++n_batches & 15u) == 0 && sq == 0) st_relaxed_sys(&p.hctl->sequenced, s);
             ws[GPUOS_WS_SEQ] = n_seq;
             ws[GPUOS_WS_IDLE] = n_idle;
             ws[GPUOS_WS_SLEEPS] = n_sleep;
@@ -2075,7 +2170,7 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, uint
                         dstatus = GPUOS_ST_ABORTED;
                         break;
                     }
-                    backoff(dp, p.spin_polls, p.backoff_min_ns, p.backoff_max_ns, &n_sleep);
+                    backoff(dp, p.spin_polls, p.backoff_min_ns, short_cap(p), &n_sleep);
                 }
                 if (dstatus) break;
                 fence_acq_rel_gpu(); /* the acquire, once */
@@ -2164,16 +2259,22 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, uint
 extern "C" __global__ void __launch_bounds__(GPUOS_MAX_WPB * 32, 1) gpuos_executor_kernel(gpuos_exec_params p)
 {
     __shared__ __align__(16) gpuos_devdesc sdesc[GPUOS_MAX_WPB];
-    __shared__ unsigned long long s_table[GPUOS_MAX_OPS]; /* the sequencer's copy of one table slot */
+    __shared__ unsigned long long s_table[GPUOS_MAX_SEQ][GPUOS_MAX_OPS]; /* each sequencer's copy of one table slot */
     __shared__ uint64_t s_prof[GPUOS_MAX_WPB][GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS]; /* tile profiles */
+    __shared__ SeqBaton s_baton;
     const uint32_t warp = threadIdx.x >> 5;
     for (uint32_t i = threadIdx.x & 31u; i < GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS; i += 32) s_prof[warp][i] = 0;
-    stage_init(p.stage_bytes); /* (its block barriers also order the clearing above) */
+    if (threadIdx.x == 0) {
+        s_baton.pub_next = p.ticket_base;
+        s_baton.tq_head = p.tq_base;
+    }
+    stage_init(p.stage_bytes); /* (its block barriers also order the writes above) */
     const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
-    /* Block 0 is the sequencer's alone (unless it is the only block): worker
-     * warps beside it would share its issue slots and load/store pipe, and
-     * the sequencer's batch time sets the executor's dispatch rate. */
-    if (blockIdx.x == 0 && warp == 0) sequencer(p, &sdesc[0], gw, s_table);
+    /* Block 0 holds the sequencer warps alone (unless it is the only block):
+     * worker warps beside them would share their issue slots and
+     * load/store pipe, and the sequencers set the executor's dispatch rate. */
+    const uint32_t S = p.sequencers;
+    if (blockIdx.x == 0 && warp < S) sequencer(p, &sdesc[warp], gw, s_table[warp], warp, S, &s_baton);
     else if (blockIdx.x != 0 || gridDim.x == 1) worker(p, &sdesc[warp], gw, s_prof[warp]);
 }
 

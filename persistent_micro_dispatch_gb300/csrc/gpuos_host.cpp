@@ -217,8 +217,16 @@ struct gpuos_ctx {
     uint64_t n_completed = 0, n_errors = 0;
     uint64_t host_wait_ns = 0; /* submitters' time waiting for a free slot */
     uint64_t pending_errors = 0; /* errors harvested since the last sync report */
-    /* operator table shadow */
+    /* operator table shadow, and what each entry is bound to (a built-in op,
+     * or a `__device__` variable of a loaded module holding the function's
+     * address): function addresses are valid only inside one loaded module,
+     * so a relaunch from a newly linked module rebuilds the table from these */
     uint64_t table_host[2][GPUOS_MAX_OPS];
+    struct Binding {
+        int builtin = -1; /* built-in op id, or -1 */
+        std::string sym;  /* module symbol, when builtin < 0 */
+    };
+    Binding binding[2][GPUOS_MAX_OPS];
     bool user_registered[GPUOS_MAX_OPS];
     uint32_t version = 0;
     uint64_t flip_head = 0; /* head when the current version was published */
@@ -231,6 +239,7 @@ struct gpuos_ctx {
     CUfunction linked_exec = nullptr;
     uint32_t regs = 0, smem = 0;
     gpuos_exec_params params;
+    uint32_t n_handoffs = 0; /* executor relaunches that took in a new module */
     bool accepting = false; /* submissions allowed (until stop) */
     bool launched = false;  /* executor kernel launched */
     bool running = false;   /* executor believed resident */
@@ -297,7 +306,7 @@ void gpuos_default_config(gpuos_config *c)
     c->warps_per_block = 12;
     c->blocks = 0;
     c->backoff_min_ns = 32;
-    c->backoff_max_ns = 256;
+    c->backoff_max_ns = 8000;
     c->spin_polls = 4096;
     c->idle_exit_ms = 10000;
     c->dep_timeout_ms = 5000;
@@ -481,6 +490,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     if (cfg.backoff_min_ns == 0 || cfg.backoff_max_ns < cfg.backoff_min_ns) return GPUOS_EINVAL;
     if ((cfg.stage_bytes & 1023u) || cfg.stage_bytes > 24576u) return GPUOS_EINVAL;
     if (cfg.multi_producer > 1u) return GPUOS_EINVAL;
+    if (cfg.sequencers > GPUOS_MAX_SEQ) return GPUOS_EINVAL;
     /* every warp's staging region and the executor's static shared memory
      * (descriptor copies, the sequencer's table copy, tile profiles) must fit
      * the 227 KB a block can hold */
@@ -510,6 +520,12 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device));
     c->blocks = cfg.blocks ? cfg.blocks : (uint32_t)sms;
     c->wpb = cfg.warps_per_block;
+    if (cfg.sequencers == 0) cfg.sequencers = c->blocks > 1 ? (GPUOS_MAX_SEQ < c->wpb ? GPUOS_MAX_SEQ : c->wpb) : 1u;
+    if (cfg.sequencers > c->wpb || (c->blocks == 1 && cfg.sequencers >= c->wpb)) {
+        free_all(c);
+        return GPUOS_EINVAL;
+    }
+    c->cfg.sequencers = cfg.sequencers;
     if (gpuos_dev_preload() != 0) {
         free_all(c);
         return GPUOS_ECUDA;
@@ -584,7 +600,10 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
         return GPUOS_ECUDA;
     }
     for (int s = 0; s < 2; s++)
-        for (int i = 0; i < GPUOS_OP_BUILTIN_COUNT; i++) c->table_host[s][i] = (uint64_t)(uintptr_t)builtin[i];
+        for (int i = 0; i < GPUOS_OP_BUILTIN_COUNT; i++) {
+            c->table_host[s][i] = (uint64_t)(uintptr_t)builtin[i];
+            c->binding[s][i].builtin = i;
+        }
     CK(cudaMemcpyAsync(c->table, c->table_host, sizeof(c->table_host), cudaMemcpyHostToDevice, c->ctl_stream));
     CK(cudaStreamSynchronize(c->ctl_stream));
 
@@ -615,8 +634,9 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     p.backoff_max_ns = cfg.backoff_max_ns;
     p.spin_polls = cfg.spin_polls;
     p.stage_bytes = cfg.stage_bytes;
-    /* worker warps: block 0 holds only the sequencer (when there are others) */
-    p.workers = c->blocks > 1 ? (c->blocks - 1) * c->wpb : c->wpb - 1;
+    /* worker warps: block 0 holds only the sequencers (when there are others) */
+    p.sequencers = cfg.sequencers;
+    p.workers = c->blocks > 1 ? (c->blocks - 1) * c->wpb : c->wpb - cfg.sequencers;
     p.idle_exit_ns = (uint64_t)cfg.idle_exit_ms * 1000000ull;
     p.dep_timeout_ns = (uint64_t)(cfg.dep_timeout_ms ? cfg.dep_timeout_ms : 5000) * 1000000ull;
     p.exit_after = cfg.exit_after;
@@ -636,14 +656,18 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
 /* With op modules loaded: link them with the relocatable executor, load the
  * result, take the built-in table from it (function pointers are valid only
  * inside the module that holds the code) and launch its executor. */
-static int launch_linked(gpuos_ctx *c)
+static int launch_linked(gpuos_ctx *c, const std::vector<unsigned char> *prelinked)
 {
     Driver &drv = driver();
-    std::vector<std::vector<unsigned char>> objs;
-    for (auto &m : c->modules) objs.push_back(m.bytes);
     std::vector<unsigned char> img;
-    int rc = link_images(objs, &img);
-    if (rc) return rc;
+    if (prelinked) {
+        img = *prelinked;
+    } else {
+        std::vector<std::vector<unsigned char>> objs;
+        for (auto &m : c->modules) objs.push_back(m.bytes);
+        const int rc = link_images(objs, &img);
+        if (rc) return rc;
+    }
     if (drv.load(&c->linked, img.data()) != CUDA_SUCCESS) return GPUOS_ECUDA;
     CUdeviceptr tab = 0;
     size_t tsz = 0;
@@ -653,8 +677,22 @@ static int launch_linked(gpuos_ctx *c)
     uint64_t builtin[GPUOS_OP_BUILTIN_COUNT];
     if (cudaMemcpy(builtin, (const void *)tab, sizeof(builtin), cudaMemcpyDeviceToHost) != cudaSuccess)
         return GPUOS_ECUDA;
+    /* both table slots from the bindings, with this module's addresses */
     for (int sl = 0; sl < 2; sl++)
-        for (int i = 0; i < GPUOS_OP_BUILTIN_COUNT; i++) c->table_host[sl][i] = builtin[i];
+        for (int i = 0; i < GPUOS_MAX_OPS; i++) {
+            const gpuos_ctx::Binding &b = c->binding[sl][i];
+            uint64_t v = 0;
+            if (b.builtin >= 0) {
+                v = builtin[b.builtin];
+            } else if (!b.sym.empty()) {
+                CUdeviceptr gp = 0;
+                size_t gsz = 0;
+                if (drv.get_global(&gp, &gsz, c->linked, b.sym.c_str()) != CUDA_SUCCESS || gsz != sizeof(uint64_t) ||
+                    cudaMemcpy(&v, (const void *)gp, 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+                    return GPUOS_ECUDA;
+            }
+            c->table_host[sl][i] = v;
+        }
     if (cudaMemcpy(c->table, c->table_host, sizeof(c->table_host), cudaMemcpyHostToDevice) != cudaSuccess)
         return GPUOS_ECUDA;
     if (drv.get_function(&c->linked_exec, c->linked, "gpuos_executor_kernel") != CUDA_SUCCESS) return GPUOS_ECUDA;
@@ -684,7 +722,7 @@ int gpuos_start(gpuos_ctx *c)
     if (cudaSetDevice(c->device) != cudaSuccess) return GPUOS_ECUDA;
     heartbeat(c);
     if (!c->modules.empty()) {
-        const int rc = launch_linked(c);
+        const int rc = launch_linked(c, nullptr);
         if (rc) {
             fprintf(stderr, "gpuos: linked executor launch failed (%d)\n", rc);
             return rc;
@@ -1129,7 +1167,7 @@ int gpuos_set_history(gpuos_ctx *c, gpuos_record *buf, uint64_t base, uint64_t c
 }
 
 /* ---- dual-slot table flip ------------------------------------------------------- */
-static int flip_entry(gpuos_ctx *c, uint16_t op_id, uint64_t fnval)
+static int flip_entry(gpuos_ctx *c, uint16_t op_id, uint64_t fnval, const gpuos_ctx::Binding &bind)
 {
     /* grace period: descriptors sequenced under version-1 (all tickets below
      * the head recorded at the last flip) must have completed before the
@@ -1150,6 +1188,8 @@ static int flip_entry(gpuos_ctx *c, uint16_t op_id, uint64_t fnval)
     const uint32_t ns = nv & 1u;
     memcpy(c->table_host[ns], c->table_host[c->version & 1u], sizeof(c->table_host[0]));
     c->table_host[ns][op_id] = fnval;
+    for (int i = 0; i < GPUOS_MAX_OPS; i++) c->binding[ns][i] = c->binding[c->version & 1u][i];
+    c->binding[ns][op_id] = bind;
     if (cudaMemcpyAsync(c->table + (size_t)ns * GPUOS_MAX_OPS, c->table_host[ns], sizeof(c->table_host[0]),
                         cudaMemcpyHostToDevice, c->ctl_stream) != cudaSuccess)
         return GPUOS_ECUDA;
@@ -1187,12 +1227,92 @@ static int find_module(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
     return -1;
 }
 
+/* Take a new operator module into a running executor (an executor hand-off).
+ * A module load waits for the device to go idle, and a function address is
+ * callable only inside the module that holds its code, so the module cannot
+ * join the resident kernel: every submitted descriptor completes, the
+ * executor leaves, the module set is linked again with the new module and
+ * the executor is launched from it. The ring, the completion records, the
+ * tickets and the operator bindings carry over: the new kernel starts at the
+ * next ticket and after the last work-queue index the old one handed out,
+ * and its table is rebuilt from the bindings with the new module's
+ * addresses. Single-producer contexts only (the caller's thread is the only
+ * submitter, so nothing is committed meanwhile). */
+static int handoff(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
+{
+    if (c->mp) return GPUOS_EBUSY;
+    if (!c->running) return GPUOS_ESTOPPED;
+    Driver &drv = driver();
+    if (!drv.ok) return GPUOS_ECUDA;
+    /* the new set must link before anything stops */
+    std::vector<std::vector<unsigned char>> objs;
+    for (auto &m : c->modules) objs.push_back(m.bytes);
+    objs.emplace_back((const unsigned char *)image, (const unsigned char *)image + len);
+    std::vector<unsigned char> img;
+    int rc = link_images(objs, &img);
+    if (rc) return rc;
+    /* drain under the old executor (an error status harvested here stays
+     * pending for the caller's next gpuos_sync) */
+    rc = gpuos_sync(c, UINT64_MAX, 2 * c->cfg.dep_timeout_ms + 1000);
+    if (rc == GPUOS_EDEVICE) __atomic_fetch_add(&c->pending_errors, (uint64_t)1, __ATOMIC_RELAXED);
+    else if (rc != GPUOS_OK) return rc;
+    /* the executor is idle: let it leave */
+    store_rel(&c->hctl->stop, 1u);
+    const uint64_t t0 = now_ns();
+    while (cudaStreamQuery(c->exec_stream) == cudaErrorNotReady) {
+        if (now_ns() - t0 > 10000000000ull) {
+            c->running = false;
+            return GPUOS_ETIMEDOUT;
+        }
+        cpu_relax();
+    }
+    c->running = false;
+    c->launched = false;
+    if (cudaStreamQuery(c->exec_stream) != cudaSuccess) return GPUOS_ECUDA;
+    gpuos_ctx::Module m;
+    m.hash = h;
+    m.bytes = std::move(objs.back());
+    c->modules.push_back(std::move(m));
+    if (c->linked) drv.unload(c->linked);
+    c->linked = nullptr;
+    c->linked_exec = nullptr;
+    /* where the new kernel starts: the next ticket, and the work-queue index
+     * after every one the old kernel's workers claimed (none past it was
+     * ever written in this lap, so no stale entry matches) */
+    uint64_t *claim = reinterpret_cast<uint64_t *>(c->version_stage + 4);
+    if (cudaMemcpyAsync(claim, &c->dctl->tq_claim, 8, cudaMemcpyDeviceToHost, c->ctl_stream) != cudaSuccess ||
+        cudaMemsetAsync(&c->dctl->exit_flag, 0, 4, c->ctl_stream) != cudaSuccess ||
+        cudaStreamSynchronize(c->ctl_stream) != cudaSuccess)
+        return GPUOS_ECUDA;
+    c->params.ticket_base = c->head;
+    c->params.tq_base = *claim;
+    store_rel(&c->hctl->stop, 0u);
+    __atomic_store_n(&c->hctl->exit_reason, 0u, __ATOMIC_RELAXED);
+    store_rel(&c->hctl->state, 0u);
+    c->flip_head = c->head; /* nothing sequenced under an older version is in flight */
+    heartbeat(c);
+    rc = launch_linked(c, &img);
+    if (rc) return rc;
+    c->launched = true;
+    const uint64_t t1 = now_ns();
+    while (load_acq(&c->hctl->state) == 0u) {
+        if (cudaStreamQuery(c->exec_stream) != cudaErrorNotReady || now_ns() - t1 > 10000000000ull) {
+            store_rel(&c->hctl->stop, 1u);
+            return GPUOS_ECUDA;
+        }
+        cpu_relax();
+    }
+    c->running = true;
+    c->n_handoffs++;
+    return GPUOS_OK;
+}
+
 int gpuos_load_module(gpuos_ctx *c, const void *image, size_t len)
 {
     if (!c || !image || !len) return GPUOS_EINVAL;
     const uint64_t h = fnv1a(image, len);
     if (find_module(c, image, len, h) >= 0) return GPUOS_OK;
-    if (c->launched) return GPUOS_EBUSY; /* linked into the executor at gpuos_start */
+    if (c->launched) return handoff(c, image, len, h); /* a running executor: hand off */
     /* check now that the object links with the executor */
     std::vector<std::vector<unsigned char>> objs(1);
     objs[0].assign((const unsigned char *)image, (const unsigned char *)image + len);
@@ -1212,7 +1332,8 @@ int gpuos_register_op(gpuos_ctx *c, uint16_t op_id, const void *image, size_t le
     if (op_id >= GPUOS_OP_BUILTIN_COUNT && op_id < GPUOS_OP_USER_FIRST) return GPUOS_EINVAL;
     if (!c->accepting) return GPUOS_ESTOPPED;
     if (find_module(c, image, len, fnv1a(image, len)) < 0) {
-        /* not linked into the executor: only possible before the launch */
+        /* not linked into the executor: linked at the launch, or, with the
+         * executor running, taken in by a hand-off */
         const int rc = gpuos_load_module(c, image, len);
         if (rc) return rc;
     }
@@ -1229,7 +1350,9 @@ int gpuos_register_op(gpuos_ctx *c, uint16_t op_id, const void *image, size_t le
         return GPUOS_ECUDA;
     memcpy(&fnval, c->version_stage + 2, 8);
     if (fnval == 0) return GPUOS_EINVAL;
-    const int rc = flip_entry(c, op_id, fnval);
+    gpuos_ctx::Binding bind;
+    bind.sym = sym;
+    const int rc = flip_entry(c, op_id, fnval, bind);
     if (rc == GPUOS_OK && op_id >= GPUOS_OP_USER_FIRST) c->user_registered[op_id] = true;
     return rc;
 }
@@ -1241,7 +1364,7 @@ int gpuos_alias_op(gpuos_ctx *c, uint16_t op_id, uint16_t source_op)
     if (!c->accepting) return GPUOS_ESTOPPED;
     const uint64_t v = c->table_host[c->version & 1u][source_op];
     if (v == 0) return GPUOS_EINVAL;
-    const int rc = flip_entry(c, op_id, v);
+    const int rc = flip_entry(c, op_id, v, c->binding[c->version & 1u][source_op]);
     if (rc == GPUOS_OK && op_id >= GPUOS_OP_USER_FIRST) c->user_registered[op_id] = true;
     return rc;
 }
@@ -1262,11 +1385,17 @@ int gpuos_stats(gpuos_ctx *c, gpuos_stats_t *st)
         st->sleeps += x[GPUOS_WS_SLEEPS];
         st->dep_waits += x[GPUOS_WS_DEPWAIT];
     }
-    /* warp 0 of block 0 is the sequencer: its phase timers */
-    st->seq_body_ns = ws[GPUOS_WS_T_BODY];
-    st->seq_mirror_ns = ws[GPUOS_WS_T_MIRROR];
-    st->seq_publish_ns = ws[GPUOS_WS_T_PUB];
-    st->seq_batches = ws[GPUOS_WS_BATCHES];
+    /* warps 0 .. sequencers-1 of block 0 are the sequencers: their phase
+     * timers (summed) and the descriptors they took off the ring */
+    uint64_t seq_taken = 0;
+    for (uint32_t w = 0; w < c->cfg.sequencers && w < tw; w++) {
+        const uint64_t *x = &ws[(size_t)w * GPUOS_WS_N];
+        st->seq_body_ns += x[GPUOS_WS_T_BODY];
+        st->seq_mirror_ns += x[GPUOS_WS_T_MIRROR];
+        st->seq_publish_ns += x[GPUOS_WS_T_PUB];
+        st->seq_batches += x[GPUOS_WS_BATCHES];
+        seq_taken += x[GPUOS_WS_SEQ];
+    }
     st->host_wait_ns = __atomic_load_n(&c->host_wait_ns, __ATOMIC_RELAXED);
     {
         HarvestLock lk(c);
@@ -1275,7 +1404,7 @@ int gpuos_stats(gpuos_ctx *c, gpuos_stats_t *st)
         st->errors = __atomic_load_n(&c->n_errors, __ATOMIC_RELAXED);
     }
     st->submitted = head_of(c);
-    st->sequenced = __atomic_load_n(&c->hctl->sequenced, __ATOMIC_RELAXED);
+    st->sequenced = seq_taken;
     st->version = c->version;
     st->running = (c->running && !executor_gone(c)) ? 1u : 0u;
     st->exit_reason = __atomic_load_n(&c->hctl->exit_reason, __ATOMIC_RELAXED);

@@ -24,9 +24,12 @@
 #define GPUOS_VM_COLS 8                   /* output columns per vecmat tile (16 bytes of a row) */
 #define GPUOS_ROW_REG_MAX 4096            /* rows up to this width stay in registers */
 #define GPUOS_MAX_WPB 12
+#define GPUOS_MAX_SEQ 4 /* sequencer warps at most */
+#define GPUOS_SHORT_SLEEP_NS 256u /* longest idle sleep on the dispatch path (ring poll, dependency waits) */
 /* static shared memory of the executor kernel: descriptor copies, the
- * sequencer's table copy, per-warp tile profiles */
-#define GPUOS_EXEC_STATIC_SMEM (GPUOS_MAX_WPB * 128 + 256 * 8 + GPUOS_MAX_WPB * GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS * 8)
+ * sequencers' table copies, per-warp tile profiles, the sequencers' turn */
+#define GPUOS_EXEC_STATIC_SMEM \
+    (GPUOS_MAX_WPB * 128 + GPUOS_MAX_SEQ * 256 * 8 + GPUOS_MAX_WPB * GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS * 8 + 16)
 #define GPUOS_MAX_REGS 168 /* registers per thread: 65536 / (12 warps x 32), in steps of 8 */
 #define GPUOS_TILE_MAX (1u << 30)          /* tiles per descriptor */
 #define GPUOS_HELPERS 2048                 /* work-queue entries (helper warps) per descriptor at most */
@@ -118,8 +121,11 @@ typedef struct gpuos_exec_params {
     uint64_t *warp_stats;    /* [total warps][GPUOS_WS_N] */
     uint32_t ring_mask, tq_mask;
     uint32_t backoff_min_ns, backoff_max_ns, spin_polls, stage_bytes;
-    uint32_t workers, pad_w;  /* worker warps (all warps but the sequencer) */
+    uint32_t workers;        /* worker warps (all warps but the sequencers) */
+    uint32_t sequencers;     /* sequencer warps (warps 0.. of block 0) */
     uint64_t idle_exit_ns, dep_timeout_ns, exit_after;
+    uint64_t ticket_base;    /* first ticket this launch takes (0, or where a hand-off resumes) */
+    uint64_t tq_base;        /* first work-queue index this launch reserves */
 } gpuos_exec_params;
 
 #ifdef __cplusplus

@@ -262,6 +262,10 @@ def test_in_order_comparison_passes_the_oracle_own_results(make):
     s = make()
     full = Machine(s)
     full.run()
-    rep, _ = compare_in_order(s, HostDS(s, [b.copy() for b in full.buf]))
+    bufs = [b.copy() for b in full.buf]
+    for i, b in enumerate(s.buffers):
+        if b.name.startswith("sdpa_ws"):  # the GPU leaves partials in its scratch
+            bufs[i].view(np.uint8)[:] = 0x3C
+    rep, _ = compare_in_order(s, HostDS(s, bufs))
     assert rep.ok(), rep.failures
     assert rep.checked >= len([o for o in s.ops if o.op != "nop"]) // 2
