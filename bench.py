@@ -365,46 +365,19 @@ def pct(x, q):
     return float(np.percentile(x, q)) if len(x) else None
 
 
-def producers_sweep(G, cfg_kw) -> int:
+def producers_sweep(local: int) -> int:
     """Aggregate submission throughput of T concurrent host threads, each
     committing NOP descriptors in batches of 16 through one ring (the page's
-    ring-contention question). The single-thread line without the
-    multi-producer path (plain SPSC ring) is the reference."""
-    import threading
-    per_thread = 20_000
-    batch = 16
-    nop = G.make_descs(batch)
-    rows = []
-    for T, mp in [(1, 0), (1, 1), (2, 1), (4, 1), (8, 1), (16, 1), (32, 1), (64, 1)]:
-        ex = G.Executor(**cfg_kw, multi_producer=mp)
-        try:
-            go = threading.Barrier(T + 1)
-
-            def work():
-                go.wait()
-                for _ in range(per_thread // batch):
-                    ex.submit_batch(nop)
-
-            th = [threading.Thread(target=work) for _ in range(T)]
-            for t in th:
-                t.start()
-            go.wait()
-            t0 = time.perf_counter()
-            for t in th:
-                t.join()
-            t_sub = time.perf_counter() - t0
-            ex.sync(timeout_ms=60_000)
-            t_all = time.perf_counter() - t0
-            st = ex.stats()
-        finally:
-            ex.shutdown()
-        n = T * (per_thread // batch) * batch
-        assert st["completed"] >= n, st
-        rows.append({"threads": T, "multi_producer": mp, "descriptors": n,
-                     "submit_per_s": n / t_sub, "complete_per_s": n / t_all})
-    print(json.dumps({"metric": "host submission throughput vs producer threads (NOP batches of 16)",
-                      "unit": "descriptors/s", "rows": rows}), flush=True)
-    return 0
+    ring-contention question). The threads are native (the library's
+    measurement program, C ABI only): Python threads would serialise on the
+    interpreter lock around every call and measure that instead. The
+    single-thread line on the single-producer ring is the reference."""
+    from persistent_micro_dispatch_gb300 import build as pkg_build
+    exe = pkg_build.PRODUCERS
+    r = subprocess.run([exe, "64", "20000", "16", str(local)], stdout=subprocess.PIPE, text=True, timeout=600)
+    line = r.stdout.strip().splitlines()[-1] if r.stdout.strip() else "{}"
+    print(line, flush=True)
+    return r.returncode
 
 
 def isolated_latency(G, ex, descs, n_ops, n=300):
@@ -722,7 +695,7 @@ def main():
     torch.cuda.synchronize()
 
     if args.producers_sweep:
-        return producers_sweep(G, cfg_kw)
+        return producers_sweep(local)
     if args.profile_run:
         # bounded run with the ring filled before the single launch: the
         # kernel ends on its own after len(descs) completions (replayable),

@@ -23,6 +23,8 @@ LIB = os.path.join(HERE, "libgpuos.so")
 EXT_CUBIN = os.path.join(HERE, "gpuos_ext_ops.cubin")
 # relocatable build of the executor: op modules are linked with it at run time
 EXEC_RDC = os.path.join(HERE, "gpuos_exec_rdc.cubin")
+# native host-thread contention measurement (links libgpuos.so)
+PRODUCERS = os.path.join(HERE, "gpuos_producers")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc")
@@ -91,6 +93,13 @@ def build(force: bool = False) -> str:
         tmp = LIB + ".tmp"
         _run([NVCC] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"])
         os.replace(tmp, LIB)
+    # the native multi-producer measurement (C ABI only, pthreads)
+    prod_src = os.path.join(CSRC, "gpuos_producers.cpp")
+    if os.path.exists(prod_src) and (force or _stale(PRODUCERS, [prod_src, LIB, os.path.join(INCLUDE, "gpuos.h")])):
+        cxx = shutil.which("g++") or "g++"
+        _run([cxx, "-O2", "-std=c++17", "-I" + INCLUDE, prod_src, "-o", PRODUCERS + ".tmp", "-L" + HERE,
+              "-lgpuos", "-Wl,-rpath,$ORIGIN", "-lpthread"])
+        os.replace(PRODUCERS + ".tmp", PRODUCERS)
     # The example op module is a relocatable object (linked into the executor
     # at run time); it must not use more registers than the executor holds
     # per thread, so it is compiled with the executor's count as its cap.

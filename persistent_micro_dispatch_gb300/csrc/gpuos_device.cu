@@ -1710,6 +1710,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
      * descriptors is read and mirrored in halves of 64 (two per lane) under
      * one acquire fence, one mirror fence and one publication. */
     uint64_t seqv[SEQ_POLL];
+    uint32_t cheap = 0; /* the last poll read slot s only */
 #pragma unroll
     for (int h = 0; h < SEQ_POLL; h++)
         seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
@@ -1727,6 +1728,17 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
         uint32_t k = (rm[0] != ~0ull) ? (uint32_t)(__ffsll((long long)~rm[0]) - 1)
                                       : 64u + ((rm[1] == ~0ull) ? 64u : (uint32_t)(__ffsll((long long)~rm[1]) - 1));
         if (k > wend - s) k = (uint32_t)(wend - s);
+        if (cheap) {
+            /* the last poll read slot s alone: it only tells whether the
+             * window has started; count the batch with a full poll */
+            cheap = 0;
+            if (k) {
+#pragma unroll
+                for (int h = 0; h < SEQ_POLL; h++)
+                    seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
+                continue;
+            }
+        }
         if (k == 0) {
             /* idle: stop flag, exit_after, watchdog */
             if (n_idle++ == 0 || polls == 0) {
@@ -1760,9 +1772,21 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                 }
             }
             backoff(polls, p.spin_polls, p.backoff_min_ns, short_cap(p), &n_sleep);
+            /* Idle. The warp whose window holds the next ticket to be given
+             * work-queue space polls all of its slots; the others read only
+             * their window's first slot (one line across NVLink-C2C instead
+             * of 128), so that idle sequencers do not crowd the SM's
+             * outstanding loads and slow the poll that matters. */
+            if (S > 1 && vb->pub_next != s) {
+                cheap = 1;
 #pragma unroll
-            for (int h = 0; h < SEQ_POLL; h++)
-                seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
+                for (int h = 0; h < SEQ_POLL; h++) seqv[h] = 0;
+                if (lane == 0) seqv[0] = ld_relaxed_sys(&p.ring[(uint32_t)(s & p.ring_mask)].seq);
+            } else {
+#pragma unroll
+                for (int h = 0; h < SEQ_POLL; h++)
+                    seqv[h] = ld_relaxed_sys(&p.ring[(uint32_t)((s + lane + 32u * h) & p.ring_mask)].seq);
+            }
             continue;
         }
         const uint64_t t_obs = globaltimer();

@@ -245,9 +245,16 @@ struct gpuos_ctx {
     bool running = false;   /* executor believed resident */
 };
 
+/* Host activity for the executor's idle watchdog: the host clock in units
+ * of 2^20 ns (about a millisecond), stored only when it has moved on. The
+ * device polls this line, so every store is an invalidation across
+ * NVLink-C2C, and several producer threads would contend for it; one store
+ * a millisecond is plenty for a watchdog counted in seconds. */
 static inline void heartbeat(gpuos_ctx *c)
 {
-    __atomic_fetch_add(&c->hctl->heartbeat, (uint64_t)1, __ATOMIC_RELAXED);
+    const uint64_t ms = now_ns() >> 20;
+    if (__atomic_load_n(&c->hctl->heartbeat, __ATOMIC_RELAXED) != ms)
+        __atomic_store_n(&c->hctl->heartbeat, ms, __ATOMIC_RELAXED);
 }
 
 static inline uint64_t head_of(gpuos_ctx *c) { return __atomic_load_n(&c->head, __ATOMIC_ACQUIRE); }
@@ -754,7 +761,10 @@ int gpuos_executor_stream(gpuos_ctx *c, void **stream)
 }
 
 /* ---- harvesting completion records ------------------------------------------ */
-static void harvest_one(gpuos_ctx *c, uint64_t t)
+/* Harvest ticket t's completion record (once). Counts it in n_completed,
+ * unless `tally` is given: then the caller adds *tally later (several
+ * producers would otherwise contend for the counter once per ticket). */
+static void harvest_one(gpuos_ctx *c, uint64_t t, uint64_t *tally = nullptr)
 {
     const uint32_t slot = (uint32_t)(t & c->mask);
     uint64_t seen = __atomic_load_n(&c->hv[slot], __ATOMIC_ACQUIRE);
@@ -780,7 +790,9 @@ static void harvest_one(gpuos_ctx *c, uint64_t t)
     R.t_done_dev_ns = __atomic_load_n(&r->t_done, __ATOMIC_RELAXED);
     c->recent[slot] = R;
     if (c->history && t >= c->hist_base && t - c->hist_base < c->hist_cap) c->history[t - c->hist_base] = R;
-    if (c->mp)
+    if (tally)
+        (*tally)++;
+    else if (c->mp)
         __atomic_fetch_add(&c->n_completed, (uint64_t)1, __ATOMIC_RELAXED);
     else
         __atomic_store_n(&c->n_completed, __atomic_load_n(&c->n_completed, __ATOMIC_RELAXED) + 1, __ATOMIC_RELAXED);
@@ -1033,6 +1045,9 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
     if (spins) __atomic_fetch_add(&c->host_wait_ns, now_ns() - t_start, __ATOMIC_RELAXED);
     const uint64_t t0 = __atomic_fetch_add(&c->head, (uint64_t)count, __ATOMIC_ACQ_REL);
     if (first_ticket) *first_ticket = t0;
+    /* bodies of the reserved tickets, each once its slot is free; then one
+     * release fence and the commit words (as the single-producer run) */
+    uint64_t harvested = 0;
     for (uint32_t i = 0; i < count; i++) {
         const uint64_t t = t0 + i;
         const uint32_t slot = (uint32_t)(t & c->mask);
@@ -1048,7 +1063,7 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
                 }
                 cpu_relax();
             }
-            harvest_one(c, prev); /* lock-free: one harvester per ticket */
+            harvest_one(c, prev, &harvested); /* lock-free: one harvester per ticket */
         }
         gpuos_desc w = d[i];
         w.ntiles = nts[i];
@@ -1056,14 +1071,18 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
             if (w.dep[k] && (d[i].flags & GPUOS_FLAG_DEP_REL)) w.dep[k] = t - w.dep[k] + 1;
         w.flags = (uint8_t)(d[i].flags & GPUOS_FLAG_FENCE);
         w.ticket = t;
-        gpuos_desc *sl = c->ring + slot;
-        const uint64_t *src = reinterpret_cast<const uint64_t *>(&w);
-        uint64_t *dst = reinterpret_cast<uint64_t *>(sl);
-        for (int q = 0; q < 15; q++) __atomic_store_n(dst + q, src[q], __ATOMIC_RELAXED);
-        c->commit_ns[slot] = now_ns();
-        store_rel(&sl->seq, t + 1);
-        if (n_done) *n_done = i + 1;
+        memcpy(c->ring + slot, &w, offsetof(gpuos_desc, seq));
     }
+    const uint64_t stamp = now_ns();
+    __atomic_thread_fence(__ATOMIC_RELEASE);
+    for (uint32_t i = 0; i < count; i++) {
+        const uint64_t t = t0 + i;
+        const uint32_t slot = (uint32_t)(t & c->mask);
+        c->commit_ns[slot] = stamp;
+        __atomic_store_n(&c->ring[slot].seq, t + 1, __ATOMIC_RELAXED);
+    }
+    if (n_done) *n_done = count;
+    if (harvested) __atomic_fetch_add(&c->n_completed, harvested, __ATOMIC_RELAXED);
     heartbeat(c);
     return GPUOS_OK;
 }
@@ -1244,6 +1263,7 @@ static int handoff(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
     if (!c->running) return GPUOS_ESTOPPED;
     Driver &drv = driver();
     if (!drv.ok) return GPUOS_ECUDA;
+    const uint64_t ts0 = now_ns();
     /* the new set must link before anything stops */
     std::vector<std::vector<unsigned char>> objs;
     for (auto &m : c->modules) objs.push_back(m.bytes);
@@ -1251,6 +1271,7 @@ static int handoff(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
     std::vector<unsigned char> img;
     int rc = link_images(objs, &img);
     if (rc) return rc;
+    const uint64_t ts1 = now_ns();
     /* drain under the old executor (an error status harvested here stays
      * pending for the caller's next gpuos_sync) */
     rc = gpuos_sync(c, UINT64_MAX, 2 * c->cfg.dep_timeout_ms + 1000);
@@ -1269,6 +1290,7 @@ static int handoff(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
     c->running = false;
     c->launched = false;
     if (cudaStreamQuery(c->exec_stream) != cudaSuccess) return GPUOS_ECUDA;
+    const uint64_t ts2 = now_ns();
     gpuos_ctx::Module m;
     m.hash = h;
     m.bytes = std::move(objs.back());
@@ -1304,6 +1326,9 @@ static int handoff(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
     }
     c->running = true;
     c->n_handoffs++;
+    if (getenv("GPUOS_DEBUG"))
+        fprintf(stderr, "gpuos: hand-off %u: link %.2f ms, drain and leave %.2f ms, load and relaunch %.2f ms\n",
+                c->n_handoffs, (ts1 - ts0) / 1e6, (ts2 - ts1) / 1e6, (now_ns() - ts2) / 1e6);
     return GPUOS_OK;
 }
 

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 from oracle.interp import Machine
-from tests.parity import Report, compare_op, writers_of
+from tests.parity import Report, compare_op, operand_accesses, writers_of
 from workloads.streams import NPTYPE, Stream, op_accesses
 
 
@@ -54,7 +54,7 @@ def final_output_ops(s: Stream, candidates: Iterable[int]) -> List[int]:
     """Ops whose written ranges no later op writes (comparable at the end)."""
     out = []
     for j in candidates:
-        if not any(i > j for (b, lo, hi, w) in op_accesses(s, s.ops[j]) if w for i in writers_of(s, b, lo, hi)):
+        if not any(i > j for (b, lo, hi, w) in operand_accesses(s, s.ops[j]) if w for i in writers_of(s, b, lo, hi)):
             out.append(j)
     return out
 
@@ -122,7 +122,7 @@ def comparable_ops(s: Stream, view: TimedView, candidates: Iterable[int]) -> Lis
     written range is final or lies in a buffer the view rebuilds."""
     out = []
     for j in candidates:
-        if not any(i > j for (b, lo, hi, w) in op_accesses(s, s.ops[j]) if w and not view.timed(b)
+        if not any(i > j for (b, lo, hi, w) in operand_accesses(s, s.ops[j]) if w and not view.timed(b)
                    for i in writers_of(s, b, lo, hi)):
             out.append(j)
     return out

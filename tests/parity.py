@@ -124,9 +124,17 @@ def writers_of(s: Stream, b: int, lo: int, hi: int) -> list:
 
 def _scratch(o: Op):
     """The op's scratch operand (decode attention's split-K workspace): the
-    CUDA path's own working memory, whose contents are not an input of the
-    op's result (the oracle never touches it)."""
+    CUDA path's own working memory, whose contents are neither an input nor
+    an output of the op's result (the oracle never touches it)."""
     return o.aux2 if o.op == "sdpa" else None
+
+
+def operand_accesses(s: Stream, o: Op) -> list:
+    """op_accesses without the op's scratch: the ranges its result reads and
+    writes."""
+    sc = _scratch(o)
+    return [(b, lo, hi, w) for (b, lo, hi, w) in op_accesses(s, o)
+            if not (sc is not None and b == sc.buf and lo == sc.off)]
 
 
 def _differing_inputs(s: Stream, o: Op, gpu_read, mach) -> list:
@@ -134,12 +142,9 @@ def _differing_inputs(s: Stream, o: Op, gpu_read, mach) -> list:
     oracle. Inputs no earlier op wrote are identical by construction (the
     seeded inputs); others are compared as the reader returns them."""
     j = mach._op_index[id(o)]
-    sc = _scratch(o)
     diff = []
-    for (b, lo, hi, w) in op_accesses(s, o):
+    for (b, lo, hi, w) in operand_accesses(s, o):
         if w or not written_before(s, b, lo, hi, j):
-            continue
-        if sc is not None and b == sc.buf and lo == sc.off:
             continue
         g = gpu_read(Ref(b, lo), hi - lo)
         r = mach.buf[b][lo:hi]

@@ -633,7 +633,9 @@ def test_operator_compiled_after_launch_enters_by_handoff():
         assert ex.shutdown() == 0
     print(f"hand-off times (s): {times}")
     assert st["errors"] == 0 and st["version"] == 3
-    ver = hist["version"][:len(d)]
+    # tickets: d[:2500] are 0..2499, the scale op 2500, d[2500:] 2501..3000
+    ver = np.concatenate([hist["version"][:2500], hist["version"][2501:]])
+    assert hist["version"][2500] == 2
     assert (ver[:1000] == 0).all() and (ver[1000:2000] == 1).all() and (ver[2000:2500] == 2).all()
     assert (ver[2500:] == 3).all()
     # the relaunched kernel picked up where the old one stopped

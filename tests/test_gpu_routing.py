@@ -84,13 +84,14 @@ def test_routed_ops_match_the_oracle_and_mix_with_normal_launches():
     _ = _[0].float().sum()
     xw = x0.clone()
     xw.add_(1.0)
+    xs = [x0.clone() for _ in range(4)]
+    # (no device-wide synchronize once the executor is resident: it would
+    # wait for a kernel that does not end)
     torch.cuda.synchronize()
     # an executor that leaves room on every SM for the ordinary kernels of the
     # same program (4 warps); the default one fills the SMs and ordinary
     # kernels would wait for it
     ex = G.Executor(warps_per_block=4)
-    xs = [x0.clone() for _ in range(4)]
-    torch.cuda.synchronize()
     try:
         with GpuosRouting(ex, min_calls=2) as r:
             outs = []
