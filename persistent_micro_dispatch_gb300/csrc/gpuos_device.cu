@@ -952,6 +952,15 @@ DEV int row_tile(const gpuos_devdesc *d, uint32_t row)
     const uint32_t R = d->dims[0], H = d->dims[1];
     if (row >= R) return GPUOS_ST_OK;
     if (H == 0) return GPUOS_ST_BAD_ARGS;
+    /* In the executor a helper takes every `helpers`-th row (the count is in
+     * the mirror's last word; 0 elsewhere): start the row it runs next on its
+     * way into L2 while this one is worked on, so that its copy then comes
+     * from L2 rather than HBM. */
+    const uint32_t hs = d->pad;
+    if (hs && row + hs < R && lane_id() == 0 && ((H & 7u) | (uint32_t)(d->a & 15u)) == 0) {
+        const uint16_t *nx = reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)(row + hs) * H;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nx), "r"(2u * H) : "memory");
+    }
     bool ok = (H & 7u) == 0 && (d->a & 15u) == 0;
     if (K == ROW_SOFTMAX || K == ROW_LN) ok = ok && (d->out & 15u) == 0;
     if (K == ROW_LN) ok = ok && ((d->b | d->aux0) & 15u) == 0;
@@ -2215,15 +2224,21 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, uint
          * claim. */
         int32_t status = dstatus;
         uint32_t count = 0;
+        /* Row ops: every row is the same work, so helper h takes rows h,
+         * h + helpers, ... with no counter round trip, and the op knows which
+         * row to prefetch next. Other ops take later tiles from the counter
+         * (tiles of decode attention past a short request are cheap). */
+        const bool strided = sd->op_id >= GPUOS_OP_SOFTMAX && sd->op_id <= GPUOS_OP_ROWMIN;
         while (true) {
             uint32_t next = ntiles;
-            if (ntiles > helpers && lane == 0) next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
+            if (strided) next = tile + helpers;
+            else if (ntiles > helpers && lane == 0) next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
             if (status == GPUOS_ST_OK) {
                 if (fn == nullptr) status = GPUOS_ST_BAD_OP;
                 else status = fn(sd, tile);
             }
             count++;
-            next = __shfl_sync(0xFFFFFFFFu, next, 0);
+            if (!strided) next = __shfl_sync(0xFFFFFFFFu, next, 0);
             if (next >= ntiles) break;
             tile = next;
         }

@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include <dlfcn.h>
+#include <sched.h>
 
 #include <atomic>
 #include <cstddef>
@@ -809,10 +810,12 @@ static bool is_done(gpuos_ctx *c, uint64_t t)
 
 static void sweep(gpuos_ctx *c)
 {
-    /* tickets older than head - N were harvested when their slot was reused
-     * (reserved tickets not yet committed are simply not done) */
+    /* one producer: tickets older than head - N were harvested when their
+     * slot was reused (it is reused only after they completed). Several
+     * producers reserve tickets before their slots are free, so there every
+     * ticket is checked */
     const uint64_t head = head_of(c);
-    if (head > c->N && c->low < head - c->N) __atomic_store_n(&c->low, head - c->N, __ATOMIC_RELEASE);
+    if (!c->mp && head > c->N && c->low < head - c->N) __atomic_store_n(&c->low, head - c->N, __ATOMIC_RELEASE);
     uint64_t low = c->low;
     while (low < head) {
         const uint32_t slot = (uint32_t)(low & c->mask);
@@ -996,9 +999,45 @@ static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, ui
     return rc;
 }
 
-/* Multiple producers: validate every descriptor, wait for room, reserve
- * count consecutive tickets with one atomic add, then write and commit them
- * (each slot once its previous ticket completed). */
+/* A waiting producer's spin step. Every 256 polls: the deadline (when one
+ * is given), the heartbeat and, when the device has flagged that it is
+ * leaving or 10 ms have passed, whether the executor kernel has ended (a
+ * CUDA runtime query, which takes a lock the other producers would fight
+ * over if it ran on every poll). After a few thousand polls the thread
+ * yields its core: there may be more producer threads than cores. */
+struct ProducerWait {
+    uint64_t t0 = 0, last = 0;
+    uint32_t spins = 0;
+    int step(gpuos_ctx *c, uint64_t timeout_ns)
+    {
+        if ((++spins & 255u) != 0) {
+            cpu_relax();
+            return GPUOS_OK;
+        }
+        const uint64_t now = now_ns();
+        if (t0 == 0) t0 = last = now;
+        heartbeat(c);
+        if (timeout_ns && now - t0 > timeout_ns) return GPUOS_EAGAIN;
+        if (__atomic_load_n(&c->hctl->state, __ATOMIC_RELAXED) == 2u || now - last > 10000000ull) {
+            last = now;
+            if (executor_gone(c)) {
+                c->running = false;
+                return GPUOS_ESTOPPED;
+            }
+        }
+        if (spins > 4096u) sched_yield();
+        return GPUOS_OK;
+    }
+};
+
+/* Multiple producers: validate every descriptor, wait (up to the timeout)
+ * until the slot the batch's last ticket would take is free, reserve count
+ * consecutive tickets with one atomic add, then write every body (each once
+ * its slot is free: another producer may have taken the tickets counted on),
+ * one release fence and the commit words. Each producer harvests the
+ * records of the slots it reuses, so no lock is taken on this path. The
+ * work queue hands out space in ticket order, which with these per-slot
+ * waits keeps its wrap-around safe. */
 static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t *first_ticket,
                      uint32_t *n_done, uint32_t timeout_us)
 {
@@ -1011,7 +1050,13 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
     }
     if (count == 0) return GPUOS_OK;
     if (count > c->N) return GPUOS_EINVAL;
-    std::vector<uint32_t> nts(count);
+    uint32_t nts_small[64];
+    std::vector<uint32_t> nts_big;
+    uint32_t *nts = nts_small;
+    if (count > 64) {
+        nts_big.resize(count);
+        nts = nts_big.data();
+    }
     const uint64_t h0 = head_of(c);
     for (uint32_t i = 0; i < count; i++) {
         const bool user_known = d[i].op_id >= GPUOS_OP_USER_FIRST && c->user_registered[d[i].op_id];
@@ -1021,47 +1066,30 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
         for (int k = 0; k < 2; k++)
             if (d[i].dep[k] > h0 + i) return GPUOS_EINVAL;
     }
-    /* room for the batch (other producers may take it first: then the
-     * reserved slots below are waited for) */
-    const uint64_t t_start = now_ns();
-    uint32_t spins = 0;
+    /* room: the slot of the last ticket the batch would take from the
+     * current head is free */
+    ProducerWait wt;
     while (true) {
-        if (head_of(c) + count <= __atomic_load_n(&c->low, __ATOMIC_ACQUIRE) + c->N) break;
-        if (c->hmu.try_lock()) { /* one producer advances the harvest; the others spin */
-            sweep(c);
-            c->hmu.unlock();
-            if (head_of(c) + count <= __atomic_load_n(&c->low, __ATOMIC_ACQUIRE) + c->N) break;
-        }
-        if ((++spins & 255u) == 0) {
-            heartbeat(c);
-            if (now_ns() - t_start > (uint64_t)timeout_us * 1000ull) return GPUOS_EAGAIN;
-            if (executor_gone(c)) {
-                c->running = false;
-                return GPUOS_ESTOPPED;
-            }
-        }
-        cpu_relax();
+        const uint64_t h = head_of(c);
+        if (h + count <= c->N || is_done(c, h + count - 1 - c->N)) break;
+        const int rc = wt.step(c, (uint64_t)timeout_us * 1000ull);
+        if (rc) return rc;
     }
-    if (spins) __atomic_fetch_add(&c->host_wait_ns, now_ns() - t_start, __ATOMIC_RELAXED);
+    if (wt.t0) __atomic_fetch_add(&c->host_wait_ns, now_ns() - wt.t0, __ATOMIC_RELAXED);
     const uint64_t t0 = __atomic_fetch_add(&c->head, (uint64_t)count, __ATOMIC_ACQ_REL);
     if (first_ticket) *first_ticket = t0;
-    /* bodies of the reserved tickets, each once its slot is free; then one
-     * release fence and the commit words (as the single-producer run) */
+    /* A reserved ticket is always committed (the executor takes tickets in
+     * order): from here the waits have no deadline, only the executor's end. */
     uint64_t harvested = 0;
+    ProducerWait ws;
     for (uint32_t i = 0; i < count; i++) {
         const uint64_t t = t0 + i;
         const uint32_t slot = (uint32_t)(t & c->mask);
         if (t >= c->N) {
             const uint64_t prev = t - c->N;
             while (!is_done(c, prev)) {
-                if ((++spins & 1023u) == 0) {
-                    heartbeat(c);
-                    if (executor_gone(c)) {
-                        c->running = false;
-                        return GPUOS_ESTOPPED;
-                    }
-                }
-                cpu_relax();
+                const int rc = ws.step(c, 0);
+                if (rc) return rc;
             }
             harvest_one(c, prev, &harvested); /* lock-free: one harvester per ticket */
         }
@@ -1083,6 +1111,7 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
     }
     if (n_done) *n_done = count;
     if (harvested) __atomic_fetch_add(&c->n_completed, harvested, __ATOMIC_RELAXED);
+    if (ws.t0) __atomic_fetch_add(&c->host_wait_ns, now_ns() - ws.t0, __ATOMIC_RELAXED);
     heartbeat(c);
     return GPUOS_OK;
 }
