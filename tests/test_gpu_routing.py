@@ -126,11 +126,16 @@ def test_routed_ops_match_the_oracle_and_mix_with_normal_launches():
     rl_want, _ = O.ew("relu", 0, X0)
     for k, (y, gl, p, mx, mn, sm, m, tot, rl) in enumerate(outs):
         assert np.array_equal(_bits(y).view(np.uint32), y_want.view(np.uint32))  # fp32 add, ReLU, mul: exact
-        # the first pass is PyTorch's own GELU (routing starts at the second
-        # call of a signature); routed passes meet the parity bar
-        rel = 1e-4 if k == 0 else 1e-5
         ge = np.abs(_bits(gl).astype(np.float64) - g_exact)
-        assert (ge <= rel * np.maximum(np.abs(g_exact), 1e-3 * np.sqrt(np.mean(g_exact ** 2)))).all(), (k, ge.max())
+        if k == 0:
+            # the first pass is PyTorch's own GELU (routing starts at the
+            # second call of a signature): 0.5 x (1 + erf(x / sqrt 2)) loses
+            # relative accuracy in the negative tail, where 1 + erf cancels
+            assert (ge <= 1e-6 + 1e-4 * np.abs(g_exact)).all(), ge.max()
+        else:
+            # routed passes: the parity bar (the library's GELU uses erfc)
+            bound = 1e-5 * np.maximum(np.abs(g_exact), 1e-3 * np.sqrt(np.mean(g_exact ** 2)))
+            assert (ge <= bound).all(), (k, ge.max())
         pe = np.abs(_f64(_bits(p).reshape(-1)) - p_exact)
         assert (pe <= np.maximum(2e-2, ulp_bf16(p_exact))).all(), pe.max()
         assert np.array_equal(_bits(mx), mx_want) and np.array_equal(_bits(mn), mn_want)
