@@ -242,9 +242,7 @@ struct StageHdr {
 struct WarpStage {
     unsigned long long mbar[2]; /* completion barriers of the warp's bulk copies */
     uint32_t phase[2];          /* parity of the next phase to wait for, per barrier */
-    uint32_t pf_row;            /* row ops: row + 1 of the copy in flight into half pf_row >> 31
-                                   (0: none) ... */
-    uint32_t pf_ticket;         /* ... for the descriptor with this ticket (low 32 bits) */
+    uint32_t pad[2];
 };
 #define GPUOS_WARP_STAGE_HDR 32u
 extern __shared__ __align__(16) unsigned char g_dyn_smem[];
@@ -271,8 +269,6 @@ DEV void stage_init(uint32_t stage_bytes)
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&w->mbar[1])) : "memory");
         w->phase[0] = 0;
         w->phase[1] = 0;
-        w->pf_row = 0;
-        w->pf_ticket = 0;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
@@ -750,99 +746,24 @@ DEV bool stage_wait0(WarpStage *w)
     return ok;
 }
 
-/* Lane 0: start the copy of row `row` (and LayerNorm's first C columns of
- * gamma and beta) into `buf`, completing on barrier `mb`. */
-template <int K>
-DEV void row_issue(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C, unsigned char *buf,
-                   unsigned long long *mb)
-{
-    const uint16_t *x = reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)row * H;
-    mbar_expect(mb, 2u * H + (K == ROW_LN ? 4u * C : 0u));
-    bulk_g2s(buf, x, 2u * H, mb);
-    if (K == ROW_LN) {
-        bulk_g2s(buf + 2u * H, reinterpret_cast<const void *>(d->b), 2u * C, mb);
-        bulk_g2s(buf + 2u * H + 2u * C, reinterpret_cast<const void *>(d->aux0), 2u * C, mb);
-    }
-}
-
-/* Wait (bounded, every lane) for barrier i's next phase and flip its parity. */
-DEV bool stage_wait(WarpStage *w, uint32_t i)
-{
-    const uint32_t ph = w->phase[i];
-    const bool ok = mbar_wait(&w->mbar[i], ph);
-    if (!ok) mbar_wait(&w->mbar[i], ph); /* leave no copy writing the buffer */
-    __syncwarp();
-    if (lane_id() == 0) w->phase[i] = ph ^ 1u;
-    __syncwarp();
-    return ok;
-}
-
-template <int K>
-DEV int row_compute(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C, unsigned char *buf, WarpStage *w);
-
-/* One row staged in the whole buffer (single-buffered). */
 template <int K>
 DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
 {
+    const uint32_t lane = lane_id(), nv = H / 8;
     WarpStage *w = warp_stage();
     unsigned char *buf = warp_stage_buf();
-    if (lane_id() == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        row_issue<K>(d, row, H, C, buf, &w->mbar[0]);
-    }
-    if (!stage_wait0(w)) return GPUOS_ST_COPY_TIMEOUT;
-    return row_compute<K>(d, row, H, C, buf, w);
-}
-
-/* Rows whose copy fits half the buffer, in the executor: while this row is
- * worked on in one half, the helper's next row (row + hs: a helper takes
- * every hs-th row) is copied into the other half, and the next call finds
- * it there. A copy is started only for a row this helper runs next, so it
- * is always consumed by the helper's next tile; one left over all the
- * same (not expected) is waited for before its half is reused. */
-template <int K>
-DEV int row_double(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t hs)
-{
-    WarpStage *w = warp_stage();
-    const uint32_t lane = lane_id(), R = d->dims[0];
-    const uint32_t hb = (stage_hdr()->stage_bytes / 2u) & ~15u;
-    unsigned char *base = warp_stage_buf();
-    const uint32_t tk = (uint32_t)d->ticket;
-    const uint32_t tag = w->pf_row;
-    const bool have = tag != 0 && (tag & 0x7FFFFFFFu) == row + 1u && w->pf_ticket == tk;
-    const uint32_t cur = have ? (tag >> 31) : 0u;
-    bool ok = true;
-    if (!have && tag != 0) ok = stage_wait(w, tag >> 31); /* a stray copy: let it land first */
+    const uint4 *sx = reinterpret_cast<const uint4 *>(buf);
+    const uint16_t *x = reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)row * H;
     if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (!have) row_issue<K>(d, row, H, H, base + cur * hb, &w->mbar[cur]);
-        if (hs && row + hs < R) {
-            const uint32_t nx = cur ^ 1u;
-            row_issue<K>(d, row + hs, H, H, base + nx * hb, &w->mbar[nx]);
-            w->pf_row = (row + hs + 1u) | (nx << 31);
-            w->pf_ticket = tk;
-        } else {
-            w->pf_row = 0;
+        mbar_expect(&w->mbar[0], 2u * H + (K == ROW_LN ? 4u * C : 0u));
+        bulk_g2s(buf, x, 2u * H, &w->mbar[0]);
+        if (K == ROW_LN) {
+            bulk_g2s(buf + 2u * H, reinterpret_cast<const void *>(d->b), 2u * C, &w->mbar[0]);
+            bulk_g2s(buf + 2u * H + 2u * C, reinterpret_cast<const void *>(d->aux0), 2u * C, &w->mbar[0]);
         }
     }
-    __syncwarp();
-    if (!stage_wait(w, cur)) ok = false;
-    if (!ok) {
-        const uint32_t t2 = w->pf_row;
-        if (t2 != 0) stage_wait(w, t2 >> 31); /* no copy may outlive this tile's failure */
-        __syncwarp();
-        if (lane == 0) w->pf_row = 0;
-        __syncwarp();
-        return GPUOS_ST_COPY_TIMEOUT;
-    }
-    return row_compute<K>(d, row, H, H, base + cur * hb, w);
-}
-
-template <int K>
-DEV int row_compute(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C, unsigned char *buf, WarpStage *w)
-{
-    const uint32_t lane = lane_id(), nv = H / 8;
-    const uint4 *sx = reinterpret_cast<const uint4 *>(buf);
+    if (!stage_wait0(w)) return GPUOS_ST_COPY_TIMEOUT;
     if (K == ROW_SUM || K == ROW_MAX || K == ROW_MIN) {
         const float init = (K == ROW_SUM) ? 0.0f : (K == ROW_MAX ? -INFINITY : INFINITY);
         float a8[8];
@@ -1038,11 +959,6 @@ DEV int row_tile(const gpuos_devdesc *d, uint32_t row)
     /* staged: the row, plus (LayerNorm) gamma and beta in chunks of C
      * columns, a multiple of 8 of at least 256 (or all H) */
     const uint32_t sb = stage_hdr()->stage_bytes;
-    /* In the executor a helper takes every hs-th row (hs, the helper count,
-     * is in the mirror's last word; 0 elsewhere): rows whose copy (with
-     * LayerNorm's gamma and beta) fits half the buffer are double-buffered */
-    const uint32_t hs = d->pad;
-    if (hs && (2u * H + (K == ROW_LN ? 4u * H : 0u)) <= ((sb / 2u) & ~15u)) return row_double<K>(d, row, H, hs);
     if (2u * H <= sb) {
         uint32_t C = 0;
         if (K == ROW_LN) {
@@ -2299,21 +2215,15 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, uint
          * claim. */
         int32_t status = dstatus;
         uint32_t count = 0;
-        /* Row ops: every row is the same work, so helper h takes rows h,
-         * h + helpers, ... with no counter round trip, and the op knows which
-         * row to prefetch next. Other ops take later tiles from the counter
-         * (tiles of decode attention past a short request are cheap). */
-        const bool strided = sd->op_id >= GPUOS_OP_SOFTMAX && sd->op_id <= GPUOS_OP_ROWMIN;
         while (true) {
             uint32_t next = ntiles;
-            if (strided) next = tile + helpers;
-            else if (ntiles > helpers && lane == 0) next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
+            if (ntiles > helpers && lane == 0) next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
             if (status == GPUOS_ST_OK) {
                 if (fn == nullptr) status = GPUOS_ST_BAD_OP;
                 else status = fn(sd, tile);
             }
             count++;
-            if (!strided) next = __shfl_sync(0xFFFFFFFFu, next, 0);
+            next = __shfl_sync(0xFFFFFFFFu, next, 0);
             if (next >= ntiles) break;
             tile = next;
         }
