@@ -167,11 +167,12 @@ typedef struct gpuos_config {
     uint32_t multi_producer;  /* 0 (default): one submitting thread (SPSC ring, no locks);
                                  1: any number of host threads may call gpuos_submit /
                                  gpuos_submit_batch concurrently (see gpuos_submit) */
-    uint32_t sequencers;      /* warps of block 0 that take descriptors off the ring, 1..4
-                                 (and below warps_per_block when blocks == 1); 0 = default:
-                                 4 with more than one block, else 1. Tickets are cut into
-                                 windows of 128 (or ring_entries, if smaller), taken in turn;
-                                 work-queue space is still given out in ticket order */
+    uint32_t sequencers;      /* warps that take descriptors off the ring, 1..4, one per block
+                                 (blocks 0 .. sequencers-1 run no workers; fewer than blocks;
+                                 1 when blocks == 1); 0 = default: 4 on 32 blocks or more, 2
+                                 on 16 or more, else 1. Tickets are cut into windows of 128
+                                 (or ring_entries, if smaller), taken in turn; work-queue
+                                 space is still given out in ticket order */
     uint32_t reserved;
 } gpuos_config;
 

@@ -1639,49 +1639,49 @@ DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles, uint32_t workers)
     return hlp < cap ? hlp : cap;
 }
 
-/* Work-queue reservation shared by the sequencer warps of block 0 (shared
- * memory). Work-queue space is given out in ticket order: the warp whose
- * batch starts at ticket pub_next takes tq_head, advances it by the batch's
- * entries and passes the turn on. Workers claim entries in queue order, so
- * an entry of a descriptor is never queued behind the entries of a later
- * descriptor that may wait for it (with several sequencers, a later window
- * may be ready first). */
-struct SeqBaton {
-    unsigned long long pub_next; /* first ticket whose entries are not reserved yet */
-    unsigned long long tq_head;  /* next free work-queue index */
-};
+/* Work-queue reservation shared by the sequencer warps (each on an SM of its
+ * own; the turn lives in device memory, dctl->pub_next and dctl->tq_head).
+ * Work-queue space is given out in ticket order: the warp whose batch starts
+ * at ticket pub_next takes tq_head, advances it by the batch's entries and
+ * passes the turn on. Workers claim entries in queue order, so an entry of a
+ * descriptor is never queued behind the entries of a later descriptor that
+ * may wait for it (with several sequencers, a later window may be ready
+ * first). */
 
-/* Lane 0: wait (bounded) for the turn of the batch starting at ticket s. */
-DEV bool baton_wait(volatile SeqBaton *b, uint64_t s, uint64_t bound_ns)
+/* Lane 0: wait (bounded) for the turn of the batch starting at ticket s;
+ * then the previous holder's tq_head is visible. */
+DEV bool baton_wait(const gpuos_exec_params &p, uint64_t s, uint64_t bound_ns)
 {
     Elapsed w;
     w.start();
     uint32_t n = 0;
-    while (b->pub_next != s) {
+    while (ld_relaxed_gpu(&p.dctl->pub_next) != s) {
         if ((++n & 63u) == 0 && w.tick(globaltimer()) > bound_ns) return false;
     }
-    __threadfence_block(); /* the previous holder's tq_head before it */
+    fence_acq_rel_gpu(); /* the acquire, once */
     return true;
 }
 
-/* Lane 0: pass the turn on to the batch starting at ticket `next`. */
-DEV void baton_pass(volatile SeqBaton *b, uint64_t next)
+/* Lane 0: record the next free work-queue index and pass the turn on to the
+ * batch starting at ticket `next`. */
+DEV void baton_pass(const gpuos_exec_params &p, uint64_t tq_head, uint64_t next)
 {
-    __threadfence_block(); /* tq_head before the turn moves */
-    b->pub_next = next;
+    st_relaxed_gpu(reinterpret_cast<unsigned long long *>(&p.dctl->tq_head), tq_head);
+    st_release_gpu(&p.dctl->pub_next, next);
 }
 
 /* A sequencer warp: ring -> mirror + work queue, up to 128 descriptors per
  * batch (four ring slots per lane: slot s + lane + 32 h). With S sequencer
- * warps, tickets are cut into windows of 128 (or the ring size, if smaller)
- * and warp sq takes windows sq, sq + S, sq + 2S, ...: reading, checking and
- * mirroring descriptors run in parallel; only the reservation of
- * work-queue space follows ticket order (SeqBaton). */
+ * warps (warp 0 of blocks 0 .. S-1), tickets are cut into windows of 128
+ * (or the ring size, if smaller) and sequencer sq takes windows sq,
+ * sq + S, sq + 2S, ...: reading, checking and mirroring descriptors run in
+ * parallel on S SMs; only the reservation of work-queue space follows
+ * ticket order (baton_wait / baton_pass). */
 #define SEQ_SPL 2    /* ring slots per lane in one half of a batch (64 descriptors) */
 #define SEQ_HALVES 2 /* halves per batch */
 #define SEQ_POLL (SEQ_SPL * SEQ_HALVES)
 DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, unsigned long long *s_table,
-                   uint32_t sq, uint32_t S, SeqBaton *baton)
+                   uint32_t sq, uint32_t S)
 {
     const uint32_t lane = lane_id();
     uint32_t cached_version = 0xFFFFFFFFu; /* version whose table slot s_table holds */
@@ -1700,7 +1700,6 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
     s = p.ticket_base + (uint64_t)WIN * sq;
     e = p.tq_base;
     uint64_t wend = s + WIN;
-    volatile SeqBaton *vb = baton;
     if (lane == 0 && sq == 0) st_relaxed_sys32(&p.hctl->state, 1u);
 
     /* commit words of slots s + lane + 32 h (h < SEQ_POLL), polled ahead
@@ -1777,7 +1776,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
              * their window's first slot (one line across NVLink-C2C instead
              * of 128), so that idle sequencers do not crowd the SM's
              * outstanding loads and slow the poll that matters. */
-            if (S > 1 && vb->pub_next != s) {
+            if (S > 1 && ld_relaxed_gpu(&p.dctl->pub_next) != s) {
                 cheap = 1;
 #pragma unroll
                 for (int h = 0; h < SEQ_POLL; h++) seqv[h] = 0;
@@ -1923,8 +1922,8 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                 /* no work-queue space, but the turn passes through it */
                 uint32_t ok = 1;
                 if (lane == 0) {
-                    ok = baton_wait(vb, s, p.dep_timeout_ns) ? 1u : 0u;
-                    if (ok) baton_pass(vb, s + 1);
+                    ok = baton_wait(p, s, p.dep_timeout_ns) ? 1u : 0u;
+                    if (ok) baton_pass(p, ld_relaxed_gpu(&p.dctl->tq_head), s + 1);
                     else set_exit(p, 4u);
                 }
                 if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
@@ -2008,11 +2007,10 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             uint32_t ok = 1;
             unsigned long long e0 = 0;
             if (lane == 0) {
-                ok = baton_wait(vb, s, p.dep_timeout_ns) ? 1u : 0u;
+                ok = baton_wait(p, s, p.dep_timeout_ns) ? 1u : 0u;
                 if (ok) {
-                    e0 = vb->tq_head;
-                    vb->tq_head = e0 + total;
-                    baton_pass(vb, s + k);
+                    e0 = ld_relaxed_gpu(&p.dctl->tq_head);
+                    baton_pass(p, e0 + total, s + k);
                 } else {
                     set_exit(p, 4u);
                 }
@@ -2283,23 +2281,25 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, uint
 extern "C" __global__ void __launch_bounds__(GPUOS_MAX_WPB * 32, 1) gpuos_executor_kernel(gpuos_exec_params p)
 {
     __shared__ __align__(16) gpuos_devdesc sdesc[GPUOS_MAX_WPB];
-    __shared__ unsigned long long s_table[GPUOS_MAX_SEQ][GPUOS_MAX_OPS]; /* each sequencer's copy of one table slot */
+    __shared__ unsigned long long s_table[GPUOS_MAX_OPS]; /* the sequencer's copy of one table slot */
     __shared__ uint64_t s_prof[GPUOS_MAX_WPB][GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS]; /* tile profiles */
-    __shared__ SeqBaton s_baton;
     const uint32_t warp = threadIdx.x >> 5;
     for (uint32_t i = threadIdx.x & 31u; i < GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS; i += 32) s_prof[warp][i] = 0;
-    if (threadIdx.x == 0) {
-        s_baton.pub_next = p.ticket_base;
-        s_baton.tq_head = p.tq_base;
-    }
-    stage_init(p.stage_bytes); /* (its block barriers also order the writes above) */
+    stage_init(p.stage_bytes); /* (its block barriers also order the clearing above) */
     const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
-    /* Block 0 holds the sequencer warps alone (unless it is the only block):
-     * worker warps beside them would share their issue slots and
-     * load/store pipe, and the sequencers set the executor's dispatch rate. */
+    /* Blocks 0 .. S-1 each hold one sequencer warp and nothing else (unless
+     * there is only one block): worker warps beside a sequencer would share
+     * its issue slots and load/store pipe, and sequencers on one SM slowed
+     * each other (one SM's outstanding loads across NVLink-C2C). */
     const uint32_t S = p.sequencers;
-    if (blockIdx.x == 0 && warp < S) sequencer(p, &sdesc[warp], gw, s_table[warp], warp, S, &s_baton);
-    else if (blockIdx.x != 0 || gridDim.x == 1) worker(p, &sdesc[warp], gw, s_prof[warp]);
+    if (gridDim.x == 1) {
+        if (warp == 0) sequencer(p, &sdesc[0], gw, s_table, 0u, 1u);
+        else worker(p, &sdesc[warp], gw, s_prof[warp]);
+    } else if (blockIdx.x < S) {
+        if (warp == 0) sequencer(p, &sdesc[0], gw, s_table, blockIdx.x, S);
+    } else {
+        worker(p, &sdesc[warp], gw, s_prof[warp]);
+    }
 }
 
 /* ===========================================================================

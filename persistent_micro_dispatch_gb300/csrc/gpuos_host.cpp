@@ -528,8 +528,10 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device));
     c->blocks = cfg.blocks ? cfg.blocks : (uint32_t)sms;
     c->wpb = cfg.warps_per_block;
-    if (cfg.sequencers == 0) cfg.sequencers = c->blocks > 1 ? (GPUOS_MAX_SEQ < c->wpb ? GPUOS_MAX_SEQ : c->wpb) : 1u;
-    if (cfg.sequencers > c->wpb || (c->blocks == 1 && cfg.sequencers >= c->wpb)) {
+    /* sequencers (warp 0 of blocks 0 .. S-1, SMs without workers): four on a
+     * large grid, fewer on a small one, one with a single block */
+    if (cfg.sequencers == 0) cfg.sequencers = c->blocks >= 32 ? 4u : (c->blocks >= 16 ? 2u : 1u);
+    if ((c->blocks == 1 && cfg.sequencers != 1) || (c->blocks > 1 && cfg.sequencers >= c->blocks)) {
         free_all(c);
         return GPUOS_EINVAL;
     }
@@ -644,7 +646,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     p.stage_bytes = cfg.stage_bytes;
     /* worker warps: block 0 holds only the sequencers (when there are others) */
     p.sequencers = cfg.sequencers;
-    p.workers = c->blocks > 1 ? (c->blocks - 1) * c->wpb : c->wpb - cfg.sequencers;
+    p.workers = c->blocks > 1 ? (c->blocks - cfg.sequencers) * c->wpb : c->wpb - 1;
     p.idle_exit_ns = (uint64_t)cfg.idle_exit_ms * 1000000ull;
     p.dep_timeout_ns = (uint64_t)(cfg.dep_timeout_ms ? cfg.dep_timeout_ms : 5000) * 1000000ull;
     p.exit_after = cfg.exit_after;
@@ -1337,6 +1339,13 @@ static int handoff(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
         return GPUOS_ECUDA;
     c->params.ticket_base = c->head;
     c->params.tq_base = *claim;
+    /* the sequencers' turn starts there too */
+    uint64_t *turn = reinterpret_cast<uint64_t *>(c->version_stage + 8);
+    turn[0] = c->params.ticket_base;
+    turn[1] = c->params.tq_base;
+    if (cudaMemcpyAsync(&c->dctl->pub_next, turn, 16, cudaMemcpyHostToDevice, c->ctl_stream) != cudaSuccess ||
+        cudaStreamSynchronize(c->ctl_stream) != cudaSuccess)
+        return GPUOS_ECUDA;
     store_rel(&c->hctl->stop, 0u);
     __atomic_store_n(&c->hctl->exit_reason, 0u, __ATOMIC_RELAXED);
     store_rel(&c->hctl->state, 0u);
@@ -1439,11 +1448,11 @@ int gpuos_stats(gpuos_ctx *c, gpuos_stats_t *st)
         st->sleeps += x[GPUOS_WS_SLEEPS];
         st->dep_waits += x[GPUOS_WS_DEPWAIT];
     }
-    /* warps 0 .. sequencers-1 of block 0 are the sequencers: their phase
+    /* warp 0 of blocks 0 .. sequencers-1 are the sequencers: their phase
      * timers (summed) and the descriptors they took off the ring */
     uint64_t seq_taken = 0;
-    for (uint32_t w = 0; w < c->cfg.sequencers && w < tw; w++) {
-        const uint64_t *x = &ws[(size_t)w * GPUOS_WS_N];
+    for (uint32_t b = 0; b < c->cfg.sequencers && b < c->blocks; b++) {
+        const uint64_t *x = &ws[(size_t)b * c->wpb * GPUOS_WS_N];
         st->seq_body_ns += x[GPUOS_WS_T_BODY];
         st->seq_mirror_ns += x[GPUOS_WS_T_MIRROR];
         st->seq_publish_ns += x[GPUOS_WS_T_PUB];

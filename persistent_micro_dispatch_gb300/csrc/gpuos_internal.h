@@ -27,9 +27,8 @@
 #define GPUOS_MAX_SEQ 4 /* sequencer warps at most */
 #define GPUOS_SHORT_SLEEP_NS 256u /* longest idle sleep on the dispatch path (ring poll, dependency waits) */
 /* static shared memory of the executor kernel: descriptor copies, the
- * sequencers' table copies, per-warp tile profiles, the sequencers' turn */
-#define GPUOS_EXEC_STATIC_SMEM \
-    (GPUOS_MAX_WPB * 128 + GPUOS_MAX_SEQ * 256 * 8 + GPUOS_MAX_WPB * GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS * 8 + 16)
+ * sequencer's table copy, per-warp tile profiles */
+#define GPUOS_EXEC_STATIC_SMEM (GPUOS_MAX_WPB * 128 + 256 * 8 + GPUOS_MAX_WPB * GPUOS_PROF_FIELDS * GPUOS_PROF_BUCKETS * 8)
 #define GPUOS_MAX_REGS 168 /* registers per thread: 65536 / (12 warps x 32), in steps of 8 */
 #define GPUOS_TILE_MAX (1u << 30)          /* tiles per descriptor */
 #define GPUOS_HELPERS 2048                 /* work-queue entries (helper warps) per descriptor at most */
@@ -91,6 +90,9 @@ typedef struct gpuos_devctl {
     uint32_t exit_flag; /* nonzero: workers leave when they find no work */
     uint32_t version;   /* operator-table version */
     uint64_t pad2[15];
+    uint64_t pub_next;  /* sequencers' turn: first ticket whose work-queue space is not reserved */
+    uint64_t tq_head;   /* ... and the next free work-queue index */
+    uint64_t pad3[14];
 } gpuos_devctl;
 
 /* Per-warp counters (owned by one warp each, plain stores). */
