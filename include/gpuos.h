@@ -177,7 +177,8 @@ typedef struct gpuos_config {
                                  least 2,048 descriptors (gpuos_submit_batch), the caller and
                                  submit_threads - 1 helpers started by gpuos_init, 0 or 1 = the
                                  caller alone (default), at most 16. Such a batch is validated
-                                 first, then runs of 64 are written and committed in turn by
+                                 first, then runs of 128 tickets (the sequencers' windows)
+                                 are written and committed in turn by
                                  every thread; once started it waits for ring slots without a
                                  timeout (only the executor's end stops it) */
 } gpuos_config;

@@ -1068,16 +1068,21 @@ static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, ui
  * another in a cycle. Slot waits have no deadline: every ticket of the batch
  * is already given out and must be committed; only the executor's end
  * stops them. */
+#define GPUOS_PAR_RUN 128u /* a run of the parallel path: one sequencer window of tickets */
 static void write_runs(gpuos_ctx *c, uint32_t part)
 {
     auto &P = c->pool;
-    const uint32_t nrun = (P.count + GPUOS_COMMIT_RUN - 1) / GPUOS_COMMIT_RUN;
+    /* runs follow the sequencers' windows (ticket multiples of 128), so a
+     * window is committed by one writer in one piece */
+    const uint64_t w0 = P.t0 / GPUOS_PAR_RUN, w1 = (P.t0 + P.count + GPUOS_PAR_RUN - 1) / GPUOS_PAR_RUN;
+    const uint32_t nrun = (uint32_t)(w1 - w0);
     uint64_t harvested = 0;
     ProducerWait ws;
     for (uint32_t r = part; r < nrun; r += P.parts) {
         if (P.err.load(std::memory_order_relaxed)) break;
-        const uint32_t i0 = r * GPUOS_COMMIT_RUN;
-        const uint32_t i1 = P.count - i0 < GPUOS_COMMIT_RUN ? P.count : i0 + GPUOS_COMMIT_RUN;
+        const uint64_t a = (w0 + r) * GPUOS_PAR_RUN, b = a + GPUOS_PAR_RUN;
+        const uint32_t i0 = (uint32_t)((a > P.t0 ? a : P.t0) - P.t0);
+        const uint32_t i1 = (uint32_t)((b < P.t0 + P.count ? b : P.t0 + P.count) - P.t0);
         for (uint32_t i = i0; i < i1; i++) {
             const uint64_t t = P.t0 + i;
             const uint32_t slot = (uint32_t)(t & c->mask);
