@@ -640,8 +640,6 @@ def main():
     ap.add_argument("--stage-bytes", type=int, default=16384, help="shared-memory staging per warp (0 = none)")
     ap.add_argument("--blocks", type=int, default=0, help="executor blocks (0 = one per SM)")
     ap.add_argument("--sequencers", type=int, default=0, help="sequencer warps (0 = the library's default)")
-    ap.add_argument("--submit-threads", type=int, default=1,
-                    help="host threads writing each step's batch (the caller and helpers inside the library)")
     ap.add_argument("--spin-polls", type=int, default=0, help="idle polls before backoff sleeps (0 = default)")
     ap.add_argument("--backoff-max-ns", type=int, default=0, help="longest idle sleep (0 = default)")
     ap.add_argument("--producers-sweep", action="store_true",
@@ -675,8 +673,6 @@ def main():
         cfg_kw["warps_per_block"] = args.warps
     if args.sequencers:
         cfg_kw["sequencers"] = args.sequencers
-    if args.submit_threads > 1:
-        cfg_kw["submit_threads"] = args.submit_threads
     if args.spin_polls:
         cfg_kw["spin_polls"] = args.spin_polls
     if args.backoff_max_ns:

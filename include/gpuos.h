@@ -173,14 +173,7 @@ typedef struct gpuos_config {
                                  on 16 or more, else 1. Tickets are cut into windows of 128
                                  (or ring_entries, if smaller), taken in turn; work-queue
                                  space is still given out in ticket order */
-    uint32_t submit_threads;  /* single producer only: host threads that write a batch of at
-                                 least 2,048 descriptors (gpuos_submit_batch), the caller and
-                                 submit_threads - 1 helpers started by gpuos_init, 0 or 1 = the
-                                 caller alone (default), at most 16. Such a batch is validated
-                                 first, then runs of 128 tickets (the sequencers' windows)
-                                 are written and committed in turn by
-                                 every thread; once started it waits for ring slots without a
-                                 timeout (only the executor's end stops it) */
+    uint32_t reserved;
 } gpuos_config;
 
 /* Completion record of one ticket (device clock = %globaltimer, host clock =

@@ -31,11 +31,9 @@
 #include <cstdlib>
 #include <cstring>
 #include <ctime>
-#include <condition_variable>
 #include <mutex>
 #include <new>
 #include <string>
-#include <thread>
 #include <vector>
 
 #include "gpuos_internal.h"
@@ -243,24 +241,6 @@ struct gpuos_ctx {
     uint32_t regs = 0, smem = 0;
     gpuos_exec_params params;
     uint32_t n_handoffs = 0; /* executor relaunches that took in a new module */
-    /* single producer, large batches: submit_threads - 1 helper threads
-     * write the bodies and commit words of every submit_threads-th run of a
-     * batch, beside the caller */
-    struct Pool {
-        std::vector<std::thread> th;
-        std::mutex m;
-        std::condition_variable cv;
-        uint64_t gen = 0; /* job number (under m) */
-        bool quit = false;
-        const gpuos_desc *d = nullptr;
-        const uint32_t *nts = nullptr;
-        uint64_t t0 = 0;
-        uint32_t count = 0, parts = 1;
-        std::atomic<uint32_t> finished{0};
-        std::atomic<int> err{0};
-        std::atomic<uint64_t> harvested{0};
-    } pool;
-    std::vector<uint32_t> nts_buf; /* tile counts of a batch, validated up front */
     bool accepting = false; /* submissions allowed (until stop) */
     bool launched = false;  /* executor kernel launched */
     bool running = false;   /* executor believed resident */
@@ -459,12 +439,8 @@ int gpuos_op_ntiles(const gpuos_desc *d, uint32_t *ntiles)
     return validate_and_tile(d, ntiles, true);
 }
 
-static void pool_stop(gpuos_ctx *c);
-static void pool_main(gpuos_ctx *c, uint32_t part);
-
 static void free_all(gpuos_ctx *c)
 {
-    pool_stop(c);
     if (c->linked && driver().ok) driver().unload(c->linked);
     c->linked = nullptr;
     c->modules.clear();
@@ -523,7 +499,6 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     if ((cfg.stage_bytes & 1023u) || cfg.stage_bytes > 24576u) return GPUOS_EINVAL;
     if (cfg.multi_producer > 1u) return GPUOS_EINVAL;
     if (cfg.sequencers > GPUOS_MAX_SEQ) return GPUOS_EINVAL;
-    if (cfg.submit_threads > 16) return GPUOS_EINVAL;
     /* every warp's staging region and the executor's static shared memory
      * (descriptor copies, the sequencer's table copy, tile profiles) must fit
      * the 227 KB a block can hold */
@@ -676,9 +651,6 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     p.dep_timeout_ns = (uint64_t)(cfg.dep_timeout_ms ? cfg.dep_timeout_ms : 5000) * 1000000ull;
     p.exit_after = cfg.exit_after;
     c->accepting = true;
-    if (cfg.submit_threads > 1 && !cfg.multi_producer) {
-        for (uint32_t i = 1; i < cfg.submit_threads; i++) c->pool.th.emplace_back(pool_main, c, i);
-    }
     if (!cfg.deferred_start) {
         const int rc = gpuos_start(c);
         if (rc != GPUOS_OK) {
@@ -929,37 +901,6 @@ static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint3
     return GPUOS_OK;
 }
 
-/* A waiting producer's spin step. Every 256 polls: the deadline (when one
- * is given), the heartbeat and, when the device has flagged that it is
- * leaving or 10 ms have passed, whether the executor kernel has ended (a
- * CUDA runtime query, which takes a lock the other producers would fight
- * over if it ran on every poll). After a few thousand polls the thread
- * yields its core: there may be more producer threads than cores. */
-struct ProducerWait {
-    uint64_t t0 = 0, last = 0;
-    uint32_t spins = 0;
-    int step(gpuos_ctx *c, uint64_t timeout_ns)
-    {
-        if ((++spins & 255u) != 0) {
-            cpu_relax();
-            return GPUOS_OK;
-        }
-        const uint64_t now = now_ns();
-        if (t0 == 0) t0 = last = now;
-        heartbeat(c);
-        if (timeout_ns && now - t0 > timeout_ns) return GPUOS_EAGAIN;
-        if (__atomic_load_n(&c->hctl->state, __ATOMIC_RELAXED) == 2u || now - last > 10000000ull) {
-            last = now;
-            if (executor_gone(c)) {
-                c->running = false;
-                return GPUOS_ESTOPPED;
-            }
-        }
-        if (spins > 4096u) sched_yield();
-        return GPUOS_OK;
-    }
-};
-
 /* Single producer, a run of descriptors. Up to GPUOS_COMMIT_RUN at a time:
  * each is validated and tiled, takes its slot (once the slot's previous
  * ticket has completed) and has its body written; then one release fence
@@ -1060,152 +1001,36 @@ static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, ui
     return rc;
 }
 
-/* One writer's share of a parallel single-producer batch: runs r = part,
- * part + parts, ... of GPUOS_COMMIT_RUN tickets, each written and committed
- * like submit_run_spsc's runs (bodies, one release fence, commit words).
- * A writer waits for a slot only on the ticket N before it, which some
- * writer commits before it (tickets in a lower run), so no writer waits on
- * another in a cycle. Slot waits have no deadline: every ticket of the batch
- * is already given out and must be committed; only the executor's end
- * stops them. */
-#define GPUOS_PAR_RUN 128u /* a run of the parallel path: one sequencer window of tickets */
-static void write_runs(gpuos_ctx *c, uint32_t part)
-{
-    auto &P = c->pool;
-    /* runs follow the sequencers' windows (ticket multiples of 128), so a
-     * window is committed by one writer in one piece */
-    const uint64_t w0 = P.t0 / GPUOS_PAR_RUN, w1 = (P.t0 + P.count + GPUOS_PAR_RUN - 1) / GPUOS_PAR_RUN;
-    const uint32_t nrun = (uint32_t)(w1 - w0);
-    uint64_t harvested = 0;
-    ProducerWait ws;
-    for (uint32_t r = part; r < nrun; r += P.parts) {
-        if (P.err.load(std::memory_order_relaxed)) break;
-        const uint64_t a = (w0 + r) * GPUOS_PAR_RUN, b = a + GPUOS_PAR_RUN;
-        const uint32_t i0 = (uint32_t)((a > P.t0 ? a : P.t0) - P.t0);
-        const uint32_t i1 = (uint32_t)((b < P.t0 + P.count ? b : P.t0 + P.count) - P.t0);
-        for (uint32_t i = i0; i < i1; i++) {
-            const uint64_t t = P.t0 + i;
-            const uint32_t slot = (uint32_t)(t & c->mask);
-            if (t >= c->N) {
-                const uint64_t prev = t - c->N;
-                while (!is_done(c, prev)) {
-                    const int rc = ws.step(c, 0);
-                    if (rc) {
-                        P.err.store(rc);
-                        goto out;
-                    }
-                }
-                harvest_one(c, prev, &harvested);
-            }
-            gpuos_desc w = P.d[i];
-            w.ntiles = P.nts[i];
-            for (int q = 0; q < 2; q++)
-                if (w.dep[q] && (P.d[i].flags & GPUOS_FLAG_DEP_REL)) w.dep[q] = t - w.dep[q] + 1;
-            w.flags = (uint8_t)(P.d[i].flags & GPUOS_FLAG_FENCE);
-            w.ticket = t;
-            memcpy(c->ring + slot, &w, offsetof(gpuos_desc, seq));
-        }
-        {
-            const uint64_t stamp = now_ns();
-            __atomic_thread_fence(__ATOMIC_RELEASE);
-            for (uint32_t i = i0; i < i1; i++) {
-                const uint64_t t = P.t0 + i;
-                const uint32_t slot = (uint32_t)(t & c->mask);
-                c->commit_ns[slot] = stamp;
-                __atomic_store_n(&c->ring[slot].seq, t + 1, __ATOMIC_RELAXED);
-            }
-        }
-    }
-out:
-    P.harvested.fetch_add(harvested, std::memory_order_relaxed);
-    if (ws.t0) __atomic_fetch_add(&c->host_wait_ns, now_ns() - ws.t0, __ATOMIC_RELAXED);
-}
-
-static void pool_main(gpuos_ctx *c, uint32_t part)
-{
-    auto &P = c->pool;
-    cudaSetDevice(c->device); /* for the executor check in waits */
-    uint64_t seen = 0;
-    while (true) {
-        {
-            std::unique_lock<std::mutex> lk(P.m);
-            P.cv.wait(lk, [&] { return P.quit || P.gen != seen; });
-            if (P.quit) return;
-            seen = P.gen;
-        }
-        write_runs(c, part);
-        P.finished.fetch_add(1, std::memory_order_release);
-    }
-}
-
-static void pool_stop(gpuos_ctx *c)
-{
-    auto &P = c->pool;
+/* A waiting producer's spin step. Every 256 polls: the deadline (when one
+ * is given), the heartbeat and, when the device has flagged that it is
+ * leaving or 10 ms have passed, whether the executor kernel has ended (a
+ * CUDA runtime query, which takes a lock the other producers would fight
+ * over if it ran on every poll). After a few thousand polls the thread
+ * yields its core: there may be more producer threads than cores. */
+struct ProducerWait {
+    uint64_t t0 = 0, last = 0;
+    uint32_t spins = 0;
+    int step(gpuos_ctx *c, uint64_t timeout_ns)
     {
-        std::lock_guard<std::mutex> lk(P.m);
-        P.quit = true;
-    }
-    P.cv.notify_all();
-    for (auto &th : P.th)
-        if (th.joinable()) th.join();
-    P.th.clear();
-}
-
-/* Single producer, a large batch, with helper threads: validate and tile
- * every descriptor first (so a bad one stops the batch before any ticket
- * past it is given out), then the caller and the helpers write and commit
- * interleaved runs. */
-static int submit_parallel(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint32_t *n_done)
-{
-    if (!c->accepting || !c->running) return GPUOS_ESTOPPED;
-    if (__atomic_load_n(&c->hctl->state, __ATOMIC_RELAXED) == 2u) {
-        c->running = false;
-        return GPUOS_ESTOPPED;
-    }
-    if (c->nts_buf.size() < count) c->nts_buf.resize(count);
-    const uint64_t t0 = c->head;
-    uint32_t good = 0;
-    int rc = GPUOS_OK;
-    for (; good < count; good++) {
-        const gpuos_desc *di = d + good;
-        const uint64_t t = t0 + good;
-        const bool user_known = di->op_id >= GPUOS_OP_USER_FIRST && c->user_registered[di->op_id];
-        rc = validate_and_tile(di, &c->nts_buf[good], user_known);
-        for (int q = 0; q < 2 && rc == GPUOS_OK; q++) {
-            const uint64_t v = di->dep[q];
-            if (v > t) rc = GPUOS_EINVAL; /* a distance back, or ticket + 1, beyond the past */
+        if ((++spins & 255u) != 0) {
+            cpu_relax();
+            return GPUOS_OK;
         }
-        if (rc) break;
-    }
-    auto &P = c->pool;
-    if (good) {
-        P.d = d;
-        P.nts = c->nts_buf.data();
-        P.t0 = t0;
-        P.count = good;
-        P.parts = (uint32_t)P.th.size() + 1;
-        P.finished.store(0);
-        P.err.store(0);
-        P.harvested.store(0);
-        {
-            std::lock_guard<std::mutex> lk(P.m);
-            P.gen++;
+        const uint64_t now = now_ns();
+        if (t0 == 0) t0 = last = now;
+        heartbeat(c);
+        if (timeout_ns && now - t0 > timeout_ns) return GPUOS_EAGAIN;
+        if (__atomic_load_n(&c->hctl->state, __ATOMIC_RELAXED) == 2u || now - last > 10000000ull) {
+            last = now;
+            if (executor_gone(c)) {
+                c->running = false;
+                return GPUOS_ESTOPPED;
+            }
         }
-        P.cv.notify_all();
-        write_runs(c, 0);
-        while (P.finished.load(std::memory_order_acquire) < P.parts - 1) cpu_relax();
-        __atomic_fetch_add(&c->n_completed, P.harvested.load(), __ATOMIC_RELAXED);
-        const int err = P.err.load();
-        if (err) {
-            if (n_done) *n_done = 0;
-            return err; /* the executor has ended: the context accepts no more work */
-        }
-        __atomic_store_n(&c->head, t0 + good, __ATOMIC_RELEASE);
+        if (spins > 4096u) sched_yield();
+        return GPUOS_OK;
     }
-    heartbeat(c);
-    if (n_done) *n_done = good;
-    return rc;
-}
+};
 
 /* Multiple producers: validate every descriptor, wait (up to the timeout)
  * until the slot the batch's last ticket would take is free, reserve count
@@ -1317,8 +1142,6 @@ int gpuos_submit_batch(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64
         if (n_done) *n_done = rc == GPUOS_OK ? 1u : 0u;
         return rc;
     }
-    if (!c->pool.th.empty() && c->launched && count >= 32u * GPUOS_COMMIT_RUN)
-        return submit_parallel(c, d, count, n_done);
     return submit_run_spsc(c, d, count, n_done, timeout_us);
 }
 
@@ -1758,7 +1581,6 @@ int gpuos_shutdown(gpuos_ctx *c, uint32_t timeout_ms)
     if (c->launched && cudaStreamQuery(c->exec_stream) == cudaErrorNotReady) {
         /* the kernel still runs (it will leave through its watchdog); device
          * memory cannot be released under it, so only the host side goes */
-        pool_stop(c);
         delete c;
         return rc;
     }

@@ -53,7 +53,7 @@ class Config(C.Structure):
                 ("idle_exit_ms", C.c_uint32), ("dep_timeout_ms", C.c_uint32),
                 ("ring_in_device_mem", C.c_uint32), ("device", C.c_int32), ("exit_after", C.c_uint64),
                 ("tq_entries", C.c_uint32), ("deferred_start", C.c_uint32), ("stage_bytes", C.c_uint32),
-                ("multi_producer", C.c_uint32), ("sequencers", C.c_uint32), ("submit_threads", C.c_uint32)]
+                ("multi_producer", C.c_uint32), ("sequencers", C.c_uint32), ("reserved", C.c_uint32)]
 
 
 class Record(C.Structure):

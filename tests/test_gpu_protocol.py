@@ -674,52 +674,3 @@ def test_handoff_needs_a_single_producer():
     finally:
         ex.shutdown()
 
-
-
-@pytest.mark.parametrize("threads", [2, 4])
-def test_parallel_single_producer_batch(threads):
-    """A batch of 3,000 descriptors written by the caller and helper threads
-    (runs of 64 in turn) through a 256-entry ring: every output equals the
-    oracle's, including the 30 % chained ones, whose relative dependencies
-    count in ticket order as for one writer."""
-    from workloads.device import DeviceStream
-    s = S.stream_c2(n_desc=3000, pool_elems=1 << 22)
-    ds = DeviceStream(s)
-    ex = G().Executor(ring_entries=256, submit_threads=threads)
-    try:
-        h = ex.set_history(0, len(s.ops))
-        ex.submit_batch(ds.descs())
-        ex.sync(timeout_ms=60_000)
-        st = ex.stats()
-    finally:
-        assert ex.shutdown() == 0
-    assert st["completed"] == len(s.ops) and st["errors"] == 0
-    assert (h["ticket"] == np.arange(len(s.ops))).all()
-    from tests.gpu_harness import compare_in_order
-    rep, _ = compare_in_order(s, ds)
-    assert rep.ok(), "\n".join(rep.failures)
-
-
-def test_parallel_batch_stops_before_a_bad_descriptor():
-    """A bad descriptor at index 2,500 of a parallel batch: the 2,500 before
-    it are submitted and run, nothing after it is, and the call says so."""
-    g = G()
-    s, ds = _c1_small(n_desc=3000)
-    d = ds.descs()
-    d["op_id"][2500] = 40  # reserved id
-    ex = g.Executor(submit_threads=3)
-    try:
-        with pytest.raises(g.GpuosError) as e:
-            ex.submit_batch(d)
-        assert e.value.code == g.EINVAL and "submitted 2500 of 3000" in str(e.value)
-        ex.sync(timeout_ms=30_000)
-        st = ex.stats()
-    finally:
-        assert ex.shutdown() == 0
-    assert st["submitted"] == 2500 and st["completed"] == 2500
-    m = Machine(s)
-    for j in range(2500):
-        m.apply(j)
-    for j in range(2500):
-        o = s.ops[j]
-        assert np.array_equal(ds.read(o.out, o.dims[0]).view(np.uint32), m.view(o.out, o.dims[0]).view(np.uint32))
