@@ -137,11 +137,11 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
                    "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
 TRAFFIC = {
-    "c2": dict(bytes=249_464_832, descs=4096, sources="5daa6d1650495ac2"),
-    "c2l": dict(bytes=998_394_368, descs=400, sources="5daa6d1650495ac2"),
-    "c3": dict(bytes=400_407_296, descs=2048, sources="5daa6d1650495ac2"),
-    "c4": dict(bytes=30_850_434_000, descs=600, sources="5daa6d1650495ac2"),
-    "c5": dict(bytes=493_723_136, descs=224, sources="5daa6d1650495ac2"),
+    "c2": dict(bytes=249_710_336, descs=4096, sources="e6908f94426d4bf7"),
+    "c2l": dict(bytes=1_066_138_112, descs=400, sources="e6908f94426d4bf7"),
+    "c3": dict(bytes=400_427_776, descs=2048, sources="e6908f94426d4bf7"),
+    "c4": dict(bytes=30_808_755_000, descs=600, sources="e6908f94426d4bf7"),
+    "c5": dict(bytes=492_960_768, descs=224, sources="e6908f94426d4bf7"),
 }
 
 
@@ -608,6 +608,76 @@ def corun_curve(G, descs, cfg_kw, gemm, args):
             "alone_tflops": gemm.alone_tflops, "curve": rows}
 
 
+# An operator that did not exist when the executor was launched, compiled
+# at run time: out[i] = a[i] * 2 (fp32), tiles split like the built-in
+# element-wise ops so it can serve under a built-in id's tile count.
+_HANDOFF_OP_SRC = r'''
+__device__ int op_twice(const gpuos_devdesc *d, uint32_t tile)
+{
+    const uint32_t n = d->dims[0], lane = threadIdx.x & 31u;
+    const uint32_t nt = d->ntiles ? d->ntiles : 1u;
+    const uint32_t te = ((n + nt - 1u) / nt + 255u) / 256u * 256u;
+    const float *a = reinterpret_cast<const float *>(d->a);
+    float *o = reinterpret_cast<float *>(d->out);
+    const unsigned long long start = (unsigned long long)tile * te;
+    const unsigned long long end = start + te < n ? start + te : n;
+    for (unsigned long long i = start + lane; i < end; i += 32) o[i] = a[i] * 2.0f;
+    return GPUOS_ST_OK;
+}
+__device__ gpuos_op_fn op_twice_ptr = op_twice;
+'''
+
+
+def handoff_measure(G, local, cfg_kw):
+    """Operator injection into a running executor (the page's dynamic
+    operator table, §3 Q2): the smallest stream runs, an operator compiled
+    with NVRTC after the launch is registered (a hand-off: drain, the kernel
+    leaves, the module set is linked again, the kernel relaunches at the
+    next ticket), and the stream runs again. Reports the call's host time,
+    the executor's downtime on the device clock (last completion before ->
+    first dispatch after) and the operator's own round trip."""
+    import torch
+    from workloads import streams as S
+    from workloads.device import DeviceStream
+    s = S.stream_c1()
+    ds = DeviceStream(s, device=f"cuda:{local}")
+    d = ds.descs()
+    t0 = time.perf_counter()
+    img = G.compile_op(_HANDOFF_OP_SRC, "twice.cu")
+    compile_s = time.perf_counter() - t0
+    n = 4096
+    x = torch.randn(n, device=f"cuda:{local}")
+    y = torch.zeros(n, device=f"cuda:{local}")
+    torch.cuda.synchronize()
+    op = G.make_descs(1)
+    op["op_id"] = 90
+    op["dtype"] = G.F32
+    op["a"], op["out"] = x.data_ptr(), y.data_ptr()
+    op["dims"][0, 0] = n
+    op["ntiles"] = 4
+    ex = G.Executor(**cfg_kw)
+    try:
+        hist = ex.set_history(0, 2 * len(d) + 1)
+        ex.submit_batch(d)
+        ex.sync(timeout_ms=60_000)
+        a = time.perf_counter()
+        ex.register_op(90, img, "op_twice_ptr")
+        call_s = time.perf_counter() - a
+        ex.submit_batch(d)
+        ex.submit(op)
+        ex.sync(timeout_ms=60_000)
+        st = ex.stats()
+    finally:
+        ex.shutdown()
+    ok = bool(torch.equal(y, x * 2.0))
+    m = len(d)
+    down_us = (int(hist["t_dispatch_dev_ns"][m]) - int(hist["t_done_dev_ns"][:m].max())) / 1e3
+    op_us = (int(hist["t_done_dev_ns"][2 * m]) - int(hist["t_dispatch_dev_ns"][2 * m])) / 1e3
+    return {"compile_s": compile_s, "register_call_s": call_s, "executor_down_us": down_us,
+            "op_dispatch_to_done_us": op_us, "result_ok": ok, "errors": int(st["errors"]),
+            "version": int(st["version"])}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -620,6 +690,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-eager", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-handoff", action="store_true")
     ap.add_argument("--streams", default="c1,c2l,c3,c4,c5",
                     help="other workloads measured into the same line ('' = none)")
     ap.add_argument("--stream-steps", type=int, default=3, help="timed steps of each other workload")
@@ -859,6 +930,10 @@ def main():
         result["e2e"] = {"value": eu / esec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": 1e3 * (b - a) / args.steps}
         del host_in, host_out
+
+    # ---- operator injection into the running executor (hand-off)
+    if not args.no_handoff:
+        result["handoff"] = handoff_measure(G, local, cfg_kw)
 
     # ---- the other workloads, measured the same way (rank 0's GPU only
     # matters for the line; every rank runs them so the ranks stay aligned)
