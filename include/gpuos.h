@@ -423,7 +423,7 @@ GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
  *                      elements;
  *                      the device splits n into ntiles ranges of
  *                      round_up(ceil(n / ntiles), 256) elements
- *   row ops            R (one row per tile)
+ *   row ops            ceil(R / 2) (two consecutive rows per tile)
  *   rope, kv_write     B * ceil(H / 4) (one request, four heads per tile)
  *   sdpa               B * H * ceil(Lmax / c), c = round_up(ceil(Lmax / w), 32)
  *                      key rows (at least 32), w = floor(1536 / (B * H)) or 1

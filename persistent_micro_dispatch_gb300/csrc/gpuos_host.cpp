@@ -395,7 +395,7 @@ static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool use
         if (d->dtype != GPUOS_BF16) return GPUOS_EINVAL;
         if (m[0] && (m[1] == 0 || !d->a || !d->out)) return GPUOS_EINVAL;
         if (m[0] && d->op_id == GPUOS_OP_LAYERNORM && (!d->b || !d->aux0)) return GPUOS_EINVAL;
-        nt = m[0];
+        nt = ceil_div(m[0], 2); /* two consecutive rows per tile */
         break;
     case GPUOS_OP_ROPE:
         if (m[0] && (!d->a || !d->b || !d->aux0 || m[1] == 0 || m[2] == 0 || (m[2] & 1) || m[2] > 256))
