@@ -634,8 +634,9 @@ def handoff_measure(G, local, cfg_kw):
     with NVRTC after the launch is registered (a hand-off: drain, the kernel
     leaves, the module set is linked again, the kernel relaunches at the
     next ticket), and the stream runs again. Reports the call's host time,
-    the executor's downtime on the device clock (last completion before ->
-    first dispatch after) and the operator's own round trip."""
+    the time spent linking (while the old executor still runs), the
+    executor's downtime (stop request to the new kernel running) and the
+    operator's own dispatch-to-done time."""
     import torch
     from workloads import streams as S
     from workloads.device import DeviceStream
@@ -671,9 +672,9 @@ def handoff_measure(G, local, cfg_kw):
         ex.shutdown()
     ok = bool(torch.equal(y, x * 2.0))
     m = len(d)
-    down_us = (int(hist["t_dispatch_dev_ns"][m]) - int(hist["t_done_dev_ns"][:m].max())) / 1e3
     op_us = (int(hist["t_done_dev_ns"][2 * m]) - int(hist["t_dispatch_dev_ns"][2 * m])) / 1e3
-    return {"compile_s": compile_s, "register_call_s": call_s, "executor_down_us": down_us,
+    return {"compile_s": compile_s, "register_call_s": call_s, "handoffs": int(st["handoffs"]),
+            "link_ms": st["handoff_link_ns"] / 1e6, "executor_down_ms": st["handoff_down_ns"] / 1e6,
             "op_dispatch_to_done_us": op_us, "result_ok": ok, "errors": int(st["errors"]),
             "version": int(st["version"])}
 

@@ -213,6 +213,11 @@ typedef struct gpuos_stats_t {
     uint64_t seq_batches;    /* device: batches the sequencer took off the ring (lone descriptors
                                 it ran itself not counted) */
     uint64_t host_wait_ns;   /* host: time submitting threads waited for a free ring slot */
+    uint64_t handoffs;        /* host: executor relaunches that took in a new operator module */
+    uint64_t handoff_link_ns; /* host, last hand-off: linking the module set (the old executor
+                                 still runs meanwhile) */
+    uint64_t handoff_down_ns; /* host, last hand-off: from the stop request to the new
+                                 executor running (nothing is dispatched meanwhile) */
 } gpuos_stats_t;
 
 /* Where the executor's worker warps spent their time, per op id (device
@@ -423,7 +428,7 @@ GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
  *                      elements;
  *                      the device splits n into ntiles ranges of
  *                      round_up(ceil(n / ntiles), 256) elements
- *   row ops            ceil(R / 2) (two consecutive rows per tile)
+ *   row ops            R (one row per tile)
  *   rope, kv_write     B * ceil(H / 4) (one request, four heads per tile)
  *   sdpa               B * H * ceil(Lmax / c), c = round_up(ceil(Lmax / w), 32)
  *                      key rows (at least 32), w = floor(1536 / (B * H)) or 1

@@ -550,7 +550,7 @@ DEV int ew_dispatch(const gpuos_devdesc *d, uint32_t tile)
     return GPUOS_ST_BAD_ARGS;
 }
 
-/* ---- row ops: two consecutive rows per tile ------------------------------ */
+/* ---- row ops: one row per tile -------------------------------------------- */
 enum { ROW_SOFTMAX = 0, ROW_LN = 1, ROW_SUM = 2, ROW_MAX = 3, ROW_MIN = 4 };
 
 /* Rows of H <= GPUOS_ROW_REG_MAX bf16 with H % 8 == 0 and 16-byte aligned
@@ -747,16 +747,12 @@ DEV bool stage_wait0(WarpStage *w)
 }
 
 template <int K>
-DEV int row_passes(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C, const uint4 *sx, const uint4 *sg,
-                   WarpStage *w);
-
-/* One row staged in the buffer: [x | gamma chunk | beta chunk]. */
-template <int K>
 DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
 {
-    const uint32_t lane = lane_id();
+    const uint32_t lane = lane_id(), nv = H / 8;
     WarpStage *w = warp_stage();
     unsigned char *buf = warp_stage_buf();
+    const uint4 *sx = reinterpret_cast<const uint4 *>(buf);
     const uint16_t *x = reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)row * H;
     if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -768,43 +764,6 @@ DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
         }
     }
     if (!stage_wait0(w)) return GPUOS_ST_COPY_TIMEOUT;
-    return row_passes<K>(d, row, H, C, reinterpret_cast<const uint4 *>(buf),
-                         reinterpret_cast<const uint4 *>(buf + 2u * H), w);
-}
-
-/* Two consecutive rows staged together, [x0 | x1 | gamma | beta], their
- * copies in flight at once (one round trip for both rows). */
-template <int K>
-DEV int row_staged_pair(const gpuos_devdesc *d, uint32_t row, uint32_t H)
-{
-    WarpStage *w = warp_stage();
-    unsigned char *buf = warp_stage_buf();
-    const uint16_t *x = reinterpret_cast<const uint16_t *>(d->a) + (uint64_t)row * H;
-    if (lane_id() == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_expect(&w->mbar[0], 4u * H + (K == ROW_LN ? 4u * H : 0u));
-        bulk_g2s(buf, x, 4u * H, &w->mbar[0]);
-        if (K == ROW_LN) {
-            bulk_g2s(buf + 4u * H, reinterpret_cast<const void *>(d->b), 2u * H, &w->mbar[0]);
-            bulk_g2s(buf + 6u * H, reinterpret_cast<const void *>(d->aux0), 2u * H, &w->mbar[0]);
-        }
-    }
-    if (!stage_wait0(w)) return GPUOS_ST_COPY_TIMEOUT;
-    const uint4 *sg = reinterpret_cast<const uint4 *>(buf + 4u * H);
-    const int st = row_passes<K>(d, row, H, H, reinterpret_cast<const uint4 *>(buf), sg, w);
-    if (st) return st;
-    return row_passes<K>(d, row + 1, H, H, reinterpret_cast<const uint4 *>(buf + 2u * H), sg, w);
-}
-
-/* The passes over one staged row x (at sx, H / 8 vectors). LayerNorm's
- * gamma and beta for the first C columns are at sg and sg + C / 8 vectors;
- * with C < H the rest is streamed into those places in chunks of C. */
-template <int K>
-DEV int row_passes(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C, const uint4 *sx, const uint4 *sg,
-                   WarpStage *w)
-{
-    const uint32_t lane = lane_id(), nv = H / 8;
-    unsigned char *sgb = reinterpret_cast<unsigned char *>(const_cast<uint4 *>(sg));
     if (K == ROW_SUM || K == ROW_MAX || K == ROW_MIN) {
         const float init = (K == ROW_SUM) ? 0.0f : (K == ROW_MAX ? -INFINITY : INFINITY);
         float a8[8];
@@ -905,6 +864,7 @@ DEV int row_passes(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C,
 #pragma unroll
     for (int i = 0; i < 8; i++) q += s8[i];
     const float rstd = rsqrtf(warp_sum(q) / (float)H + d->fparam[0]);
+    const uint4 *sg = sx + nv;
     const uint32_t cv = C / 8; /* vectors per gamma/beta chunk */
     for (uint32_t c0 = 0; c0 < nv; c0 += cv) {
         if (c0 > 0) {
@@ -914,8 +874,8 @@ DEV int row_passes(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C,
             if (lane == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_expect(&w->mbar[0], 2u * cb);
-                bulk_g2s(sgb, reinterpret_cast<const unsigned char *>(d->b) + c0 * 16u, cb, &w->mbar[0]);
-                bulk_g2s(sgb + 2u * C, reinterpret_cast<const unsigned char *>(d->aux0) + c0 * 16u, cb,
+                bulk_g2s(buf + 2u * H, reinterpret_cast<const unsigned char *>(d->b) + c0 * 16u, cb, &w->mbar[0]);
+                bulk_g2s(buf + 2u * H + 2u * C, reinterpret_cast<const unsigned char *>(d->aux0) + c0 * 16u, cb,
                          &w->mbar[0]);
             }
             if (!stage_wait0(w)) return GPUOS_ST_COPY_TIMEOUT;
@@ -986,13 +946,19 @@ DEV int row_generic(const gpuos_devdesc *d, uint32_t row, uint32_t H)
     return GPUOS_ST_OK;
 }
 
-/* One row by the best path for its width, alignment and the staging. */
 template <int K>
-DEV int row_one(const gpuos_devdesc *d, uint32_t row, uint32_t H, bool ok, uint32_t sb)
+DEV int row_tile(const gpuos_devdesc *d, uint32_t row)
 {
+    const uint32_t R = d->dims[0], H = d->dims[1];
+    if (row >= R) return GPUOS_ST_OK;
+    if (H == 0) return GPUOS_ST_BAD_ARGS;
+    bool ok = (H & 7u) == 0 && (d->a & 15u) == 0;
+    if (K == ROW_SOFTMAX || K == ROW_LN) ok = ok && (d->out & 15u) == 0;
+    if (K == ROW_LN) ok = ok && ((d->b | d->aux0) & 15u) == 0;
     if (!ok) return row_generic<K>(d, row, H);
     /* staged: the row, plus (LayerNorm) gamma and beta in chunks of C
      * columns, a multiple of 8 of at least 256 (or all H) */
+    const uint32_t sb = stage_hdr()->stage_bytes;
     if (2u * H <= sb) {
         uint32_t C = 0;
         if (K == ROW_LN) {
@@ -1002,29 +968,6 @@ DEV int row_one(const gpuos_devdesc *d, uint32_t row, uint32_t H, bool ok, uint3
         if (K != ROW_LN || C == H || C >= 256u) return row_staged<K>(d, row, H, C);
     }
     return H <= GPUOS_ROW_REG_MAX ? row_reg<K>(d, row, H) : row_generic<K>(d, row, H);
-}
-
-/* A tile is ceil(R / ntiles) consecutive rows: two (the host's rule for
- * R >= 2) or one. Two rows that fit the staging buffer together ([x0 | x1],
- * and LayerNorm's gamma and beta once) arrive in one round trip. */
-template <int K>
-DEV int row_tile(const gpuos_devdesc *d, uint32_t tile)
-{
-    const uint32_t R = d->dims[0], H = d->dims[1];
-    const uint32_t nt = d->ntiles ? d->ntiles : 1u;
-    const uint32_t rpt = (R + nt - 1u) / nt;
-    const uint64_t r0 = (uint64_t)tile * rpt;
-    if (r0 >= R) return GPUOS_ST_OK;
-    if (H == 0 || rpt > 2u) return GPUOS_ST_BAD_ARGS;
-    const uint32_t row = (uint32_t)r0, rows = R - row < rpt ? R - row : rpt;
-    bool ok = (H & 7u) == 0 && (d->a & 15u) == 0;
-    if (K == ROW_SOFTMAX || K == ROW_LN) ok = ok && (d->out & 15u) == 0;
-    if (K == ROW_LN) ok = ok && ((d->b | d->aux0) & 15u) == 0;
-    const uint32_t sb = stage_hdr()->stage_bytes;
-    if (ok && rows == 2u && (K == ROW_LN ? 8u * H : 4u * H) <= sb) return row_staged_pair<K>(d, row, H);
-    int st = row_one<K>(d, row, H, ok, sb);
-    if (st == GPUOS_ST_OK && rows == 2u) st = row_one<K>(d, row + 1, H, ok, sb);
-    return st;
 }
 
 /* ---- RoPE: one (request, group of GPUOS_HEAD_GROUP heads) per tile --------
@@ -1686,12 +1629,12 @@ DEV void set_exit(const gpuos_exec_params &p, uint32_t reason)
 }
 
 /* Helper warps per descriptor: one per tile, except row ops, whose tiles
- * (two rows) are small: one helper per two tiles (four rows); at most GPUOS_HELPERS and
+ * (one row) are small: one helper per four rows; at most GPUOS_HELPERS and
  * at most the executor's worker warps (more would only queue). */
 DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles, uint32_t workers)
 {
     uint32_t hlp = ntiles;
-    if (op_id >= GPUOS_OP_SOFTMAX && op_id <= GPUOS_OP_ROWMIN) hlp = (ntiles + 1u) / 2u;
+    if (op_id >= GPUOS_OP_SOFTMAX && op_id <= GPUOS_OP_ROWMIN) hlp = (ntiles + 3u) / 4u;
     const uint32_t cap = workers < GPUOS_HELPERS ? (workers ? workers : 1u) : GPUOS_HELPERS;
     return hlp < cap ? hlp : cap;
 }

@@ -71,7 +71,8 @@ class Stats(C.Structure):
                 ("warps_per_block", C.c_uint32), ("regs_per_thread", C.c_uint32),
                 ("static_smem_bytes", C.c_uint32), ("reserved", C.c_uint32),
                 ("seq_body_ns", C.c_uint64), ("seq_mirror_ns", C.c_uint64), ("seq_publish_ns", C.c_uint64),
-                ("seq_batches", C.c_uint64), ("host_wait_ns", C.c_uint64)]
+                ("seq_batches", C.c_uint64), ("host_wait_ns", C.c_uint64), ("handoffs", C.c_uint64),
+                ("handoff_link_ns", C.c_uint64), ("handoff_down_ns", C.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
