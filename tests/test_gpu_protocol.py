@@ -631,8 +631,13 @@ def test_operator_compiled_after_launch_enters_by_handoff():
         st = ex.stats()
     finally:
         assert ex.shutdown() == 0
-    print(f"hand-off times (s): {times}")
+    print(f"hand-off times (s): {times}; last: link {st['handoff_link_ns'] / 1e6:.2f} ms, "
+          f"executor down {st['handoff_down_ns'] / 1e6:.2f} ms")
     assert st["errors"] == 0 and st["version"] == 3
+    assert st["handoffs"] == 2
+    # the executor is down only for the drain, the exit and the relaunch (the
+    # link runs while the old executor still serves)
+    assert 0 < st["handoff_down_ns"] < 100_000_000 and st["handoff_down_ns"] < st["handoff_link_ns"]
     # tickets: d[:2500] are 0..2499, the scale op 2500, d[2500:] 2501..3000
     ver = np.concatenate([hist["version"][:2500], hist["version"][2501:]])
     assert hist["version"][2500] == 2
