@@ -921,12 +921,9 @@ static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, ui
     }
     uint32_t done = 0;
     int rc = GPUOS_OK;
-    uint32_t nts[GPUOS_COMMIT_RUN];
-    uint64_t deps[GPUOS_COMMIT_RUN][2];
     while (done < count && rc == GPUOS_OK) {
         const uint32_t m = count - done < GPUOS_COMMIT_RUN ? count - done : GPUOS_COMMIT_RUN;
         const uint64_t t0 = c->head;
-        /* 1. validate and tile the run (it ends before a bad descriptor) */
         uint32_t k = 0;
         for (; k < m; k++) {
             const gpuos_desc *di = d + done + k;
@@ -935,8 +932,11 @@ static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, ui
                 rc = GPUOS_EAGAIN; /* deferred start: ring capacity */
                 break;
             }
+            uint32_t nt = 0;
             const bool user_known = di->op_id >= GPUOS_OP_USER_FIRST && c->user_registered[di->op_id];
-            rc = validate_and_tile(di, &nts[k], user_known);
+            rc = validate_and_tile(di, &nt, user_known);
+            if (rc) break;
+            uint64_t deps[2];
             for (int q = 0; q < 2 && rc == GPUOS_OK; q++) {
                 uint64_t v = di->dep[q];
                 if (v && (di->flags & GPUOS_FLAG_DEP_REL)) {
@@ -944,61 +944,46 @@ static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, ui
                     v = t - v + 1;
                 }
                 if (v > t) rc = GPUOS_EINVAL;
-                deps[k][q] = v;
+                deps[q] = v;
             }
             if (rc) break;
-        }
-        /* 2. every slot of the run free (relaxed polls; one acquire fence
-         * below covers the records read in 3) */
-        uint32_t ready = 0;
-        for (; ready < k; ready++) {
-            const uint64_t t = t0 + ready;
-            if (t < c->N) continue;
-            const uint64_t prev = t - c->N;
-            if (__atomic_load_n(&c->rec[prev & c->mask].done_seq, __ATOMIC_RELAXED) >= prev + 1) continue;
-            const uint64_t w0 = now_ns();
-            uint32_t spins = 0;
-            int wrc = GPUOS_OK;
-            while (__atomic_load_n(&c->rec[prev & c->mask].done_seq, __ATOMIC_RELAXED) < prev + 1) {
-                if ((++spins & 1023u) == 0) {
-                    heartbeat(c);
-                    if (now_ns() - w0 > (uint64_t)timeout_us * 1000ull) {
-                        wrc = GPUOS_EAGAIN;
-                        break;
-                    }
-                    if (executor_gone(c)) {
-                        c->running = false;
-                        wrc = GPUOS_ESTOPPED;
-                        break;
-                    }
-                }
-                cpu_relax();
-            }
-            __atomic_fetch_add(&c->host_wait_ns, now_ns() - w0, __ATOMIC_RELAXED);
-            if (wrc) {
-                rc = wrc;
-                break;
-            }
-        }
-        k = ready;
-        __atomic_thread_fence(__ATOMIC_ACQUIRE);
-        /* 3. harvest each slot's previous record and write the bodies: the
-         * slot's previous descriptor completed, so the device no longer
-         * reads it, and nothing reads the new body before its commit word */
-        for (uint32_t q = 0; q < k; q++) {
-            const gpuos_desc *di = d + done + q;
-            const uint64_t t = t0 + q;
             const uint32_t slot = (uint32_t)(t & c->mask);
-            if (t >= c->N) harvest_one(c, t - c->N);
-            gpuos_desc *dst = c->ring + slot;
-            memcpy(dst, di, offsetof(gpuos_desc, seq));
-            dst->ntiles = nts[q];
-            dst->dep[0] = deps[q][0];
-            dst->dep[1] = deps[q][1];
-            dst->flags = (uint8_t)(di->flags & GPUOS_FLAG_FENCE);
-            dst->ticket = t;
+            if (t >= c->N) {
+                const uint64_t prev = t - c->N;
+                if (!is_done(c, prev)) {
+                    const uint64_t w0 = now_ns();
+                    uint32_t spins = 0;
+                    while (!is_done(c, prev)) {
+                        if ((++spins & 1023u) == 0) {
+                            heartbeat(c);
+                            if (now_ns() - w0 > (uint64_t)timeout_us * 1000ull) {
+                                rc = GPUOS_EAGAIN;
+                                break;
+                            }
+                            if (executor_gone(c)) {
+                                c->running = false;
+                                rc = GPUOS_ESTOPPED;
+                                break;
+                            }
+                        }
+                        cpu_relax();
+                    }
+                    __atomic_fetch_add(&c->host_wait_ns, now_ns() - w0, __ATOMIC_RELAXED);
+                    if (rc) break;
+                }
+                harvest_one(c, prev);
+            }
+            gpuos_desc w = *di;
+            w.ntiles = nt;
+            w.dep[0] = deps[0];
+            w.dep[1] = deps[1];
+            w.flags = (uint8_t)(di->flags & GPUOS_FLAG_FENCE);
+            w.ticket = t;
+            /* the body: the slot's previous descriptor completed, so the
+             * device no longer reads it; nothing reads the new body before
+             * its commit word */
+            memcpy(c->ring + slot, &w, offsetof(gpuos_desc, seq));
         }
-        /* 4. one release fence, then the commit words */
         if (k) {
             const uint64_t stamp = now_ns();
             __atomic_thread_fence(__ATOMIC_RELEASE);
