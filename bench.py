@@ -440,9 +440,11 @@ def timed_executor(G, descs, cfg_kw, steps, gemm=None, history=True):
                 gemm=gemm_report, config=ex.config)
 
 
-def op_kind_table(s, h, n_ops, tprof):
+def op_kind_table(s, h, n_ops, tprof, passes):
     """Per op kind: p50 duration (tile 0 start -> completion), bandwidth,
-    the dependency gap and the per-tile device times."""
+    the dependency gap (from the records in `h`, one pass over the stream)
+    and the per-tile device times (the tile profile covers all `passes`
+    passes of the launch)."""
     from workloads import streams as S
     kinds = {}
     if not len(h):
@@ -473,7 +475,7 @@ def op_kind_table(s, h, n_ops, tprof):
             kinds[k]["dep_gap_us_p50"] = float(np.median(gk))
         if k in tprof:
             tp = tprof[k]
-            kinds[k].update(tiles_per_op=tp["tiles"] / max(1, int(m.sum())), tile_body_us=tp["body_us"],
+            kinds[k].update(tiles_per_op=tp["tiles"] / max(1, passes * int(m.sum())), tile_body_us=tp["body_us"],
                             tile_finish_us=tp["finish_us"], tile_dep_us=tp["dep_us"])
     return kinds
 
@@ -576,7 +578,7 @@ def stream_phase(G, name, args, cfg_kw, local, peak, gemm=None):
            "host_submit_ns_per_desc": r["submit_ns"] / (K * n_ops),
            "executor": {k: r["stats"][k] for k in ("seq_body_ns", "seq_mirror_ns", "seq_publish_ns",
                                                     "seq_batches", "host_wait_ns", "dep_waits")},
-           "op_kinds": op_kind_table(s, h, n_ops, r["tprof"]), "generate_and_upload_s": gen_s}
+           "op_kinds": op_kind_table(s, h, n_ops, r["tprof"], K), "generate_and_upload_s": gen_s}
     if name == "c4":
         out["decode_steps_per_s"] = value / 3
     if name == "c5":
@@ -872,7 +874,7 @@ def main():
                      "kernel": "gpuos_executor_kernel", "kernel_ms": kern_ms,
                      "device_busy_ms_last_step": busy_ns / 1e6},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
-        "op_kinds": op_kind_table(s, h, n_ops, r["tprof"]),
+        "op_kinds": op_kind_table(s, h, n_ops, r["tprof"], args.steps),
         "executor": {k: st[k] for k in ("tiles", "idle_polls", "sleeps", "dep_waits", "regs_per_thread",
                                         "static_smem_bytes", "seq_body_ns", "seq_mirror_ns", "seq_publish_ns",
                                         "seq_batches", "host_wait_ns")},

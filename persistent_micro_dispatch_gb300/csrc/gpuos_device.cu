@@ -1835,15 +1835,18 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
                 }
             }
             if (q == 0) {
-                if (lane == 0) version = ld_acquire_gpu32(&p.dctl->version);
+                /* the table version: a relaxed load after the fence above,
+                 * so at least the version stored before these commits */
+                if (lane == 0) version = ld_relaxed_sys32(&p.hctl->version);
                 version = __shfl_sync(0xFFFFFFFFu, version, 0);
                 if (version != cached_version) {
-                    /* a new version: copy its table slot (written before the
-                     * flip the acquire above saw) into shared memory */
+                    /* a new version: the fence makes the host's slot writes,
+                     * which preceded its store of this version, visible;
+                     * then the slot is copied into shared memory */
+                    fence_acq_rel_sys();
                     __syncwarp();
                     for (uint32_t i = lane; i < GPUOS_MAX_OPS; i += 32)
-                        s_table[i] = __ldcg(reinterpret_cast<const unsigned long long *>(p.table) +
-                                            (version & 1u) * GPUOS_MAX_OPS + i);
+                        s_table[i] = ld_relaxed_sys(p.table + (version & 1u) * GPUOS_MAX_OPS + i);
                     __syncwarp();
                     cached_version = version;
                 }

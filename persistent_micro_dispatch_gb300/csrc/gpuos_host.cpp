@@ -201,9 +201,10 @@ struct gpuos_ctx {
     uint64_t *t_pub = nullptr;
     uint64_t *t_disp = nullptr;
     gpuos_devctl *dctl = nullptr;
-    gpuos_op_fn *table = nullptr;
+    uint64_t *table = nullptr;     /* [2][GPUOS_MAX_OPS], pinned host memory */
+    uint64_t *table_dev = nullptr; /* its device address */
     uint64_t *warp_stats = nullptr;
-    uint32_t *version_stage = nullptr; /* pinned 4 bytes for version flips */
+    uint32_t *version_stage = nullptr; /* pinned staging words (hand-off) */
     cudaStream_t exec_stream = nullptr, ctl_stream = nullptr;
     /* host state */
     bool mp = false;       /* multi-producer submission */
@@ -462,7 +463,7 @@ static void free_all(gpuos_ctx *c)
     cudaFree(c->t_disp);
     cudaFree(c->tq);
     cudaFree(c->dctl);
-    cudaFree(c->table);
+    if (c->table) cudaFreeHost(c->table);
     cudaFree(c->warp_stats);
     if (c->exec_stream) cudaStreamDestroy(c->exec_stream);
     if (c->ctl_stream) cudaStreamDestroy(c->ctl_stream);
@@ -579,6 +580,10 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     memset(c->hctl, 0, sizeof(gpuos_hostctl));
     CK(cudaHostGetDevicePointer((void **)&c->hctl_dev, c->hctl, 0));
     CK(cudaHostAlloc((void **)&c->version_stage, 64, cudaHostAllocPortable));
+    /* the operator table: both slots in pinned host memory, written by the
+     * host with plain stores and published by the version's store-release */
+    CK(cudaHostAlloc((void **)&c->table, sizeof(c->table_host), cudaHostAllocMapped | cudaHostAllocPortable));
+    CK(cudaHostGetDevicePointer((void **)&c->table_dev, c->table, 0));
 
     const uint32_t total_warps = c->blocks * c->wpb;
     CK(cudaMalloc((void **)&c->mirror, (size_t)c->N * sizeof(gpuos_devdesc)));
@@ -591,7 +596,6 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     CK(cudaMalloc((void **)&c->t_pub, (size_t)c->N * 8));
     CK(cudaMalloc((void **)&c->t_disp, (size_t)c->N * 8));
     CK(cudaMalloc((void **)&c->dctl, sizeof(gpuos_devctl)));
-    CK(cudaMalloc((void **)&c->table, sizeof(c->table_host)));
     CK(cudaMalloc((void **)&c->warp_stats, (size_t)total_warps * GPUOS_WS_N * 8));
     CK(cudaMemsetAsync(c->mirror, 0, (size_t)c->N * sizeof(gpuos_devdesc), c->ctl_stream));
     CK(cudaMemsetAsync(c->tiles_done, 0, (size_t)c->N * 8, c->ctl_stream));
@@ -615,7 +619,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
             c->table_host[s][i] = (uint64_t)(uintptr_t)builtin[i];
             c->binding[s][i].builtin = i;
         }
-    CK(cudaMemcpyAsync(c->table, c->table_host, sizeof(c->table_host), cudaMemcpyHostToDevice, c->ctl_stream));
+    memcpy(c->table, c->table_host, sizeof(c->table_host));
     CK(cudaStreamSynchronize(c->ctl_stream));
 
     c->commit_ns.assign(c->N, 0);
@@ -637,7 +641,7 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     p.t_disp = c->t_disp;
     p.tq = c->tq;
     p.dctl = c->dctl;
-    p.table = c->table;
+    p.table = c->table_dev;
     p.warp_stats = c->warp_stats;
     p.ring_mask = c->mask;
     p.tq_mask = c->Q - 1;
@@ -704,8 +708,8 @@ static int launch_linked(gpuos_ctx *c, const std::vector<unsigned char> *prelink
             }
             c->table_host[sl][i] = v;
         }
-    if (cudaMemcpy(c->table, c->table_host, sizeof(c->table_host), cudaMemcpyHostToDevice) != cudaSuccess)
-        return GPUOS_ECUDA;
+    /* no executor runs here (not yet launched, or the old one has left) */
+    memcpy(c->table, c->table_host, sizeof(c->table_host));
     if (drv.get_function(&c->linked_exec, c->linked, "gpuos_executor_kernel") != CUDA_SUCCESS) return GPUOS_ECUDA;
     /* every function of the executor and of the op modules was compiled with
      * at most GPUOS_MAX_REGS registers; the linked kernel must hold that many
@@ -1241,14 +1245,13 @@ static int flip_entry(gpuos_ctx *c, uint16_t op_id, uint64_t fnval, const gpuos_
     c->table_host[ns][op_id] = fnval;
     for (int i = 0; i < GPUOS_MAX_OPS; i++) c->binding[ns][i] = c->binding[c->version & 1u][i];
     c->binding[ns][op_id] = bind;
-    if (cudaMemcpyAsync(c->table + (size_t)ns * GPUOS_MAX_OPS, c->table_host[ns], sizeof(c->table_host[0]),
-                        cudaMemcpyHostToDevice, c->ctl_stream) != cudaSuccess)
-        return GPUOS_ECUDA;
-    /* the version word lands only after the table slot (stream order) */
-    *c->version_stage = nv;
-    if (cudaMemcpyAsync(&c->dctl->version, c->version_stage, 4, cudaMemcpyHostToDevice, c->ctl_stream) != cudaSuccess)
-        return GPUOS_ECUDA;
-    if (cudaStreamSynchronize(c->ctl_stream) != cudaSuccess) return GPUOS_ECUDA;
+    /* the inactive slot with plain stores (no sequencer reads it: each copies
+     * a slot only when it first sees that slot's version), then the version
+     * with a store-release: a sequencer that sees the new version sees the
+     * slot written, and every descriptor committed after this store runs
+     * with it (the run's release fence orders the two) */
+    memcpy(c->table + (size_t)ns * GPUOS_MAX_OPS, c->table_host[ns], sizeof(c->table_host[0]));
+    store_rel(&c->hctl->version, nv);
     c->version = nv;
     c->flip_head = head_of(c);
     heartbeat(c);

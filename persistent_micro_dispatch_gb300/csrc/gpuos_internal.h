@@ -73,6 +73,9 @@ typedef struct gpuos_hostctl {
     uint64_t heartbeat; /* host: bumped by API calls */
     uint32_t stop;      /* host: 1 = leave when idle */
     uint32_t pad0[29];
+    uint32_t version;   /* host: operator-table version, flipped with a store-release
+                         * after the inactive slot of the table is written */
+    uint32_t padv[31];
     uint32_t state;       /* device: 1 running, 2 leaving */
     uint32_t exit_reason; /* device: see gpuos_stats_t */
     uint64_t sequenced;   /* device: tickets taken off the ring */
@@ -88,7 +91,7 @@ typedef struct gpuos_devctl {
     unsigned long long completed; /* descriptors completed */
     uint64_t pad1[15];
     uint32_t exit_flag; /* nonzero: workers leave when they find no work */
-    uint32_t version;   /* operator-table version */
+    uint32_t pad_x;
     uint64_t pad2[15];
     uint64_t pub_next;  /* sequencers' turn: first ticket whose work-queue space is not reserved */
     uint64_t tq_head;   /* ... and the next free work-queue index */
@@ -119,7 +122,7 @@ typedef struct gpuos_exec_params {
     uint64_t *t_disp;        /* [ring_entries], device clock when the commit was seen */
     unsigned long long *tq;  /* [tq_entries] work-queue words */
     gpuos_devctl *dctl;
-    gpuos_op_fn *table;      /* [2][GPUOS_MAX_OPS] */
+    const uint64_t *table;   /* [2][GPUOS_MAX_OPS] op entry points, host-visible (pinned) */
     uint64_t *warp_stats;    /* [total warps][GPUOS_WS_N] */
     uint32_t ring_mask, tq_mask;
     uint32_t backoff_min_ns, backoff_max_ns, spin_polls, stage_bytes;
