@@ -137,11 +137,11 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
                    "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
 TRAFFIC = {
-    "c2": dict(bytes=249_710_336, descs=4096, sources="e6908f94426d4bf7"),
-    "c2l": dict(bytes=1_066_138_112, descs=400, sources="e6908f94426d4bf7"),
-    "c3": dict(bytes=400_427_776, descs=2048, sources="e6908f94426d4bf7"),
-    "c4": dict(bytes=30_808_755_000, descs=600, sources="e6908f94426d4bf7"),
-    "c5": dict(bytes=492_960_768, descs=224, sources="e6908f94426d4bf7"),
+    "c2": dict(bytes=248_996_864, descs=4096, sources="d048251c383fb5bd"),
+    "c2l": dict(bytes=1_066_511_872, descs=400, sources="d048251c383fb5bd"),
+    "c3": dict(bytes=399_550_464, descs=2048, sources="d048251c383fb5bd"),
+    "c4": dict(bytes=30_818_519_040, descs=600, sources="d048251c383fb5bd"),
+    "c5": dict(bytes=493_531_136, descs=224, sources="d048251c383fb5bd"),
 }
 
 
