@@ -347,11 +347,23 @@ static bool al16(uint64_t p) { return (p & 15u) == 0; }
  * down to 1,024 elements (their arithmetic, not their bytes, sets the time).
  * The device recovers the tile size from n and ntiles alone
  * (round_up(ceil(n / ntiles), 256)). */
+static_assert((GPUOS_EW_TILE_MIN & (GPUOS_EW_TILE_MIN - 1)) == 0 && (GPUOS_GELU_TILE_MIN & (GPUOS_GELU_TILE_MIN - 1)) == 0 &&
+                  (GPUOS_EW_TILE_F32 & (GPUOS_EW_TILE_F32 - 1)) == 0 &&
+                  (GPUOS_EW_TILE_BF16 & (GPUOS_EW_TILE_BF16 - 1)) == 0,
+              "element-wise tile sizes are powers of two");
+/* The tile: the smallest of tile_min, 2 tile_min, 4 tile_min, ... that cuts
+ * n into at most GPUOS_EW_SPLIT tiles, capped at tile_max. With powers of
+ * two that is the power of two at or above ceil(n / SPLIT), clamped to
+ * [tile_min, tile_max]: computed without a loop (the descriptor mix makes a
+ * data-dependent loop a branch the host mispredicts). */
 static uint64_t ew_tiles(uint64_t n, uint64_t tile_min, uint64_t tile_max)
 {
-    uint64_t te = tile_min < tile_max ? tile_min : tile_max;
-    while (te < tile_max && te * GPUOS_EW_SPLIT < n) te <<= 1;
-    return ceil_div(n, te);
+    const uint64_t lo = tile_min < tile_max ? tile_min : tile_max;
+    const uint64_t need = (n + GPUOS_EW_SPLIT - 1) / GPUOS_EW_SPLIT;
+    const uint64_t p2 = need <= 1 ? 1 : 2ull << (63 - __builtin_clzll(need - 1));
+    uint64_t te = p2 > lo ? p2 : lo;
+    te = te < tile_max ? te : tile_max;
+    return (n + te - 1) >> __builtin_ctzll(te);
 }
 
 /* Decode-attention chunks: every (b, h) pair's keys are cut into at most
@@ -835,6 +847,34 @@ static void sweep(gpuos_ctx *c)
     __atomic_store_n(&c->low, low, __ATOMIC_RELEASE);
 }
 
+/* Write a descriptor's body (everything before the commit word) into its
+ * ring slot: the caller's words, with the library's fields (tile count,
+ * resolved dependencies, flags the device reads, ticket) put in on the way,
+ * in registers: patching a stack copy with narrow stores and reading it back
+ * in wide pieces would stall on store forwarding. */
+static inline void write_body(gpuos_desc *slot, const gpuos_desc *d, uint32_t nt, uint64_t dep0, uint64_t dep1,
+                              uint64_t t)
+{
+    struct Head {
+        uint16_t op_id;
+        uint8_t dtype;
+        uint8_t flags;
+        uint32_t ntiles;
+    } h = {d->op_id, d->dtype, (uint8_t)(d->flags & GPUOS_FLAG_FENCE), nt};
+    static_assert(sizeof(Head) == 8 && offsetof(gpuos_desc, dep) == 8, "descriptor head is 8 bytes");
+    static_assert(offsetof(gpuos_desc, ticket) == 14 * 8 && offsetof(gpuos_desc, seq) == 15 * 8,
+                  "ticket and commit word are the last two words");
+    uint64_t w0;
+    memcpy(&w0, &h, 8);
+    const uint64_t *src = reinterpret_cast<const uint64_t *>(d);
+    uint64_t *dst = reinterpret_cast<uint64_t *>(slot);
+    dst[0] = w0;
+    dst[1] = dep0;
+    dst[2] = dep1;
+    for (int i = 3; i < 14; i++) dst[i] = src[i];
+    dst[14] = t;
+}
+
 static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint32_t timeout_us)
 {
     if (!c || !d) return GPUOS_EINVAL;
@@ -888,16 +928,8 @@ static int submit_one(gpuos_ctx *c, const gpuos_desc *d, uint64_t *ticket, uint3
         harvest_one(c, prev);
     }
     gpuos_desc *s = c->ring + slot;
-    gpuos_desc w = *d;
-    w.ntiles = nt;
-    w.dep[0] = deps[0];
-    w.dep[1] = deps[1];
-    w.flags = (uint8_t)(d->flags & GPUOS_FLAG_FENCE);
-    w.ticket = t;
     /* body (first 120 bytes), then the commit word with a store-release */
-    const uint64_t *src = reinterpret_cast<const uint64_t *>(&w);
-    uint64_t *dst = reinterpret_cast<uint64_t *>(s);
-    for (int i = 0; i < 15; i++) __atomic_store_n(dst + i, src[i], __ATOMIC_RELAXED);
+    write_body(s, d, nt, deps[0], deps[1], t);
     c->commit_ns[slot] = now_ns();
     store_rel(&s->seq, t + 1);
     c->head = t + 1;
@@ -977,16 +1009,10 @@ static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, ui
                 }
                 harvest_one(c, prev);
             }
-            gpuos_desc w = *di;
-            w.ntiles = nt;
-            w.dep[0] = deps[0];
-            w.dep[1] = deps[1];
-            w.flags = (uint8_t)(di->flags & GPUOS_FLAG_FENCE);
-            w.ticket = t;
             /* the body: the slot's previous descriptor completed, so the
              * device no longer reads it; nothing reads the new body before
              * its commit word */
-            memcpy(c->ring + slot, &w, offsetof(gpuos_desc, seq));
+            write_body(c->ring + slot, di, nt, deps[0], deps[1], t);
         }
         if (k) {
             const uint64_t stamp = now_ns();
@@ -1100,13 +1126,12 @@ static int submit_mp(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, uint64_t
             }
             harvest_one(c, prev, &harvested); /* lock-free: one harvester per ticket */
         }
-        gpuos_desc w = d[i];
-        w.ntiles = nts[i];
-        for (int k = 0; k < 2; k++)
-            if (w.dep[k] && (d[i].flags & GPUOS_FLAG_DEP_REL)) w.dep[k] = t - w.dep[k] + 1;
-        w.flags = (uint8_t)(d[i].flags & GPUOS_FLAG_FENCE);
-        w.ticket = t;
-        memcpy(c->ring + slot, &w, offsetof(gpuos_desc, seq));
+        uint64_t dv[2];
+        for (int k = 0; k < 2; k++) {
+            dv[k] = d[i].dep[k];
+            if (dv[k] && (d[i].flags & GPUOS_FLAG_DEP_REL)) dv[k] = t - dv[k] + 1;
+        }
+        write_body(c->ring + slot, d + i, nts[i], dv[0], dv[1], t);
     }
     const uint64_t stamp = now_ns();
     __atomic_thread_fence(__ATOMIC_RELEASE);

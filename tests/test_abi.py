@@ -70,6 +70,30 @@ def _desc(G, op, dtype=1, dims=(), ptr=0x1000, **kw):
     return d
 
 
+def test_elementwise_tiling_over_sizes(G):
+    """The element-wise tile count over many sizes, against the rule stated
+    as a loop: start at the op's smallest tile (add/mul/ReLU 4096 elements,
+    GELU 1024), double it while it is below the dtype's largest tile (fp32
+    4096, bf16 8192) and would cut n into more than 16 tiles; the count is
+    ceil(n / tile), and an empty op has one tile."""
+    rng = np.random.default_rng(5)
+    ns = sorted(set(list(range(0, 300)) + [k * m + e for k in range(1, 22) for m in (1024, 4096, 65536)
+                                           for e in (-1, 0, 1) if k * m + e >= 0]
+                    + rng.integers(1, 1 << 31, size=300).tolist()))
+    for op in ("add", "mul", "relu", "gelu"):
+        for dt in (0, 1):
+            tmin = 1024 if op == "gelu" else 4096
+            tmax = 4096 if dt == 0 else 8192
+            for n in ns:
+                te = min(tmin, tmax)
+                while te < tmax and te * 16 < n:
+                    te *= 2
+                want = max(1, -(-n // te))
+                if want > 0xFFFFFFFF:
+                    continue
+                assert G.op_ntiles(_desc(G, op, dt, (n,))) == want, (op, dt, n)
+
+
 def test_tiling_rule(G):
     # element-wise: te = smallest power of two >= n/16 within [4096 (GELU 1024), 4096 | 8192]
     assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 1          # te 4096
