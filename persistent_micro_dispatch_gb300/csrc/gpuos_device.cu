@@ -1640,34 +1640,51 @@ DEV uint32_t helper_count(uint32_t op_id, uint32_t ntiles, uint32_t workers)
 }
 
 /* Work-queue reservation shared by the sequencer warps (each on an SM of its
- * own; the turn lives in device memory, dctl->pub_next and dctl->tq_head).
- * Work-queue space is given out in ticket order: the warp whose batch starts
- * at ticket pub_next takes tq_head, advances it by the batch's entries and
- * passes the turn on. Workers claim entries in queue order, so an entry of a
- * descriptor is never queued behind the entries of a later descriptor that
- * may wait for it (with several sequencers, a later window may be ready
- * first). */
+ * own; the turn lives in device memory, dctl->turn). Work-queue space is
+ * given out in ticket order: the warp whose batch starts at the turn's
+ * ticket takes the turn's queue index, advances it by the batch's entries
+ * and passes the turn on. Workers claim entries in queue order, so an entry
+ * of a descriptor is never queued behind the entries of a later descriptor
+ * that may wait for it (with several sequencers, a later window may be
+ * ready first).
+ *
+ * Ticket and queue index travel in one 64-bit word (32 bits each), so a
+ * hand-over is one relaxed store and one relaxed load that finds it: the
+ * next holder needs nothing else from the previous one (its work-queue
+ * stores are found by the workers through their stamps), so neither side
+ * takes a fence. A fence here would also wait for the holder's next ring
+ * poll, in flight across NVLink-C2C, and the turn passes once per batch.
+ * Both fields are taken modulo 2^32 and widened against what the waiter
+ * already knows: its ticket (the turn it waits for), and a work-queue
+ * index at or below the current one and less than 2^32 below it (its own
+ * last reservation: between two reservations of one sequencer the other
+ * sequencers reserve at most S windows of 128 descriptors of at most
+ * GPUOS_HELPERS entries each). */
+DEV uint64_t turn_word(uint64_t ticket, uint64_t tq)
+{
+    return (tq << 32) | (ticket & 0xFFFFFFFFull);
+}
 
 /* Lane 0: wait (bounded) for the turn of the batch starting at ticket s;
- * then the previous holder's tq_head is visible. */
-DEV bool baton_wait(const gpuos_exec_params &p, uint64_t s, uint64_t bound_ns)
+ * on success *tq is the next free work-queue index, widened from `known`. */
+DEV bool baton_wait(const gpuos_exec_params &p, uint64_t s, uint64_t known, uint64_t bound_ns, unsigned long long *tq)
 {
     Elapsed w;
     w.start();
     uint32_t n = 0;
-    while (ld_relaxed_gpu(&p.dctl->pub_next) != s) {
+    uint64_t v;
+    while ((uint32_t)(v = ld_relaxed_gpu(&p.dctl->turn)) != (uint32_t)s) {
         if ((++n & 63u) == 0 && w.tick(globaltimer()) > bound_ns) return false;
     }
-    fence_acq_rel_gpu(); /* the acquire, once */
+    *tq = known + (uint32_t)((uint32_t)(v >> 32) - (uint32_t)known);
     return true;
 }
 
-/* Lane 0: record the next free work-queue index and pass the turn on to the
- * batch starting at ticket `next`. */
+/* Lane 0: pass the turn on to the batch starting at ticket `next`, with the
+ * next free work-queue index. */
 DEV void baton_pass(const gpuos_exec_params &p, uint64_t tq_head, uint64_t next)
 {
-    st_relaxed_gpu(reinterpret_cast<unsigned long long *>(&p.dctl->tq_head), tq_head);
-    st_release_gpu(&p.dctl->pub_next, next);
+    st_relaxed_gpu(reinterpret_cast<unsigned long long *>(&p.dctl->turn), turn_word(next, tq_head));
 }
 
 /* A sequencer warp: ring -> mirror + work queue, up to 128 descriptors per
@@ -1776,7 +1793,7 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
              * their window's first slot (one line across NVLink-C2C instead
              * of 128), so that idle sequencers do not crowd the SM's
              * outstanding loads and slow the poll that matters. */
-            if (S > 1 && ld_relaxed_gpu(&p.dctl->pub_next) != s) {
+            if (S > 1 && (uint32_t)ld_relaxed_gpu(&p.dctl->turn) != (uint32_t)s) {
                 cheap = 1;
 #pragma unroll
                 for (int h = 0; h < SEQ_POLL; h++) seqv[h] = 0;
@@ -1924,12 +1941,14 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             if (S > 1) {
                 /* no work-queue space, but the turn passes through it */
                 uint32_t ok = 1;
+                unsigned long long e0 = 0;
                 if (lane == 0) {
-                    ok = baton_wait(p, s, p.dep_timeout_ns) ? 1u : 0u;
-                    if (ok) baton_pass(p, ld_relaxed_gpu(&p.dctl->tq_head), s + 1);
+                    ok = baton_wait(p, s, e, p.dep_timeout_ns, &e0) ? 1u : 0u;
+                    if (ok) baton_pass(p, e0, s + 1);
                     else set_exit(p, 4u);
                 }
                 if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+                e = __shfl_sync(0xFFFFFFFFu, e0, 0);
             }
             if (lane == 0) {
                 uint4 *sv = reinterpret_cast<uint4 *>(sd);
@@ -2010,9 +2029,8 @@ DEV void sequencer(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, u
             uint32_t ok = 1;
             unsigned long long e0 = 0;
             if (lane == 0) {
-                ok = baton_wait(p, s, p.dep_timeout_ns) ? 1u : 0u;
+                ok = baton_wait(p, s, e, p.dep_timeout_ns, &e0) ? 1u : 0u;
                 if (ok) {
-                    e0 = ld_relaxed_gpu(&p.dctl->tq_head);
                     baton_pass(p, e0 + total, s + k);
                 } else {
                     set_exit(p, 4u);

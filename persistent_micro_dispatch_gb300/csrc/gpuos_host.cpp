@@ -1370,11 +1370,10 @@ static int handoff(gpuos_ctx *c, const void *image, size_t len, uint64_t h)
         return GPUOS_ECUDA;
     c->params.ticket_base = c->head;
     c->params.tq_base = *claim;
-    /* the sequencers' turn starts there too */
+    /* the sequencers' turn starts there too (both fields modulo 2^32) */
     uint64_t *turn = reinterpret_cast<uint64_t *>(c->version_stage + 8);
-    turn[0] = c->params.ticket_base;
-    turn[1] = c->params.tq_base;
-    if (cudaMemcpyAsync(&c->dctl->pub_next, turn, 16, cudaMemcpyHostToDevice, c->ctl_stream) != cudaSuccess ||
+    turn[0] = ((c->params.tq_base & 0xFFFFFFFFull) << 32) | (c->params.ticket_base & 0xFFFFFFFFull);
+    if (cudaMemcpyAsync(&c->dctl->turn, turn, 8, cudaMemcpyHostToDevice, c->ctl_stream) != cudaSuccess ||
         cudaStreamSynchronize(c->ctl_stream) != cudaSuccess)
         return GPUOS_ECUDA;
     store_rel(&c->hctl->stop, 0u);

@@ -93,9 +93,10 @@ typedef struct gpuos_devctl {
     uint32_t exit_flag; /* nonzero: workers leave when they find no work */
     uint32_t pad_x;
     uint64_t pad2[15];
-    uint64_t pub_next;  /* sequencers' turn: first ticket whose work-queue space is not reserved */
-    uint64_t tq_head;   /* ... and the next free work-queue index */
-    uint64_t pad3[14];
+    uint64_t turn;      /* sequencers' turn, one word: [31:0] the first ticket whose work-queue
+                           space is not reserved (mod 2^32), [63:32] the next free work-queue
+                           index (mod 2^32) */
+    uint64_t pad3[15];
 } gpuos_devctl;
 
 /* Per-warp counters (owned by one warp each, plain stores). */
