@@ -424,7 +424,7 @@ GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
  * Host tiling rule of a built-in op (what ntiles the library will write);
  * one tile is one warp's unit of work:
  *   add/mul/relu/gelu  ceil(n / te), te the smallest power of two >= n / 16
- *                      within [4096 (GELU: 1024), 4096 (f32) or 8192 (bf16)]
+ *                      within [16384 (GELU: 1024), 16384 (f32) or 32768 (bf16)]
  *                      elements;
  *                      the device splits n into ntiles ranges of
  *                      round_up(ceil(n / ntiles), 256) elements
@@ -451,7 +451,10 @@ GPUOS_API size_t gpuos_sdpa_workspace_bytes(uint32_t B, uint32_t H, uint32_t D, 
  * breakdown: one kernel launch per operation).
  * Eager baseline: launch the same op bodies as ordinary kernels, one
  * cudaLaunchKernel per descriptor (one warp per tile, one warp per block), in
- * order, on `stream` (a cudaStream_t; 0 = legacy default), with stage_bytes
+ * order, on `stream` (a cudaStream_t; 0 = legacy default). Element-wise ops
+ * take smaller tiles than in the executor (te within [4096 (GELU: 1024),
+ * 4096 (f32) or 8192 (bf16)], the rule above otherwise): a launch runs one
+ * op, so its tiles are all its parallelism. With stage_bytes
  * of shared-memory staging per warp as in gpuos_config. Deps are implied by
  * stream order. Does not synchronize. Errors: EINVAL (as gpuos_submit),
  * ECUDA. */

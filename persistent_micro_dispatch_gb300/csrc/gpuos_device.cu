@@ -396,9 +396,9 @@ DEV uint32_t ew_tile_elems(uint64_t n, uint32_t ntiles)
     return (uint32_t)((per + GPUOS_EW_ALIGN - 1) / GPUOS_EW_ALIGN * GPUOS_EW_ALIGN);
 }
 
-/* Element-wise tile: up to GPUOS_EW_VPT 16-byte vectors per lane, in rounds
- * of 8 independent vector loads per operand per lane. Unaligned operands take
- * a scalar path with the same arithmetic. */
+/* Element-wise tile in registers: rounds of 8 (GELU: 2) independent 16-byte
+ * vector loads per operand per lane. Unaligned operands take a scalar path
+ * with the same arithmetic. */
 template <int OP, bool BF>
 DEV int ew_tile(const gpuos_devdesc *d, uint32_t tile)
 {

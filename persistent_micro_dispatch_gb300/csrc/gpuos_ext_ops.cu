@@ -35,8 +35,12 @@ extern "C" __device__ __noinline__ int gpuos_ext_sub(const gpuos_devdesc *d, uin
 {
     const uint32_t lane = threadIdx.x & 31u;
     const bool bf = d->dtype == GPUOS_BF16;
-    const uint64_t T = bf ? GPUOS_EW_TILE_BF16 : GPUOS_EW_TILE_F32;
     const uint64_t n = d->dims[0];
+    /* the built-in element-wise ops' tile rule: ntiles ranges of
+     * round_up(ceil(n / ntiles), GPUOS_EW_ALIGN) elements (so the op can
+     * stand in for add, whose ntiles the library computes) */
+    const uint64_t nt = d->ntiles ? d->ntiles : 1u;
+    const uint64_t T = ((n + nt - 1) / nt + GPUOS_EW_ALIGN - 1) / GPUOS_EW_ALIGN * GPUOS_EW_ALIGN;
     const uint64_t start = (uint64_t)tile * T;
     if (start >= n) return GPUOS_ST_OK;
     const uint64_t end = (n - start) < T ? n : start + T;

@@ -72,9 +72,9 @@ def _desc(G, op, dtype=1, dims=(), ptr=0x1000, **kw):
 
 def test_elementwise_tiling_over_sizes(G):
     """The element-wise tile count over many sizes, against the rule stated
-    as a loop: start at the op's smallest tile (add/mul/ReLU 4096 elements,
+    as a loop: start at the op's smallest tile (add/mul/ReLU 16384 elements,
     GELU 1024), double it while it is below the dtype's largest tile (fp32
-    4096, bf16 8192) and would cut n into more than 16 tiles; the count is
+    16384, bf16 32768) and would cut n into more than 16 tiles; the count is
     ceil(n / tile), and an empty op has one tile."""
     rng = np.random.default_rng(5)
     ns = sorted(set(list(range(0, 300)) + [k * m + e for k in range(1, 22) for m in (1024, 4096, 65536)
@@ -82,8 +82,8 @@ def test_elementwise_tiling_over_sizes(G):
                     + rng.integers(1, 1 << 31, size=300).tolist()))
     for op in ("add", "mul", "relu", "gelu"):
         for dt in (0, 1):
-            tmin = 1024 if op == "gelu" else 4096
-            tmax = 4096 if dt == 0 else 8192
+            tmin = 1024 if op == "gelu" else 16384
+            tmax = 16384 if dt == 0 else 32768
             for n in ns:
                 te = min(tmin, tmax)
                 while te < tmax and te * 16 < n:
@@ -95,17 +95,19 @@ def test_elementwise_tiling_over_sizes(G):
 
 
 def test_tiling_rule(G):
-    # element-wise: te = smallest power of two >= n/16 within [4096 (GELU 1024), 4096 | 8192]
-    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 1          # te 4096
+    # element-wise: te = smallest power of two >= n/16 within [16384 (GELU 1024), 16384 | 32768]
+    assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 1          # te 16384
     assert G.op_ntiles(_desc(G, "gelu", 0, (4096,))) == 4         # te 1024
-    assert G.op_ntiles(_desc(G, "add", 1, (16384,))) == 4         # te 4096
+    assert G.op_ntiles(_desc(G, "add", 1, (16384,))) == 1         # te 16384
     assert G.op_ntiles(_desc(G, "gelu", 1, (16384,))) == 16       # te 1024
-    assert G.op_ntiles(_desc(G, "relu", 0, (8193,))) == 3         # te 4096
+    assert G.op_ntiles(_desc(G, "relu", 0, (8193,))) == 1         # te 16384
+    assert G.op_ntiles(_desc(G, "relu", 0, (16385,))) == 2        # te 16384
     assert G.op_ntiles(_desc(G, "mul", 0, (1000,))) == 1
-    assert G.op_ntiles(_desc(G, "add", 0, (65536,))) == 16        # te 4096 (fp32 cap)
-    assert G.op_ntiles(_desc(G, "add", 1, (65536,))) == 16        # te 4096
-    assert G.op_ntiles(_desc(G, "add", 0, (1 << 20,))) == 256     # te 4096
-    assert G.op_ntiles(_desc(G, "gelu", 1, (1 << 20,))) == 128    # te 8192 (bf16 cap)
+    assert G.op_ntiles(_desc(G, "add", 0, (65536,))) == 4         # te 16384
+    assert G.op_ntiles(_desc(G, "add", 1, (65536,))) == 4         # te 16384
+    assert G.op_ntiles(_desc(G, "add", 0, (1 << 20,))) == 64      # te 16384 (fp32 cap)
+    assert G.op_ntiles(_desc(G, "add", 1, (1 << 20,))) == 32      # te 32768 (bf16 cap)
+    assert G.op_ntiles(_desc(G, "gelu", 1, (1 << 20,))) == 32     # te 32768 (bf16 cap)
     assert G.op_ntiles(_desc(G, "gelu", 1, (40000,))) == 10       # te 4096 >= 40000/16
     assert G.op_ntiles(_desc(G, "gelu", 0, (0,))) == 1            # empty op: one tile
     assert G.op_ntiles(_desc(G, "softmax", 1, (37, 1024))) == 37  # one row per tile
@@ -130,7 +132,7 @@ def test_device_tile_ranges_cover_each_op(G):
     length from the host's ntiles (the rule stated in gpuos.h); for every
     size the ranges must cover the op, stay 16-byte aligned, fit the largest
     tile, and (attention) use no more partials than the workspace holds."""
-    for (dt, cap), op in [(dc, o) for dc in ((0, 4096), (1, 8192)) for o in ("add", "gelu")]:
+    for (dt, cap), op in [(dc, o) for dc in ((0, 16384), (1, 32768)) for o in ("add", "gelu")]:
         for n in [1, 255, 256, 257, 1023, 1024, 1025, 4095, 4096, 4097, 16383, 16385, 65535, 65536,
                   65537, 100003, 1 << 20, (1 << 20) + 7, 3 * 8192 + 1]:
             nt = G.op_ntiles(_desc(G, op, dt, (n,)))
