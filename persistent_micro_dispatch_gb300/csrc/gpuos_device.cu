@@ -23,8 +23,8 @@
  *     is one tile on one warp.
  *   - The last tile of a descriptor completes it: status and timestamps into
  *     the host-visible record, a device-memory done stamp for dependency waits
- *     and the store-release of the record's done_seq, which also releases the
- *     ring slot to the host.
+ *     and the store-release of the slot's host-visible completion word, which
+ *     also releases the ring slot to the host.
  *   - Every wait is bounded (dependency and fence waits by dep_timeout_ns,
  *     idle polling by the host-heartbeat watchdog) and ends in a status, never
  *     a trap.
@@ -1615,9 +1615,10 @@ DEV void complete_desc(const gpuos_exec_params &p, uint64_t ticket, uint32_t slo
     st_relaxed_sys(&r->t_publish, t_pub);
     st_relaxed_sys(&r->t_start, t_start);
     st_relaxed_sys(&r->t_done, t_done);
-    /* release: the record's fields before its done word (which also frees
-     * the ring slot for the host) */
-    st_release_sys(&r->done_seq, ticket + 1);
+    /* release: the record's fields before the slot's completion word (which
+     * also frees the ring slot for the host); the words of eight slots
+     * share a line, so the host's check of a run of slots reads few lines */
+    st_release_sys(p.done_host + slot, (ticket + 1) | (status != GPUOS_ST_OK ? GPUOS_DONE_FAILED : 0ull));
     atomicAdd(&p.dctl->completed, 1ull);
 }
 

@@ -188,6 +188,8 @@ struct gpuos_ctx {
     gpuos_desc *ring_dev = nullptr;  /* device view */
     gpuos_rec_dev *rec = nullptr;
     gpuos_rec_dev *rec_dev = nullptr;
+    uint64_t *cw = nullptr; /* completion words, one per slot (host-visible) */
+    uint64_t *cw_dev = nullptr;
     gpuos_hostctl *hctl = nullptr;
     gpuos_hostctl *hctl_dev = nullptr;
     bool ring_managed = false;
@@ -208,12 +210,11 @@ struct gpuos_ctx {
     cudaStream_t exec_stream = nullptr, ctl_stream = nullptr;
     /* host state */
     bool mp = false;       /* multi-producer submission */
-    std::mutex hmu;        /* (multi-producer) harvest state: low, hv, recent, history, counts */
+    std::mutex hmu;        /* (multi-producer) harvest state: low, hv, history, counts */
     uint64_t head = 0;     /* next ticket (reserved, with multiple producers) */
     uint64_t low = 0;      /* every ticket < low harvested */
     std::vector<uint64_t> commit_ns;
     std::vector<uint64_t> hv; /* per slot: ticket + 1 last harvested */
-    std::vector<gpuos_record> recent; /* per slot: last harvested record */
     gpuos_record *history = nullptr;
     uint64_t hist_base = 0, hist_cap = 0;
     uint64_t n_completed = 0, n_errors = 0;
@@ -468,6 +469,7 @@ static void free_all(gpuos_ctx *c)
         else cudaFreeHost(c->ring);
     }
     if (c->rec) cudaFreeHost(c->rec);
+    if (c->cw) cudaFreeHost(c->cw);
     if (c->hctl) cudaFreeHost(c->hctl);
     if (c->version_stage) cudaFreeHost(c->version_stage);
     cudaFree(c->mirror);
@@ -593,6 +595,9 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
     CK(cudaHostAlloc((void **)&c->rec, (size_t)c->N * sizeof(gpuos_rec_dev), cudaHostAllocMapped | cudaHostAllocPortable));
     memset(c->rec, 0, (size_t)c->N * sizeof(gpuos_rec_dev));
     CK(cudaHostGetDevicePointer((void **)&c->rec_dev, c->rec, 0));
+    CK(cudaHostAlloc((void **)&c->cw, (size_t)c->N * sizeof(uint64_t), cudaHostAllocMapped | cudaHostAllocPortable));
+    memset(c->cw, 0, (size_t)c->N * sizeof(uint64_t));
+    CK(cudaHostGetDevicePointer((void **)&c->cw_dev, c->cw, 0));
     CK(cudaHostAlloc((void **)&c->hctl, sizeof(gpuos_hostctl), cudaHostAllocMapped | cudaHostAllocPortable));
     memset(c->hctl, 0, sizeof(gpuos_hostctl));
     CK(cudaHostGetDevicePointer((void **)&c->hctl_dev, c->hctl, 0));
@@ -641,12 +646,12 @@ int gpuos_init(const gpuos_config *cfg_in, gpuos_ctx **out)
 
     c->commit_ns.assign(c->N, 0);
     c->hv.assign(c->N, 0);
-    c->recent.assign(c->N, gpuos_record());
 
     gpuos_exec_params &p = c->params;
     memset(&p, 0, sizeof(p));
     p.ring = c->ring_dev;
     p.rec = c->rec_dev;
+    p.done_host = c->cw_dev;
     p.hctl = c->hctl_dev;
     p.mirror = c->mirror;
     p.tiles_done = c->tiles_done;
@@ -786,24 +791,23 @@ int gpuos_executor_stream(gpuos_ctx *c, void **stream)
 }
 
 /* ---- harvesting completion records ------------------------------------------ */
-/* Harvest ticket t's completion record (once). Counts it in n_completed,
- * unless `tally` is given: then the caller adds *tally later (several
- * producers would otherwise contend for the counter once per ticket). */
-static void harvest_one(gpuos_ctx *c, uint64_t t, uint64_t *tally = nullptr)
+/* Ticket t's completion: the slot's completion word (ticket + 1, and a flag
+ * for a nonzero status) frees the slot; the record (status, version,
+ * timestamps) stays in its slot until ticket t + ring_entries completes, and
+ * is read only when asked for (gpuos_query, the history). The word is a
+ * quarter of the bytes and eight slots share a line, so the submitting
+ * thread's check of a slot rarely misses on a line the device wrote. */
+static bool is_done(gpuos_ctx *c, uint64_t t)
+{
+    return (load_acq(&c->cw[t & c->mask]) & GPUOS_DONE_TICKET_MASK) >= t + 1;
+}
+
+/* The record of a completed ticket whose slot has not been reused (the
+ * caller's is_done(t) acquired it). */
+static gpuos_record read_record(gpuos_ctx *c, uint64_t t)
 {
     const uint32_t slot = (uint32_t)(t & c->mask);
-    uint64_t seen = __atomic_load_n(&c->hv[slot], __ATOMIC_ACQUIRE);
-    if (seen >= t + 1) return;
-    /* one harvester per ticket: with several producers, a producer reusing
-     * the slot and a sweeping thread may reach the same ticket together; a
-     * single-producer context harvests from one thread */
-    if (c->mp) {
-        if (!__atomic_compare_exchange_n(&c->hv[slot], &seen, t + 1, false, __ATOMIC_ACQ_REL, __ATOMIC_ACQUIRE))
-            return;
-    } else {
-        __atomic_store_n(&c->hv[slot], t + 1, __ATOMIC_RELAXED);
-    }
-    gpuos_rec_dev *r = c->rec + slot;
+    const gpuos_rec_dev *r = c->rec + slot;
     gpuos_record R;
     R.ticket = t;
     R.status = __atomic_load_n(&r->status, __ATOMIC_RELAXED);
@@ -813,23 +817,45 @@ static void harvest_one(gpuos_ctx *c, uint64_t t, uint64_t *tally = nullptr)
     R.t_publish_dev_ns = __atomic_load_n(&r->t_publish, __ATOMIC_RELAXED);
     R.t_start_dev_ns = __atomic_load_n(&r->t_start, __ATOMIC_RELAXED);
     R.t_done_dev_ns = __atomic_load_n(&r->t_done, __ATOMIC_RELAXED);
-    c->recent[slot] = R;
-    if (c->history && t >= c->hist_base && t - c->hist_base < c->hist_cap) c->history[t - c->hist_base] = R;
+    return R;
+}
+
+/* Harvest completed ticket t (once; the caller's is_done(t) acquired it):
+ * count it, note a failure, keep its record if the history covers it.
+ * Counts it in n_completed, unless `tally` is given: then the caller adds
+ * *tally later (several producers would otherwise contend for the counter
+ * once per ticket). */
+static void harvest_one(gpuos_ctx *c, uint64_t t, uint64_t *tally = nullptr)
+{
+    const uint32_t slot = (uint32_t)(t & c->mask);
+    uint64_t seen = __atomic_load_n(&c->hv[slot], __ATOMIC_ACQUIRE);
+    if (seen >= t + 1) return;
+    /* read before the ticket is marked harvested: a producer reuses the
+     * slot (and the device then rewrites word and record) only after that */
+    const uint64_t w = __atomic_load_n(&c->cw[slot], __ATOMIC_RELAXED);
+    const bool keep = c->history && t >= c->hist_base && t - c->hist_base < c->hist_cap;
+    gpuos_record R;
+    if (keep) R = read_record(c, t);
+    /* one harvester per ticket: with several producers, a producer reusing
+     * the slot and a sweeping thread may reach the same ticket together; a
+     * single-producer context harvests from one thread */
+    if (c->mp) {
+        if (!__atomic_compare_exchange_n(&c->hv[slot], &seen, t + 1, false, __ATOMIC_ACQ_REL, __ATOMIC_ACQUIRE))
+            return;
+    } else {
+        __atomic_store_n(&c->hv[slot], t + 1, __ATOMIC_RELAXED);
+    }
+    if (keep) c->history[t - c->hist_base] = R;
     if (tally)
         (*tally)++;
     else if (c->mp)
         __atomic_fetch_add(&c->n_completed, (uint64_t)1, __ATOMIC_RELAXED);
     else
         __atomic_store_n(&c->n_completed, __atomic_load_n(&c->n_completed, __ATOMIC_RELAXED) + 1, __ATOMIC_RELAXED);
-    if (R.status != GPUOS_ST_OK) {
+    if (w & GPUOS_DONE_FAILED) {
         __atomic_fetch_add(&c->n_errors, (uint64_t)1, __ATOMIC_RELAXED);
         __atomic_fetch_add(&c->pending_errors, (uint64_t)1, __ATOMIC_RELAXED);
     }
-}
-
-static bool is_done(gpuos_ctx *c, uint64_t t)
-{
-    return load_acq(&c->rec[t & c->mask].done_seq) >= t + 1;
 }
 
 static void sweep(gpuos_ctx *c)
@@ -1231,12 +1257,11 @@ int gpuos_query(gpuos_ctx *c, uint64_t ticket, gpuos_record *rec)
         return GPUOS_OK;
     }
     if (head_of(c) - ticket > c->N) return GPUOS_EINVAL;
-    const uint32_t slot = (uint32_t)(ticket & c->mask);
-    if (c->hv[slot] != ticket + 1) {
-        if (!is_done(c, ticket)) return GPUOS_EAGAIN;
-        harvest_one(c, ticket);
-    }
-    *rec = c->recent[slot];
+    /* inside the window the slot still holds this ticket's record: the
+     * ticket ring_entries later has not been taken */
+    if (!is_done(c, ticket)) return GPUOS_EAGAIN;
+    *rec = read_record(c, ticket);
+    harvest_one(c, ticket);
     return GPUOS_OK;
 }
 
@@ -1568,7 +1593,7 @@ int gpuos_calibrate(gpuos_ctx *c, uint32_t pings, int64_t *off_lo, int64_t *off_
             if ((++spins & 0xFFFFFu) == 0 && executor_gone(c)) return GPUOS_ESTOPPED;
         }
         const uint64_t t1 = now_ns();
-        while (load_acq(&r->done_seq) < t + 1) {
+        while (!is_done(c, t)) {
             if ((++spins & 0xFFFFFu) == 0 && executor_gone(c)) return GPUOS_ESTOPPED;
         }
         const uint64_t rtt = t1 - t0;

@@ -59,8 +59,16 @@ typedef struct gpuos_devdesc {
  * code): 36-bit stamp, 16-bit ring slot, 12-bit helper index. */
 
 /* Completion record in host-visible memory, written by the device. */
+/* Completion word of a ring slot (host-visible, one 8-byte word per slot,
+ * eight slots to a cache line): ticket + 1 in bits 0..55 once the ticket is
+ * complete, bit 63 set if it completed with a nonzero status (the record
+ * holds the status itself). Stored with release at system scope after the
+ * record's fields; the host's load-acquire of it frees the slot. */
+#define GPUOS_DONE_TICKET_MASK ((1ull << 56) - 1ull)
+#define GPUOS_DONE_FAILED (1ull << 63)
+
 typedef struct gpuos_rec_dev {
-    uint64_t done_seq; /* ticket + 1 once complete (store-release, system scope) */
+    uint64_t reserved; /* (the completion word lives in the compact done array) */
     int32_t status;
     uint32_t version;
     uint64_t t_dispatch;
@@ -114,6 +122,7 @@ typedef int (*gpuos_op_fn)(const gpuos_devdesc *d, uint32_t tile);
 typedef struct gpuos_exec_params {
     const gpuos_desc *ring;  /* host-visible ring */
     gpuos_rec_dev *rec;      /* host-visible completion records */
+    uint64_t *done_host;     /* host-visible completion words, [ring_entries] */
     gpuos_hostctl *hctl;
     gpuos_devdesc *mirror;   /* [ring_entries] */
     unsigned long long *tiles_done; /* [ring_entries]: tiles done (low 32 bits), failed helpers (high 32) */
