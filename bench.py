@@ -556,6 +556,8 @@ def stream_phase(G, name, args, cfg_kw, local, peak, gemm=None):
     torch.cuda.synchronize()
     gen_s = time.perf_counter() - t_gen
     K = args.stream_steps
+    if name == "c1" and not args.ring_entries:
+        cfg_kw = dict(cfg_kw, ring_entries=4096)  # as the smallest stream is defined
     ex = G.Executor(**cfg_kw)
     for _ in range(args.stream_warmup):
         ex.submit_batch(descs)
@@ -717,6 +719,7 @@ def main():
     ap.add_argument("--stage-bytes", type=int, default=16384, help="shared-memory staging per warp (0 = none)")
     ap.add_argument("--blocks", type=int, default=0, help="executor blocks (0 = one per SM)")
     ap.add_argument("--sequencers", type=int, default=0, help="sequencer warps (0 = the library's default)")
+    ap.add_argument("--ring-entries", type=int, default=0, help="ring slots (0 = the library's default, 4096)")
     ap.add_argument("--spin-polls", type=int, default=0, help="idle polls before backoff sleeps (0 = default)")
     ap.add_argument("--backoff-max-ns", type=int, default=0, help="longest idle sleep (0 = default)")
     ap.add_argument("--producers-sweep", action="store_true",
@@ -750,6 +753,10 @@ def main():
         cfg_kw["warps_per_block"] = args.warps
     if args.sequencers:
         cfg_kw["sequencers"] = args.sequencers
+    if args.ring_entries:
+        cfg_kw["ring_entries"] = args.ring_entries
+    elif args.workload == "c1":
+        cfg_kw["ring_entries"] = 4096  # as the smallest stream is defined
     if args.spin_polls:
         cfg_kw["spin_polls"] = args.spin_polls
     if args.backoff_max_ns:

@@ -142,7 +142,10 @@ typedef struct gpuos_desc {
 
 /* Executor / ring configuration. gpuos_default_config() fills defaults. */
 typedef struct gpuos_config {
-    uint32_t ring_entries;    /* power of two in [64, 65536]; default 4096 (the page's default) */
+    uint32_t ring_entries;    /* power of two in [64, 65536]; default 8192 (the page's default is
+                                 4096: with 8192 the submitting thread waits less often for the
+                                 one slot a slow descriptor still holds, and the ring's 1 MB
+                                 stays in a Grace core's L2) */
     uint32_t warps_per_block; /* 2..12; default 12 */
     uint32_t blocks;          /* 0 = one block per SM; block 0 holds only the sequencer warp
                                  (when blocks > 1) */
@@ -236,7 +239,8 @@ typedef struct gpuos_tile_profile {
 typedef struct gpuos_ctx gpuos_ctx;
 
 /* Fill *cfg with defaults. Source: GPUOS page, §3 Q2 "1. Ring Buffer
- * Communication Channel" (4096 ring entries by default) and "2. Persistent
+ * Communication Channel" (4096 ring entries by default there; 8192 here,
+ * as ring_entries says) and "2. Persistent
  * Kernel Executor" (one block per SM; spin under load, exponential backoff
  * when idle). */
 GPUOS_API void gpuos_default_config(gpuos_config *cfg);

@@ -313,7 +313,7 @@ const char *gpuos_strerror(int code, int is_status)
 void gpuos_default_config(gpuos_config *c)
 {
     memset(c, 0, sizeof(*c));
-    c->ring_entries = 4096;
+    c->ring_entries = 8192;
     c->warps_per_block = 12;
     c->blocks = 0;
     c->backoff_min_ns = 32;

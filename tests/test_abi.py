@@ -55,7 +55,7 @@ def test_descriptor_layout_matches_header(G):
 
 def test_default_config(G):
     c = G.default_config()
-    assert c.ring_entries == 4096 and c.warps_per_block == 12 and c.tq_entries == 0
+    assert c.ring_entries == 8192 and c.warps_per_block == 12 and c.tq_entries == 0
     assert c.idle_exit_ms > 0 and c.dep_timeout_ms > 0
 
 

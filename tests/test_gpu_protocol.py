@@ -625,6 +625,10 @@ def test_operator_compiled_after_launch_enters_by_handoff():
         times.append(time.perf_counter() - t0)
         ex.submit_batch(d[2000:2500])                   # id 1 still neg
         ex.submit(sc)
+        # a flip applies to descriptors sequenced after it, not to those
+        # submitted after it: wait until these have run, so that the
+        # versions asserted below are fixed
+        ex.sync(timeout_ms=30_000)
         ex.alias_op(g.OP["add"], g.OP["mul"])           # version 3: id 1 = mul
         ex.submit_batch(d[2500:])
         ex.sync(timeout_ms=30_000)
