@@ -437,8 +437,10 @@ GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
  *   sdpa               B * H * ceil(Lmax / c), c = round_up(ceil(Lmax / w), 32)
  *                      key rows (at least 32), w = floor(1536 / (B * H)) or 1
  *                      if B * H >= 1536: at most 1536 tiles (or B * H), one
- *                      wave on the default executor; a tile attends
- *                      round_up(ceil(Lmax / chunks), 32) rows
+ *                      wave on the default executor; a tile attends at most
+ *                      round_up(ceil(Lmax / chunks), 32) rows (the device
+ *                      shortens the chunks when the requests' lengths lens[b]
+ *                      leave tiles idle: see the sdpa op body)
  *   vecmat             ceil(N / 8) (eight output columns per tile)
  *   nop / empty op     1
  * Returns GPUOS_EINVAL for a descriptor the library would reject. */

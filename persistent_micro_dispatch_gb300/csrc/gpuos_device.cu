@@ -1212,20 +1212,96 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
     const uint32_t nch = d->ntiles / BH;
     if (nch == 0) return GPUOS_ST_BAD_ARGS;
     if (tile >= BH * nch) return GPUOS_ST_OK;
-    const uint32_t CH = ((Lmax + nch - 1) / nch + 31u) & ~31u; /* key rows per chunk */
-    const uint32_t b = tile / (H * nch), rem = tile - b * H * nch, h = rem / nch, c = rem - h * nch;
     const uint32_t lane = lane_id(), g = lane >> 3, li = lane & 7u;
+    const int32_t *lens = reinterpret_cast<const int32_t *>(d->aux0);
+    /* Chunks. The host's rule cuts every (request, head) pair's keys into
+     * at most nch chunks of CH = round_up(ceil(Lmax / nch), 32) rows; a
+     * request shorter than Lmax then leaves some of its nch tiles idle, and
+     * the op takes as long as one CH-row chunk whatever the other requests'
+     * lengths. With the lengths known here the chunk shrinks to what lets
+     * the requests' chunks fill the op's tiles:
+     *   CH' = round_up(ceil(H sum_b L_b / (ntiles - B H)), 32), at least 32,
+     * which gives at most H sum_b ceil(L_b / CH') <= H sum_b L_b / CH' + B H
+     * <= ntiles chunks. Chunks are numbered request by request (b, then h,
+     * then c), so a tile finds its request by a prefix sum over the
+     * requests' chunk counts H ceil(L_b / CH); its partial (split-K) is
+     * slot `tile` of the workspace, below ntiles like before. */
+    uint32_t CH = ((Lmax + nch - 1) / nch + 31u) & ~31u; /* key rows per chunk */
+    uint32_t b, h, c, nchb, L;
+    uint64_t pfirst; /* workspace slot of the (b, h) pair's first chunk */
+    uint4 q0, q1;
+    if (nch == 1 || B == 1) {
+        /* one chunk per pair, or one request (whose length is Lmax): the
+         * host's chunks; the length and the query in one round trip */
+        b = tile / (H * nch);
+        const uint32_t rem = tile - b * H * nch;
+        h = rem / nch;
+        c = rem - h * nch;
+        const int32_t Lb = __ldcg(lens + b);
+        const uint16_t *qp = reinterpret_cast<const uint16_t *>(d->a) + ((uint64_t)b * H + h) * 128;
+        q0 = __ldcg(reinterpret_cast<const uint4 *>(qp + 8 * li));
+        q1 = __ldcg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * li));
+        if (Lb < 1 || (uint32_t)Lb > Lmax) return GPUOS_ST_BAD_ARGS;
+        L = (uint32_t)Lb;
+        nchb = (L + CH - 1u) / CH;
+        if (c >= nchb) return GPUOS_ST_OK;
+        pfirst = (uint64_t)tile - c;
+    } else {
+        /* every length, checked and summed (one round trip for B <= 32) */
+        const int32_t l0 = lane < B ? __ldcg(lens + lane) : 1;
+        bool bad = l0 < 1 || (uint32_t)l0 > Lmax;
+        unsigned long long sum = lane < B ? (unsigned long long)l0 : 0ull;
+        for (uint32_t i = lane + 32u; i < B; i += 32) {
+            const int32_t v = __ldcg(lens + i);
+            bad |= v < 1 || (uint32_t)v > Lmax;
+            sum += (unsigned long long)(v > 0 ? v : 0);
+        }
+        if (__any_sync(0xFFFFFFFFu, bad)) return GPUOS_ST_BAD_ARGS;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        const unsigned long long spare = (unsigned long long)BH * (nch - 1u);
+        unsigned long long cn = ((unsigned long long)H * sum + spare - 1ull) / spare;
+        cn = (cn + 31ull) & ~31ull;
+        if (cn < GPUOS_SDPA_CHUNK_MIN) cn = GPUOS_SDPA_CHUNK_MIN;
+        if (cn < CH) CH = (uint32_t)cn;
+        /* the tile's request: prefix sums of H ceil(L_i / CH), 32 requests at a time */
+        uint32_t base = 0, off = 0, found = 0;
+        L = 0;
+        b = 0;
+        for (uint32_t i0 = 0; i0 < B; i0 += 32) {
+            const uint32_t i = i0 + lane;
+            const uint32_t Li = i >= B ? 0u : (i0 == 0 ? (uint32_t)l0 : (uint32_t)__ldcg(lens + i));
+            const uint32_t cnt = H * ((Li + CH - 1u) / CH);
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= (uint32_t)o) incl += v;
+            }
+            const uint32_t lo = base + incl - cnt;
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, cnt && tile >= lo && tile < lo + cnt);
+            if (bal) {
+                const int src = __ffs(bal) - 1;
+                b = i0 + (uint32_t)src;
+                L = __shfl_sync(0xFFFFFFFFu, Li, src);
+                off = tile - __shfl_sync(0xFFFFFFFFu, lo, src);
+                found = 1;
+                break;
+            }
+            base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (!found) return GPUOS_ST_OK; /* past the last chunk */
+        nchb = (L + CH - 1u) / CH;
+        h = off / nchb;
+        c = off - h * nchb;
+        pfirst = (uint64_t)tile - c;
+        const uint16_t *qp = reinterpret_cast<const uint16_t *>(d->a) + ((uint64_t)b * H + h) * 128;
+        q0 = __ldcg(reinterpret_cast<const uint4 *>(qp + 8 * li));
+        q1 = __ldcg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * li));
+    }
     const uint64_t bh = (uint64_t)b * H + h;
-    /* the length and the query in one round trip, then the first copies */
-    const int32_t L = __ldcg(reinterpret_cast<const int32_t *>(d->aux0) + b);
-    const uint16_t *qp = reinterpret_cast<const uint16_t *>(d->a) + bh * 128;
-    const uint4 q0 = __ldcg(reinterpret_cast<const uint4 *>(qp + 8 * li));
-    const uint4 q1 = __ldcg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * li));
-    if (L < 1 || (uint32_t)L > Lmax) return GPUOS_ST_BAD_ARGS;
-    const uint32_t nchb = ((uint32_t)L + CH - 1) / CH;
-    if (c >= nchb) return GPUOS_ST_OK;
     const uint32_t t0 = c * CH;
-    const uint32_t t1 = min((uint32_t)L, t0 + CH);
+    const uint32_t t1 = min(L, t0 + CH);
     const uint16_t *Kb = reinterpret_cast<const uint16_t *>(d->b) + bh * Lcap * 128;
     const uint16_t *Vb = reinterpret_cast<const uint16_t *>(d->aux1) + bh * Lcap * 128;
     const uint32_t SUB = stage_hdr()->stage_bytes / 1024u; /* key rows per half: K and V, 256 bytes each */
@@ -1343,8 +1419,7 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
      * GPUOS_SDPA_PART floats {m, l, -, -, acc[128]} */
     uint32_t *cnt = reinterpret_cast<uint32_t *>(d->aux2);
     float *ws = reinterpret_cast<float *>(d->aux2) + ((d->dims[5] + 3u) & ~3u);
-    const uint64_t p0 = bh * nch;
-    float *part = ws + (p0 + c) * GPUOS_SDPA_PART;
+    float *part = ws + (uint64_t)tile * GPUOS_SDPA_PART;
     if (g == 0) {
         float4 *pa = reinterpret_cast<float4 *>(part + 4);
         __stcg(pa + 2 * li, make_float4(acc[0], acc[1], acc[2], acc[3]));
@@ -1374,7 +1449,7 @@ DEV int sdpa_tile(const gpuos_devdesc *d, uint32_t tile)
 #pragma unroll
         for (int k = 0; k < 16; k++) {
             const uint32_t kc = min(k0 + (uint32_t)k, nchb - 1); /* duplicates past the end weigh 0 below */
-            const float *pk = ws + (p0 + kc) * GPUOS_SDPA_PART;
+            const float *pk = ws + (pfirst + kc) * GPUOS_SDPA_PART;
             mk[k] = __ldcg(pk);
             lk[k] = __ldcg(pk + 1);
             vk[k] = __ldcg(reinterpret_cast<const float4 *>(pk + 4) + lane);

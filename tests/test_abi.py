@@ -150,6 +150,63 @@ def test_device_tile_ranges_cover_each_op(G):
         assert nt <= max(1536, B * H)  # one wave on the default executor
 
 
+def _sdpa_device_chunks(B, H, Lmax, nt, lens):
+    """The decode-attention op body's chunk rule, restated: with one request
+    or one chunk per pair, the host's chunks; otherwise the host's chunk
+    length, shortened to round_up(ceil(H sum(lens) / (nt - B H)), 32) (at
+    least 32) when that is shorter; chunks numbered request by request, then
+    head, then chunk; a tile's partial goes to workspace slot `tile`.
+    Returns {tile: (b, h, first_row, end_row, slot of the pair's first chunk)}."""
+    nch = nt // (B * H)
+    ch = -(-(-(-Lmax // nch)) // 32) * 32
+    out = {}
+    if nch == 1 or B == 1:  # the host's chunks
+        for t in range(nt):
+            b, rem = divmod(t, H * nch)
+            h, c = divmod(rem, nch)
+            if c * ch < lens[b]:
+                out[t] = (b, h, c * ch, min(lens[b], (c + 1) * ch), t - c)
+        return out
+    spare = B * H * (nch - 1)
+    cn = max(32, -(-(-(-(H * sum(lens)) // spare)) // 32) * 32)
+    ch = min(ch, cn)
+    t = 0
+    for b in range(B):
+        nb = -(-lens[b] // ch)
+        for h in range(H):
+            first = t
+            for c in range(nb):
+                out[t] = (b, h, c * ch, min(lens[b], (c + 1) * ch), first)
+                t += 1
+    assert t <= nt, (B, H, Lmax, nt, t)
+    return out
+
+
+def test_sdpa_device_chunks_cover_every_request(G):
+    """For request lengths of every spread, the chunks the op body derives
+    cover each (request, head) pair's rows [0, L_b) once, stay within the op's
+    tiles (so within the workspace's partials), and a pair's chunks sit in
+    consecutive workspace slots, where its last chunk merges them."""
+    rng = np.random.default_rng(9)
+    cases = [(1, 32, [2000]), (8, 32, [4096] * 8), (8, 32, [128, 4096, 33, 1, 700, 4095, 2048, 64]),
+             (3, 32, [1025, 1, 1]), (2, 1, [4096, 32]), (4, 8, [777, 776, 1, 500]), (47, 32, list(range(1, 48)))]
+    for _ in range(40):
+        B = int(rng.integers(1, 12))
+        cases.append((B, int(rng.choice([1, 4, 32])), rng.integers(1, 4097, size=B).tolist()))
+    for B, H, lens in cases:
+        Lmax = max(lens)
+        nt = G.op_ntiles(_desc(G, "sdpa", 1, (B, H, 128, 4096, Lmax, B * H)))
+        m = _sdpa_device_chunks(B, H, Lmax, nt, lens)
+        assert max(m) < nt
+        for b in range(B):
+            for h in range(H):
+                rows = sorted((v[2], v[3], t, v[4]) for t, v in m.items() if v[0] == b and v[1] == h)
+                assert rows[0][0] == 0 and rows[-1][1] == lens[b]
+                assert all(x[1] == y[0] for x, y in zip(rows, rows[1:]))
+                assert all(r[0] % 32 == 0 and r[1] > r[0] for r in rows)
+                assert [r[2] for r in rows] == list(range(rows[0][3], rows[0][3] + len(rows)))
+
+
 @pytest.mark.parametrize("bad", [
     dict(op=20, dims=(4,)),                                      # reserved id
     dict(op="add", dtype=7, dims=(4,)),                          # bad dtype
