@@ -393,6 +393,23 @@ static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool use
 {
     const uint32_t *m = d->dims;
     uint64_t nt = 1;
+    /* element-wise ops, the bulk of a throughput stream: the same checks and
+     * tiling as the general path below, with the conditions combined into
+     * one branch (the op mix would make each its own mispredicted branch) */
+    if ((uint32_t)d->op_id - GPUOS_OP_ADD < 4u) {
+        const uint32_t op = d->op_id;
+        const bool f32 = d->dtype == GPUOS_F32;
+        const bool bin = op <= GPUOS_OP_MUL;
+        const bool bad = (!f32 && d->dtype != GPUOS_BF16) |
+                         (m[0] != 0 && ((d->a == 0) | (d->out == 0) | (bin & (d->b == 0)))) |
+                         ((d->flags & ~(GPUOS_FLAG_FENCE | GPUOS_FLAG_DEP_REL)) != 0);
+        nt = ew_tiles(m[0], op == GPUOS_OP_GELU ? GPUOS_GELU_TILE_MIN : GPUOS_EW_TILE_MIN,
+                      f32 ? GPUOS_EW_TILE_F32 : GPUOS_EW_TILE_BF16);
+        nt += (nt == 0);
+        if (bad | (nt > GPUOS_TILE_MAX)) return GPUOS_EINVAL;
+        *ntiles_out = (uint32_t)nt;
+        return GPUOS_OK;
+    }
     if (d->op_id >= GPUOS_MAX_OPS) return GPUOS_EINVAL;
     switch (d->op_id) {
     case GPUOS_OP_NOP: nt = 1; break;
@@ -1003,17 +1020,20 @@ static int submit_run_spsc(gpuos_ctx *c, const gpuos_desc *d, uint32_t count, ui
             const bool user_known = di->op_id >= GPUOS_OP_USER_FIRST && c->user_registered[di->op_id];
             rc = validate_and_tile(di, &nt, user_known);
             if (rc) break;
+            /* dependencies: an absolute ticket + 1 must be at most t, a
+             * distance (DEP_REL) at most t as well (then t - v + 1 <= t) */
             uint64_t deps[2];
-            for (int q = 0; q < 2 && rc == GPUOS_OK; q++) {
-                uint64_t v = di->dep[q];
-                if (v && (di->flags & GPUOS_FLAG_DEP_REL)) {
-                    if (v > t) rc = GPUOS_EINVAL;
-                    v = t - v + 1;
-                }
-                if (v > t) rc = GPUOS_EINVAL;
-                deps[q] = v;
+            bool dbad = false;
+            const bool rel = (di->flags & GPUOS_FLAG_DEP_REL) != 0;
+            for (int q = 0; q < 2; q++) {
+                const uint64_t v = di->dep[q];
+                dbad |= v > t;
+                deps[q] = (rel && v) ? t - v + 1 : v;
             }
-            if (rc) break;
+            if (dbad) {
+                rc = GPUOS_EINVAL;
+                break;
+            }
             const uint32_t slot = (uint32_t)(t & c->mask);
             if (t >= c->N) {
                 const uint64_t prev = t - c->N;
