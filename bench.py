@@ -556,6 +556,11 @@ def stream_phase(G, name, args, cfg_kw, local, peak, gemm=None):
     torch.cuda.synchronize()
     gen_s = time.perf_counter() - t_gen
     K = args.stream_steps
+    if name == "c1":
+        # a step of the smallest stream lasts tens of microseconds: over a
+        # few steps the launch and the stop of the single executor launch
+        # (included in the timed region) would outweigh the steps themselves
+        K = max(K, args.c1_steps)
     if name == "c1" and not args.ring_entries:
         cfg_kw = dict(cfg_kw, ring_entries=4096)  # as the smallest stream is defined
     ex = G.Executor(**cfg_kw)
@@ -702,6 +707,7 @@ def main():
     ap.add_argument("--streams", default="c1,c2l,c3,c4,c5",
                     help="other workloads measured into the same line ('' = none)")
     ap.add_argument("--stream-steps", type=int, default=3, help="timed steps of each other workload")
+    ap.add_argument("--c1-steps", type=int, default=200, help="timed steps of the smallest stream, at least")
     ap.add_argument("--stream-warmup", type=int, default=3, help="warm-up steps of each other workload")
     ap.add_argument("--corun-blocks", default="8,19,38,76,152",
                     help="executor blocks of the GEMM co-run curve (mixed pipeline); '' = none")

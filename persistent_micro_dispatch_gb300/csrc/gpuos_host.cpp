@@ -349,9 +349,10 @@ static bool al16(uint64_t p) { return (p & 15u) == 0; }
  * 5-7 us of copying, so fewer, larger tiles raise what the worker warps
  * sustain (measured on the variable-shape stream from a pre-filled ring:
  * 40.5 -> 49.4 M descriptors/s with 4,096-element tiles -> 16,384; large
- * ops 0.89 -> 0.95 of the copy peak). Small GELUs split down to 1,024 elements
+ * ops 0.89 -> 0.95 of the copy peak). Small GELUs split down to 2,048 elements
  * (their arithmetic, not their bytes, sets the time, and a chain of them
- * waits on each). The device recovers the tile size from n and ntiles
+ * waits on each; 1,024 made the mixed pipeline 1.5 % faster and the
+ * variable-shape stream 3 % slower). The device recovers the tile size from n and ntiles
  * alone (round_up(ceil(n / ntiles), 256)). */
 static_assert((GPUOS_EW_TILE_MIN & (GPUOS_EW_TILE_MIN - 1)) == 0 && (GPUOS_GELU_TILE_MIN & (GPUOS_GELU_TILE_MIN - 1)) == 0 &&
                   (GPUOS_EW_TILE_F32 & (GPUOS_EW_TILE_F32 - 1)) == 0 &&
@@ -1688,7 +1689,7 @@ int gpuos_eager_run(const gpuos_desc *d, uint32_t count, uint32_t stage_bytes, v
          * once */
         const uint16_t op = d[i].op_id;
         if (op == GPUOS_OP_ADD || op == GPUOS_OP_MUL || op == GPUOS_OP_RELU || op == GPUOS_OP_GELU) {
-            const uint64_t e = ew_tiles(d[i].dims[0], op == GPUOS_OP_GELU ? GPUOS_GELU_TILE_MIN : GPUOS_EAGER_TILE_MIN,
+            const uint64_t e = ew_tiles(d[i].dims[0], op == GPUOS_OP_GELU ? GPUOS_EAGER_GELU_TILE_MIN : GPUOS_EAGER_TILE_MIN,
                                         d[i].dtype == GPUOS_F32 ? GPUOS_EAGER_TILE_F32 : GPUOS_EAGER_TILE_BF16);
             if (e > GPUOS_TILE_MAX) return GPUOS_EINVAL;
             nt = e ? (uint32_t)e : 1u;
