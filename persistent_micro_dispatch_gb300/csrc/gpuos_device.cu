@@ -243,8 +243,19 @@ struct WarpStage {
     unsigned long long mbar[2]; /* completion barriers of the warp's bulk copies */
     uint32_t phase[2];          /* parity of the next phase to wait for, per barrier */
     uint32_t pad[2];
+    /* A row op may take its helper's further rows itself (row_pipe), so
+     * that it can copy the next row while it works on the current one. The
+     * worker sets claim_ctr (the descriptor's tile counter; null: one tile
+     * per call) and claim_base (its helper count) before the call; an op
+     * that took rows itself sets claim_done and reports the tiles it ran or
+     * skipped (claim_count) and the next claimed tile (claim_next, >= the
+     * tile count once none is left). */
+    uint32_t *claim_ctr;
+    uint32_t claim_base, claim_count, claim_next, claim_done;
+    uint32_t pad2[2];
 };
-#define GPUOS_WARP_STAGE_HDR 32u
+#define GPUOS_WARP_STAGE_HDR 64u
+static_assert(sizeof(WarpStage) == GPUOS_WARP_STAGE_HDR, "warp staging header");
 extern __shared__ __align__(16) unsigned char g_dyn_smem[];
 
 DEV StageHdr *stage_hdr() { return reinterpret_cast<StageHdr *>(g_dyn_smem); }
@@ -269,6 +280,8 @@ DEV void stage_init(uint32_t stage_bytes)
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&w->mbar[1])) : "memory");
         w->phase[0] = 0;
         w->phase[1] = 0;
+        w->claim_ctr = nullptr;
+        w->claim_done = 0;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
@@ -946,6 +959,202 @@ DEV int row_generic(const gpuos_devdesc *d, uint32_t row, uint32_t H)
     return GPUOS_ST_OK;
 }
 
+/* Lane 0: bulk-copy row `row` (2H bytes) into half hb of the warp's buffer. */
+DEV void row_issue(WarpStage *w, unsigned char *half, const uint16_t *X, uint32_t row, uint32_t H, uint32_t hb)
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect(&w->mbar[hb], 2u * H);
+    bulk_g2s(half, X + (uint64_t)row * H, 2u * H, &w->mbar[hb]);
+}
+
+/* Rows that fit half the staging buffer (softmax, row sum/max/min:
+ * 4H <= stage_bytes; LayerNorm, whose gamma and beta stay in the buffer for
+ * all of the helper's rows: 8H <= stage_bytes; H % 8 == 0, 16-byte aligned):
+ * the op takes its helper's rows itself. While one row is worked on in one
+ * half of the row space, the next row (claimed from the descriptor's tile
+ * counter) is already on its way into the other, so a helper's rows after
+ * the first cost their passes, not a copy round trip each; and the helper's
+ * rows run in one call of the op. Without a claim context (the eager
+ * kernel) it runs the one row. Buffer: [gamma | beta] (LayerNorm only),
+ * then two row halves. */
+template <int K>
+DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
+{
+    const uint32_t lane = lane_id(), nv = H / 8;
+    WarpStage *w = warp_stage();
+    unsigned char *buf = warp_stage_buf();
+    const uint32_t roff = (K == ROW_LN) ? 4u * H : 0u;
+    const uint32_t hbytes = (K == ROW_LN) ? 2u * H : stage_hdr()->stage_bytes / 2u;
+    uint32_t *ctr = w->claim_ctr;
+    const uint32_t base = w->claim_base;
+    const bool claim = ctr != nullptr && base < R;
+    const uint16_t *X = reinterpret_cast<const uint16_t *>(d->a);
+    uint32_t ph = w->phase[0] | (w->phase[1] << 1); /* bit hb: parity to wait for on half hb */
+    uint32_t hb = 0, count = 0, next = R;
+    int32_t st = GPUOS_ST_OK;
+    if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect(&w->mbar[0], 2u * H + (K == ROW_LN ? 4u * H : 0u));
+        bulk_g2s(buf + roff, X + (uint64_t)row * H, 2u * H, &w->mbar[0]);
+        if (K == ROW_LN) {
+            bulk_g2s(buf, reinterpret_cast<const void *>(d->b), 2u * H, &w->mbar[0]);
+            bulk_g2s(buf + 2u * H, reinterpret_cast<const void *>(d->aux0), 2u * H, &w->mbar[0]);
+        }
+    }
+    while (true) {
+        /* the next row: claimed, and its copy started into the other half */
+        uint32_t nx = R;
+        if (claim && lane == 0) {
+            nx = base + atomicAdd(ctr, 1u);
+            if (nx < R) row_issue(w, buf + roff + (hb ^ 1u) * hbytes, X, nx, H, hb ^ 1u);
+        }
+        nx = __shfl_sync(0xFFFFFFFFu, nx, 0);
+        count++;
+        if (!mbar_wait(&w->mbar[hb], (ph >> hb) & 1u)) {
+            /* leave no copy writing the buffer: wait once more (bounded) on
+             * this half and on the other if a copy went out to it; the
+             * claimed next row goes back to the worker, which counts it */
+            mbar_wait(&w->mbar[hb], (ph >> hb) & 1u);
+            ph ^= 1u << hb;
+            if (nx < R) {
+                mbar_wait(&w->mbar[hb ^ 1u], (ph >> (hb ^ 1u)) & 1u);
+                ph ^= 1u << (hb ^ 1u);
+            }
+            st = GPUOS_ST_COPY_TIMEOUT;
+            next = nx;
+            break;
+        }
+        ph ^= 1u << hb;
+        const uint4 *sx = reinterpret_cast<const uint4 *>(buf + roff + hb * hbytes);
+        if (K == ROW_LN) {
+            /* biased variance, mean and variance in two passes */
+            uint4 *y = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(d->out) + (uint64_t)row * H);
+            const uint4 *sg = reinterpret_cast<const uint4 *>(buf);
+            const uint4 *sbt = sg + nv;
+            float s8[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) s8[i] = 0.0f;
+#pragma unroll 2
+            for (uint32_t v = lane; v < nv; v += 32) {
+                float f[8];
+                unpack8(sx[v], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) s8[i] += f[i];
+            }
+            float sum = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) sum += s8[i];
+            const float mean = warp_sum(sum) / (float)H;
+#pragma unroll
+            for (int i = 0; i < 8; i++) s8[i] = 0.0f;
+#pragma unroll 2
+            for (uint32_t v = lane; v < nv; v += 32) {
+                float f[8];
+                unpack8(sx[v], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const float t = f[i] - mean;
+                    s8[i] = fmaf(t, t, s8[i]);
+                }
+            }
+            float q = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) q += s8[i];
+            const float rstd = rsqrtf(warp_sum(q) / (float)H + d->fparam[0]);
+#pragma unroll 2
+            for (uint32_t v = lane; v < nv; v += 32) {
+                float f[8], gf[8], bf[8];
+                unpack8(sx[v], f);
+                unpack8(sg[v], gf);
+                unpack8(sbt[v], bf);
+#pragma unroll
+                for (int i = 0; i < 8; i++) f[i] = (f[i] - mean) * rstd * gf[i] + bf[i];
+                __stcg(y + v, pack8(f));
+            }
+        } else if (K == ROW_SUM || K == ROW_MAX || K == ROW_MIN) {
+            const float init = (K == ROW_SUM) ? 0.0f : (K == ROW_MAX ? -INFINITY : INFINITY);
+            float a8[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) a8[i] = init;
+#pragma unroll 2
+            for (uint32_t v = lane; v < nv; v += 32) {
+                float f[8];
+                unpack8(sx[v], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    if (K == ROW_SUM) a8[i] += f[i];
+                    else if (K == ROW_MAX) a8[i] = fmaxf(a8[i], f[i]);
+                    else a8[i] = fminf(a8[i], f[i]);
+                }
+            }
+            float acc = a8[0];
+#pragma unroll
+            for (int i = 1; i < 8; i++) {
+                if (K == ROW_SUM) acc += a8[i];
+                else if (K == ROW_MAX) acc = fmaxf(acc, a8[i]);
+                else acc = fminf(acc, a8[i]);
+            }
+            if (K == ROW_SUM) acc = warp_sum(acc);
+            else if (K == ROW_MAX) acc = warp_max(acc);
+            else acc = warp_min(acc);
+            if (lane == 0) {
+                if (K == ROW_SUM) reinterpret_cast<float *>(d->out)[row] = acc;
+                else reinterpret_cast<uint16_t *>(d->out)[row] = to_bf(acc);
+            }
+        } else {
+            uint4 *y = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(d->out) + (uint64_t)row * H);
+            float m = -INFINITY;
+#pragma unroll 2
+            for (uint32_t v = lane; v < nv; v += 32) {
+                float f[8];
+                unpack8(sx[v], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) m = fmaxf(m, f[i]);
+            }
+            m = warp_max(m);
+            float s8[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) s8[i] = 0.0f;
+#pragma unroll 2
+            for (uint32_t v = lane; v < nv; v += 32) {
+                float f[8];
+                unpack8(sx[v], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) s8[i] += __expf(f[i] - m);
+            }
+            float sum = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) sum += s8[i];
+            const float inv = 1.0f / warp_sum(sum);
+#pragma unroll 2
+            for (uint32_t v = lane; v < nv; v += 32) {
+                float f[8];
+                unpack8(sx[v], f);
+#pragma unroll
+                for (int i = 0; i < 8; i++) f[i] = __expf(f[i] - m) * inv;
+                __stcg(y + v, pack8(f));
+            }
+        }
+        /* every lane is done with half hb before the next claim refills it */
+        __syncwarp();
+        if (nx >= R) {
+            next = nx;
+            break;
+        }
+        row = nx;
+        hb ^= 1u;
+    }
+    if (lane == 0) {
+        w->phase[0] = ph & 1u;
+        w->phase[1] = (ph >> 1) & 1u;
+        w->claim_count = count;
+        w->claim_next = next;
+        w->claim_done = ctr != nullptr ? 1u : 0u;
+    }
+    __syncwarp();
+    return st;
+}
+
 template <int K>
 DEV int row_tile(const gpuos_devdesc *d, uint32_t row)
 {
@@ -956,9 +1165,12 @@ DEV int row_tile(const gpuos_devdesc *d, uint32_t row)
     if (K == ROW_SOFTMAX || K == ROW_LN) ok = ok && (d->out & 15u) == 0;
     if (K == ROW_LN) ok = ok && ((d->b | d->aux0) & 15u) == 0;
     if (!ok) return row_generic<K>(d, row, H);
-    /* staged: the row, plus (LayerNorm) gamma and beta in chunks of C
-     * columns, a multiple of 8 of at least 256 (or all H) */
+    /* staged: two rows at a time (with LayerNorm's gamma and beta, if they
+     * fit beside them); else the row, plus
+     * (LayerNorm) gamma and beta in chunks of C columns, a multiple of 8 of
+     * at least 256 (or all H) */
     const uint32_t sb = stage_hdr()->stage_bytes;
+    if ((K == ROW_LN ? 8u : 4u) * H <= sb) return row_pipe<K>(d, row, R, H);
     if (2u * H <= sb) {
         uint32_t C = 0;
         if (K == ROW_LN) {
@@ -2310,14 +2522,43 @@ DEV void worker(const gpuos_exec_params &p, gpuos_devdesc *sd, uint32_t gw, uint
          * claim. */
         int32_t status = dstatus;
         uint32_t count = 0;
+        /* row ops may take the helper's further rows themselves (the claim
+         * context in the warp's staging header); anything else, or a row op
+         * that did not, gets one tile per call */
+        const bool rowop = sd->op_id >= GPUOS_OP_SOFTMAX && sd->op_id <= GPUOS_OP_ROWMIN;
+        WarpStage *wst = warp_stage();
         while (true) {
             uint32_t next = ntiles;
-            if (ntiles > helpers && lane == 0) next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
+            if (rowop) {
+                if (lane == 0) {
+                    wst->claim_ctr = ntiles > helpers ? p.tile_ctr + slot : nullptr;
+                    wst->claim_base = helpers;
+                    wst->claim_done = 0;
+                }
+                __syncwarp();
+            } else if (ntiles > helpers && lane == 0) {
+                next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
+            }
             if (status == GPUOS_ST_OK) {
                 if (fn == nullptr) status = GPUOS_ST_BAD_OP;
                 else status = fn(sd, tile);
             }
-            count++;
+            if (rowop) {
+                __syncwarp();
+                if (wst->claim_done) {
+                    count += wst->claim_count;
+                    next = wst->claim_next;
+                } else {
+                    count++;
+                    if (ntiles > helpers && lane == 0) next = helpers + atomicAdd(p.tile_ctr + slot, 1u);
+                }
+                if (lane == 0) {
+                    wst->claim_ctr = nullptr;
+                    wst->claim_done = 0;
+                }
+            } else {
+                count++;
+            }
             next = __shfl_sync(0xFFFFFFFFu, next, 0);
             if (next >= ntiles) break;
             tile = next;
