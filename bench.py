@@ -137,11 +137,11 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
                    "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
 TRAFFIC = {
-    "c2": dict(bytes=248_996_864, descs=4096, sources="d048251c383fb5bd"),
-    "c2l": dict(bytes=1_066_511_872, descs=400, sources="d048251c383fb5bd"),
-    "c3": dict(bytes=399_550_464, descs=2048, sources="d048251c383fb5bd"),
-    "c4": dict(bytes=30_818_519_040, descs=600, sources="d048251c383fb5bd"),
-    "c5": dict(bytes=493_531_136, descs=224, sources="d048251c383fb5bd"),
+    "c2": dict(bytes=249_576_704, descs=4096, sources="69554615600b3df4"),
+    "c2l": dict(bytes=1_091_012_096, descs=400, sources="69554615600b3df4"),
+    "c3": dict(bytes=414_430_208, descs=2048, sources="69554615600b3df4"),
+    "c4": dict(bytes=31_055_150_592, descs=600, sources="69554615600b3df4"),
+    "c5": dict(bytes=492_371_968, descs=224, sources="69554615600b3df4"),
 }
 
 

@@ -428,7 +428,8 @@ GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
  * Host tiling rule of a built-in op (what ntiles the library will write);
  * one tile is one warp's unit of work:
  *   add/mul/relu/gelu  ceil(n / te), te the smallest power of two >= n / 16
- *                      within [16384 (GELU: 2048), 16384 (f32) or 32768 (bf16)]
+ *                      within [16384 (GELU: 2048, or 1024 with a dependency),
+ *                      16384 (f32) or 32768 (bf16)]
  *                      elements;
  *                      the device splits n into ntiles ranges of
  *                      round_up(ceil(n / ntiles), 256) elements

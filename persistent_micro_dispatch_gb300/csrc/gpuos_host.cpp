@@ -349,12 +349,12 @@ static bool al16(uint64_t p) { return (p & 15u) == 0; }
  * 5-7 us of copying, so fewer, larger tiles raise what the worker warps
  * sustain (measured on the variable-shape stream from a pre-filled ring:
  * 40.5 -> 49.4 M descriptors/s with 4,096-element tiles -> 16,384; large
- * ops 0.89 -> 0.95 of the copy peak). Small GELUs split down to 2,048 elements
- * (their arithmetic, not their bytes, sets the time, and a chain of them
- * waits on each; 1,024 made the mixed pipeline 1.5 % faster and the
- * variable-shape stream 3 % slower). The device recovers the tile size from n and ntiles
+ * ops 0.89 -> 0.95 of the copy peak). Small GELUs split down to 2,048
+ * elements, or 1,024 with a dependency (gelu_tile_min): their arithmetic,
+ * not their bytes, sets the time. The device recovers the tile size from n and ntiles
  * alone (round_up(ceil(n / ntiles), 256)). */
 static_assert((GPUOS_EW_TILE_MIN & (GPUOS_EW_TILE_MIN - 1)) == 0 && (GPUOS_GELU_TILE_MIN & (GPUOS_GELU_TILE_MIN - 1)) == 0 &&
+                  (GPUOS_GELU_DEP_TILE_MIN & (GPUOS_GELU_DEP_TILE_MIN - 1)) == 0 &&
                   (GPUOS_EW_TILE_F32 & (GPUOS_EW_TILE_F32 - 1)) == 0 &&
                   (GPUOS_EW_TILE_BF16 & (GPUOS_EW_TILE_BF16 - 1)) == 0,
               "element-wise tile sizes are powers of two");
@@ -371,6 +371,17 @@ static uint64_t ew_tiles(uint64_t n, uint64_t tile_min, uint64_t tile_max)
     uint64_t te = p2 > lo ? p2 : lo;
     te = te < tile_max ? te : tile_max;
     return (n + te - 1) >> __builtin_ctzll(te);
+}
+
+/* A GELU that waits on another descriptor sits on a dependency chain, where
+ * its latency adds up: it keeps the finer split (measured on the mixed
+ * pipeline, whose every op has a dependency: 1,024-element tiles 129.4 K
+ * ops/s, 2,048 127.5 K); a free GELU only needs throughput, which the
+ * coarser split serves better (variable-shape stream 50.6 -> 52.3 M
+ * descriptors/s with 2,048 for all GELUs). */
+static uint64_t gelu_tile_min(const gpuos_desc *d)
+{
+    return (d->dep[0] | d->dep[1]) ? GPUOS_GELU_DEP_TILE_MIN : GPUOS_GELU_TILE_MIN;
 }
 
 /* Decode-attention chunks: every (b, h) pair's keys are cut into at most
@@ -404,7 +415,7 @@ static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool use
         const bool bad = (!f32 && d->dtype != GPUOS_BF16) |
                          (m[0] != 0 && ((d->a == 0) | (d->out == 0) | (bin & (d->b == 0)))) |
                          ((d->flags & ~(GPUOS_FLAG_FENCE | GPUOS_FLAG_DEP_REL)) != 0);
-        nt = ew_tiles(m[0], op == GPUOS_OP_GELU ? GPUOS_GELU_TILE_MIN : GPUOS_EW_TILE_MIN,
+        nt = ew_tiles(m[0], op == GPUOS_OP_GELU ? gelu_tile_min(d) : GPUOS_EW_TILE_MIN,
                       f32 ? GPUOS_EW_TILE_F32 : GPUOS_EW_TILE_BF16);
         nt += (nt == 0);
         if (bad | (nt > GPUOS_TILE_MAX)) return GPUOS_EINVAL;
@@ -421,7 +432,7 @@ static int validate_and_tile(const gpuos_desc *d, uint32_t *ntiles_out, bool use
         if (d->dtype != GPUOS_F32 && d->dtype != GPUOS_BF16) return GPUOS_EINVAL;
         const bool bin = d->op_id == GPUOS_OP_ADD || d->op_id == GPUOS_OP_MUL;
         if (m[0] && (!d->a || !d->out || (bin && !d->b))) return GPUOS_EINVAL;
-        nt = ew_tiles(m[0], d->op_id == GPUOS_OP_GELU ? GPUOS_GELU_TILE_MIN : GPUOS_EW_TILE_MIN,
+        nt = ew_tiles(m[0], d->op_id == GPUOS_OP_GELU ? gelu_tile_min(d) : GPUOS_EW_TILE_MIN,
                       d->dtype == GPUOS_F32 ? GPUOS_EW_TILE_F32 : GPUOS_EW_TILE_BF16);
         break;
     }

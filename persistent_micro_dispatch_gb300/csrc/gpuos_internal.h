@@ -14,6 +14,7 @@
 #define GPUOS_EW_TILE_BF16 32768          /* ... and bf16 tile */
 #define GPUOS_EW_TILE_MIN 16384           /* smallest add/mul/ReLU tile the host picks */
 #define GPUOS_GELU_TILE_MIN 2048          /* ... and GELU tile (more arithmetic per element) */
+#define GPUOS_GELU_DEP_TILE_MIN 1024      /* ... and GELU tile of a descriptor with a dependency */
 #define GPUOS_EAGER_TILE_F32 4096         /* element-wise tiles of the eager baseline: largest fp32 */
 #define GPUOS_EAGER_TILE_BF16 8192        /* ... largest bf16 */
 #define GPUOS_EAGER_TILE_MIN 4096         /* ... smallest add/mul/ReLU */

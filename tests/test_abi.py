@@ -67,6 +67,8 @@ def _desc(G, op, dtype=1, dims=(), ptr=0x1000, **kw):
     d["dims"] = dd
     for f in ("a", "b", "out", "aux0", "aux1", "aux2"):
         d[f] = kw.get(f, ptr)
+    if "dep" in kw:
+        d["dep"] = kw["dep"]
     return d
 
 
@@ -109,6 +111,11 @@ def test_tiling_rule(G):
     assert G.op_ntiles(_desc(G, "add", 1, (1 << 20,))) == 32      # te 32768 (bf16 cap)
     assert G.op_ntiles(_desc(G, "gelu", 1, (1 << 20,))) == 32     # te 32768 (bf16 cap)
     assert G.op_ntiles(_desc(G, "gelu", 1, (40000,))) == 10       # te 4096 >= 40000/16
+    # a GELU with a dependency keeps the finer split: te from 1024
+    assert G.op_ntiles(_desc(G, "gelu", 1, (4096,), dep=(5, 0))) == 4      # te 1024
+    assert G.op_ntiles(_desc(G, "gelu", 1, (4096,), dep=(0, 5))) == 4
+    assert G.op_ntiles(_desc(G, "gelu", 1, (1000,), dep=(5, 0))) == 1
+    assert G.op_ntiles(_desc(G, "add", 1, (4096,), dep=(5, 0))) == 1       # add/mul/ReLU: no change
     assert G.op_ntiles(_desc(G, "gelu", 0, (0,))) == 1            # empty op: one tile
     assert G.op_ntiles(_desc(G, "softmax", 1, (37, 1024))) == 37  # one row per tile
     assert G.op_ntiles(_desc(G, "rope", 1, (5, 32, 128))) == 5 * 8  # four heads per tile
