@@ -924,27 +924,41 @@ def main():
         host_out = [torch.empty(ds.bufs[i].numel(), dtype=torch.uint8).pin_memory() for i in out_idx]
         h2d = sum(t.numel() for t in host_in)
         d2h = sum(t.numel() for t in host_out)
-        cs = torch.cuda.Stream()
+        # two sets of device buffers, used by alternate steps: the copy of a
+        # step's results back to the host overlaps the next step's input copy
+        # and run (copy engines run both directions at once), and a set is
+        # reused only once its previous results have left
+        ds2 = DeviceStream(s, device=f"cuda:{local}")
+        sets = [(ds, descs), (ds2, ds2.descs())]
+        cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+        out_done = [None, None]
         # device-wide synchronisation only while no executor is resident: a
         # resident persistent kernel never lets it return
         torch.cuda.synchronize()
         ex = G.Executor(**cfg_kw)
         barrier(world)
         a = time.perf_counter()
-        for _ in range(args.steps):
-            with torch.cuda.stream(cs):
+        for k in range(args.steps):
+            dsk, dk = sets[k % 2]
+            with torch.cuda.stream(cin):
                 for i, t in zip(in_idx, host_in):
-                    ds.bufs[i].copy_(t, non_blocking=True)
-            cs.synchronize()
-            ex.submit_batch(descs)
+                    dsk.bufs[i].copy_(t, non_blocking=True)
+            cin.synchronize()
+            if out_done[k % 2] is not None:
+                out_done[k % 2].synchronize()  # this set's previous results have left
+            ex.submit_batch(dk)
             ex.sync(timeout_ms=600_000)
-            with torch.cuda.stream(cs):
+            with torch.cuda.stream(cout):
                 for i, t in zip(out_idx, host_out):
-                    t.copy_(ds.bufs[i], non_blocking=True)
-            cs.synchronize()
+                    t.copy_(dsk.bufs[i], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cout)
+            out_done[k % 2] = ev
+        cout.synchronize()
         b = time.perf_counter()
         ex.shutdown()
         torch.cuda.synchronize()
+        del sets, ds2
         eu, esec = aggregate(n_ops * args.steps, b - a, world)
         result["e2e"] = {"value": eu / esec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": 1e3 * (b - a) / args.steps}
