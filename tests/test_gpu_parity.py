@@ -78,6 +78,22 @@ def test_c4_decode_small_and_kv_copy_bit_exact():
 
 
 @pytest.mark.parametrize("stage_bytes", [16384, 0])
+def test_c4_decode_wide_length_spread(stage_bytes):
+    """Decode steps whose requests' lengths run from 1 to 4,096 rows in one
+    op (the attention body shortens its chunks from the lengths, so a step
+    mixes single-row requests, requests of one chunk and requests of many),
+    staged and register paths; every output against the oracle."""
+    s = S.stream_c4(n_steps=16, L_lo=1, seed=41)
+    lens = s.buffers[s.buf_index("lens")].data
+    for o in s.ops:
+        if o.op == "sdpa" and o.dims[0] >= 2:
+            lens[o.aux0.off] = 1        # a one-row request beside long ones
+            lens[o.aux0.off + 1] = 33   # and one just past a 32-row chunk
+    s, ds, rep, st, hist = _run_and_compare(s, cfg=dict(stage_bytes=stage_bytes))
+    check_kv_copies(s, ds)
+
+
+@pytest.mark.parametrize("stage_bytes", [16384, 0])
 def test_mixed_small_every_op_kind(stage_bytes):
     """Every op kind at small, ragged sizes (tails, 1-row and 8-column tiles,
     ragged head groups, multi-chunk attention), staged and register paths."""
