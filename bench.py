@@ -137,11 +137,11 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
                    "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
 TRAFFIC = {
-    "c2": dict(bytes=249_576_704, descs=4096, sources="69554615600b3df4"),
-    "c2l": dict(bytes=1_091_012_096, descs=400, sources="69554615600b3df4"),
-    "c3": dict(bytes=414_430_208, descs=2048, sources="69554615600b3df4"),
-    "c4": dict(bytes=31_055_150_592, descs=600, sources="69554615600b3df4"),
-    "c5": dict(bytes=492_371_968, descs=224, sources="69554615600b3df4"),
+    "c2": dict(bytes=249_955_072, descs=4096, sources="b891b1c155834497"),
+    "c2l": dict(bytes=1_089_352_704, descs=400, sources="b891b1c155834497"),
+    "c3": dict(bytes=414_108_672, descs=2048, sources="b891b1c155834497"),
+    "c4": dict(bytes=31_066_064_896, descs=600, sources="b891b1c155834497"),
+    "c5": dict(bytes=493_653_760, descs=224, sources="b891b1c155834497"),
 }
 
 
