@@ -358,7 +358,10 @@ GPUOS_API int gpuos_load_module(gpuos_ctx *ctx, const void *image, size_t len);
 GPUOS_API int gpuos_compile_op(const char *source, const char *name, void **image, size_t *size, char *log,
                                size_t log_cap);
 GPUOS_API void gpuos_free_image(void *image);
-/* The header text gpuos_compile_op puts before every operator source. */
+/* The header text gpuos_compile_op puts before every operator source (the
+ * operator ABI of §3 Q2 "3. Dynamic Operator Table": the descriptor an
+ * operator receives, its signature and status codes). A static string owned
+ * by the library; never fails. */
 GPUOS_API const char *gpuos_op_header(void);
 
 /* Runtime operator injection (§3 Q2 "3. Dynamic Operator Table", steps 3-5):
