@@ -202,16 +202,24 @@ def test_sdpa_device_chunks_cover_every_request(G):
         cases.append((B, int(rng.choice([1, 4, 32])), rng.integers(1, 4097, size=B).tolist()))
     for B, H, lens in cases:
         Lmax = max(lens)
-        nt = G.op_ntiles(_desc(G, "sdpa", 1, (B, H, 128, 4096, Lmax, B * H)))
-        m = _sdpa_device_chunks(B, H, Lmax, nt, lens)
-        assert max(m) < nt
-        for b in range(B):
-            for h in range(H):
-                rows = sorted((v[2], v[3], t, v[4]) for t, v in m.items() if v[0] == b and v[1] == h)
-                assert rows[0][0] == 0 and rows[-1][1] == lens[b]
-                assert all(x[1] == y[0] for x, y in zip(rows, rows[1:]))
-                assert all(r[0] % 32 == 0 and r[1] > r[0] for r in rows)
-                assert [r[2] for r in rows] == list(range(rows[0][3], rows[0][3] + len(rows)))
+        nts = [G.op_ntiles(_desc(G, "sdpa", 1, (B, H, 128, 4096, Lmax, B * H)))]
+        if B * H <= 256:
+            # the allocation-free entry point's split: chunks of 256 rows
+            nts.append(B * H * -(-Lmax // 256))
+        for nt in nts:
+            _check_sdpa_chunks(B, H, Lmax, nt, lens)
+
+
+def _check_sdpa_chunks(B, H, Lmax, nt, lens):
+    m = _sdpa_device_chunks(B, H, Lmax, nt, lens)
+    assert max(m) < nt
+    for b in range(B):
+        for h in range(H):
+            rows = sorted((v[2], v[3], t, v[4]) for t, v in m.items() if v[0] == b and v[1] == h)
+            assert rows[0][0] == 0 and rows[-1][1] == lens[b]
+            assert all(x[1] == y[0] for x, y in zip(rows, rows[1:]))
+            assert all(r[0] % 32 == 0 and r[1] > r[0] for r in rows)
+            assert [r[2] for r in rows] == list(range(rows[0][3], rows[0][3] + len(rows)))
 
 
 @pytest.mark.parametrize("bad", [
