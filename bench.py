@@ -137,11 +137,11 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
                    "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
 TRAFFIC = {
-    "c2": dict(bytes=249_955_072, descs=4096, sources="b891b1c155834497"),
-    "c2l": dict(bytes=1_089_352_704, descs=400, sources="b891b1c155834497"),
-    "c3": dict(bytes=414_108_672, descs=2048, sources="b891b1c155834497"),
-    "c4": dict(bytes=31_066_064_896, descs=600, sources="b891b1c155834497"),
-    "c5": dict(bytes=493_653_760, descs=224, sources="b891b1c155834497"),
+    "c2": dict(bytes=250_042_624, descs=4096, sources="e050cb5b55caeecd"),
+    "c2l": dict(bytes=1_091_287_040, descs=400, sources="e050cb5b55caeecd"),
+    "c3": dict(bytes=414_025_984, descs=2048, sources="e050cb5b55caeecd"),
+    "c4": dict(bytes=31_064_849_920, descs=600, sources="e050cb5b55caeecd"),
+    "c5": dict(bytes=493_201_664, descs=224, sources="e050cb5b55caeecd"),
 }
 
 

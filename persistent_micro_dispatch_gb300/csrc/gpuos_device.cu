@@ -10,28 +10,33 @@
  * counter.
  *
  * GB300 design (what differs from the page's per-warp poll/claim):
- *   - One warp of block 0 is the *sequencer*. It alone polls the host ring
- *     (32 slots per poll, one per lane, ld.acquire.sys across NVLink-C2C),
- *     copies each committed descriptor into a device-memory mirror, fixes the
- *     table version the descriptor runs with, and publishes one work-queue
- *     entry per tile. The host ring therefore sees one reader, and workers
- *     never touch host memory on the hot path.
+ *   - Warp 0 of blocks 0..S-1 (S = 4 by default; those blocks run nothing
+ *     else) are the *sequencers*. They take the host ring in windows of 128
+ *     tickets in turn: a sequencer polls its window's commit words with
+ *     relaxed system-scope loads across NVLink-C2C, takes the committed ones
+ *     under one acquire fence, copies them into a device-memory mirror with
+ *     the entry point of the table version they run with, and publishes one
+ *     work-queue entry per helper warp. Work-queue space is reserved in
+ *     ticket order by a turn passed from batch to batch as one word. Only
+ *     the sequencers read host memory on the hot path.
  *   - Every other warp is a *worker*. It claims work-queue entries with one
- *     64-bit atomicAdd each (the page's atomic claim), so a large op is split
- *     across many warps on many SMs (the page lists in-kernel multi-block
- *     cooperation as missing, §4 "design binding critique"), while a tiny op
- *     is one tile on one warp.
- *   - The last tile of a descriptor completes it: status and timestamps into
- *     the host-visible record, a device-memory done stamp for dependency waits
- *     and the store-release of the slot's host-visible completion word, which
- *     also releases the ring slot to the host.
+ *     64-bit atomicAdd each (the page's atomic claim); a helper starts with
+ *     its own tile and takes further ones from the descriptor's tile counter,
+ *     so a large op is split across many warps on many SMs (the page lists
+ *     in-kernel multi-block cooperation as missing, §4 "design binding
+ *     critique"), while a tiny op is one tile on one warp.
+ *   - The last tile of a descriptor completes it: a device-memory done stamp
+ *     for dependency waits (released first), then status and timestamps into
+ *     the host-visible record and the store-release of the slot's
+ *     host-visible completion word, which releases the ring slot to the host.
  *   - Every wait is bounded (dependency and fence waits by dep_timeout_ns,
- *     idle polling by the host-heartbeat watchdog) and ends in a status, never
- *     a trap.
- *   - Ops are memory-bound and use no tensor cores: 16-byte vector loads that
- *     bypass L1 (data produced by other SMs inside this same kernel must not
- *     be read from a stale L1 line), fp32 arithmetic, warp shuffles for
- *     reductions, registers for row staging.
+ *     copies into shared memory by an iteration limit, idle polling by the
+ *     host-heartbeat watchdog) and ends in a status, never a trap.
+ *   - Ops are memory-bound and use no tensor cores: operands arrive in each
+ *     warp's shared-memory staging buffer by TMA bulk copies (or by 16-byte
+ *     vector loads that bypass L1: data produced by other SMs inside this
+ *     same kernel must not be read from a stale L1 line), fp32 arithmetic,
+ *     warp shuffles for reductions.
  */
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -1340,9 +1345,10 @@ DEV int kv_tile(const gpuos_devdesc *d, uint32_t tile)
 }
 
 /* ---- decode SDPA: one (request, head, chunk of key rows) per tile ---------
- * The host picks the number of chunks per head (chunks of 256 rows, halved
- * down to 64 while the op has few tiles); the tile recovers the chunk length
- * from Lmax and ntiles. Four 8-lane groups walk interleaved key rows; in a
+ * The host picks the number of chunks per head (at most 1,536 tiles in all,
+ * chunks of at least 32 rows); the tile recovers the chunk length from Lmax
+ * and ntiles, and shortens it when the requests' lengths would leave tiles
+ * idle (see sdpa_tile). Four 8-lane groups walk interleaved key rows; in a
  * group lane li owns dims [8 li, 8 li + 8) and [64 + 8 li, 64 + 8 li + 8) of
  * q, K and V (two 16-byte pieces 128 bytes apart, so a quarter-warp reads 128
  * contiguous bytes of a row: no shared-memory bank conflicts). Scores use

@@ -39,7 +39,7 @@
 #define GPUOS_TQ_MAX (1u << 30)            /* work-queue entries */
 #define GPUOS_TQ_STAMP_MASK 0xFFFFFFFFFull /* 36-bit stamps */
 
-/* Mirror of a descriptor in device memory, written by the sequencer warp.
+/* Mirror of a descriptor in device memory, written by a sequencer warp.
  * Same layout as gpuos_desc except the last fields. */
 typedef struct gpuos_devdesc {
     uint16_t op_id;
@@ -54,7 +54,7 @@ typedef struct gpuos_devdesc {
     uint64_t fn;         /* op entry point, fixed with the version at sequencing (replaces `user`) */
     uint64_t ticket;
     uint32_t version;    /* table version fixed at sequencing (replaces `seq`) */
-    uint32_t pad;
+    uint32_t pad;        /* the helper warps (work-queue entries) published for it */
 } gpuos_devdesc;
 
 /* Work-queue entries are single 64-bit words (see tq_word in the device
