@@ -93,6 +93,28 @@ def test_c4_decode_wide_length_spread(stage_bytes):
     check_kv_copies(s, ds)
 
 
+def test_decode_attention_many_requests():
+    """One attention op over 40 requests of one head (more than 32, so the
+    op body's prefix over the requests' chunk counts runs in two rounds),
+    lengths from 1 to 1,024 rows; every output against the oracle."""
+    import math
+    rng = np.random.default_rng(43)
+    s = S.Stream("sdpa_many", meta=dict(seed=43))
+    B, H, D, Lc = 40, 1, 128, 1024
+    iq = s.add_buf("q", "bf16", B * H * D, S._pool(rng, B * H * D, "bf16"))
+    iK = s.add_buf("Kc", "bf16", B * H * Lc * D, S._pool(rng, B * H * Lc * D, "bf16"))
+    iV = s.add_buf("Vc", "bf16", B * H * Lc * D, S._pool(rng, B * H * Lc * D, "bf16"))
+    lens = rng.integers(1, Lc + 1, size=B).astype(np.int32)
+    lens[0], lens[1], lens[33] = 1, Lc, 33
+    il = s.add_buf("lens", "i32", B, lens)
+    io = s.add_buf("out_bf16", "bf16", B * H * D)
+    ws = s.add_buf("sdpa_ws", "u8", S.sdpa_workspace_bytes(B, H, D, Lc), fill=0)
+    s.ops.append(S.Op("sdpa", "bf16", a=S.Ref(iq, 0), b=S.Ref(iK, 0), aux1=S.Ref(iV, 0), aux0=S.Ref(il, 0),
+                      out=S.Ref(io, 0), aux2=S.Ref(ws, 0), dims=(B, H, D, Lc, int(lens.max()), B * H),
+                      fparam=(1.0 / math.sqrt(D),)))
+    _run_and_compare(s)
+
+
 @pytest.mark.parametrize("stage_bytes", [16384, 0])
 def test_mixed_small_every_op_kind(stage_bytes):
     """Every op kind at small, ragged sizes (tails, 1-row and 8-column tiles,
