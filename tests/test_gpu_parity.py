@@ -93,6 +93,28 @@ def test_c4_decode_wide_length_spread(stage_bytes):
     check_kv_copies(s, ds)
 
 
+def test_row_ops_many_rows():
+    """Row ops of thousands of rows (about a thousand helper warps each,
+    every helper taking further rows from the descriptor's counter and
+    copying the next one while it works on the current one), including a
+    LayerNorm whose gamma and beta stay in the staging buffer; every output
+    against the oracle."""
+    rng = np.random.default_rng(44)
+    s = S.Stream("rows_many", meta=dict(seed=44))
+    x1 = s.add_buf("x1", "bf16", 4096 * 1024, S._pool(rng, 4096 * 1024, "bf16", std=2.0))
+    x2 = s.add_buf("x2", "bf16", 2048 * 2048, S._pool(rng, 2048 * 2048, "bf16", std=2.0))
+    g = s.add_buf("gamma", "bf16", 2048, S._pool(rng, 2048, "bf16", std=0.1, mean=1.0))
+    b = s.add_buf("beta", "bf16", 2048, S._pool(rng, 2048, "bf16", std=0.1))
+    ob = s.add_buf("out_bf16", "bf16", 4096 * 1024 + 2048 * 2048 + 8192)
+    of = s.add_buf("out_f32", "f32", 4096)
+    s.ops.append(S.Op("softmax", "bf16", a=S.Ref(x1, 0), out=S.Ref(ob, 0), dims=(4096, 1024)))
+    s.ops.append(S.Op("layernorm", "bf16", a=S.Ref(x2, 0), b=S.Ref(g, 0), aux0=S.Ref(b, 0),
+                      out=S.Ref(ob, 4096 * 1024), dims=(2048, 2048), fparam=(1e-5,)))
+    s.ops.append(S.Op("rowmax", "bf16", a=S.Ref(x1, 0), out=S.Ref(ob, 4096 * 1024 + 2048 * 2048), dims=(4096, 1024)))
+    s.ops.append(S.Op("rowsum", "bf16", a=S.Ref(x1, 0), out=S.Ref(of, 0), dims=(4096, 1024)))
+    _run_and_compare(s)
+
+
 def test_decode_attention_many_requests():
     """One attention op over 40 requests of one head (more than 32, so the
     op body's prefix over the requests' chunk counts runs in two rounds),
