@@ -93,6 +93,41 @@ def test_c4_decode_wide_length_spread(stage_bytes):
     check_kv_copies(s, ds)
 
 
+@pytest.mark.parametrize("stage_bytes", [16384, 0])
+def test_elementwise_sizes_around_tile_boundaries(stage_bytes):
+    """add/mul/ReLU/GELU in fp32 and bf16 at sizes around the tile sizes
+    (1,024, 2,048, 16,384, 32,768 elements and their multiples), aligned and
+    at odd element offsets (the scalar path), some with a dependency (a
+    GELU then keeps its finer tiles); every output against the oracle."""
+    rng = np.random.default_rng(45)
+    s = S.Stream("ew_bounds", meta=dict(seed=45))
+    n_pool = 1 << 20
+    pf = s.add_buf("pool_f32", "f32", n_pool, S._pool(rng, n_pool, "f32"))
+    pb = s.add_buf("pool_bf16", "bf16", n_pool, S._pool(rng, n_pool, "bf16"))
+    sizes = [1, 255, 256, 257, 1023, 1025, 2049, 16383, 16384, 16385, 32767, 32768, 32769, 65539, 262147]
+    total = {"f32": 0, "bf16": 0}
+    plan = []
+    for dt in ("f32", "bf16"):
+        for op in ("add", "mul", "relu", "gelu"):
+            for k, n in enumerate(sizes):
+                off = 0 if k % 3 else 1  # every third at an odd element offset
+                plan.append((dt, op, n, off, k % 4 == 1))
+                total[dt] += n + 64
+    of = s.add_buf("out_f32", "f32", total["f32"])
+    ob = s.add_buf("out_bf16", "bf16", total["bf16"])
+    top = {"f32": 0, "bf16": 0}
+    for dt, op, n, off, chained in plan:
+        src, dst = (pf, of) if dt == "f32" else (pb, ob)
+        a_off = int(rng.integers(0, n_pool - n - 2)) // 256 * 256 + off
+        b_off = int(rng.integers(0, n_pool - n - 2)) // 256 * 256
+        o = top[dt] + off
+        top[dt] += n + 64
+        deps = (len(s.ops) - 1,) if chained and s.ops else ()
+        bref = S.Ref(src, b_off) if op in ("add", "mul") else None
+        s.ops.append(S.Op(op, dt, a=S.Ref(src, a_off), b=bref, out=S.Ref(dst, o), dims=(n,), deps=deps))
+    _run_and_compare(s, cfg=dict(stage_bytes=stage_bytes))
+
+
 def test_row_ops_many_rows():
     """Row ops of thousands of rows (about a thousand helper warps each,
     every helper taking further rows from the descriptor's counter and
