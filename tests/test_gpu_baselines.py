@@ -64,6 +64,16 @@ def test_c1_baseline_bit_exact(graph):
     assert rep.exact == len(s.ops)
 
 
+def test_c2_baseline_small():
+    """3,000 variable-shape element-wise descriptors launched eagerly (the
+    eager path's own 4,096-element tiles, not the executor's), every output
+    against the oracle."""
+    s = S.stream_c2(n_desc=3000, pool_elems=1 << 22)
+    ds = _eager(s, False)
+    rep, _ = compare_in_order(s, ds)
+    assert rep.ok(), "\n".join(rep.failures)
+
+
 @pytest.mark.parametrize("graph", [False, True])
 def test_mixed_small_baseline_every_op_kind(graph):
     s = S.stream_mixed_small()
