@@ -243,6 +243,32 @@ def test_host_bounds_checks_reject(G, bad):
     assert G.lib().gpuos_op_ntiles(d.ctypes.data, C.byref(n)) == G.EINVAL
 
 
+def test_elementwise_validation_cases(G):
+    """The element-wise checks (taken without data-dependent branches on the
+    host): each bad field alone is rejected, and what the op does not read
+    may be null."""
+    n = C.c_uint32()
+
+    def rc(op, dt=1, dims=(4096,), **kw):
+        return G.lib().gpuos_op_ntiles(_desc(G, op, dt, dims, **kw).ctypes.data, C.byref(n))
+
+    for op in ("add", "mul", "relu", "gelu"):
+        for dt in (0, 1):
+            assert rc(op, dt) == G.OK
+            assert rc(op, dt, a=0) == G.EINVAL
+            assert rc(op, dt, out=0) == G.EINVAL
+            assert rc(op, 5) == G.EINVAL                          # dtype
+            assert rc(op, dt, dims=(0,), a=0, b=0, out=0) == G.OK  # empty: nothing is read
+            assert n.value == 1
+    assert rc("add", b=0) == G.EINVAL and rc("mul", b=0) == G.EINVAL
+    assert rc("relu", b=0) == G.OK and rc("gelu", b=0) == G.OK      # unary: b unused
+    d = _desc(G, "add", 1, (4096,))
+    d["flags"] = 4                                                 # unknown flag bit
+    assert G.lib().gpuos_op_ntiles(d.ctypes.data, C.byref(n)) == G.EINVAL
+    d["flags"] = 1 | 2                                             # FENCE | DEP_REL
+    assert G.lib().gpuos_op_ntiles(d.ctypes.data, C.byref(n)) == G.OK
+
+
 def test_sdpa_workspace_formula_matches_stream_layout(G):
     from workloads.streams import sdpa_workspace_bytes
     for B, H, L in ((1, 32, 4096), (8, 32, 4096), (3, 4, 513), (2, 1, 1)):
