@@ -351,8 +351,8 @@ static bool al16(uint64_t p) { return (p & 15u) == 0; }
  * 40.5 -> 49.4 M descriptors/s with 4,096-element tiles -> 16,384; large
  * ops 0.89 -> 0.95 of the copy peak). Small GELUs split down to 2,048
  * elements, or 1,024 with a dependency (gelu_tile_min): their arithmetic,
- * not their bytes, sets the time. The device recovers the tile size from n and ntiles
- * alone (round_up(ceil(n / ntiles), 256)). */
+ * not their bytes, sets the time. The device recovers the tile size from n
+ * and ntiles alone (round_up(ceil(n / ntiles), 256)). */
 static_assert((GPUOS_EW_TILE_MIN & (GPUOS_EW_TILE_MIN - 1)) == 0 && (GPUOS_GELU_TILE_MIN & (GPUOS_GELU_TILE_MIN - 1)) == 0 &&
                   (GPUOS_GELU_DEP_TILE_MIN & (GPUOS_GELU_DEP_TILE_MIN - 1)) == 0 &&
                   (GPUOS_EW_TILE_F32 & (GPUOS_EW_TILE_F32 - 1)) == 0 &&
