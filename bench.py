@@ -137,11 +137,11 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
                    "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
 TRAFFIC = {
-    "c2": dict(bytes=250_042_624, descs=4096, sources="e050cb5b55caeecd"),
-    "c2l": dict(bytes=1_091_287_040, descs=400, sources="e050cb5b55caeecd"),
-    "c3": dict(bytes=414_025_984, descs=2048, sources="e050cb5b55caeecd"),
-    "c4": dict(bytes=31_064_849_920, descs=600, sources="e050cb5b55caeecd"),
-    "c5": dict(bytes=493_201_664, descs=224, sources="e050cb5b55caeecd"),
+    "c2": dict(bytes=250_250_240, descs=4096, sources="f01f21b62b9228d2"),
+    "c2l": dict(bytes=1_089_362_432, descs=400, sources="f01f21b62b9228d2"),
+    "c3": dict(bytes=412_231_680, descs=2048, sources="f01f21b62b9228d2"),
+    "c4": dict(bytes=31_043_868_160, descs=600, sources="f01f21b62b9228d2"),
+    "c5": dict(bytes=493_095_936, descs=224, sources="f01f21b62b9228d2"),
 }
 
 

@@ -787,7 +787,7 @@ DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
         float a8[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) a8[i] = init;
-#pragma unroll 2
+#pragma unroll 1
         for (uint32_t v = lane; v < nv; v += 32) {
             float f[8];
             unpack8(sx[v], f);
@@ -818,7 +818,7 @@ DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
     uint4 *y = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(d->out) + (uint64_t)row * H);
     if (K == ROW_SOFTMAX) {
         float m = -INFINITY;
-#pragma unroll 2
+#pragma unroll 1
         for (uint32_t v = lane; v < nv; v += 32) {
             float f[8];
             unpack8(sx[v], f);
@@ -829,7 +829,7 @@ DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
         float s8[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) s8[i] = 0.0f;
-#pragma unroll 2
+#pragma unroll 1
         for (uint32_t v = lane; v < nv; v += 32) {
             float f[8];
             unpack8(sx[v], f);
@@ -840,7 +840,7 @@ DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
 #pragma unroll
         for (int i = 0; i < 8; i++) sum += s8[i];
         const float inv = 1.0f / warp_sum(sum);
-#pragma unroll 2
+#pragma unroll 1
         for (uint32_t v = lane; v < nv; v += 32) {
             float f[8];
             unpack8(sx[v], f);
@@ -855,7 +855,7 @@ DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
     float s8[8];
 #pragma unroll
     for (int i = 0; i < 8; i++) s8[i] = 0.0f;
-#pragma unroll 2
+#pragma unroll 1
     for (uint32_t v = lane; v < nv; v += 32) {
         float f[8];
         unpack8(sx[v], f);
@@ -868,7 +868,7 @@ DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
     const float mean = warp_sum(sum) / (float)H;
 #pragma unroll
     for (int i = 0; i < 8; i++) s8[i] = 0.0f;
-#pragma unroll 2
+#pragma unroll 1
     for (uint32_t v = lane; v < nv; v += 32) {
         float f[8];
         unpack8(sx[v], f);
@@ -899,7 +899,7 @@ DEV int row_staged(const gpuos_devdesc *d, uint32_t row, uint32_t H, uint32_t C)
             if (!stage_wait0(w)) return GPUOS_ST_COPY_TIMEOUT;
         }
         const uint32_t ce = min(nv, c0 + cv);
-#pragma unroll 2
+#pragma unroll 1
         for (uint32_t v = c0 + lane; v < ce; v += 32) {
             float f[8], gf[8], bf[8];
             unpack8(sx[v], f);
@@ -981,7 +981,9 @@ DEV void row_issue(WarpStage *w, unsigned char *half, const uint16_t *X, uint32_
  * the first cost their passes, not a copy round trip each; and the helper's
  * rows run in one call of the op. Without a claim context (the eager
  * kernel) it runs the one row. Buffer: [gamma | beta] (LayerNorm only),
- * then two row halves. */
+ * then two row halves. The passes are rolled loops: unrolled twice, the
+ * row stream ran 17 % slower (more code to fetch per op, five row ops in
+ * turn on every SM). */
 template <int K>
 DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
 {
@@ -1039,7 +1041,7 @@ DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
             float s8[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) s8[i] = 0.0f;
-#pragma unroll 2
+#pragma unroll 1
             for (uint32_t v = lane; v < nv; v += 32) {
                 float f[8];
                 unpack8(sx[v], f);
@@ -1052,7 +1054,7 @@ DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
             const float mean = warp_sum(sum) / (float)H;
 #pragma unroll
             for (int i = 0; i < 8; i++) s8[i] = 0.0f;
-#pragma unroll 2
+#pragma unroll 1
             for (uint32_t v = lane; v < nv; v += 32) {
                 float f[8];
                 unpack8(sx[v], f);
@@ -1066,7 +1068,7 @@ DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
 #pragma unroll
             for (int i = 0; i < 8; i++) q += s8[i];
             const float rstd = rsqrtf(warp_sum(q) / (float)H + d->fparam[0]);
-#pragma unroll 2
+#pragma unroll 1
             for (uint32_t v = lane; v < nv; v += 32) {
                 float f[8], gf[8], bf[8];
                 unpack8(sx[v], f);
@@ -1081,7 +1083,7 @@ DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
             float a8[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) a8[i] = init;
-#pragma unroll 2
+#pragma unroll 1
             for (uint32_t v = lane; v < nv; v += 32) {
                 float f[8];
                 unpack8(sx[v], f);
@@ -1109,7 +1111,7 @@ DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
         } else {
             uint4 *y = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(d->out) + (uint64_t)row * H);
             float m = -INFINITY;
-#pragma unroll 2
+#pragma unroll 1
             for (uint32_t v = lane; v < nv; v += 32) {
                 float f[8];
                 unpack8(sx[v], f);
@@ -1120,7 +1122,7 @@ DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
             float s8[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) s8[i] = 0.0f;
-#pragma unroll 2
+#pragma unroll 1
             for (uint32_t v = lane; v < nv; v += 32) {
                 float f[8];
                 unpack8(sx[v], f);
@@ -1131,7 +1133,7 @@ DEV int row_pipe(const gpuos_devdesc *d, uint32_t row, uint32_t R, uint32_t H)
 #pragma unroll
             for (int i = 0; i < 8; i++) sum += s8[i];
             const float inv = 1.0f / warp_sum(sum);
-#pragma unroll 2
+#pragma unroll 1
             for (uint32_t v = lane; v < nv; v += 32) {
                 float f[8];
                 unpack8(sx[v], f);
