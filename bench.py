@@ -725,7 +725,7 @@ def main():
     ap.add_argument("--stage-bytes", type=int, default=16384, help="shared-memory staging per warp (0 = none)")
     ap.add_argument("--blocks", type=int, default=0, help="executor blocks (0 = one per SM)")
     ap.add_argument("--sequencers", type=int, default=0, help="sequencer warps (0 = the library's default)")
-    ap.add_argument("--ring-entries", type=int, default=0, help="ring slots (0 = the library's default, 4096)")
+    ap.add_argument("--ring-entries", type=int, default=0, help="ring slots (0 = the library's default, 8192)")
     ap.add_argument("--spin-polls", type=int, default=0, help="idle polls before backoff sleeps (0 = default)")
     ap.add_argument("--backoff-max-ns", type=int, default=0, help="longest idle sleep (0 = default)")
     ap.add_argument("--producers-sweep", action="store_true",
