@@ -75,6 +75,46 @@ def test_deferred_start_fills_ring_then_wraps():
     _check_all(s, ds)
 
 
+def test_stop_stream_and_tile_profile():
+    """The executor's own stream brackets its single launch (an event recorded
+    after it completes only when the kernel ends), stop drains the ring and
+    ends the kernel (exit reason 1), and the tile profile counts every tile
+    of every descriptor once, per op kind, as the host's tiling rule gives
+    them; the results match the oracle."""
+    import torch
+    from workloads.device import DeviceStream
+    s = S.stream_elementwise("ew_profile", 300, 256, 65536, 0.30, 1 << 22, 21)
+    ds = DeviceStream(s)
+    d = ds.descs()
+    expected = {}
+    for i, o in enumerate(s.ops):
+        expected[o.op] = expected.get(o.op, 0) + G().op_ntiles(d[i:i + 1])
+    ex = G().Executor(deferred_start=1)
+    try:
+        sp = ex.stream
+        assert sp != 0
+        xs = torch.cuda.ExternalStream(sp)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(xs)
+        ex.start()
+        e1.record(xs)
+        ex.submit_batch(d)
+        ex.sync(timeout_ms=30_000)
+        assert not e1.query()  # still resident: the event waits for the kernel's end
+        assert ex.stop() == 0
+        e1.synchronize()
+        assert e0.elapsed_time(e1) > 0.0
+        st = ex.stats()
+        prof = ex.tile_profile()
+    finally:
+        assert ex.shutdown() == 0
+    assert st["completed"] == len(s.ops) and st["errors"] == 0 and st["exit_reason"] == 1
+    assert {k: v["tiles"] for k, v in prof.items()} == expected
+    assert all(v["body_us"] > 0.0 and v["finish_us"] >= 0.0 and v["dep_us"] >= 0.0 for v in prof.values())
+    _check_all(s, ds)
+
+
 def _big_add(n):
     import torch
     a = torch.ones(n, dtype=torch.float32, device="cuda")
