@@ -137,11 +137,11 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("persistent_micro_dispatch_gb300/csrc/gpuos_device.cu",
                    "persistent_micro_dispatch_gb300/csrc/gpuos_internal.h")
 TRAFFIC = {
-    "c2": dict(bytes=250_250_240, descs=4096, sources="f01f21b62b9228d2"),
-    "c2l": dict(bytes=1_089_362_432, descs=400, sources="f01f21b62b9228d2"),
-    "c3": dict(bytes=412_231_680, descs=2048, sources="f01f21b62b9228d2"),
-    "c4": dict(bytes=31_043_868_160, descs=600, sources="f01f21b62b9228d2"),
-    "c5": dict(bytes=493_095_936, descs=224, sources="f01f21b62b9228d2"),
+    "c2": dict(bytes=251_875_840, descs=4096, sources="59f0042f3e66b557"),
+    "c2l": dict(bytes=1_089_941_760, descs=400, sources="59f0042f3e66b557"),
+    "c3": dict(bytes=417_755_392, descs=2048, sources="59f0042f3e66b557"),
+    "c4": dict(bytes=31_051_235_584, descs=600, sources="59f0042f3e66b557"),
+    "c5": dict(bytes=492_626_176, descs=224, sources="59f0042f3e66b557"),
 }
 
 

@@ -431,7 +431,7 @@ GPUOS_API int gpuos_tile_profile_get(gpuos_ctx *ctx, gpuos_tile_profile *out);
  * Host tiling rule of a built-in op (what ntiles the library will write);
  * one tile is one warp's unit of work:
  *   add/mul/relu/gelu  ceil(n / te), te the smallest power of two >= n / 16
- *                      within [16384 (GELU: 2048, or 1024 with a dependency),
+ *                      within [16384 (a GELU with a dependency: 1024),
  *                      16384 (f32) or 32768 (bf16)]
  *                      elements;
  *                      the device splits n into ntiles ranges of

@@ -349,10 +349,10 @@ static bool al16(uint64_t p) { return (p & 15u) == 0; }
  * 5-7 us of copying, so fewer, larger tiles raise what the worker warps
  * sustain (measured on the variable-shape stream from a pre-filled ring:
  * 40.5 -> 49.4 M descriptors/s with 4,096-element tiles -> 16,384; large
- * ops 0.89 -> 0.95 of the copy peak). Small GELUs split down to 2,048
- * elements, or 1,024 with a dependency (gelu_tile_min): their arithmetic,
- * not their bytes, sets the time. The device recovers the tile size from n
- * and ntiles alone (round_up(ceil(n / ntiles), 256)). */
+ * ops 0.89 -> 0.95 of the copy peak). A free GELU takes the same tiles; a
+ * GELU with a dependency splits down to 1,024 elements (gelu_tile_min).
+ * The device recovers the tile size from n and ntiles alone
+ * (round_up(ceil(n / ntiles), 256)). */
 static_assert((GPUOS_EW_TILE_MIN & (GPUOS_EW_TILE_MIN - 1)) == 0 && (GPUOS_GELU_TILE_MIN & (GPUOS_GELU_TILE_MIN - 1)) == 0 &&
                   (GPUOS_GELU_DEP_TILE_MIN & (GPUOS_GELU_DEP_TILE_MIN - 1)) == 0 &&
                   (GPUOS_EW_TILE_F32 & (GPUOS_EW_TILE_F32 - 1)) == 0 &&
@@ -376,9 +376,11 @@ static uint64_t ew_tiles(uint64_t n, uint64_t tile_min, uint64_t tile_max)
 /* A GELU that waits on another descriptor sits on a dependency chain, where
  * its latency adds up: it keeps the finer split (measured on the mixed
  * pipeline, whose every op has a dependency: 1,024-element tiles 129.4 K
- * ops/s, 2,048 127.5 K); a free GELU only needs throughput, which the
- * coarser split serves better (variable-shape stream 50.6 -> 52.3 M
- * descriptors/s with 2,048 for all GELUs). */
+ * ops/s, 2,048 127.5 K); a free GELU only needs throughput, which fewer,
+ * larger tiles serve better (variable-shape stream, free GELUs from 2,048 /
+ * 4,096 / 8,192 / 16,384 elements: 49.2-50.8 / 51.6-53.0 / 55.1 / 55.8 M
+ * descriptors/s, each step measured against the one before on one box;
+ * the mixed pipeline unchanged). */
 static uint64_t gelu_tile_min(const gpuos_desc *d)
 {
     return (d->dep[0] | d->dep[1]) ? GPUOS_GELU_DEP_TILE_MIN : GPUOS_GELU_TILE_MIN;

@@ -13,7 +13,7 @@
 #define GPUOS_EW_TILE_F32 16384           /* largest fp32 element-wise tile the host picks (64 KB an operand) */
 #define GPUOS_EW_TILE_BF16 32768          /* ... and bf16 tile */
 #define GPUOS_EW_TILE_MIN 16384           /* smallest add/mul/ReLU tile the host picks */
-#define GPUOS_GELU_TILE_MIN 2048          /* ... and GELU tile (more arithmetic per element) */
+#define GPUOS_GELU_TILE_MIN 16384         /* ... and GELU tile (as add/mul/ReLU) */
 #define GPUOS_GELU_DEP_TILE_MIN 1024      /* ... and GELU tile of a descriptor with a dependency */
 #define GPUOS_EAGER_TILE_F32 4096         /* element-wise tiles of the eager baseline: largest fp32 */
 #define GPUOS_EAGER_TILE_BF16 8192        /* ... largest bf16 */

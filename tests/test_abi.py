@@ -74,8 +74,9 @@ def _desc(G, op, dtype=1, dims=(), ptr=0x1000, **kw):
 
 def test_elementwise_tiling_over_sizes(G):
     """The element-wise tile count over many sizes, against the rule stated
-    as a loop: start at the op's smallest tile (add/mul/ReLU 16384 elements,
-    GELU 2048), double it while it is below the dtype's largest tile (fp32
+    as a loop: start at the op's smallest tile (16384 elements; a GELU with
+    a dependency 1024, see test_tiling_rule), double it while it is below
+    the dtype's largest tile (fp32
     16384, bf16 32768) and would cut n into more than 16 tiles; the count is
     ceil(n / tile), and an empty op has one tile."""
     rng = np.random.default_rng(5)
@@ -84,7 +85,7 @@ def test_elementwise_tiling_over_sizes(G):
                     + rng.integers(1, 1 << 31, size=300).tolist()))
     for op in ("add", "mul", "relu", "gelu"):
         for dt in (0, 1):
-            tmin = 2048 if op == "gelu" else 16384
+            tmin = 16384
             tmax = 16384 if dt == 0 else 32768
             for n in ns:
                 te = min(tmin, tmax)
@@ -97,11 +98,13 @@ def test_elementwise_tiling_over_sizes(G):
 
 
 def test_tiling_rule(G):
-    # element-wise: te = smallest power of two >= n/16 within [16384 (GELU 2048), 16384 | 32768]
+    # element-wise: te = smallest power of two >= n/16 within [16384 (a GELU with a dependency:
+    # 1024), 16384 | 32768]
     assert G.op_ntiles(_desc(G, "add", 0, (4096,))) == 1          # te 16384
-    assert G.op_ntiles(_desc(G, "gelu", 0, (4096,))) == 2         # te 2048
+    assert G.op_ntiles(_desc(G, "gelu", 0, (4096,))) == 1         # te 16384
     assert G.op_ntiles(_desc(G, "add", 1, (16384,))) == 1         # te 16384
-    assert G.op_ntiles(_desc(G, "gelu", 1, (16384,))) == 8        # te 2048
+    assert G.op_ntiles(_desc(G, "gelu", 1, (16384,))) == 1        # te 16384
+    assert G.op_ntiles(_desc(G, "gelu", 0, (16385,))) == 2        # te 16384
     assert G.op_ntiles(_desc(G, "relu", 0, (8193,))) == 1         # te 16384
     assert G.op_ntiles(_desc(G, "relu", 0, (16385,))) == 2        # te 16384
     assert G.op_ntiles(_desc(G, "mul", 0, (1000,))) == 1
@@ -110,7 +113,8 @@ def test_tiling_rule(G):
     assert G.op_ntiles(_desc(G, "add", 0, (1 << 20,))) == 64      # te 16384 (fp32 cap)
     assert G.op_ntiles(_desc(G, "add", 1, (1 << 20,))) == 32      # te 32768 (bf16 cap)
     assert G.op_ntiles(_desc(G, "gelu", 1, (1 << 20,))) == 32     # te 32768 (bf16 cap)
-    assert G.op_ntiles(_desc(G, "gelu", 1, (40000,))) == 10       # te 4096 >= 40000/16
+    assert G.op_ntiles(_desc(G, "gelu", 1, (40000,))) == 3        # te 16384 >= 40000/16
+    assert G.op_ntiles(_desc(G, "gelu", 1, (600000,))) == 19      # n/16 wants 65536: te 32768 (bf16 cap)
     # a GELU with a dependency keeps the finer split: te from 1024
     assert G.op_ntiles(_desc(G, "gelu", 1, (4096,), dep=(5, 0))) == 4      # te 1024
     assert G.op_ntiles(_desc(G, "gelu", 1, (4096,), dep=(0, 5))) == 4

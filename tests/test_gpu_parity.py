@@ -96,9 +96,10 @@ def test_c4_decode_wide_length_spread(stage_bytes):
 @pytest.mark.parametrize("stage_bytes", [16384, 0])
 def test_elementwise_sizes_around_tile_boundaries(stage_bytes):
     """add/mul/ReLU/GELU in fp32 and bf16 at sizes around the tile sizes
-    (1,024, 2,048, 16,384, 32,768 elements and their multiples), aligned and
-    at odd element offsets (the scalar path), some with a dependency (a
-    GELU then keeps its finer tiles); every output against the oracle."""
+    (1,024 for a GELU with a dependency, 16,384 and 32,768 elements, and
+    their multiples), aligned and at odd element offsets (the scalar path),
+    some with a dependency (a GELU then keeps its finer tiles); every output
+    against the oracle."""
     rng = np.random.default_rng(45)
     s = S.Stream("ew_bounds", meta=dict(seed=45))
     n_pool = 1 << 20
